@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one pass of the whole decode path over the batch: the host
+allocator reserves every sequence's next slot (new block when full,
+copy-on-write when shared), slots/tables go to the device, block copies run,
+the new keys/values are appended, and paged decode (split-K + log-sum-exp
+merge) attends over the grown contexts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is KV-read GB/s of whole steps
+(algorithmic KV bytes: every context token's key and value row read once per
+step) with the step inputs resident in HBM; ``e2e`` is the same metric with
+each step's new tokens copied from pinned host memory and the output copied
+back inside the timed region.  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, context_lens, free_order, pool_blocks, queries, random_pool  # noqa: E402
+from workloads import serving_step_tokens  # noqa: E402
+
+DEFAULT_WORKLOAD = "mha_bf16"
+METRIC = "paged-decode KV-read GB/s"
+UNIT = "GB/s"
+
+
+def kv_bytes(ctx: np.ndarray, w) -> int:
+    return int(np.asarray(ctx, dtype=np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen([exe, "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        import torch
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def workload_for(name: str, rank: int):
+    w = WORKLOADS[name]
+    return w.replace(seed=w.seed + 1000 * rank) if rank else w
+
+
+def _host_tokens(w, steps):
+    """Per-step new tokens (q, k, v) as numpy bf16 bits / fp32."""
+    return [serving_step_tokens(w, i) for i in range(steps)]
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import paged_kv_cache_216_gb300 as pa
+    from paged_kv_cache_216_gb300 import build
+    from paged_kv_cache_216_gb300.prefix import populate
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload_for(args.workload, rank)
+    K, W = args.steps, args.warmup
+    total_steps = W + 2 * K  # device-resident run, then the end-to-end run
+    ctx0 = context_lens(w)
+    nb = pool_blocks(w, ctx0, extra_steps=total_steps) + w.prefix_share
+    order = free_order(w, nb)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    k_cache = to_dev(random_pool(w, nb, "k"))
+    v_cache = to_dev(random_pool(w, nb, "v"))
+    alloc = pa.BlockAllocator(nb, w.block_size, order)
+    pairs = populate(alloc, ctx0, w.prefix_len, w.prefix_share)
+    if len(pairs):
+        pa.copy_blocks(k_cache, v_cache, to_dev(pairs))
+    seq_ids = np.arange(w.num_seqs)
+    eng = pa.ServingEngine(k_cache, v_cache, alloc, seq_ids, w.num_heads, w.scale,
+                           int(ctx0.max()) + total_steps, w.partition_size)
+    toks = _host_tokens(w, total_steps)
+    dev_toks = [tuple(to_dev(x) for x in t) for t in toks[: W + K]]
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=k_cache.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ctx_bytes0 = kv_bytes(ctx0, w)
+    flush = None
+    if ctx_bytes0 < 2 * l2:
+        flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device=dev)
+
+    # warm-up
+    for i in range(W):
+        if flush is not None:
+            flush.add_(1)
+        eng.step(*dev_toks[i], out=out)
+    torch.cuda.synchronize()
+
+    # device-resident run: K steps, events around every decode launch
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    bytes_steps = []
+    launches0 = eng.launches
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        if flush is not None:
+            flush.add_(1)
+        q, kn, vn = dev_toks[W + i]
+        step_ev[i][0].record(stream)
+        eng.step(q, kn, vn, out=out, events=dec_ev[i])
+        step_ev[i][1].record(stream)
+        bytes_steps.append(kv_bytes(eng.ctx_h.numpy(), w))
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    launches = eng.launches - launches0
+    clk = clocks.stop()
+    if flush is None:
+        t_dev = step_ev[0][0].elapsed_time(step_ev[-1][1]) / 1e3
+    else:
+        t_dev = sum(a.elapsed_time(b) for a, b in step_ev) / 1e3
+    t_dec = [a.elapsed_time(b) / 1e3 for a, b in dec_ev]
+    local_bytes = float(sum(bytes_steps))
+    t_max = allreduce_max(t_dev, world)
+    total_bytes = allreduce_sum(local_bytes, world)
+    value = total_bytes / t_max / 1e9
+    tokens_s = allreduce_sum(float(w.num_seqs * K), world) / t_max
+
+    # end-to-end run: host (pinned) tokens in, host output back, every step
+    pin = [tuple(torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if x.dtype == np.uint16 else x)
+                 .pin_memory() for x in t) for t in toks[W + K:]]
+    if w.dtype == "bf16":
+        pin = [tuple(x.view(torch.bfloat16) for x in t) for t in pin]
+    staging = {"q": torch.empty_like(dev_toks[0][0]), "k": torch.empty_like(dev_toks[0][1]),
+               "v": torch.empty_like(dev_toks[0][2]), "out": out}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_bytes = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        if flush is not None:
+            flush.add_(1)
+        eng.step_host(*pin[i], out_h, staging)
+        e2e_bytes += kv_bytes(eng.ctx_h.numpy(), w)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_e2e = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = allreduce_sum(float(e2e_bytes), world) / t_e2e / 1e9
+    h2d = sum(x.numel() * x.element_size() for x in pin[0])
+    d2h = out_h.numel() * out_h.element_size()
+
+    # roofline of the decode call (main kernel + its merge), from the live events
+    dec_avg = sum(t_dec) / len(t_dec)
+    dec_bytes = sum(bytes_steps) / len(bytes_steps)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    achieved = dec_bytes / dec_avg / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            traffic = json.load(f).get(args.workload)
+    status = pa.get_status()
+    if status:
+        raise RuntimeError(f"device status word {status:#x} after the benchmark")
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(t_max / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.num_seqs, "query_heads": w.num_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": eng.partition_size,
+            "context_start_mean": float(ctx0.mean()), "context_start_max": int(ctx0.max()),
+            "kv_bytes_per_step": int(dec_bytes),
+            "l2": ("flushed before every step" if flush is not None else
+                   f"inputs larger than L2 ({dec_bytes / 1e9:.2f} GB KV per step vs {l2 / 1e6:.0f} MB L2)"),
+            "parallelism": f"replicas x{world}",
+        },
+        "decode_tokens_per_s": round(tokens_s, 1),
+        "wall_s": round(wall, 4),
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "paged_decode_tc_kernel + lse_merge_kernel",
+                     "peak_source": f"{peak_src} hbm_gbs", "decode_ms": round(dec_avg * 1e3, 4)},
+        "clocks": clk,
+    }
+    return res, eng, w
+
+
+def oracle_sample(w, budget_s: float):
+    """Time the CPU oracle on a bounded sample of the workload: decode of as
+    many whole sequences as fit the time budget.  Returns (GB/s, sample
+    description, threads)."""
+    from oracle.attention import paged_decode
+    from oracle.serving import initial_state, tables_array
+
+    ctx = context_lens(w)
+    nb = pool_blocks(w, ctx) + w.prefix_share
+    order = free_order(w, nb)
+    alloc, _ = initial_state(w.num_seqs, w.block_size, ctx, nb, order, w.prefix_len, w.prefix_share)
+    tables = tables_array(alloc, range(w.num_seqs), -(-int(ctx.max()) // w.block_size))
+    kp = random_pool(w, nb, "k")
+    vp = random_pool(w, nb, "v")
+    q = queries(w)
+    done, t, nbytes = 0, 0.0, 0
+    rng = np.random.default_rng(0)
+    order_s = rng.permutation(w.num_seqs)
+    while done < w.num_seqs and t < budget_s:
+        s = int(order_s[done])
+        t0 = time.perf_counter()
+        paged_decode(q, kp, vp, tables, ctx, w.scale, w.dtype, seqs=[s])
+        t += time.perf_counter() - t0
+        nbytes += kv_bytes(ctx[[s]], w)
+        done += 1
+    gbs = nbytes / t / 1e9
+    return gbs, f"oracle decode of {done} of {w.num_seqs} sequences ({nbytes / 1e6:.1f} MB KV) in {t:.1f} s", t
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    vals = []
+    desc = ""
+    for _ in range(args.steps):
+        gbs, desc, _ = oracle_sample(w, budget_s=max(1.0, args.ref_budget / max(1, args.steps)))
+        vals.append(gbs)
+    value = statistics.median(vals)
+    res = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "batch": w.num_seqs, "query_heads": w.num_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--ref-budget", type=float, default=20.0, help="seconds of oracle time in the reference arm")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, eng, w = run_ours(args, rank, world, local)
+    if rank == 0:
+        gbs, desc, _ = oracle_sample(WORKLOADS[args.workload], args.cpu_budget)
+        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                               "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * pa.h -- C ABI of the paged KV cache library (libpa.so): KV append, paged
+ * decode attention with split-K and log-sum-exp merge, block copy for
+ * copy-on-write, and a host-side block allocator.
+ *
+ * Sources (web pages on paged KV caches):
+ *   [Day6]  "Day 6/90 of Inference Engineering" (post on
+ *           bittide.aicompass.dev), notes on PagedAttention: paragraph 2
+ *           (the cache manager hands out one fixed-size block at a time, a
+ *           new one when the last is full), paragraph 5 (a shared prefix
+ *           shares blocks; a diverging sequence writes to a new block),
+ *           paragraph 6 (the block table makes scattered blocks read as a
+ *           contiguous KV cache).
+ *   [PAK]   "PagedAttention Kernel：大模型推理优化的显存管理革新"
+ *           (intelliparadigm.com), section 3.1 (Q·Kᵀ by blocks, softmax,
+ *           P·V by blocks) and section 2.2 (prefetch the next page while
+ *           computing the current one).
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or retains them.  Pointers named
+ *     "host" are ordinary host memory, also caller-owned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and is asynchronous: the call returns once the kernels are
+ *     launched.  Buffers must stay valid until the stream reaches that point.
+ *   - Return value: PA_OK (0) or a negative PA_ERR_* code.  On error nothing
+ *     was launched and no buffer was touched; pa_last_error() describes it.
+ *   - Host-visible arguments are validated before any launch.  Arguments
+ *     that live on the device (slots, block ids, context lengths) are
+ *     checked in the kernels: an out-of-range value skips the access and
+ *     sets a bit in the device status word (pa_get_status), never faults.
+ *
+ * Cache layout (the pages give none; this library's choice):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim],
+ *   row-major, element type `dtype`.  Token t of a sequence lives in
+ *   physical block block_tables[seq][t / block_size], row t % block_size.
+ *   Slot s = block * block_size + row.
+ *
+ * Supported set: dtype PA_BF16 or PA_F32; head_dim 64 or 128; block_size 8,
+ * 16 or 32; g = num_heads / num_kv_heads in {1, 2, 4, 8}.  Anything else
+ * returns PA_ERR_UNSUPPORTED.  Decode in bf16 runs on tensor cores with fp32
+ * accumulation; fp32 decode runs on CUDA cores in fp32.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define PA_OK 0
+#define PA_ERR_INVALID (-1)     /* bad argument (null pointer, size, range) */
+#define PA_ERR_UNSUPPORTED (-2) /* valid but outside the supported set */
+#define PA_ERR_OOM (-3)         /* allocator: not enough free blocks */
+#define PA_ERR_STATE (-4)       /* allocator: unknown or duplicate sequence */
+#define PA_ERR_CUDA (-5)        /* a CUDA runtime call failed */
+
+/* Element types of q, k, v, caches and out (all the same in one call). */
+#define PA_F32 0
+#define PA_BF16 1
+
+/* Bits of the device status word. */
+#define PA_STATUS_BAD_SLOT 1u    /* append: slot >= num_blocks*block_size */
+#define PA_STATUS_BAD_BLOCK 2u   /* block id outside [0, num_blocks) */
+#define PA_STATUS_BAD_CONTEXT 4u /* context_len < 1 or > max_context_len */
+#define PA_STATUS_TIMEOUT 8u     /* a pipeline wait gave up (kernel aborted) */
+
+/* Message for the last error on the calling thread ("" if none). */
+const char* pa_last_error(void);
+
+/* Library ABI version (increments on any signature change). */
+int pa_version(void);
+
+/*
+ * Read and clear the device status word of the current device (a bitwise OR
+ * of PA_STATUS_* raised by kernels since the last call).  Synchronizes
+ * `stream`.  *status (host) receives the word.
+ */
+int pa_get_status(void* stream, uint32_t* status);
+
+/*
+ * KV append [Day6 paragraph 2]: write each new token's key and value into
+ * its slot of the paged cache.
+ *   k, v          device, [num_tokens][num_kv_heads][head_dim], dtype
+ *   slot_mapping  device, [num_tokens] int64; slot = block*block_size + row;
+ *                 a negative slot skips the token; slots must be distinct
+ *                 (two tokens writing one slot leave either value)
+ *   k_cache, v_cache  device, cache layout above, written in place
+ * A slot >= num_blocks*block_size is skipped and sets PA_STATUS_BAD_SLOT.
+ * The copy is bitwise.
+ */
+int pa_cache_append(const void* k, const void* v, const int64_t* slot_mapping,
+                    int num_tokens, void* k_cache, void* v_cache, int num_blocks,
+                    int num_kv_heads, int head_dim, int block_size, int dtype,
+                    void* stream);
+
+/*
+ * Block copy for copy-on-write [Day6 paragraph 5]: for each pair
+ * (src, dst) in `pairs` (device, [num_pairs][2] int32) copy the whole block
+ * src of k_cache and of v_cache (every KV head, every row) to block dst.
+ * dst blocks must be distinct and must not appear as a src in the same call.
+ * An id outside [0, num_blocks) skips the pair and sets PA_STATUS_BAD_BLOCK.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs,
+                   int num_pairs, int num_blocks, int num_kv_heads,
+                   int head_dim, int block_size, int dtype, void* stream);
+
+/*
+ * Partition size (tokens) that pa_decode uses for these sizes: the given
+ * `partition_size` if > 0 (it must be a positive multiple of 32), else the
+ * library's choice (a multiple of 32).  Returns the size, or a negative
+ * PA_ERR_* code.
+ */
+int pa_decode_partition_size(int num_seqs, int num_kv_heads,
+                             int max_context_len, int partition_size);
+
+/*
+ * Bytes of device workspace pa_decode needs for these sizes (0 when no
+ * sequence can span more than one partition).  The workspace holds the
+ * split-K partials: per (sequence, partition, query head) head_dim fp32
+ * un-normalised outputs and a (max, sum) pair.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                 int max_context_len, int partition_size);
+
+/*
+ * Paged decode attention [PAK section 3.1; Day6 paragraph 6]: for every
+ * sequence s and query head h, with n = context_lens[s] and kv = h / g,
+ *     out[s][h] = softmax(scale * K_s q[s][h]) V_s
+ * where K_s, V_s are the sequence's first n key/value rows of KV head kv,
+ * gathered through block_tables[s].  Contexts are split into partitions of
+ * partition_size tokens (0 = library choice) processed in parallel and
+ * merged by log-sum-exp.
+ *   q             device, [num_seqs][num_heads][head_dim], dtype
+ *   k_cache, v_cache  device, cache layout above
+ *   block_tables  device, [num_seqs][max_blocks_per_seq] int32; entries past
+ *                 a sequence's last block are not read
+ *   context_lens  device, [num_seqs] int32, each in [1, max_context_len]
+ *   max_context_len  host upper bound of context_lens;
+ *                 ceil(max_context_len / block_size) <= max_blocks_per_seq
+ *   out           device, [num_seqs][num_heads][head_dim], dtype
+ *   workspace     device, >= pa_decode_workspace_bytes(...) bytes, 256-byte
+ *                 aligned (may be NULL when that size is 0); contents on
+ *                 entry do not matter
+ * q and the caches must be 16-byte aligned.  A context length outside
+ * [1, max_context_len] sets PA_STATUS_BAD_CONTEXT (length 0 gives a zero
+ * output row; longer ones are cut to max_context_len).
+ */
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq,
+              const int32_t* context_lens, int max_context_len, float scale,
+              void* out, int num_seqs, int num_heads, int num_kv_heads,
+              int head_dim, int block_size, int num_blocks, int partition_size,
+              void* workspace, size_t workspace_bytes, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator [Day6 paragraphs 2, 5, 6].  CPU only; no CUDA call.
+ *
+ * Free list: a stack.  A fresh allocator hands out free_order[0] first, then
+ * free_order[1], ...; a freed block goes on top.  Sharing is ref-counted:
+ * pa_seq_fork gives the child the parent's blocks and one more reference to
+ * each.  Appending to a sequence whose last block is partly filled and
+ * shared takes a new block and reports the copy (src -> dst) the caller must
+ * apply with pa_copy_blocks before writing the token (copy-on-write).  A
+ * call that fails (PA_ERR_OOM, PA_ERR_STATE, PA_ERR_INVALID) changes
+ * nothing.  Not thread-safe: one allocator per thread at a time.
+ * ------------------------------------------------------------------------ */
+typedef struct pa_alloc pa_alloc;
+
+/* New allocator over blocks 0..num_blocks-1.  free_order (host, nullable):
+ * a permutation of 0..num_blocks-1 giving the hand-out order; NULL means
+ * ascending.  *out receives the handle. */
+int pa_alloc_create(int num_blocks, int block_size, const int32_t* free_order,
+                    pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* a);
+int pa_alloc_num_free(const pa_alloc* a);
+
+/* Add sequence seq_id holding num_tokens tokens in ceil(num_tokens /
+ * block_size) fresh blocks. */
+int pa_seq_add(pa_alloc* a, int64_t seq_id, int num_tokens);
+/* Child shares every block of parent (refcount + 1 each). */
+int pa_seq_fork(pa_alloc* a, int64_t parent_id, int64_t child_id);
+/* Reserve the slot of the sequence's next token.  *slot receives it;
+ * *cow_src, *cow_dst receive the block copy to apply first, or -1, -1. */
+int pa_seq_append_slot(pa_alloc* a, int64_t seq_id, int64_t* slot,
+                       int32_t* cow_src, int32_t* cow_dst);
+/* Drop the sequence: one reference less on each of its blocks, in table
+ * order; blocks reaching zero go on top of the free list in that order. */
+int pa_seq_free(pa_alloc* a, int64_t seq_id);
+/* Token count of the sequence (>= 0), or a negative PA_ERR_* code. */
+int pa_seq_num_tokens(const pa_alloc* a, int64_t seq_id);
+/* Copy up to cap block ids of the sequence's table into out (host);
+ * *n_out receives the table length (PA_ERR_INVALID if cap is too small). */
+int pa_seq_block_table(const pa_alloc* a, int64_t seq_id, int32_t* out,
+                       int cap, int* n_out);
+/* Reference count of a block (>= 0), or a negative PA_ERR_* code. */
+int pa_block_refcount(const pa_alloc* a, int block_id);
+
+/*
+ * Batched serving step on the host: reserve the next slot of each of the n
+ * sequences seq_ids[0..n-1], in order.  Outputs (host):
+ *   slot_mapping [n] int64; cow_pairs [n][2] int32 with *num_cow pairs used;
+ *   block_tables [n][width] int32 (nullable): row i is updated in place
+ *   where sequence i's table changed (rows are assumed to hold its table
+ *   already; width must cover the grown table);
+ *   context_lens [n] int32 (nullable): the new token counts.
+ * If the pool cannot cover every new block of the batch, returns PA_ERR_OOM
+ * and changes nothing.
+ */
+int pa_seqs_append_slots(pa_alloc* a, const int64_t* seq_ids, int n,
+                         int64_t* slot_mapping, int32_t* cow_pairs,
+                         int* num_cow, int32_t* block_tables, int width,
+                         int32_t* context_lens);
+
+/* Write the tables of seq_ids (host) into block_tables [n][width] (host),
+ * padding with -1, and their token counts into context_lens [n] (nullable). */
+int pa_seqs_block_tables(const pa_alloc* a, const int64_t* seq_ids, int n,
+                         int32_t* block_tables, int width,
+                         int32_t* context_lens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,266 @@
+// C ABI entry points (include/pa.h): argument validation, partition and
+// workspace sizing, TMA descriptor set-up and kernel dispatch.  No device
+// memory is allocated here; every buffer is the caller's.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "kernels.h"
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+// Device status word: OR of PA_STATUS_* bits raised by kernels.  Each device
+// that loads the library has its own copy.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  static thread_local char buf[256];
+  std::snprintf(buf, sizeof(buf), "%s: %s", what, cudaGetErrorString(e));
+  return pa_fail(PA_ERR_CUDA, buf);
+}
+
+// Address of this device's status word (looked up once per device).
+int status_ptr(unsigned** out) {
+  static unsigned* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return pa_fail(PA_ERR_UNSUPPORTED, "device ordinal too large");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  *out = ptrs[dev];
+  return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a bf16 cache viewed as a 2D array [N*Hkv*B rows][D]; one
+// box is B rows x 64 dims with 128-byte swizzle.
+int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D) {
+  auto fn = encode_fn();
+  if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * Hkv * B};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)B};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  return PA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool supported_shape(int D, int B) { return (D == 64 || D == 128) && (B == 8 || B == 16 || B == 32); }
+
+int elem_bytes(int dtype) { return dtype == PA_BF16 ? 2 : dtype == PA_F32 ? 4 : 0; }
+
+// Work items (sequence x partition x KV head) below which the library
+// splits contexts into smaller partitions; about four per resident CTA.
+constexpr long long kMinItems = 1216;
+constexpr int kDefaultPartition = 512;
+constexpr int kMinPartition = 64;
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+int pa_get_status(void* stream, uint32_t* status) {
+  if (!status) return pa_fail(PA_ERR_INVALID, "pa_get_status: null status");
+  unsigned* dptr = nullptr;
+  int rc = status_ptr(&dptr);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, dptr, sizeof(unsigned), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dptr, 0, sizeof(unsigned), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_get_status");
+  *status = host;
+  return PA_OK;
+}
+
+int pa_cache_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens, void* k_cache,
+                    void* v_cache, int num_blocks, int num_kv_heads, int head_dim, int block_size, int dtype,
+                    void* stream) {
+  const int es = elem_bytes(dtype);
+  if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_cache_append: dtype");
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_cache_append: sizes");
+  if (!supported_shape(head_dim, block_size)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_cache_append: head_dim/block_size");
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return pa_fail(PA_ERR_INVALID, "pa_cache_append: null pointer");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return pa_fail(PA_ERR_INVALID, "pa_cache_append: misaligned pointer");
+  unsigned* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  cudaError_t e = pa::launch_cache_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                                          num_kv_heads, head_dim, block_size, es, status,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pa_cache_append launch");
+  return PA_OK;
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs, int num_blocks,
+                   int num_kv_heads, int head_dim, int block_size, int dtype, void* stream) {
+  const int es = elem_bytes(dtype);
+  if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: dtype");
+  if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0) return pa_fail(PA_ERR_INVALID, "pa_copy_blocks: sizes");
+  if (!supported_shape(head_dim, block_size)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: head_dim/block_size");
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !pairs) return pa_fail(PA_ERR_INVALID, "pa_copy_blocks: null pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(pairs, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_copy_blocks: misaligned pointer");
+  unsigned* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * es;
+  for (int off = 0; off < num_pairs; off += 65535) {
+    const int n = std::min(65535, num_pairs - off);
+    cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, pairs + 2 * (size_t)off, n, num_blocks, block_bytes,
+                                           status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_copy_blocks launch");
+  }
+  return PA_OK;
+}
+
+int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len, int partition_size) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 1)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_partition_size: sizes");
+  if (partition_size > 0) {
+    if (partition_size % 32) return pa_fail(PA_ERR_INVALID, "partition_size must be a multiple of 32");
+    return partition_size;
+  }
+  if (partition_size < 0) return pa_fail(PA_ERR_INVALID, "partition_size < 0");
+  int P = kDefaultPartition;
+  while (P > kMinPartition && (long long)num_seqs * num_kv_heads * cdiv(max_context_len, P) < kMinItems) P /= 2;
+  return P;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                 int partition_size) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 1 || partition_size < 32) return 0;
+  const long long parts = cdiv(max_context_len, partition_size);
+  if (parts <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * parts * num_heads;
+  const size_t o_bytes = (rows * head_dim * 4 + 255) & ~size_t(255);
+  return o_bytes + rows * 8;
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale, void* out,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+              int partition_size, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  const int es = elem_bytes(dtype);
+  if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_context_len < 1 ||
+      max_blocks_per_seq <= 0 || !std::isfinite(scale))
+    return pa_fail(PA_ERR_INVALID, "pa_decode: sizes");
+  if (num_heads % num_kv_heads) return pa_fail(PA_ERR_INVALID, "pa_decode: num_heads % num_kv_heads != 0");
+  const int g = num_heads / num_kv_heads;
+  if (!(g == 1 || g == 2 || g == 4 || g == 8)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: heads per KV head");
+  if (!supported_shape(head_dim, block_size)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim/block_size");
+  if (cdiv(max_context_len, block_size) > max_blocks_per_seq)
+    return pa_fail(PA_ERR_INVALID, "pa_decode: max_blocks_per_seq < ceil(max_context_len / block_size)");
+  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: pool rows exceed 2^31");
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return pa_fail(PA_ERR_INVALID, "pa_decode: null pointer");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_decode: misaligned pointer");
+  const int P = pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size);
+  if (P < 0) return P;
+  const long long parts = cdiv(max_context_len, P);
+  if (parts * num_seqs * num_kv_heads >= (1LL << 31)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: too many work items");
+  const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, P);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return pa_fail(PA_ERR_INVALID, "pa_decode: workspace too small");
+  if (need > 0 && !aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace not 256-byte aligned");
+
+  pa::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  if (need > 0) {
+    const size_t rows = (size_t)num_seqs * parts * num_heads;
+    const size_t o_bytes = (rows * head_dim * 4 + 255) & ~size_t(255);
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
+  }
+  int rc = status_ptr(&a.status);
+  if (rc) return rc;
+  a.S = num_seqs;
+  a.H = num_heads;
+  a.Hkv = num_kv_heads;
+  a.g = g;
+  a.D = head_dim;
+  a.B = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_ctx = max_context_len;
+  a.P = P;
+  a.max_parts = (int)parts;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e;
+  if (dtype == PA_BF16) {
+    if (pa::decode_tc_smem_bytes(head_dim, num_seqs) > 227 * 1024)
+      return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: too many sequences for one launch");
+    CUtensorMap kmap, vmap;
+    rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    if (rc) return rc;
+    rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    if (rc) return rc;
+    e = pa::launch_decode_tc(a, kmap, vmap, st);
+  } else {
+    e = pa::launch_decode_simt(a, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "pa_decode launch");
+  if (parts > 1) {
+    e = pa::launch_lse_merge(a, dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "pa_decode merge launch");
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+"""Tensor-level calls of the C ABI: KV append, block copy, paged decode.
+
+Each function checks shapes/dtypes/devices of its torch tensors, passes raw
+device pointers and sizes to libpa.so on the current CUDA stream, and raises
+on a non-zero return code.  Nothing here computes any part of the method.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import PA_BF16, PA_F32, check, lib
+
+_DTYPES = {torch.bfloat16: PA_BF16, torch.float32: PA_F32}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32") from None
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(*ts):
+    for t in ts:
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+
+
+def cache_append(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """Write new tokens' keys/values ``k, v [T, Hkv, D]`` into slots
+    ``slot_mapping [T]`` (int64; negative = skip) of ``k_cache, v_cache
+    [N, Hkv, B, D]``, in place."""
+    _cuda_contig(k, v, slot_mapping, k_cache, v_cache)
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    _need(k.dtype == v.dtype == k_cache.dtype == v_cache.dtype, "k, v and caches must share a dtype")
+    n, hkv, b, d = k_cache.shape
+    _need(v_cache.shape == k_cache.shape, "k_cache and v_cache shapes differ")
+    t = slot_mapping.shape[0]
+    _need(tuple(k.shape) == (t, hkv, d) and tuple(v.shape) == (t, hkv, d), "k, v must be [T, Hkv, D]")
+    check(lib().pa_cache_append(_ptr(k), _ptr(v), _ptr(slot_mapping), t, _ptr(k_cache), _ptr(v_cache),
+                                n, hkv, d, b, _dtype_code(k_cache), _stream(stream)))
+
+
+def copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
+    """For each (src, dst) row of ``pairs [n, 2]`` (int32, device) copy block
+    src to block dst in both caches."""
+    _cuda_contig(k_cache, v_cache, pairs)
+    _need(pairs.dtype == torch.int32 and pairs.dim() == 2 and pairs.shape[1] == 2, "pairs must be int32 [n, 2]")
+    n, hkv, b, d = k_cache.shape
+    check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], n, hkv, d, b,
+                               _dtype_code(k_cache), _stream(stream)))
+
+
+def decode_partition_size(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_size: int = 0) -> int:
+    return check(lib().pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size))
+
+
+def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                           partition_size: int) -> int:
+    return int(lib().pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, partition_size))
+
+
+def decode_workspace(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, partition_size=0,
+                     device="cuda"):
+    """Allocate (with torch) the workspace pa_decode needs for these sizes;
+    None when no workspace is needed."""
+    p = decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size)
+    nbytes = decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, p)
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                 out=None, partition_size: int = 0, workspace=None, stream=None):
+    """out[s, h] = softmax(scale * K_s q[s, h]) V_s over each sequence's
+    blocks.  q ``[S, H, D]``; caches ``[N, Hkv, B, D]``; block_tables
+    ``[S, max_blocks]`` int32; context_lens ``[S]`` int32 (device);
+    ``max_context_len`` a host bound of context_lens.  Returns ``out``."""
+    _cuda_contig(q, k_cache, v_cache, block_tables, context_lens)
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and caches must share a dtype")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+          "block_tables and context_lens must be int32")
+    s, h, d = q.shape
+    n, hkv, b, d2 = k_cache.shape
+    _need(d == d2 and v_cache.shape == k_cache.shape, "head_dim mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == s and context_lens.shape == (s,),
+          "block_tables [S, max_blocks], context_lens [S]")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig(out)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = decode_workspace(s, h, hkv, d, max_context_len, partition_size, q.device)
+    ws_ptr = _ptr(workspace)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                          _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), s, h, hkv, d, b, n,
+                          int(partition_size), ws_ptr, ws_bytes, _dtype_code(q), _stream(stream)))
+    return out
+
+
+def get_status(stream=None) -> int:
+    """Read and clear the device status word (synchronizes the stream)."""
+    v = ctypes.c_uint32(0)
+    check(lib().pa_get_status(_stream(stream), ctypes.byref(v)))
+    return int(v.value)

@@ -1,0 +1,110 @@
+"""The C ABI library loads, exports every symbol its header declares, and
+rejects bad host-side arguments before touching the GPU (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests._lib_fixture import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    ensure_built()
+    from paged_kv_cache_216_gb300._lib import lib
+
+    return lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        with open(os.path.join(ROOT, "include", fn)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b(pa_[a-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pa_cache_append", "pa_decode", "pa_copy_blocks", "pa_alloc_create", "pa_seq_fork",
+                     "pa_seq_append_slot", "pa_decode_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from paged_kv_cache_216_gb300._lib import SIGNATURES
+
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in SIGNATURES, f"binding lacks {name}"
+
+
+def test_version(L):
+    assert L.pa_version() == 1
+
+
+def _decode_args(**over):
+    fake = ctypes.c_void_p(0x100000)
+    a = dict(q=fake, k=fake, v=fake, bt=fake, mb=8, ctx=fake, maxctx=100, scale=0.1, out=fake, S=2, H=8, Hkv=2,
+             D=128, B=16, N=10, P=0, ws=fake, wsb=1 << 30, dtype=1, stream=None)
+    a.update(over)
+    return [a[k] for k in ("q", "k", "v", "bt", "mb", "ctx", "maxctx", "scale", "out", "S", "H", "Hkv", "D", "B",
+                           "N", "P", "ws", "wsb", "dtype", "stream")]
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=12, Hkv=4), -2),              # g = 3
+    (dict(H=32, Hkv=2), -2),              # g = 16
+    (dict(H=8, Hkv=3), -1),               # not a multiple
+    (dict(D=96), -2),
+    (dict(B=24), -2),
+    (dict(dtype=7), -2),
+    (dict(maxctx=0), -1),
+    (dict(mb=6), -1),                     # 6 blocks of 16 < 100 tokens
+    (dict(P=48), -1),                     # not a multiple of 32
+    (dict(q=ctypes.c_void_p(0)), -1),
+    (dict(q=ctypes.c_void_p(0x100004)), -1),  # misaligned
+    (dict(wsb=16), -1),                   # workspace too small
+    (dict(scale=float("nan")), -1),
+])
+def test_decode_rejects_bad_arguments_without_a_launch(L, over, code):
+    rc = L.pa_decode(*_decode_args(**over))
+    assert rc == code
+    assert L.pa_last_error()
+
+
+def test_append_and_copy_reject_bad_arguments(L):
+    f = ctypes.c_void_p(0x100000)
+    assert L.pa_cache_append(f, f, f, 4, f, f, 10, 2, 96, 16, 1, None) == -2
+    assert L.pa_cache_append(f, f, f, -1, f, f, 10, 2, 128, 16, 1, None) == -1
+    assert L.pa_cache_append(None, f, f, 4, f, f, 10, 2, 128, 16, 1, None) == -1
+    assert L.pa_cache_append(f, f, f, 0, f, f, 10, 2, 128, 16, 1, None) == 0  # nothing to do
+    assert L.pa_copy_blocks(f, f, f, 3, 10, 2, 128, 12, 1, None) == -2
+    assert L.pa_copy_blocks(f, f, None, 3, 10, 2, 128, 16, 1, None) == -1
+    assert L.pa_copy_blocks(f, f, f, 0, 10, 2, 128, 16, 1, None) == 0
+
+
+def test_partition_and_workspace_sizing(L):
+    # explicit partition sizes pass through; auto sizing is a multiple of 32
+    assert L.pa_decode_partition_size(8, 8, 131072, 512) == 512
+    assert L.pa_decode_partition_size(256, 8, 4116, 0) == 512
+    p = L.pa_decode_partition_size(1, 1, 5000, 0)
+    assert p % 32 == 0 and 64 <= p < 512
+    assert L.pa_decode_partition_size(1, 1, 100, 33) == -1
+    # one partition: no workspace
+    assert L.pa_decode_workspace_bytes(4, 8, 128, 512, 512) == 0
+    # S * parts * H rows of D fp32 (256-byte aligned) + a float2 per row
+    rows = 8 * 256 * 64
+    assert L.pa_decode_workspace_bytes(8, 64, 128, 131072, 512) == rows * 128 * 4 + rows * 8
+    rows = 3 * 2 * 5
+    assert L.pa_decode_workspace_bytes(3, 5, 64, 600, 512) == ((rows * 64 * 4 + 255) // 256) * 256 + rows * 8

@@ -50,7 +50,13 @@ struct TcCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kRegion = kHalves * kHalfBytes;  // K (or V) of a stage
   static constexpr int kStage = 2 * kRegion;
-  static constexpr int kStages = (D == 128) ? 5 : 8;
+  // A multiple of the consumer-warp count: chunk k goes to warp k % 4 and
+  // stage k % kStages, so every stage is always consumed by the same warp.
+  // Otherwise a warp running ahead could test a stage's barrier while it is
+  // still two phases behind, and the parity wait would pass on the wrong
+  // phase.
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static_assert(kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
   static constexpr int kQSlot = kMaxGroup * D * 2;
   static constexpr int kOStride = D + 4;  // floats per (warp, head) row; +4 spreads banks
   static constexpr int kOBuf = kConsumerWarps * kMaxGroup * kOStride * 4;

@@ -71,6 +71,18 @@ def test_context_length_edges(pa, b, g):
         assert_close(run_decode(case, partition_size=partition), ref, "bf16", f"B={b} g={g} P={partition}")
 
 
+def test_many_items_per_cta_wrap_the_pipeline(pa):
+    """Small partitions over many (sequence, KV head) pairs give every
+    persistent CTA a dozen or more work items, so its stage and query rings
+    wrap many times."""
+    w = Workload(name="wrap", dtype="bf16", num_seqs=64, num_heads=32, num_kv_heads=8, head_dim=128,
+                 block_size=16, seed=25, ctx_lo=200, ctx_hi=420)
+    case = make_decode_case(w)
+    for partition in (32, 64, 4096):
+        assert_close(run_decode(case, partition_size=partition), case.oracle(), "bf16", f"P={partition}")
+    assert pa.get_status() == 0
+
+
 def test_split_and_unsplit_agree(pa):
     w = SMALL["long_small"]
     case = make_decode_case(w)

@@ -157,6 +157,33 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               int head_dim, int block_size, int num_blocks, int partition_size,
               void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
+/*
+ * Paged decode that allocates nothing: the same computation and arguments as
+ * pa_decode, but the split-K scratch is a fixed device array inside this
+ * library, so the caller passes no workspace.  The pages have no counterpart;
+ * this entry point is for callers that cannot call cudaMalloc for a
+ * workspace (device memory reserved up front by another allocator, or a loop
+ * that must not make calls that may synchronize the device).
+ *   - The array holds PA_STATIC_WORKSPACE_BYTES; sizes whose workspace
+ *     (pa_decode_workspace_bytes) exceeds it return PA_ERR_INVALID.
+ *   - Every GPU that loads the library holds the array until the process
+ *     exits.  The first call on a device looks up the array's address there
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *     the GPU (different streams or threads) race on it: serialise them.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (16u << 20)
+int pa_decode_static_workspace(const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int max_blocks_per_seq,
+                               const int32_t* context_lens, int max_context_len,
+                               float scale, void* out, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks,
+                               int partition_size, int dtype, void* stream);
+
 /* ------------------------------------------------------------------------
  * Host block allocator [Day6 paragraphs 2, 5, 6].  CPU only; no CUDA call.
  *

@@ -15,5 +15,6 @@ from .ops import (  # noqa: F401
     decode_workspace_bytes,
     get_status,
     paged_decode,
+    paged_decode_static_workspace,
 )
 from .serving import ServingEngine  # noqa: F401

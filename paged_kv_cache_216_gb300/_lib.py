@@ -21,6 +21,9 @@ PA_STATUS_BAD_BLOCK = 2
 PA_STATUS_BAD_CONTEXT = 4
 PA_STATUS_TIMEOUT = 8
 
+# Size of the library's fixed decode scratch array (pa_decode_static_workspace).
+PA_STATIC_WORKSPACE_BYTES = 16 << 20
+
 _c_int, _c_i64, _c_sz, _c_f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 _vp = ctypes.c_void_p
 _pi32 = ctypes.POINTER(ctypes.c_int32)
@@ -37,6 +40,8 @@ SIGNATURES = {
     "pa_decode_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _vp]),
+    "pa_decode_static_workspace": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
+                                            _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_alloc_create": (_c_int, [_c_int, _c_int, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_num_free": (_c_int, [_vp]),

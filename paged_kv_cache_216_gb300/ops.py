@@ -116,6 +116,27 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_le
     return out
 
 
+def paged_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                                  scale: float, out, partition_size: int = 0, stream=None):
+    """Same as :func:`paged_decode`, for callers that cannot allocate a
+    workspace: the split-K scratch is the library's fixed device array
+    (``PA_STATIC_WORKSPACE_BYTES``), shared by every call.  ``out`` must be
+    given, so this call allocates nothing.  Calls whose kernels overlap on
+    the GPU race on the shared array."""
+    _cuda_contig(q, k_cache, v_cache, block_tables, context_lens, out)
+    _need(q.dtype == k_cache.dtype == v_cache.dtype == out.dtype, "q, caches and out must share a dtype")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+          "block_tables and context_lens must be int32")
+    s, h, d = q.shape
+    n, hkv, b, _ = k_cache.shape
+    _need(out.shape == q.shape, "out must match q")
+    check(lib().pa_decode_static_workspace(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                           block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+                                           float(scale), _ptr(out), s, h, hkv, d, b, n, int(partition_size),
+                                           _dtype_code(q), _stream(stream)))
+    return out
+
+
 def get_status(stream=None) -> int:
     """Read and clear the device status word (synchronizes the stream)."""
     v = ctypes.c_uint32(0)

@@ -119,10 +119,12 @@ int pa_decode_partition_size(int num_seqs, int num_kv_heads,
                              int max_context_len, int partition_size);
 
 /*
- * Bytes of device workspace pa_decode needs for these sizes (0 when no
- * sequence can span more than one partition).  The workspace holds the
- * split-K partials: per (sequence, partition, query head) head_dim fp32
- * un-normalised outputs and a (max, sum) pair.
+ * Bytes of device workspace pa_decode needs for these sizes (0 only for
+ * invalid sizes).  The workspace holds a 256-byte header and the work list
+ * of the persistent decode kernel (8 bytes per sequence and partition) and,
+ * when a context can span more than one partition, the split-K partials:
+ * per (sequence, partition, query head) head_dim fp32 un-normalised outputs
+ * and a (max, sum) pair.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
                                  int max_context_len, int partition_size);
@@ -144,8 +146,9 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim,
  *                 ceil(max_context_len / block_size) <= max_blocks_per_seq
  *   out           device, [num_seqs][num_heads][head_dim], dtype
  *   workspace     device, >= pa_decode_workspace_bytes(...) bytes, 256-byte
- *                 aligned (may be NULL when that size is 0); contents on
- *                 entry do not matter
+ *                 aligned; contents on entry do not matter; calls whose
+ *                 kernels overlap on the GPU need separate workspaces
+ * Up to 65535 sequences and 32767 partitions per context.
  * q and the caches must be 16-byte aligned.  A context length outside
  * [1, max_context_len] sets PA_STATUS_BAD_CONTEXT (length 0 gives a zero
  * output row; longer ones are cut to max_context_len).

@@ -93,6 +93,33 @@ constexpr int kMinPartition = 64;
 
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of pa_decode: [header 256 B][work list][split-K partial outputs]
+// [split-K (max, sum) pairs]; the last two only when a context can span more
+// than one partition.
+struct WsLayout {
+  size_t plan, o, ml, total;
+  long long parts;
+};
+
+bool ws_layout(int S, int H, int D, int max_ctx, int P, WsLayout* l) {
+  if (S <= 0 || H <= 0 || D <= 0 || max_ctx < 1 || P < 32) return false;
+  l->parts = cdiv(max_ctx, P);
+  const size_t pairs = (size_t)S * l->parts;
+  l->plan = sizeof(pa::PlanHeader);
+  l->o = l->plan + align256(pairs * sizeof(int2));
+  if (l->parts > 1) {
+    const size_t rows = pairs * H;
+    l->ml = l->o + align256(rows * D * 4);
+    l->total = l->ml + rows * 8;
+  } else {
+    l->ml = l->o;
+    l->total = l->o;
+  }
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -173,12 +200,9 @@ int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len
 
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                  int partition_size) {
-  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 1 || partition_size < 32) return 0;
-  const long long parts = cdiv(max_context_len, partition_size);
-  if (parts <= 1) return 0;
-  const size_t rows = (size_t)num_seqs * parts * num_heads;
-  const size_t o_bytes = (rows * head_dim * 4 + 255) & ~size_t(255);
-  return o_bytes + rows * 8;
+  WsLayout l;
+  if (!ws_layout(num_seqs, num_heads, head_dim, max_context_len, partition_size, &l)) return 0;
+  return l.total;
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -208,10 +232,12 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   if (P < 0) return P;
   const long long parts = cdiv(max_context_len, P);
   if (parts * num_seqs * num_kv_heads >= (1LL << 31)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: too many work items");
-  const size_t need = pa_decode_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, P);
-  if (need > 0 && (!workspace || workspace_bytes < need))
-    return pa_fail(PA_ERR_INVALID, "pa_decode: workspace too small");
-  if (need > 0 && !aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace not 256-byte aligned");
+  if (num_seqs > 65535 || parts > 32767)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: more than 65535 sequences or 32767 partitions per context");
+  WsLayout wl;
+  ws_layout(num_seqs, num_heads, head_dim, max_context_len, P, &wl);
+  if (!workspace || workspace_bytes < wl.total) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace too small");
+  if (!aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace not 256-byte aligned");
 
   pa::DecodeArgs a{};
   a.q = q;
@@ -220,11 +246,12 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   a.out = out;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  if (need > 0) {
-    const size_t rows = (size_t)num_seqs * parts * num_heads;
-    const size_t o_bytes = (rows * head_dim * 4 + 255) & ~size_t(255);
-    a.ws_o = static_cast<float*>(workspace);
-    a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + o_bytes);
+  char* ws = static_cast<char*>(workspace);
+  a.hdr = reinterpret_cast<pa::PlanHeader*>(ws);
+  a.plan = reinterpret_cast<const int2*>(ws + wl.plan);
+  if (parts > 1) {
+    a.ws_o = reinterpret_cast<float*>(ws + wl.o);
+    a.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   }
   int rc = status_ptr(&a.status);
   if (rc) return rc;
@@ -244,13 +271,13 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
 
   cudaError_t e;
   if (dtype == PA_BF16) {
-    if (pa::decode_tc_smem_bytes(head_dim, num_seqs) > 227 * 1024)
-      return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: too many sequences for one launch");
     CUtensorMap kmap, vmap;
     rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
     if (rc) return rc;
     rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
     if (rc) return rc;
+    e = pa::launch_decode_plan(a, es, st);
+    if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");
     e = pa::launch_decode_tc(a, kmap, vmap, st);
   } else {
     e = pa::launch_decode_simt(a, st);

@@ -9,10 +9,12 @@
 // log-sum-exp (lse_merge.cu) when it spans more than one.
 //
 // Structure (sm_103a):
-//  * Persistent CTAs, one or two per SM.  Work items are (partition,
-//    sequence, KV head) triples taken round-robin.
-//  * Warp 4 is the producer.  For each item it bulk-copies the item's g
-//    query rows into a 2-slot Q ring, then streams the item's keys and values
+//  * Persistent CTAs, two per SM.  Work items are (sequence, partition, KV
+//    head) triples taken from a longest-first work list (decode_plan.cu)
+//    through an atomic counter, the dynamic work queue of the same page's
+//    section 3.2; the producer claims items two ahead of use.
+//  * Warp 4 is the producer.  For each item it writes the item's descriptor
+//    and bulk-copies its g query rows into a 2-slot Q ring, then streams the item's keys and values
 //    32 tokens at a time into a ring of shared-memory stages: per cache block
 //    of the chunk, one 2D TMA box of [B rows x 64 dims] per 64-dim half, for
 //    K and for V, with 128-byte swizzle.  Block ids are read 32 at a time
@@ -25,14 +27,16 @@
 //    is exactly the B-operand layout of the P·V product computed as
 //    Oᵀ = Vᵀ Pᵀ (ldmatrix.trans of V), so P never leaves registers.
 //  * At the end of an item the four warps' (max, sum, O) states are merged
-//    through shared memory; the result is written as bf16 output, or as an
-//    fp32 partial for the merge kernel.
+//    through shared memory (two mbarriers order the exchange); the result is
+//    written as bf16 output, or as an fp32 partial for the merge kernel.
 // Every wait is bounded (device_common.cuh); on time-out the kernel raises
 // PA_STATUS_TIMEOUT and winds down without touching global memory further.
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "kernels.h"
@@ -44,6 +48,7 @@ constexpr int kChunk = 32;  // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kHalfBytes = kChunk * 128;  // one 64-dim half of 32 rows
+constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>
 struct TcCfg {
@@ -61,77 +66,110 @@ struct TcCfg {
   static constexpr int kOStride = D + 4;  // floats per (warp, head) row; +4 spreads banks
   static constexpr int kOBuf = kConsumerWarps * kMaxGroup * kOStride * 4;
   static constexpr int kML = kConsumerWarps * kMaxGroup * 8;
-  static constexpr int kBars = (2 * kStages + 4) * 8;
+  // mbarriers: full[kStages], empty[kStages], qfull[2], qempty[2], epi_full, epi_done
+  static constexpr int kBars = (2 * kStages + 6) * 8;
   // byte offsets from the 1024-aligned base
   static constexpr int kOffQ = kStages * kStage;
   static constexpr int kOffO = kOffQ + 2 * kQSlot;
   static constexpr int kOffML = kOffO + kOBuf;
-  static constexpr int kOffBar = kOffML + kML;
+  static constexpr int kOffDesc = kOffML + kML;  // int4 per Q slot: {s, part, kvh, ctx or -1}
+  static constexpr int kOffBar = kOffDesc + 2 * 16;
   static constexpr int kOffAbort = kOffBar + kBars;
-  static constexpr int kOffCtx = kOffAbort + 16;
-  static size_t bytes(int S) { return 1024 + kOffCtx + (size_t)S * 4; }
+  static constexpr size_t kBytes = 1024 + kOffAbort + 16;
 };
 
-struct Item {
-  int s, part, kvh, t0, t1;
+struct Bars {
+  uint64_t *full, *empty, *qfull, *qempty, *epi_full, *epi_done;
 };
 
-// Item i of the round-robin order: partition-major, then sequence, then KV
-// head.  Returns false for an empty slot (partition past the context).
-__device__ __forceinline__ bool item_at(const DecodeArgs& p, const int* sctx, int i, Item& it) {
-  const int per_part = p.S * p.Hkv;
-  it.part = i / per_part;
-  const int r = i - it.part * per_part;
-  it.s = r / p.Hkv;
-  it.kvh = r - it.s * p.Hkv;
-  const int ctx = sctx[it.s];
-  it.t0 = it.part * p.P;
-  if (it.t0 >= ctx) return false;
-  it.t1 = min(ctx, it.t0 + p.P);
-  return true;
+template <int D>
+__device__ __forceinline__ Bars bars_at(uint8_t* base) {
+  using C = TcCfg<D>;
+  Bars b;
+  b.full = reinterpret_cast<uint64_t*>(base + C::kOffBar);
+  b.empty = b.full + C::kStages;
+  b.qfull = b.empty + C::kStages;
+  b.qempty = b.qfull + 2;
+  b.epi_full = b.qempty + 2;
+  b.epi_done = b.epi_full + 1;
+  return b;
 }
 
 __device__ __forceinline__ int load_block_id(const int32_t* row, int rel, int nblk) {
   return rel < nblk ? __ldg(row + rel) : 0;
 }
 
+__device__ __forceinline__ void give_up(const DecodeArgs& p, volatile int* abort) {
+  *abort = 1;
+  raise_status(p.status, PA_STATUS_TIMEOUT);
+}
+
 template <int D>
 __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& p, uint8_t* base,
-                         const int* sctx, volatile int* abort) {
+                         volatile int* abort) {
   using C = TcCfg<D>;
   const int lane = threadIdx.x & 31;
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kOffBar);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* qfull = empty + C::kStages;
-  uint64_t* qempty = qfull + 2;
+  const Bars bar = bars_at<D>(base);
+  int4* desc = reinterpret_cast<int4*>(base + C::kOffDesc);
   const uint64_t policy = policy_evict_first();
-  const int total = p.max_parts * p.S * p.Hkv;
   const int bpc = kChunk / p.B;  // cache blocks per chunk
   const uint32_t qbytes = (uint32_t)(p.g * D * 2);
   const uint32_t chunk_block_bytes = (uint32_t)(p.B * D * 2 * 2);  // K + V of one block
-  uint32_t kseq = 0, n = 0;
+
+  pdl_wait_primary();  // the work list is complete and visible from here on
+  const int total = __ldcg(&p.hdr->num_pairs) * p.Hkv;
+  unsigned* counter = &p.hdr->counter;
+  // Lane 0 claims work items two ahead of use, so that the atomic and the
+  // read of the list entry are off the critical path.
+  int cur_idx = total, nxt_idx = total;
+  int2 cur_pr = make_int2(0, -1);
+  if (lane == 0) {
+    cur_idx = (int)atomicAdd(counter, 1u);
+    if (cur_idx < total) {
+      cur_pr = __ldcg(p.plan + cur_idx / p.Hkv);
+      nxt_idx = (int)atomicAdd(counter, 1u);
+    }
+  }
+  uint32_t kseq = 0, nq = 0;
   bool ok = true;
-  for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-    Item it;
-    if (!item_at(p, sctx, i, it)) continue;
+  for (uint32_t n = 0;; ++n) {
+    int2 nxt_pr = make_int2(0, -1);
+    int nn_idx = total;
+    if (lane == 0 && nxt_idx < total) {
+      nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
+      nn_idx = (int)atomicAdd(counter, 1u);
+    }
+    const int idx = __shfl_sync(kFull, cur_idx, 0);
+    const int prx = __shfl_sync(kFull, cur_pr.x, 0);
+    const int ctx = __shfl_sync(kFull, cur_pr.y, 0);
     const int slot = n & 1;
-    if (!mbar_wait(&qempty[slot], ((n >> 1) & 1) ^ 1, abort)) {
+    if (!mbar_wait(&bar.qempty[slot], ((n >> 1) & 1) ^ 1, abort)) {
       ok = false;
       break;
     }
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&qfull[slot], qbytes);
-      const __nv_bfloat16* src =
-          static_cast<const __nv_bfloat16*>(p.q) + ((size_t)it.s * p.H + (size_t)it.kvh * p.g) * D;
-      bulk_load(base + C::kOffQ + slot * C::kQSlot, src, qbytes, &qfull[slot]);
+    if (idx >= total) {  // no work left: tell the consumers
+      if (lane == 0) {
+        desc[slot] = make_int4(0, 0, 0, -1);
+        mbar_arrive(&bar.qfull[slot]);
+      }
+      break;
     }
-    ++n;  // items whose Q copy has been issued
-    const int32_t* row = p.block_tables + (size_t)it.s * p.max_blocks_per_seq + it.t0 / p.B;
-    const int nblk = (it.t1 - it.t0 + p.B - 1) / p.B;
+    const int s = prx & 0xffff, part = prx >> 16, kvh = idx % p.Hkv;
+    const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
+    if (lane == 0) {
+      desc[slot] = make_int4(s, part, kvh, ctx);
+      mbar_arrive_expect_tx(&bar.qfull[slot], qbytes);
+      const __nv_bfloat16* src =
+          static_cast<const __nv_bfloat16*>(p.q) + ((size_t)s * p.H + (size_t)kvh * p.g) * D;
+      bulk_load(base + C::kOffQ + slot * C::kQSlot, src, qbytes, &bar.qfull[slot]);
+    }
+    ++nq;
+    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq + t0 / p.B;
+    const int nblk = (t1 - t0 + p.B - 1) / p.B;
     int cur = load_block_id(row, lane, nblk);
     int nxt = load_block_id(row, 32 + lane, nblk);
     int wbase = 0;
-    const int nch = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+    const int nch = (t1 - t0 + kChunk - 1) / kChunk;
     for (int ch = 0; ch < nch; ++ch, ++kseq) {
       const int jb = ch * bpc;
       if (jb >= wbase + 32) {
@@ -139,45 +177,48 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
         wbase += 32;
         nxt = load_block_id(row, wbase + 32 + lane, nblk);
       }
-      const int nv = min(kChunk, it.t1 - (it.t0 + ch * kChunk));
+      const int nv = min(kChunk, t1 - (t0 + ch * kChunk));
       const int nb = (nv + p.B - 1) / p.B;
-      int id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
+      int id = __shfl_sync(kFull, cur, (jb - wbase + lane) & 31);
       if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
         raise_status(p.status, PA_STATUS_BAD_BLOCK);
         id = 0;
       }
       const int stage = kseq % C::kStages;
-      if (!mbar_wait(&empty[stage], ((kseq / C::kStages) & 1) ^ 1, abort)) {
+      if (!mbar_wait(&bar.empty[stage], ((kseq / C::kStages) & 1) ^ 1, abort)) {
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nb * chunk_block_bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * chunk_block_bytes);
       __syncwarp();
       if (lane < nb) {
-        const int y = (id * p.Hkv + it.kvh) * p.B;
+        const int y = (id * p.Hkv + kvh) * p.B;
         uint8_t* sk = base + stage * C::kStage + lane * p.B * 128;
         uint8_t* sv = sk + C::kRegion;
 #pragma unroll
         for (int hf = 0; hf < C::kHalves; ++hf) {
-          tma_load_2d(sk + hf * kHalfBytes, kmap, &full[stage], hf * 64, y, policy);
-          tma_load_2d(sv + hf * kHalfBytes, vmap, &full[stage], hf * 64, y, policy);
+          tma_load_2d(sk + hf * kHalfBytes, kmap, &bar.full[stage], hf * 64, y, policy);
+          tma_load_2d(sv + hf * kHalfBytes, vmap, &bar.full[stage], hf * 64, y, policy);
         }
       }
     }
+    if (!ok) break;
+    cur_idx = nxt_idx;
+    cur_pr = nxt_pr;
+    nxt_idx = nn_idx;
   }
   if (!ok) {
-    raise_status(p.status, PA_STATUS_TIMEOUT);
-    *abort = 1;
+    give_up(p, abort);
     // Let copies already issued land before the CTA's shared memory goes away.
     const volatile int never = 0;
     for (uint32_t k = (kseq > (uint32_t)C::kStages ? kseq - C::kStages : 0); k < kseq; ++k)
-      mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, &never);
-    for (uint32_t k = (n > 2 ? n - 2 : 0); k < n; ++k) mbar_wait(&qfull[k & 1], (k >> 1) & 1, &never);
+      mbar_wait(&bar.full[k % C::kStages], (k / C::kStages) & 1, &never);
+    for (uint32_t k = (nq > 2 ? nq - 2 : 0); k < nq; ++k) mbar_wait(&bar.qfull[k & 1], (k >> 1) & 1, &never);
   }
 }
 
 template <int D>
-__device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, volatile int* abort) {
+__device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort) {
   using C = TcCfg<D>;
   constexpr int KS = D / 16;  // k-steps of the Q·Kᵀ product
   constexpr int MT = D / 16;  // m-tiles of the Oᵀ = Vᵀ Pᵀ product
@@ -185,55 +226,50 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, vo
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2;  // mma group id: head row of S, token row of K tiles
   const int tq = lane & 3;   // thread in group
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kOffBar);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* qfull = empty + C::kStages;
-  uint64_t* qempty = qfull + 2;
+  const Bars bar = bars_at<D>(base);
+  const int4* desc = reinterpret_cast<const int4*>(base + C::kOffDesc);
   float* sO = reinterpret_cast<float*>(base + C::kOffO);
   float2* sML = reinterpret_cast<float2*>(base + C::kOffML);
-  const int total = p.max_parts * p.S * p.Hkv;
   const uint32_t base_addr = smem_addr(base);
-  bool alive = true;
-  uint32_t kseq = 0, n = 0;
+  uint32_t kseq = 0;
 
-  for (int i = blockIdx.x; i < total; i += gridDim.x) {
-    Item it;
-    if (!item_at(p, sctx, i, it)) continue;
-    const int nch = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+  for (uint32_t n = 0;; ++n) {
     const int slot = n & 1;
-    uint32_t qa[KS][2];
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
-    if (alive && !mbar_wait(&qfull[slot], (n >> 1) & 1, abort)) {
-      alive = false;
-      *abort = 1;
-      raise_status(p.status, PA_STATUS_TIMEOUT);
+    if (!mbar_wait(&bar.qfull[slot], (n >> 1) & 1, abort)) {
+      give_up(p, abort);
+      return;
     }
-    if (alive) {
+    const int4 d = desc[slot];
+    if (d.w < 0) return;  // no work left
+    const int s = d.x, part = d.y, kvh = d.z, ctx = d.w;
+    const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
+    const int nch = (t1 - t0 + kChunk - 1) / kChunk;
+    const int np = (ctx + p.P - 1) / p.P;
+    uint32_t qa[KS][2];
+    {
       const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(base + C::kOffQ + slot * C::kQSlot);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         qa[ks][0] = gq < p.g ? *reinterpret_cast<const uint32_t*>(sq + gq * D + ks * 16 + 2 * tq) : 0u;
         qa[ks][1] = gq < p.g ? *reinterpret_cast<const uint32_t*>(sq + gq * D + ks * 16 + 8 + 2 * tq) : 0u;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&qempty[slot]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.qempty[slot]);
+
     float m_run = -INFINITY, l_run = 0.f;
     float o[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     for (int ch = 0; ch < nch; ++ch, ++kseq) {
-      if ((int)(kseq & (kConsumerWarps - 1)) != warp || !alive) continue;
+      if ((int)(kseq & (kConsumerWarps - 1)) != warp) continue;
       const int stage = kseq % C::kStages;
-      if (!mbar_wait(&full[stage], (kseq / C::kStages) & 1, abort)) {
-        alive = false;
-        *abort = 1;
-        raise_status(p.status, PA_STATUS_TIMEOUT);
-        continue;
+      if (!mbar_wait(&bar.full[stage], (kseq / C::kStages) & 1, abort)) {
+        give_up(p, abort);
+        return;
       }
-      const int nv = min(kChunk, it.t1 - (it.t0 + ch * kChunk));
+      const int nv = min(kChunk, t1 - (t0 + ch * kChunk));
       const uint32_t sk = base_addr + stage * C::kStage;
       const uint32_t sv = sk + C::kRegion;
       if (nv < kChunk) {
@@ -279,8 +315,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, vo
           mx = fmaxf(mx, v);
         }
       }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
       const float m_new = fmaxf(m_run, mx);
       const float alpha = exp2f(m_run - m_new);
       float ls = 0.f;
@@ -292,8 +328,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, vo
       }
       l_run = l_run * alpha + ls;
       m_run = m_new;
-      const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * tq);
-      const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * tq + 4);
+      const float a_lo = __shfl_sync(kFull, alpha, 8 * tq);
+      const float a_hi = __shfl_sync(kFull, alpha, 8 * tq + 4);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         o[mt][0] *= a_lo;
@@ -317,34 +353,41 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, vo
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (lane == 0) mbar_arrive(&bar.empty[stage]);
     }
 
     // ---- item epilogue: merge the four warps' states ----
+    // The previous item's combine must be over before its buffers are reused.
+    if (n > 0 && !mbar_wait(bar.epi_done, (n - 1) & 1, abort)) {
+      give_up(p, abort);
+      return;
+    }
     float l = l_run;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
     if (tq == 0 && gq < p.g) sML[warp * kMaxGroup + gq] = make_float2(m_run, l);
     float* ob = sO + warp * kMaxGroup * C::kOStride;
     const int h0 = 2 * tq, h1 = 2 * tq + 1;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      const int d = 16 * mt + gq;
+      const int dd = 16 * mt + gq;
       if (h0 < p.g) {
-        ob[h0 * C::kOStride + d] = o[mt][0];
-        ob[h0 * C::kOStride + d + 8] = o[mt][2];
+        ob[h0 * C::kOStride + dd] = o[mt][0];
+        ob[h0 * C::kOStride + dd + 8] = o[mt][2];
       }
       if (h1 < p.g) {
-        ob[h1 * C::kOStride + d] = o[mt][1];
-        ob[h1 * C::kOStride + d + 8] = o[mt][3];
+        ob[h1 * C::kOStride + dd] = o[mt][1];
+        ob[h1 * C::kOStride + dd + 8] = o[mt][3];
       }
     }
-    named_barrier_sync(1, kConsumerWarps * 32);
-    const bool live = alive && !*abort;
-    const int tid = threadIdx.x;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.epi_full);
+    if (!mbar_wait(bar.epi_full, n & 1, abort)) {
+      give_up(p, abort);
+      return;
+    }
     const int units = p.g * (D / 8);
-    const int np = (sctx[it.s] + p.P - 1) / p.P;
-    for (int u = tid; u < units && live; u += kConsumerWarps * 32) {
+    for (int u = threadIdx.x; u < units; u += kConsumerWarps * 32) {
       const int h = u / (D / 8);
       const int d0 = (u % (D / 8)) * 8;
       float mw[kConsumerWarps];
@@ -372,7 +415,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, vo
         acc[6] += wt * x1.z;
         acc[7] += wt * x1.w;
       }
-      const int qh = it.kvh * p.g + h;
+      const int qh = kvh * p.g + h;
       if (np == 1) {
         const float inv = 1.f / L;
         uint4 pk;
@@ -380,18 +423,18 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, const int* sctx, vo
         pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
         pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
         pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + ((size_t)it.s * p.H + qh) * D + d0;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + ((size_t)s * p.H + qh) * D + d0;
         *reinterpret_cast<uint4*>(dst) = pk;
       } else {
-        const size_t wi = ((size_t)it.s * p.max_parts + it.part) * p.H + qh;
+        const size_t wi = ((size_t)s * p.max_parts + part) * p.H + qh;
         float4* dst = reinterpret_cast<float4*>(p.ws_o + wi * D + d0);
         dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         if (d0 == 0) p.ws_ml[wi] = make_float2(M, L);
       }
     }
-    named_barrier_sync(1, kConsumerWarps * 32);
-    ++n;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.epi_done);
   }
 }
 
@@ -402,84 +445,89 @@ __global__ void __launch_bounds__(kThreads, 2)
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* sctx = reinterpret_cast<int*>(base + C::kOffCtx);
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffAbort);
-
-  for (int s = threadIdx.x; s < p.S; s += blockDim.x) {
-    int c = p.context_lens[s];
-    if (c < 1 || c > p.max_ctx) {
-      if (blockIdx.x == 0) raise_status(p.status, PA_STATUS_BAD_CONTEXT);
-      c = c < 1 ? 0 : p.max_ctx;
-    }
-    sctx[s] = c;
-  }
   if (threadIdx.x == 0) {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kOffBar);
+    const Bars b = bars_at<D>(base);
     for (int k = 0; k < C::kStages; ++k) {
-      mbar_init(&bars[k], 1);                            // full: producer arrival + TMA bytes
-      mbar_init(&bars[C::kStages + k], 1);               // empty: the consuming warp
+      mbar_init(&b.full[k], 1);   // producer arrival + TMA bytes
+      mbar_init(&b.empty[k], 1);  // the consuming warp
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars[2 * C::kStages + k], 1);               // Q full
-      mbar_init(&bars[2 * C::kStages + 2 + k], kConsumerWarps);  // Q empty
+      mbar_init(&b.qfull[k], 1);                // producer arrival + Q bytes
+      mbar_init(&b.qempty[k], kConsumerWarps);  // every consumer warp has read Q
     }
+    mbar_init(b.epi_full, kConsumerWarps);  // every warp's state is in shared memory
+    mbar_init(b.epi_done, kConsumerWarps);  // every warp has finished the combine
     *abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
   pdl_launch_dependents();
-
-  // Sequences with an empty context get a zero output row.
-  if (blockIdx.x == 0) {
-    for (int s = 0; s < p.S; ++s) {
-      if (sctx[s] != 0) continue;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (size_t)s * p.H * D;
-      for (int e = threadIdx.x; e < p.H * D; e += blockDim.x) dst[e] = __float2bfloat16(0.f);
-    }
-  }
-
   if ((threadIdx.x >> 5) == kConsumerWarps) {
     if ((threadIdx.x & 31) == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    producer<D>(&kmap, &vmap, p, base, sctx, abort);
+    producer<D>(&kmap, &vmap, p, base, abort);
   } else {
-    consumer<D>(p, base, sctx, abort);
+    consumer<D>(p, base, abort);
   }
 }
 
 }  // namespace
 
-size_t decode_tc_smem_bytes(int D, int S) {
-  return D == 128 ? TcCfg<128>::bytes(S) : TcCfg<64>::bytes(S);
-}
+size_t decode_tc_smem_bytes(int D) { return D == 128 ? TcCfg<128>::kBytes : TcCfg<64>::kBytes; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
-  const size_t smem = decode_tc_smem_bytes(a.D, a.S);
+  const size_t smem = decode_tc_smem_bytes(a.D);
   auto kern = a.D == 128 ? paged_decode_tc_kernel<128> : paged_decode_tc_kernel<64>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static thread_local int cached_dev = -1;
-  static thread_local int sms = 0;
-  if (cached_dev != dev) {
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    cached_dev = dev;
-  }
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const long long total = (long long)a.max_parts * a.S * a.Hkv;
-  const int grid = (int)std::min<long long>(total, (long long)sms * per_sm);
+  // Per-device launch shape, computed once (threads of one process share it).
+  struct Shape {
+    int sms = 0, per_sm128 = 0, per_sm64 = 0;
+  };
+  static Shape shapes[64];
+  static std::once_flag once[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t init_err = cudaSuccess;
+  std::call_once(once[dev], [&] {
+    Shape sh;
+    init_err = cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (init_err == cudaSuccess)
+      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)TcCfg<128>::kBytes);
+    if (init_err == cudaSuccess)
+      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)TcCfg<64>::kBytes);
+    if (init_err == cudaSuccess)
+      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm128, paged_decode_tc_kernel<128>,
+                                                               kThreads, TcCfg<128>::kBytes);
+    if (init_err == cudaSuccess)
+      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm64, paged_decode_tc_kernel<64>,
+                                                               kThreads, TcCfg<64>::kBytes);
+    shapes[dev] = sh;
+  });
+  if (init_err != cudaSuccess) return init_err;
+  const Shape& sh = shapes[dev];
+  const int per_sm = a.D == 128 ? sh.per_sm128 : sh.per_sm64;
+  if (per_sm < 1 || sh.sms < 1) return cudaErrorInvalidConfiguration;
+  const long long total = (long long)a.max_parts * a.S * a.Hkv;  // upper bound of the work items
+  const int grid = (int)std::min<long long>(total, (long long)sh.sms * per_sm);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
 }  // namespace pa

@@ -8,6 +8,14 @@
 
 namespace pa {
 
+// Head of the decode workspace: the work counter of the persistent kernel
+// and the length of the work list that follows it.
+struct PlanHeader {
+  unsigned counter;
+  int num_pairs;  // (sequence, partition) pairs in the list; items = pairs * Hkv
+  int pad[62];
+};
+
 // Everything a decode launch needs besides the cache tensor maps.
 struct DecodeArgs {
   const void* q;                // [S][H][D]
@@ -18,6 +26,8 @@ struct DecodeArgs {
   const int32_t* context_lens;  // [S]
   float* ws_o;                  // [S][max_parts][H][D] split-K partial outputs
   float2* ws_ml;                // [S][max_parts][H] (max, sum), log2 domain
+  PlanHeader* hdr;              // work counter + list length
+  const int2* plan;             // [S * max_parts] {s | part << 16, clamped ctx}
   unsigned* status;             // device status word
   int S, H, Hkv, g, D, B;
   int num_blocks, max_blocks_per_seq, max_ctx;
@@ -31,8 +41,12 @@ constexpr int kMaxGroup = 8;
 // bf16, tensor cores; grid = persistent CTAs.
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream);
-// Dynamic shared memory of the tensor-core kernel for this head_dim and S.
-size_t decode_tc_smem_bytes(int D, int S);
+// Dynamic shared memory of the tensor-core kernel for this head_dim.
+size_t decode_tc_smem_bytes(int D);
+
+// Work list (longest items first) for the tensor-core kernel; also zeroes
+// the output rows of empty contexts.  Must precede launch_decode_tc.
+cudaError_t launch_decode_plan(const DecodeArgs& a, int out_elem_bytes, cudaStream_t stream);
 
 // fp32, CUDA cores; one CTA per (sequence, partition, KV head).
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);

@@ -101,10 +101,12 @@ def test_partition_and_workspace_sizing(L):
     p = L.pa_decode_partition_size(1, 1, 5000, 0)
     assert p % 32 == 0 and 64 <= p < 512
     assert L.pa_decode_partition_size(1, 1, 100, 33) == -1
-    # one partition: no workspace
-    assert L.pa_decode_workspace_bytes(4, 8, 128, 512, 512) == 0
-    # S * parts * H rows of D fp32 (256-byte aligned) + a float2 per row
-    rows = 8 * 256 * 64
-    assert L.pa_decode_workspace_bytes(8, 64, 128, 131072, 512) == rows * 128 * 4 + rows * 8
-    rows = 3 * 2 * 5
-    assert L.pa_decode_workspace_bytes(3, 5, 64, 600, 512) == ((rows * 64 * 4 + 255) // 256) * 256 + rows * 8
+    # one partition: header + work list only
+    assert L.pa_decode_workspace_bytes(4, 8, 128, 512, 512) == 256 + 256
+    # header, work list (8 B per sequence x partition, 256-aligned), then
+    # S * parts * H rows of D fp32 (256-aligned) and a float2 per row
+    pairs, rows = 8 * 256, 8 * 256 * 64
+    assert L.pa_decode_workspace_bytes(8, 64, 128, 131072, 512) == 256 + pairs * 8 + rows * 128 * 4 + rows * 8
+    pairs, rows = 3 * 2, 3 * 2 * 5
+    assert L.pa_decode_workspace_bytes(3, 5, 64, 600, 512) == 256 + 256 + ((rows * 64 * 4 + 255) // 256) * 256 + rows * 8
+    assert L.pa_decode_workspace_bytes(0, 5, 64, 600, 512) == 0

@@ -116,3 +116,41 @@ def test_serving_full_size(pa, b):
             assert torch.isfinite(out.float()).all()
             assert_close(out[seqs], ref, "bf16", f"B={b} step {step}")
     assert pa.get_status() == 0
+
+
+def test_serving_graph_replay_matches_oracle(pa):
+    """The captured step (upload, append, plan, decode, merge as one CUDA
+    graph) replayed step after step gives the oracle's slots, caches and
+    outputs; the copy-on-write of a fork runs eagerly just before the first
+    replay."""
+    from paged_kv_cache_216_gb300.serving import graphs_supported
+
+    if not graphs_supported():
+        pytest.skip("this torch cannot record events inside a CUDA graph")
+    # one eager decode first: it sets up the library's per-device state
+    z = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    zc = torch.zeros((2, 2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    pa.paged_decode(z, zc, zc, torch.zeros((1, 1), dtype=torch.int32, device="cuda"),
+                    torch.ones(1, dtype=torch.int32, device="cuda"), 1, 1.0)
+    w = WORKLOADS["serving_bf16_b8"].replace(num_seqs=6, num_heads=16, num_kv_heads=2, ctx_mean=400.0,
+                                             ctx_hi=1500, partition_size=128)
+    ctx = context_lens(w)
+    parent = int(np.argmax(ctx % w.block_size != 0))  # a partly filled last block to share
+    child = (parent + 1) % w.num_seqs
+    steps = 7
+    eng, orc = _engine_and_oracle(pa, w, steps, fork_pairs=[(parent, child)])
+    graph = eng.capture()
+    ncow = 0
+    for step in range(steps):
+        q, k, v = serving_step_tokens(w, step)
+        out = eng.replay(graph, to_dev(q), to_dev(k), to_dev(v))
+        slots, pairs, ref = orc.step(q, k, v, eng.width)
+        ncow += len(pairs)
+        torch.cuda.synchronize()
+        assert np.array_equal(eng.slots_h.numpy(), slots)
+        assert np.array_equal(eng.tables_h.numpy(), orc.tables(eng.width))
+        assert np.array_equal(to_bits(eng.k_cache), orc.k_cache)
+        assert np.array_equal(to_bits(eng.v_cache), orc.v_cache)
+        assert_close(out, ref, "bf16", f"graph step {step}")
+    assert ncow == 1
+    assert pa.get_status() == 0

@@ -6,6 +6,7 @@ import ctypes
 
 import numpy as np
 
+from . import _lib as _libmod
 from ._lib import check, lib
 
 
@@ -33,9 +34,12 @@ class BlockAllocator:
 
     def __del__(self):
         h = getattr(self, "_h", None)
-        if h and h.value and _lib_loaded():
-            lib().pa_alloc_destroy(h)
-            self._h = ctypes.c_void_p(0)
+        try:
+            if h and h.value and _libmod._lib is not None:
+                _libmod._lib.pa_alloc_destroy(h)
+                self._h = ctypes.c_void_p(0)
+        except Exception:  # interpreter shutdown: the process frees everything anyway
+            pass
 
     def num_free(self) -> int:
         return check(lib().pa_alloc_num_free(self._h))
@@ -95,8 +99,3 @@ class BlockAllocator:
                                          block_tables.shape[1],
                                          _np_ptr(context_lens) if context_lens is not None else None))
 
-
-def _lib_loaded() -> bool:
-    from . import _lib as m
-
-    return m._lib is not None

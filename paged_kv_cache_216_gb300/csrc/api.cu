@@ -63,14 +63,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tensor map over a bf16 cache viewed as a 2D array [N*Hkv*B rows][D]; one
-// box is B rows x 64 dims with 128-byte swizzle.
-int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D) {
+// Tensor map over a bf16 cache for the tensor-core kernel.  Either a 2D
+// array [N*Hkv*B rows][D] read in boxes of B rows x 64 dims, or (interleaved)
+// [N*Hkv*B*2 lines][64] read in boxes of 2B lines, one (block, head) slab per
+// box; 128-byte swizzle in both.
+int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D, bool inter) {
   auto fn = encode_fn();
   if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * Hkv * B};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)B};
+  const cuuint64_t rows = (cuuint64_t)num_blocks * Hkv * B;
+  cuuint64_t dims[2] = {inter ? 64u : (cuuint64_t)D, inter ? rows * (D / 64) : rows};
+  cuuint64_t strides[1] = {inter ? 128u : (cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, inter ? (cuuint32_t)(B * (D / 64)) : (cuuint32_t)B};
   cuuint32_t elem_strides[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                   elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -220,8 +223,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   if (!supported_shape(head_dim, block_size)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim/block_size");
   if (cdiv(max_context_len, block_size) > max_blocks_per_seq)
     return pa_fail(PA_ERR_INVALID, "pa_decode: max_blocks_per_seq < ceil(max_context_len / block_size)");
-  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
-    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: pool rows exceed 2^31");
+  if ((long long)num_blocks * num_kv_heads * block_size * 2 >= (1LL << 31))
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: pool rows exceed 2^30 (TMA coordinates are 32-bit)");
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return pa_fail(PA_ERR_INVALID, "pa_decode: null pointer");
@@ -272,9 +275,10 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   cudaError_t e;
   if (dtype == PA_BF16) {
     CUtensorMap kmap, vmap;
-    rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    const bool inter = pa::decode_tc_interleaved(head_dim, block_size);
+    rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
     if (rc) return rc;
-    rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
     if (rc) return rc;
     e = pa::launch_decode_plan(a, es, st);
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");

@@ -104,7 +104,18 @@ __device__ __forceinline__ void give_up(const DecodeArgs& p, volatile int* abort
   raise_status(p.status, PA_STATUS_TIMEOUT);
 }
 
-template <int D>
+// kInter: each 256-byte token row is two 128-byte lines of the stage
+// (line 2t + half) and one TMA box brings a whole [B x D] slab; otherwise
+// the two 64-dim halves of a chunk are separate 32-line regions (line
+// half*32 + t) filled by one box per half.  The first halves the number of
+// TMA requests (used for 8-token blocks, whose per-half boxes are only
+// 1 KB); the second keeps ldmatrix free of bank conflicts.
+template <int D, bool kInter>
+__device__ __forceinline__ int stage_line(int t, int half) {
+  return kInter ? 2 * t + half : half * kChunk + t;
+}
+
+template <int D, bool kInter>
 __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& p, uint8_t* base,
                          volatile int* abort) {
   using C = TcCfg<D>;
@@ -193,12 +204,18 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
       __syncwarp();
       if (lane < nb) {
         const int y = (id * p.Hkv + kvh) * p.B;
-        uint8_t* sk = base + stage * C::kStage + lane * p.B * 128;
-        uint8_t* sv = sk + C::kRegion;
+        if constexpr (kInter) {
+          uint8_t* sk = base + stage * C::kStage + lane * p.B * 256;
+          tma_load_2d(sk, kmap, &bar.full[stage], 0, 2 * y, policy);
+          tma_load_2d(sk + C::kRegion, vmap, &bar.full[stage], 0, 2 * y, policy);
+        } else {
+          uint8_t* sk = base + stage * C::kStage + lane * p.B * 128;
+          uint8_t* sv = sk + C::kRegion;
 #pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          tma_load_2d(sk + hf * kHalfBytes, kmap, &bar.full[stage], hf * 64, y, policy);
-          tma_load_2d(sv + hf * kHalfBytes, vmap, &bar.full[stage], hf * 64, y, policy);
+          for (int hf = 0; hf < C::kHalves; ++hf) {
+            tma_load_2d(sk + hf * kHalfBytes, kmap, &bar.full[stage], hf * 64, y, policy);
+            tma_load_2d(sv + hf * kHalfBytes, vmap, &bar.full[stage], hf * 64, y, policy);
+          }
         }
       }
     }
@@ -217,7 +234,7 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
   }
 }
 
-template <int D>
+template <int D, bool kInter>
 __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort) {
   using C = TcCfg<D>;
   constexpr int KS = D / 16;  // k-steps of the Q·Kᵀ product
@@ -280,7 +297,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         for (int u = lane; u < units; u += 32) {
           const int r = nv + u / (C::kHalves * 8);
           const int rem = u % (C::kHalves * 8);
-          *reinterpret_cast<uint4*>(vrow + (rem >> 3) * kHalfBytes + r * 128 + (rem & 7) * 16) =
+          *reinterpret_cast<uint4*>(vrow + stage_line<D, kInter>(r, rem >> 3) * 128 + (rem & 7) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -296,7 +313,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         for (int nt = 0; nt < 4; ++nt) {
           const int t = nt * 8 + (lane & 7);
           const int cidx = 4 * kk + (lane >> 3);
-          const uint32_t addr = sk + (cidx >> 3) * kHalfBytes + t * 128 + (((cidx & 7) ^ (t & 7)) << 4);
+          const int line = stage_line<D, kInter>(t, cidx >> 3);
+          const uint32_t addr = sk + line * 128 + (((cidx & 7) ^ (line & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(addr, b0, b1, b2, b3);
           mma_bf16_16816(sc[nt], qa[2 * kk][0], 0u, qa[2 * kk][1], 0u, b0, b1);
@@ -346,7 +364,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int cidx = 2 * mt + ((lane >> 3) & 1);
-          const uint32_t addr = sv + (cidx >> 3) * kHalfBytes + t * 128 + (((cidx & 7) ^ (t & 7)) << 4);
+          const int line = stage_line<D, kInter>(t, cidx >> 3);
+          const uint32_t addr = sv + line * 128 + (((cidx & 7) ^ (line & 7)) << 4);
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4_trans(addr, a0, a1, a2, a3);
           mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
@@ -438,7 +457,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
   }
 }
 
-template <int D>
+template <int D, bool kInter>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const DecodeArgs p) {
@@ -468,9 +487,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    producer<D>(&kmap, &vmap, p, base, abort);
+    producer<D, kInter>(&kmap, &vmap, p, base, abort);
   } else {
-    consumer<D>(p, base, abort);
+    consumer<D, kInter>(p, base, abort);
   }
 }
 
@@ -478,10 +497,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 size_t decode_tc_smem_bytes(int D) { return D == 128 ? TcCfg<128>::kBytes : TcCfg<64>::kBytes; }
 
+bool decode_tc_interleaved(int D, int B) { return D == 128 && B == 8; }
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   const size_t smem = decode_tc_smem_bytes(a.D);
-  auto kern = a.D == 128 ? paged_decode_tc_kernel<128> : paged_decode_tc_kernel<64>;
+  const bool inter = decode_tc_interleaved(a.D, a.B);
+  auto kern = a.D == 128 ? (inter ? paged_decode_tc_kernel<128, true> : paged_decode_tc_kernel<128, false>)
+                         : paged_decode_tc_kernel<64, false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -497,16 +520,19 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
     Shape sh;
     init_err = cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev);
     if (init_err == cudaSuccess)
-      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)TcCfg<128>::kBytes);
+      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<128, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<128>::kBytes);
     if (init_err == cudaSuccess)
-      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)TcCfg<64>::kBytes);
+      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<128, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<128>::kBytes);
     if (init_err == cudaSuccess)
-      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm128, paged_decode_tc_kernel<128>,
+      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<64, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<64>::kBytes);
+    if (init_err == cudaSuccess)
+      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm128, paged_decode_tc_kernel<128, false>,
                                                                kThreads, TcCfg<128>::kBytes);
     if (init_err == cudaSuccess)
-      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm64, paged_decode_tc_kernel<64>,
+      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm64, paged_decode_tc_kernel<64, false>,
                                                                kThreads, TcCfg<64>::kBytes);
     shapes[dev] = sh;
   });

@@ -43,6 +43,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
                              cudaStream_t stream);
 // Dynamic shared memory of the tensor-core kernel for this head_dim.
 size_t decode_tc_smem_bytes(int D);
+// Whether the tensor-core kernel loads whole [B x D] slabs as one TMA box
+// of 2B lines of 128 bytes (true) or one box per 64-dim half (false); the
+// cache tensor maps must be made to match.
+bool decode_tc_interleaved(int D, int B);
 
 // Work list (longest items first) for the tensor-core kernel; also zeroes
 // the output rows of empty contexts.  Must precede launch_decode_tc.

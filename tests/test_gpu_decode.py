@@ -104,10 +104,11 @@ def test_single_token_returns_value_row(pa):
             assert np.array_equal(got, v_row)  # softmax of one score is 1: out = V_0 exactly
 
 
-def test_garbage_past_context_does_not_leak(pa):
+@pytest.mark.parametrize("b", [8, 16])
+def test_garbage_past_context_does_not_leak(pa, b):
     """Rows past the context in the last block (never written in serving)
     hold NaN/Inf: the output must not see them."""
-    w = SMALL["serving_b8_small"].replace(block_size=16)
+    w = SMALL["serving_b8_small"].replace(block_size=b)
     case = make_decode_case(w)
     ref = case.oracle()
     kd = case.k_cache.view(torch.int16)

@@ -48,6 +48,39 @@ def kv_bytes(ctx: np.ndarray, w) -> int:
     return int(np.asarray(ctx, dtype=np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
 
 
+DECODE_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_tc.cu", "paged_kv_cache_216_gb300/csrc/device_common.cuh",
+                  "paged_kv_cache_216_gb300/csrc/kernels.h")
+
+
+def decode_kernel_hash() -> str:
+    """Hash of the decode kernel's sources: DRAM counters taken on another
+    version of the kernel are not reported."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def decode_traffic(workload: str):
+    """DRAM bytes (read + write) of one decode-kernel launch on this workload
+    from the committed ncu summary profiles/decode_dram_traffic.txt (lines:
+    workload read_bytes write_bytes source_hash), or None if absent or taken
+    on another version of the kernel."""
+    p = os.path.join(ROOT, "profiles", "decode_dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = decode_kernel_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split("#", 1)[0].split()
+            if len(parts) == 4 and parts[0] == workload and parts[3] == cur:
+                return int(float(parts[1]) + float(parts[2]))
+    return None
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -215,30 +248,40 @@ def run_ours(args, rank, world, local):
 
     use_graphs = graphs_supported() and not args.eager
     dec_ev = [(_event(True), _event(True)) for _ in range(K)]
-    graphs = [eng.capture(events=dec_ev[i]) for i in range(K)] if use_graphs else None
+    graphs = ([eng.capture(events=dec_ev[i], inputs=(*dev_toks[W + i], out)) for i in range(K)]
+              if use_graphs else None)
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    bytes_steps = []
+    # every step adds one token to every sequence: step i of the timed run
+    # decodes contexts ctx0 + W + i + 1
+    bytes_steps = [kv_bytes(ctx0 + W + i + 1, w) for i in range(K)]
     launches0 = eng.launches
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for i in range(K):
-        if flush is not None:
+    if flush is None:
+        step_ev[0][0].record(stream)
+        for i in range(K):
+            if use_graphs:
+                eng.replay(graphs[i])
+            else:
+                eng.step(*dev_toks[W + i], out=out, events=dec_ev[i])
+        step_ev[-1][1].record(stream)
+    else:
+        for i in range(K):
             flush.add_(1)
-        q, kn, vn = dev_toks[W + i]
-        step_ev[i][0].record(stream)
-        if use_graphs:
-            eng.replay(graphs[i], q, kn, vn)
-        else:
-            eng.step(q, kn, vn, out=out, events=dec_ev[i])
-        step_ev[i][1].record(stream)
-        bytes_steps.append(kv_bytes(eng.ctx_h.numpy(), w))
+            step_ev[i][0].record(stream)
+            if use_graphs:
+                eng.replay(graphs[i])
+            else:
+                eng.step(*dev_toks[W + i], out=out, events=dec_ev[i])
+            step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     launches = eng.launches - launches0
     clk = clocks.stop()
+    assert np.array_equal(eng.ctx_h.numpy(), ctx0 + W + K)
     if flush is None:
         t_dev = step_ev[0][0].elapsed_time(step_ev[-1][1]) / 1e3
     else:
@@ -257,15 +300,15 @@ def run_ours(args, rank, world, local):
         pin = [tuple(x.view(torch.bfloat16) for x in t) for t in pin]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_bytes = 0
+    g_host = eng.capture() if use_graphs else None
+    e2e_bytes = sum(kv_bytes(ctx0 + W + K + i + 1, w) for i in range(K))
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
     for i in range(K):
         if flush is not None:
             flush.add_(1)
-        eng.step_host(*pin[i], out_h, graph=graphs[i] if use_graphs else None)
-        e2e_bytes += kv_bytes(eng.ctx_h.numpy(), w)
+        eng.step_host(*pin[i], out_h, graphs=g_host)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -282,11 +325,7 @@ def run_ours(args, rank, world, local):
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     achieved = dec_bytes / dec_avg / 1e9
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            traffic = json.load(f).get(args.workload)
+    traffic = decode_traffic(args.workload)
     status = pa.get_status()
     if status:
         raise RuntimeError(f"device status word {status:#x} after the benchmark")
@@ -303,7 +342,8 @@ def run_ours(args, rank, world, local):
             "l2": ("flushed before every step" if flush is not None else
                    f"inputs larger than L2 ({dec_bytes / 1e9:.2f} GB KV per step vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}",
-            "launch": "cuda graph per step" if use_graphs else "eager",
+            "launch": ("uploads on a side stream; append+decode+merge as a CUDA graph per step"
+                       if use_graphs else "uploads on a side stream; eager launches"),
         },
         "decode_tokens_per_s": round(tokens_s, 1),
         "wall_s": round(wall, 4),

@@ -161,6 +161,40 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*
+ * Work list of the decode kernel built on the host, for callers that know
+ * their context lengths there (a serving loop's allocator does) and can
+ * upload it with their block tables, so that no planning kernel runs in the
+ * step.  Same list as pa_decode builds on the device [PAK section 3.2: a
+ * dynamic work queue]: every full partition, then partial ones from the
+ * longest to the shortest, then one entry per empty context.
+ *   context_lens  host, [num_seqs] int32, each in [0, max_context_len]
+ *   plan          host, pa_decode_plan_bytes(...) bytes; a 256-byte header
+ *                 (work counter = 0, list length) and 8 bytes per entry
+ * partition_size must be the value pa_decode_partition_size returns for the
+ * decode call (a positive multiple of 32).
+ */
+size_t pa_decode_plan_bytes(int num_seqs, int max_context_len,
+                            int partition_size);
+int pa_decode_plan_host(const int32_t* context_lens, int num_seqs,
+                        int max_context_len, int partition_size, void* plan);
+
+/*
+ * pa_decode with a work list from pa_decode_plan_host, copied to the device
+ * (`plan`, 256-byte aligned).  bf16 only.  The call consumes the list's work
+ * counter: every call needs a fresh copy (counter 0).  The plan region of
+ * `workspace` is not used; size it with pa_decode_workspace_bytes as for
+ * pa_decode.  context_lens must hold the lengths the plan was built from.
+ */
+int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int max_context_len,
+                      float scale, void* out, int num_seqs, int num_heads,
+                      int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, int partition_size, const void* plan,
+                      void* workspace, size_t workspace_bytes, int dtype,
+                      void* stream);
+
+/*
  * Paged decode that allocates nothing: the same computation and arguments as
  * pa_decode, but the split-K scratch is a fixed device array inside this
  * library, so the caller passes no workspace.  The pages have no counterpart;
@@ -251,6 +285,43 @@ int pa_seqs_append_slots(pa_alloc* a, const int64_t* seq_ids, int n,
 int pa_seqs_block_tables(const pa_alloc* a, const int64_t* seq_ids, int n,
                          int32_t* block_tables, int width,
                          int32_t* context_lens);
+
+/* ------------------------------------------------------------------------
+ * Host side of a pipelined serving step [Day6 paragraph 2].
+ *
+ * The caller owns one pinned host buffer and two device buffers laid out by
+ * pa_stepper_layout (offsets: work list, slot mapping int64[n], context
+ * lengths int32[n], copy-on-write pairs int32[n][2], block tables
+ * int32[n][width]).  Each step:
+ *   pa_stepper_prepare  waits until the previous upload has read the host
+ *                       buffer; reserves every sequence's next slot
+ *                       (pa_seqs_append_slots, tables and lengths updated in
+ *                       place); builds the decode work list
+ *                       (pa_decode_plan_host, if partition_size > 0); on
+ *                       upload_stream waits until the step that last read
+ *                       device buffer k is over, copies the host buffer to
+ *                       it and records an event; makes main_stream wait for
+ *                       that event.  *buffer_index = k, *num_cow = copies the
+ *                       caller must apply (pa_copy_blocks on main_stream)
+ *                       before appending.
+ *   ... the step's kernels on main_stream, reading device buffer k ...
+ *   pa_stepper_finish   records on main_stream that buffer k is free again.
+ * The stepper owns four CUDA events; everything else is the caller's.  The
+ * allocator must not be changed by other calls between prepare and finish.
+ * ------------------------------------------------------------------------ */
+typedef struct pa_stepper pa_stepper;
+
+int pa_stepper_layout(int num_seqs, int max_context_len, int block_size,
+                      int partition_size, size_t* offsets /* [5] */,
+                      size_t* total);
+int pa_stepper_create(pa_alloc* alloc, const int64_t* seq_ids, int num_seqs,
+                      int max_context_len, int block_size, int partition_size,
+                      void* host_buf, void* dev_buf0, void* dev_buf1,
+                      size_t buf_bytes, pa_stepper** out);
+void pa_stepper_destroy(pa_stepper* st);
+int pa_stepper_prepare(pa_stepper* st, void* upload_stream, void* main_stream,
+                       int* buffer_index, int* num_cow);
+int pa_stepper_finish(pa_stepper* st, void* main_stream);
 
 #ifdef __cplusplus
 }

@@ -40,6 +40,10 @@ SIGNATURES = {
     "pa_decode_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _vp]),
+    "pa_decode_plan_bytes": (_c_sz, [_c_int, _c_int, _c_int]),
+    "pa_decode_plan_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp]),
+    "pa_decode_planned": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _vp, _vp, _c_sz, _c_int, _vp]),
     "pa_decode_static_workspace": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_alloc_create": (_c_int, [_c_int, _c_int, _vp, ctypes.POINTER(_vp)]),
@@ -54,6 +58,12 @@ SIGNATURES = {
     "pa_block_refcount": (_c_int, [_vp, _c_int]),
     "pa_seqs_append_slots": (_c_int, [_vp, _vp, _c_int, _vp, _vp, ctypes.POINTER(_c_int), _vp, _c_int, _vp]),
     "pa_seqs_block_tables": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _vp]),
+    "pa_stepper_layout": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_sz), ctypes.POINTER(_c_sz)]),
+    "pa_stepper_create": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_sz,
+                                   ctypes.POINTER(_vp)]),
+    "pa_stepper_destroy": (None, [_vp]),
+    "pa_stepper_prepare": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
+    "pa_stepper_finish": (_c_int, [_vp, _vp]),
 }
 
 ERRORS = {-1: "PA_ERR_INVALID", -2: "PA_ERR_UNSUPPORTED", -3: "PA_ERR_OOM", -4: "PA_ERR_STATE", -5: "PA_ERR_CUDA"}

@@ -208,10 +208,15 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
   return l.total;
 }
 
-int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-              int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale, void* out,
-              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-              int partition_size, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+}  // extern "C"
+
+// pa_decode and pa_decode_planned: `plan` (device) is a work list built by
+// pa_decode_plan_host, or NULL to build it on the device.
+static int decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
+                       void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, int partition_size, const void* plan, void* workspace,
+                       size_t workspace_bytes, int dtype, void* stream) {
   const int es = elem_bytes(dtype);
   if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_context_len < 1 ||
@@ -241,6 +246,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   ws_layout(num_seqs, num_heads, head_dim, max_context_len, P, &wl);
   if (!workspace || workspace_bytes < wl.total) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace too small");
   if (!aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace not 256-byte aligned");
+  if (plan && dtype != PA_BF16) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_planned: bf16 only");
+  if (plan && !aligned(plan, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode_planned: plan not 256-byte aligned");
 
   pa::DecodeArgs a{};
   a.q = q;
@@ -250,8 +257,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   char* ws = static_cast<char*>(workspace);
-  a.hdr = reinterpret_cast<pa::PlanHeader*>(ws);
-  a.plan = reinterpret_cast<const int2*>(ws + wl.plan);
+  char* pl = plan ? static_cast<char*>(const_cast<void*>(plan)) : ws;
+  a.hdr = reinterpret_cast<pa::PlanHeader*>(pl);
+  a.plan = reinterpret_cast<const int2*>(pl + wl.plan);
   if (parts > 1) {
     a.ws_o = reinterpret_cast<float*>(ws + wl.o);
     a.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
@@ -280,8 +288,10 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     if (rc) return rc;
     rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
     if (rc) return rc;
-    e = pa::launch_decode_plan(a, es, st);
-    if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");
+    if (!plan) {
+      e = pa::launch_decode_plan(a, st);
+      if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");
+    }
     e = pa::launch_decode_tc(a, kmap, vmap, st);
   } else {
     e = pa::launch_decode_simt(a, st);
@@ -292,6 +302,29 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode merge launch");
   }
   return PA_OK;
+}
+
+
+extern "C" {
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale, void* out,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+              int partition_size, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                     out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
+                     nullptr, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
+                      void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, int partition_size, const void* plan, void* workspace,
+                      size_t workspace_bytes, int dtype, void* stream) {
+  if (!plan) return pa_fail(PA_ERR_INVALID, "pa_decode_planned: null plan");
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                     out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
+                     plan, workspace, workspace_bytes, dtype, stream);
 }
 
 }  // extern "C"

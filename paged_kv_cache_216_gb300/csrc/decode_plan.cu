@@ -9,7 +9,8 @@
 // shortest and no CTA is left with a long item at the end.
 //
 // One CTA of 1024 threads.  It also validates the context lengths (status
-// bit, clamping) and writes the zero output rows of empty contexts.  It lets
+// bit, clamping); an empty context gets one entry of length 0 at the end of
+// the list, for which the decode kernel writes a zero output row.  It lets
 // the decode kernel launch right away (programmatic dependent launch); the
 // decode kernel waits for it before its first read of the list.
 
@@ -52,7 +53,7 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t* __restrict__ context_lens, int S,
                                                                    int P, int max_ctx, PlanHeader* hdr, int2* plan,
-                                                                   void* out, int out_row_bytes, unsigned* status) {
+                                                                   unsigned* status) {
   pdl_launch_dependents();
   __shared__ int scratch[32];
   __shared__ int bucket_count[kBuckets];
@@ -63,18 +64,15 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
   // Each thread owns a contiguous range of sequences.
   const int per = (S + kPlanThreads - 1) / kPlanThreads;
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
-  int nfull = 0;
+  int nfull = 0, nempty = 0;
   for (int s = s0; s < s1; ++s) {
     int c = context_lens[s];
     if (c < 1 || c > max_ctx) {
       raise_status(status, PA_STATUS_BAD_CONTEXT);
       c = c < 1 ? 0 : max_ctx;
-      if (c == 0) {
-        uint4* row = reinterpret_cast<uint4*>(static_cast<char*>(out) + (size_t)s * out_row_bytes);
-        for (int e = 0; e < out_row_bytes / 16; ++e) row[e] = make_uint4(0, 0, 0, 0);
-      }
     }
     nfull += c / P;
+    nempty += c == 0;
     const int rem = c % P;
     if (rem) atomicAdd(&bucket_count[(int)((long long)(rem - 1) * kBuckets / P)], 1);
   }
@@ -90,9 +88,14 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
   const int cnt = rb >= 0 ? bucket_count[rb] : 0;
   const int start = block_exclusive_scan(cnt, scratch, &total_partial);
   if (rb >= 0) bucket_cursor[rb] = total_full + start;
-  __syncthreads();
+  int total_empty = 0;
+  int epos = total_full + total_partial + block_exclusive_scan(nempty, scratch, &total_empty);
   for (int s = s0; s < s1; ++s) {
     int c = min(max(context_lens[s], 0), max_ctx);
+    if (c == 0) {
+      plan[epos++] = make_int2(s, 0);
+      continue;
+    }
     const int rem = c % P;
     if (!rem) continue;
     const int at = atomicAdd(&bucket_cursor[(int)((long long)(rem - 1) * kBuckets / P)], 1);
@@ -100,16 +103,15 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
   }
   if (tid == 0) {
     hdr->counter = 0u;
-    hdr->num_pairs = total_full + total_partial;
+    hdr->num_pairs = total_full + total_partial + total_empty;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_plan(const DecodeArgs& a, int out_elem_bytes, cudaStream_t stream) {
+cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t stream) {
   decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.context_lens, a.S, a.P, a.max_ctx, a.hdr,
-                                                     const_cast<int2*>(a.plan), a.out,
-                                                     a.H * a.D * out_elem_bytes, a.status);
+                                                     const_cast<int2*>(a.plan), a.status);
   return cudaGetLastError();
 }
 

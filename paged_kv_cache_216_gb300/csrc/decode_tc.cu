@@ -435,13 +435,15 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         acc[7] += wt * x1.w;
       }
       const int qh = kvh * p.g + h;
-      if (np == 1) {
-        const float inv = 1.f / L;
-        uint4 pk;
-        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-        pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      if (np <= 1) {  // one partition, or an empty context (zero row)
+        uint4 pk = make_uint4(0, 0, 0, 0);
+        if (np == 1) {
+          const float inv = 1.f / L;
+          pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+          pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+          pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+          pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        }
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + ((size_t)s * p.H + qh) * D + d0;
         *reinterpret_cast<uint4*>(dst) = pk;
       } else {

@@ -27,7 +27,7 @@ struct DecodeArgs {
   float* ws_o;                  // [S][max_parts][H][D] split-K partial outputs
   float2* ws_ml;                // [S][max_parts][H] (max, sum), log2 domain
   PlanHeader* hdr;              // work counter + list length
-  const int2* plan;             // [S * max_parts] {s | part << 16, clamped ctx}
+  const int2* plan;             // [S * max_parts] {s | part << 16, clamped ctx}; ctx 0 = empty context
   unsigned* status;             // device status word
   int S, H, Hkv, g, D, B;
   int num_blocks, max_blocks_per_seq, max_ctx;
@@ -48,9 +48,10 @@ size_t decode_tc_smem_bytes(int D);
 // cache tensor maps must be made to match.
 bool decode_tc_interleaved(int D, int B);
 
-// Work list (longest items first) for the tensor-core kernel; also zeroes
-// the output rows of empty contexts.  Must precede launch_decode_tc.
-cudaError_t launch_decode_plan(const DecodeArgs& a, int out_elem_bytes, cudaStream_t stream);
+// Work list (longest items first) for the tensor-core kernel, built on the
+// device from a.context_lens into a.hdr / a.plan.  Must precede
+// launch_decode_tc on the stream.
+cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t stream);
 
 // fp32, CUDA cores; one CTA per (sequence, partition, KV head).
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);

@@ -116,6 +116,35 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_le
     return out
 
 
+def decode_plan_bytes(num_seqs: int, max_context_len: int, partition_size: int) -> int:
+    return int(lib().pa_decode_plan_bytes(num_seqs, max_context_len, partition_size))
+
+
+def decode_plan_host(context_lens, max_context_len: int, partition_size: int, plan) -> None:
+    """Build the decode work list on the host into ``plan`` (a host buffer
+    of decode_plan_bytes(...) bytes, numpy or a CPU tensor) from the int32
+    host array ``context_lens``."""
+    ptr = plan.ctypes.data if hasattr(plan, "ctypes") else plan.data_ptr()
+    cptr = context_lens.ctypes.data if hasattr(context_lens, "ctypes") else context_lens.data_ptr()
+    check(lib().pa_decode_plan_host(ctypes.c_void_p(cptr), len(context_lens), int(max_context_len),
+                                    int(partition_size), ctypes.c_void_p(ptr)))
+
+
+def paged_decode_planned(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                         out, plan, workspace, partition_size: int, stream=None):
+    """:func:`paged_decode` with a work list built by :func:`decode_plan_host`
+    and copied to the device (``plan``, uint8, counter at 0; consumed by the
+    call)."""
+    s, h, d = q.shape
+    n, hkv, b, _ = k_cache.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode_planned(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                  _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), s, h, hkv, d, b,
+                                  n, int(partition_size), _ptr(plan), _ptr(workspace), ws_bytes, _dtype_code(q),
+                                  _stream(stream)))
+    return out
+
+
 def paged_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
                                   scale: float, out, partition_size: int = 0, stream=None):
     """Same as :func:`paged_decode`, for callers that cannot allocate a

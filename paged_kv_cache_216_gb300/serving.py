@@ -3,29 +3,36 @@
 One step ("Day 6/90 of Inference Engineering", PagedAttention notes,
 paragraphs 2, 5 and 6): the host allocator reserves every sequence's next
 slot (a new block when the last one is full; a copy when it is shared and
-partly filled), the slot mapping, context lengths and updated block tables
-go to the device in one copy, pending block copies run, the new keys/values
-are appended, and paged decode attends over the grown contexts (the new
-token included).
+partly filled), the slot mapping, context lengths, block copies, updated
+block tables and the decode work list go to the device in one copy, pending
+block copies run, the new keys/values are appended, and paged decode attends
+over the grown contexts (the new token included).
 
-The host-side tables live in one pinned buffer that the allocator updates in
-place.  Before rewriting it for the next step the host waits for the
-previous step's upload to have executed (an event recorded right after the
-copy), so the host runs at most one step ahead of the device.
+Pipelining (the native stepper of the C ABI, pa_stepper_*).  The host-side
+state lives in one pinned buffer that the allocator updates in place.  It is
+copied to one of two device buffers on a side stream, which first waits for
+the step that last read that device buffer; the main stream of step i waits
+only for its own upload.  So the upload of step i runs while step i-1
+decodes, and the main stream carries only append -> decode -> merge.  Before
+rewriting the pinned buffer the host waits for the previous upload to
+finish, which bounds it to about two steps ahead of the device.  The host
+work of a step is one library call before its launches and one after.
 
-The device part of a step can be captured once into a CUDA graph
-(:meth:`ServingEngine.capture`) and replayed every step: one launch instead
-of a copy and four kernel launches, with no host gaps between them.  A
-captured step reads its new tokens from the engine's staging buffers
-(``q_in``, ``k_in``, ``v_in``) and writes ``out``.
+The main-stream part of a step can be captured into CUDA graphs
+(:meth:`ServingEngine.capture`, one per device buffer) and replayed every
+step.
 """
 
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import torch
 
+from . import _lib as _libmod
 from . import ops
+from ._lib import check, lib
 from .allocator import BlockAllocator
 
 
@@ -46,6 +53,17 @@ def graphs_supported() -> bool:
         return False
 
 
+def _align(x: int, a: int) -> int:
+    return (x + a - 1) // a * a
+
+
+class StepGraphs:
+    """Captured main-stream part of a step, one graph per device buffer."""
+
+    def __init__(self, graphs):
+        self.graphs = graphs
+
+
 class ServingEngine:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, allocator: BlockAllocator, seq_ids,
                  num_heads: int, scale: float, max_context_len: int, partition_size: int = 0):
@@ -61,63 +79,94 @@ class ServingEngine:
         s = self.seq_ids.shape[0]
         self.num_seqs = s
         self.width = -(-self.max_context_len // b)
-        # one packed upload: slots int64[S] | context_lens int32[S] | tables int32[S, width]
-        t_off = (12 * s + 15) // 16 * 16
-        nbytes = t_off + 4 * s * self.width
-        self._up_h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-        self._up_d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        self.slots_h, self.ctx_h, self.tables_h = self._views(self._up_h, s, t_off)
-        self.slots_d, self.ctx_d, self.tables_d = self._views(self._up_d, s, t_off)
-        self.cow_h = torch.empty((s, 2), dtype=torch.int32, pin_memory=True)
-        self.cow_d = torch.empty((s, 2), dtype=torch.int32, device=dev)
-        self.alloc.block_tables(self.seq_ids, self.tables_h.numpy(), self.ctx_h.numpy())
-        self._up_d.copy_(self._up_h, non_blocking=True)
         self.partition_size = ops.decode_partition_size(s, hkv, self.max_context_len, partition_size)
+        self.bf16 = k_cache.dtype == torch.bfloat16
+        plan_p = self.partition_size if self.bf16 else 0
+        offs = (ctypes.c_size_t * 5)()
+        total = ctypes.c_size_t(0)
+        check(lib().pa_stepper_layout(s, self.max_context_len, b, plan_p, offs, ctypes.byref(total)))
+        self._layout = tuple(int(x) for x in offs)
+        nbytes = int(total.value)
+        self._up_h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        self._up_d = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.plan_h, self.slots_h, self.ctx_h, self.cow_h, self.tables_h = self._views(self._up_h)
+        self._dv = [self._views(x) for x in self._up_d]
+        self._st = ctypes.c_void_p(0)
+        check(lib().pa_stepper_create(allocator._h, ctypes.c_void_p(self.seq_ids.ctypes.data), s,
+                                      self.max_context_len, b, plan_p, ctypes.c_void_p(self._up_h.data_ptr()),
+                                      ctypes.c_void_p(self._up_d[0].data_ptr()),
+                                      ctypes.c_void_p(self._up_d[1].data_ptr()), nbytes, ctypes.byref(self._st)))
         self.workspace = ops.decode_workspace(s, num_heads, hkv, d, self.max_context_len, self.partition_size, dev)
-        self.uploaded = _event()
-        self.uploaded.record()
+        self.up_stream = torch.cuda.Stream(device=dev)
+        self._up_ptr = ctypes.c_void_p(self.up_stream.cuda_stream)
+        self._bi = ctypes.c_int(0)
+        self._nc = ctypes.c_int(0)
+        self.k = 0  # device buffer of the next step
         self.launches = 0  # kernels this engine has launched
         self.split = -(-self.max_context_len // self.partition_size) > 1
-        self._per_step = 2 + (1 if k_cache.dtype == torch.bfloat16 else 0) + (1 if self.split else 0)
-        # staging buffers of captured steps
+        self._per_step = 2 + (1 if self.split else 0)  # append + decode (+ merge)
+        # staging buffers for steps whose inputs come from elsewhere
         self.q_in = torch.empty((s, num_heads, d), dtype=k_cache.dtype, device=dev)
         self.k_in = torch.empty((s, hkv, d), dtype=k_cache.dtype, device=dev)
         self.v_in = torch.empty((s, hkv, d), dtype=k_cache.dtype, device=dev)
         self.out = torch.empty((s, num_heads, d), dtype=k_cache.dtype, device=dev)
         self._pool = None
 
-    @staticmethod
-    def _views(buf, s, t_off):
-        slots = buf[: 8 * s].view(torch.int64)
-        ctx = buf[8 * s: 12 * s].view(torch.int32)
-        tables = buf[t_off:].view(torch.int32).view(s, -1)
-        return slots, ctx, tables
+    def _views(self, buf):
+        s, w = self.num_seqs, self.width
+        o_plan, o_slots, o_ctx, o_cow, o_tab = self._layout
+        plan = buf[o_plan:o_slots]
+        slots = buf[o_slots:o_slots + 8 * s].view(torch.int64)
+        ctx = buf[o_ctx:o_ctx + 4 * s].view(torch.int32)
+        cow = buf[o_cow:o_cow + 8 * s].view(torch.int32).view(s, 2)
+        tables = buf[o_tab:o_tab + 4 * s * w].view(torch.int32).view(s, w)
+        return plan, slots, ctx, cow, tables
+
+    def __del__(self):
+        st = getattr(self, "_st", None)
+        try:
+            if st and st.value and _libmod._lib is not None:
+                torch.cuda.synchronize()
+                _libmod._lib.pa_stepper_destroy(st)
+                self._st = ctypes.c_void_p(0)
+        except Exception:  # interpreter shutdown
+            pass
 
     def context_lens(self) -> np.ndarray:
         return self.ctx_h.numpy().copy()
 
     # -- host part ---------------------------------------------------------
-    def _reserve(self) -> int:
-        """Reserve every sequence's next slot into the pinned upload buffer
-        and queue the block copies it requires; returns their number."""
-        self.uploaded.synchronize()
-        ncow = self.alloc.append_slots(self.seq_ids, self.slots_h.numpy(), self.cow_h.numpy(),
-                                       self.tables_h.numpy(), self.ctx_h.numpy())
+    def _prepare(self) -> int:
+        """Reserve every sequence's next slot, build the work list, upload
+        everything to device buffer ``k`` on the side stream, make the main
+        stream wait for it and queue the block copies.  Returns their number."""
+        main = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        check(_libmod._lib.pa_stepper_prepare(self._st, self._up_ptr, main, ctypes.byref(self._bi),
+                                              ctypes.byref(self._nc)))
+        self.k = k = self._bi.value
+        ncow = self._nc.value
         if ncow:
-            self.cow_d[:ncow].copy_(self.cow_h[:ncow], non_blocking=True)
-            ops.copy_blocks(self.k_cache, self.v_cache, self.cow_d[:ncow])
+            ops.copy_blocks(self.k_cache, self.v_cache, self._dv[k][3][:ncow])
             self.launches += 1
         return ncow
 
-    # -- device part -------------------------------------------------------
-    def _device(self, q, k_new, v_new, out, events=None):
-        self._up_d.copy_(self._up_h, non_blocking=True)
-        self.uploaded.record()
-        ops.cache_append(k_new, v_new, self.slots_d, self.k_cache, self.v_cache)
+    def _finish(self) -> None:
+        check(_libmod._lib.pa_stepper_finish(self._st, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+        self.k ^= 1
+        self.launches += self._per_step
+
+    # -- main-stream part (capturable) ---------------------------------------
+    def _device(self, k, q, k_new, v_new, out, events=None):
+        plan, slots, ctx, _, tables = self._dv[k]
+        ops.cache_append(k_new, v_new, slots, self.k_cache, self.v_cache)
         if events is not None:
             events[0].record()
-        out = ops.paged_decode(q, self.k_cache, self.v_cache, self.tables_d, self.ctx_d, self.max_context_len,
-                               self.scale, out=out, partition_size=self.partition_size, workspace=self.workspace)
+        if self.bf16:
+            out = ops.paged_decode_planned(q, self.k_cache, self.v_cache, tables, ctx, self.max_context_len,
+                                           self.scale, out, plan, self.workspace, self.partition_size)
+        else:
+            out = ops.paged_decode(q, self.k_cache, self.v_cache, tables, ctx, self.max_context_len, self.scale,
+                                   out=out, partition_size=self.partition_size, workspace=self.workspace)
         if events is not None:
             events[1].record()
         return out
@@ -127,52 +176,60 @@ class ServingEngine:
         """One decode step for every sequence: q ``[S, H, D]``, k_new/v_new
         ``[S, Hkv, D]`` on the device.  Returns ``out [S, H, D]``.
         ``events`` (a pair of CUDA events) are recorded around the decode."""
-        self._reserve()
-        self.launches += self._per_step
-        return self._device(q, k_new, v_new, out, events)
+        if out is None:
+            out = torch.empty_like(q)
+        self._prepare()
+        out = self._device(self.k, q, k_new, v_new, out, events)
+        self._finish()
+        return out
 
-    def capture(self, events=None) -> torch.cuda.CUDAGraph:
-        """Capture the device part of a step (reading ``q_in``, ``k_in``,
-        ``v_in``, writing ``out``) as a CUDA graph.  Call after at least one
-        eager :meth:`step`.  ``events``, if given, are recorded around the
-        decode at every replay (timing events created with ``external``)."""
+    def capture(self, events=None, inputs=None) -> StepGraphs:
+        """Capture the main-stream part of a step (append, decode, merge) as
+        CUDA graphs, one per device buffer.  ``inputs`` = (q, k_new, v_new,
+        out) device tensors the graphs read and write (default: the
+        engine's staging buffers ``q_in, k_in, v_in, out``).  ``events``, if
+        given, are recorded around the decode at every replay (timing events
+        created with ``external``).  Call after at least one eager step."""
         if not graphs_supported():
             raise RuntimeError("this torch cannot record events inside a CUDA graph")
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
+        q, kn, vn, out = inputs if inputs is not None else (self.q_in, self.k_in, self.v_in, self.out)
         if self._pool is None:
             self._pool = torch.cuda.graph_pool_handle()
-        with torch.cuda.graph(g, pool=self._pool):
-            self._device(self.q_in, self.k_in, self.v_in, self.out, events)
         torch.cuda.synchronize()
-        return g
+        graphs = []
+        for k in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, pool=self._pool):
+                self._device(k, q, kn, vn, out, events)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return StepGraphs(graphs)
 
-    def replay(self, graph: torch.cuda.CUDAGraph, q=None, k_new=None, v_new=None) -> torch.Tensor:
-        """One step through a captured graph.  New tokens given here are
-        copied into the staging buffers first (they may already be there)."""
-        self._reserve()
+    def replay(self, graphs: StepGraphs, q=None, k_new=None, v_new=None) -> torch.Tensor:
+        """One step through captured graphs.  New tokens given here are
+        copied into the staging buffers first (graphs captured on other
+        inputs need none)."""
+        self._prepare()
         for src, dst in ((q, self.q_in), (k_new, self.k_in), (v_new, self.v_in)):
             if src is not None and src.data_ptr() != dst.data_ptr():
                 dst.copy_(src, non_blocking=True)
-        graph.replay()
-        self.launches += self._per_step
+        graphs.graphs[self.k].replay()
+        self._finish()
         return self.out
 
     def step_host(self, q_h: torch.Tensor, k_h: torch.Tensor, v_h: torch.Tensor, out_h: torch.Tensor,
-                  graph: torch.cuda.CUDAGraph | None = None) -> torch.Tensor:
+                  graphs: StepGraphs | None = None) -> torch.Tensor:
         """Same step with host (pinned) inputs and output: the new tokens are
-        copied into the staging buffers, the output back to ``out_h``."""
-        if graph is None:
-            self.q_in.copy_(q_h, non_blocking=True)
-            self.k_in.copy_(k_h, non_blocking=True)
-            self.v_in.copy_(v_h, non_blocking=True)
-            self.step(self.q_in, self.k_in, self.v_in, out=self.out)
+        copied into the staging buffers, the output back to ``out_h``.
+        ``graphs`` must have been captured on the staging buffers."""
+        self._prepare()
+        self.q_in.copy_(q_h, non_blocking=True)
+        self.k_in.copy_(k_h, non_blocking=True)
+        self.v_in.copy_(v_h, non_blocking=True)
+        if graphs is None:
+            self._device(self.k, self.q_in, self.k_in, self.v_in, self.out)
         else:
-            self._reserve()
-            self.q_in.copy_(q_h, non_blocking=True)
-            self.k_in.copy_(k_h, non_blocking=True)
-            self.v_in.copy_(v_h, non_blocking=True)
-            graph.replay()
-            self.launches += self._per_step
+            graphs.graphs[self.k].replay()
+        self._finish()
         out_h.copy_(self.out, non_blocking=True)
         return out_h

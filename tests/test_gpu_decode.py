@@ -83,6 +83,31 @@ def test_many_items_per_cta_wrap_the_pipeline(pa):
     assert pa.get_status() == 0
 
 
+@pytest.mark.parametrize("name", ["gqa_prefix_small", "serving_b8_small", "long_small"])
+def test_host_plan_gives_identical_output(pa, name):
+    """pa_decode_planned with the host-built work list equals pa_decode
+    (device-built list) bit for bit: every item is computed the same way
+    whichever CTA takes it, and partitions merge in a fixed order."""
+    from paged_kv_cache_216_gb300 import ops
+
+    w = SMALL[name]
+    case = make_decode_case(w)
+    p = ops.decode_partition_size(w.num_seqs, w.num_kv_heads, case.max_ctx, 64)
+    ref = ops.paged_decode(case.q_d, case.k_cache, case.v_cache, case.tables_d, case.ctx_d, case.max_ctx, w.scale,
+                           partition_size=p)
+    plan_h = np.zeros(ops.decode_plan_bytes(w.num_seqs, case.max_ctx, p), dtype=np.uint8)
+    ops.decode_plan_host(case.ctx, case.max_ctx, p, plan_h)
+    ws = ops.decode_workspace(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, case.max_ctx, p)
+    out = torch.empty_like(case.q_d)
+    for _ in range(2):  # a fresh copy of the list each call
+        plan_d = torch.from_numpy(plan_h).cuda()
+        ops.paged_decode_planned(case.q_d, case.k_cache, case.v_cache, case.tables_d, case.ctx_d, case.max_ctx,
+                                 w.scale, out, plan_d, ws, p)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert pa.get_status() == 0
+
+
 def test_split_and_unsplit_agree(pa):
     w = SMALL["long_small"]
     case = make_decode_case(w)

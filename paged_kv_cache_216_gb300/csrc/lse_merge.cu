@@ -8,14 +8,19 @@
 // the same value the unsplit softmax(q Kᵀ) V of "PagedAttention Kernel：
 // 大模型推理优化的显存管理革新" section 3.1 gives, up to rounding.
 //
-// One warp per (sequence, query head); lanes hold D/32 consecutive dims, so
-// each partial row is read as one coalesced 4*D-byte line.  Sequences that
-// fit one partition were written by the decode kernel and are skipped.
-// Launched with programmatic dependent launch: the CTAs may start while the
-// decode kernel drains and wait for its results with griddepcontrol.wait.
+// Each (sequence, query head) gets `wpr` warps (8 for contexts of 32 or more
+// partitions, else 1) and a CTA of eight warps serves 8 / wpr of
+// them; warp w of a group folds partitions w, w + wpr, ... into a running
+// (max, sum, O) with online rescaling, lanes holding D/32 consecutive dims
+// so each partial row is one coalesced 4*D-byte line, and the group's warps
+// are combined through shared memory.  Sequences that fit one partition were written by the decode
+// kernel and are skipped.  Launched with programmatic dependent launch: the
+// CTAs may start while the decode kernel drains and wait for its results
+// with griddepcontrol.wait.
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "device_common.cuh"
@@ -24,48 +29,73 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kMaxWarps = 8;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeArgs p, int wpr) {
   constexpr int E = D / 32;
+  __shared__ float s_m[kMaxWarps], s_l[kMaxWarps];
+  __shared__ __align__(16) float s_o[kMaxWarps][D];
   pdl_wait_primary();
-  const int lane = threadIdx.x & 31;
-  const long long wid = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (wid >= (long long)p.S * p.H) return;
-  const int s = (int)(wid / p.H);
-  const int h = (int)(wid - (long long)s * p.H);
-  const int ctx = min(max(p.context_lens[s], 0), p.max_ctx);
-  const int np = (ctx + p.P - 1) / p.P;
-  if (np <= 1) return;
-  const size_t base = (size_t)s * p.max_parts * p.H + h;  // index of partition 0
-  float M = -INFINITY;
-  for (int pp = lane; pp < np; pp += 32) M = fmaxf(M, p.ws_ml[base + (size_t)pp * p.H].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.f, acc[E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long sh = (long long)blockIdx.x * (kMaxWarps / wpr) + warp / wpr;
+  const int wg = warp % wpr;  // warp within its (sequence, head) group
+  int s = 0, h = 0, np = 0;
+  if (sh < (long long)p.S * p.H) {
+    s = (int)(sh / p.H);
+    h = (int)(sh - (long long)s * p.H);
+    const int ctx = min(max(p.context_lens[s], 0), p.max_ctx);
+    np = (ctx + p.P - 1) / p.P;
+  }
+  float m = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  if (np > 1) {
+    const size_t base = (size_t)s * p.max_parts * p.H + h;  // row of partition 0
 #pragma unroll 4
-  for (int pp = 0; pp < np; ++pp) {
-    const size_t wi = base + (size_t)pp * p.H;
-    const float2 ml = p.ws_ml[wi];
-    const float wt = exp2f(ml.x - M);
-    L += wt * ml.y;
-    const float* src = p.ws_o + wi * D + lane * E;
-    if constexpr (E == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(src);
-      acc[0] += wt * x.x;
-      acc[1] += wt * x.y;
-      acc[2] += wt * x.z;
-      acc[3] += wt * x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(src);
-      acc[0] += wt * x.x;
-      acc[1] += wt * x.y;
+    for (int pp = wg; pp < np; pp += wpr) {
+      const size_t wi = base + (size_t)pp * p.H;
+      const float2 ml = p.ws_ml[wi];
+      float x[E];
+      if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p.ws_o + wi * D + lane * E);
+        x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(p.ws_o + wi * D + lane * E);
+        x[0] = v.x, x[1] = v.y;
+      }
+      const float mn = fmaxf(m, ml.x);
+      const float a = exp2f(m - mn), b = exp2f(ml.x - mn);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + x[e] * b;
+      l = l * a + ml.y * b;
+      m = mn;
     }
   }
-  const float inv = 1.f / L;
+  if (wpr > 1) {  // combine the group's warps through shared memory
+    if (lane == 0) {
+      s_m[warp] = m;
+      s_l[warp] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) s_o[warp][lane * E + e] = acc[e];
+    __syncthreads();
+    if (wg != 0 || np <= 1) return;
+    float M = -INFINITY;
+    for (int w = warp; w < warp + wpr; ++w) M = fmaxf(M, s_m[w]);
+    l = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int w = warp; w < warp + wpr; ++w) {
+      const float wt = exp2f(s_m[w] - M);  // a warp without partitions has max -inf: weight 0
+      l += wt * s_l[w];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += wt * s_o[w][lane * E + e];
+    }
+  } else if (np <= 1) {
+    return;
+  }
+  const float inv = 1.f / l;
   T* dst = static_cast<T*>(p.out) + ((size_t)s * p.H + h) * D + lane * E;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -78,10 +108,14 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const DecodeArgs
 
 template <typename T, int D>
 cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
-  const long long warps = (long long)a.S * a.H;
+  // Warps per (sequence, head): enough to keep several partial rows in
+  // flight for the longest context without idling warps on short ones.
+  const int wpr = a.max_parts >= 32 ? 8 : 1;
+  const long long pairs = (long long)a.S * a.H;
+  const int per_cta = kMaxWarps / wpr;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((warps + kWarps - 1) / kWarps));
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.gridDim = dim3((unsigned)((pairs + per_cta - 1) / per_cta));
+  cfg.blockDim = dim3(kMaxWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -89,7 +123,7 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a, wpr);
 }
 
 }  // namespace

@@ -205,7 +205,9 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     w = workload_for(args.workload, rank)
     K, W = args.steps, args.warmup
-    total_steps = W + 2 * K  # device-resident run, then the end-to-end run
+    Kp = K + (K % 2)  # untimed pass that launches every per-step graph once (even: same buffer parity)
+    # warm-up, graph warm-up, timed run, roofline warm-up, roofline run, end-to-end run
+    total_steps = W + 2 + K + Kp + K + K
     ctx0 = context_lens(w)
     nb = pool_blocks(w, ctx0, extra_steps=total_steps) + w.prefix_share
     order = free_order(w, nb)
@@ -225,35 +227,48 @@ def run_ours(args, rank, world, local):
     eng = pa.ServingEngine(k_cache, v_cache, alloc, seq_ids, w.num_heads, w.scale,
                            int(ctx0.max()) + total_steps, w.partition_size)
     toks = _host_tokens(w, total_steps)
-    dev_toks = [tuple(to_dev(x) for x in t) for t in toks[: W + K]]
+    n_dev = W + 2 + K + Kp + K
+    dev_toks = [tuple(to_dev(x) for x in t) for t in toks[:n_dev]]
+    packed = [eng.pack_tokens(*t) for t in dev_toks]  # each step's new tokens, resident in HBM
     out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=k_cache.dtype, device=dev)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    ctx_bytes0 = kv_bytes(ctx0, w)
     flush = None
-    if ctx_bytes0 < 2 * l2:
+    if kv_bytes(ctx0, w) < 2 * l2:
         flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device=dev)
+    step = 0  # steps done so far; step j decodes contexts ctx0 + j + 1
 
     # warm-up (eager steps; they also initialise the library's per-device state)
     for i in range(W):
         if flush is not None:
             flush.add_(1)
-        eng.step(*dev_toks[i], out=out)
+        eng.step(*dev_toks[step], out=out)
+        step += 1
     torch.cuda.synchronize()
 
-    # Device-resident run: K steps.  With graph support every step replays a
-    # captured graph of its device part, with timing events around the
-    # decode recorded inside the graph; otherwise steps run eagerly.
+    # Timed run: K steps.  With graph support the main-stream part of a step
+    # (append, decode, merge) replays a captured CUDA graph, one per device
+    # buffer, reading the step's new tokens from staging buffers that the
+    # upload stream fills while the previous step decodes; else steps run
+    # eagerly.
     from paged_kv_cache_216_gb300.serving import _event, graphs_supported
 
     use_graphs = graphs_supported() and not args.eager
-    dec_ev = [(_event(True), _event(True)) for _ in range(K)]
-    graphs = ([eng.capture(events=dec_ev[i], inputs=(*dev_toks[W + i], out)) for i in range(K)]
-              if use_graphs else None)
+    par = eng.capture() if use_graphs else None
+
+    def run_step(i, graphs=None, events=None):
+        if use_graphs:
+            eng.replay(graphs if graphs is not None else par, packed=packed[i])
+        else:
+            eng.step(*dev_toks[i], out=out, events=events)
+
+    for _ in range(2):  # launch each graph once before timing
+        run_step(step)
+        step += 1
+    torch.cuda.synchronize()
+    T0 = step
+    bytes_steps = [kv_bytes(ctx0 + T0 + i + 1, w) for i in range(K)]
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    # every step adds one token to every sequence: step i of the timed run
-    # decodes contexts ctx0 + W + i + 1
-    bytes_steps = [kv_bytes(ctx0 + W + i + 1, w) for i in range(K)]
     launches0 = eng.launches
     clocks = ClockSampler(local)
     barrier(world)
@@ -262,64 +277,84 @@ def run_ours(args, rank, world, local):
     if flush is None:
         step_ev[0][0].record(stream)
         for i in range(K):
-            if use_graphs:
-                eng.replay(graphs[i])
-            else:
-                eng.step(*dev_toks[W + i], out=out, events=dec_ev[i])
+            run_step(T0 + i)
         step_ev[-1][1].record(stream)
     else:
         for i in range(K):
             flush.add_(1)
             step_ev[i][0].record(stream)
-            if use_graphs:
-                eng.replay(graphs[i])
-            else:
-                eng.step(*dev_toks[W + i], out=out, events=dec_ev[i])
+            run_step(T0 + i)
             step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
     launches = eng.launches - launches0
     clk = clocks.stop()
-    assert np.array_equal(eng.ctx_h.numpy(), ctx0 + W + K)
+    step += K
+    assert np.array_equal(eng.ctx_h.numpy(), ctx0 + step)
     if flush is None:
         t_dev = step_ev[0][0].elapsed_time(step_ev[-1][1]) / 1e3
     else:
         t_dev = sum(a.elapsed_time(b) for a, b in step_ev) / 1e3
-    t_dec = [a.elapsed_time(b) / 1e3 for a, b in dec_ev]
     local_bytes = float(sum(bytes_steps))
     t_max = allreduce_max(t_dev, world)
     total_bytes = allreduce_sum(local_bytes, world)
     value = total_bytes / t_max / 1e9
     tokens_s = allreduce_sum(float(w.num_seqs * K), world) / t_max
 
+    # Roofline run: K more steps, each replaying its own graph whose timing
+    # events bracket the decode (events inside a graph add a few us per
+    # step, so the timed run above goes without them); every graph is
+    # launched once first.
+    dec_ev = [(_event(True), _event(True)) for _ in range(K)]
+    if use_graphs:
+        gsteps = [eng.capture(events=dec_ev[i], parity=(step + Kp + i) % 2) for i in range(K)]
+        for i in range(Kp):
+            if i < K and gsteps[i].graphs[eng.k] is not None:
+                run_step(step + i, gsteps[i])
+            else:
+                run_step(step + i)
+    else:
+        gsteps = [None] * K
+        for i in range(Kp):
+            run_step(step + i)
+    step += Kp
+    R0 = step
+    dec_bytes = sum(kv_bytes(ctx0 + R0 + i + 1, w) for i in range(K)) / K
+    torch.cuda.synchronize()
+    for i in range(K):
+        run_step(R0 + i, gsteps[i], events=dec_ev[i])
+    torch.cuda.synchronize()
+    step += K
+    t_dec = [a.elapsed_time(b) / 1e3 for a, b in dec_ev]
+
     # end-to-end run: host (pinned) tokens in, host output back, every step
-    pin = [tuple(torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if x.dtype == np.uint16 else x)
-                 .pin_memory() for x in t) for t in toks[W + K:]]
-    if w.dtype == "bf16":
-        pin = [tuple(x.view(torch.bfloat16) for x in t) for t in pin]
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    def host(x):
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if x.dtype == np.uint16 else x)
+        return t.view(torch.bfloat16) if x.dtype == np.uint16 else t
+
+    pin = [eng.pack_tokens(*(host(x) for x in t), pin=True) for t in toks[step:step + K]]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()  # every step's output lands here
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g_host = eng.capture() if use_graphs else None
-    e2e_bytes = sum(kv_bytes(ctx0 + W + K + i + 1, w) for i in range(K))
+    e2e_bytes = sum(kv_bytes(ctx0 + step + i + 1, w) for i in range(K))
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
     for i in range(K):
         if flush is not None:
             flush.add_(1)
-        eng.step_host(*pin[i], out_h, graphs=g_host)
+        eng.step_host(out_h=out_h, graphs=par, packed=pin[i])
+    stream.wait_stream(eng.down_stream)  # the last output copy is part of the timed region
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t_e2e = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = allreduce_sum(float(e2e_bytes), world) / t_e2e / 1e9
-    h2d = sum(x.numel() * x.element_size() for x in pin[0])
+    h2d = pin[0].numel() * pin[0].element_size()
     d2h = out_h.numel() * out_h.element_size()
 
     # roofline of the decode call (main kernel + its merge), from the live events
     dec_avg = sum(t_dec) / len(t_dec)
-    dec_bytes = sum(bytes_steps) / len(bytes_steps)
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
@@ -338,12 +373,12 @@ def run_ours(args, rank, world, local):
             "workload": w.name, "batch": w.num_seqs, "query_heads": w.num_heads, "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": eng.partition_size,
             "context_start_mean": float(ctx0.mean()), "context_start_max": int(ctx0.max()),
-            "kv_bytes_per_step": int(dec_bytes),
+            "kv_bytes_per_step": int(local_bytes / K),
             "l2": ("flushed before every step" if flush is not None else
-                   f"inputs larger than L2 ({dec_bytes / 1e9:.2f} GB KV per step vs {l2 / 1e6:.0f} MB L2)"),
+                   f"inputs larger than L2 ({local_bytes / K / 1e9:.2f} GB KV per step vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}",
-            "launch": ("uploads on a side stream; append+decode+merge as a CUDA graph per step"
-                       if use_graphs else "uploads on a side stream; eager launches"),
+            "launch": ("tables and new tokens uploaded on a side stream; append+decode+merge replayed as a "
+                       "CUDA graph per device buffer" if use_graphs else "uploads on a side stream; eager launches"),
         },
         "decode_tokens_per_s": round(tokens_s, 1),
         "wall_s": round(wall, 4),
@@ -353,7 +388,8 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "paged_decode_tc_kernel + lse_merge_kernel",
-                     "peak_source": f"{peak_src} hbm_gbs", "decode_ms": round(dec_avg * 1e3, 4)},
+                     "peak_source": f"{peak_src} hbm_gbs", "decode_ms": round(dec_avg * 1e3, 4),
+                     "timing": f"CUDA events inside each step's graph, {K} steps after the timed run"},
         "clocks": clk,
     }
     return res, eng, w

@@ -20,6 +20,10 @@ namespace {
 __global__ void cache_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                     const int64_t* __restrict__ slots, int T, uint4* k_cache, uint4* v_cache,
                                     long long num_slots, int Hkv, int B, int vpr, unsigned* status) {
+  // A decode launched right after this kernel (programmatic dependent
+  // launch) may start its prologue now; it reads the cache only after
+  // griddepcontrol.wait, i.e. after this kernel has completed.
+  pdl_launch_dependents();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long per_tok = (long long)Hkv * vpr;
   if (idx >= (long long)T * per_tok) return;

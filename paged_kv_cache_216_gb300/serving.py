@@ -105,11 +105,19 @@ class ServingEngine:
         self.launches = 0  # kernels this engine has launched
         self.split = -(-self.max_context_len // self.partition_size) > 1
         self._per_step = 2 + (1 if self.split else 0)  # append + decode (+ merge)
-        # staging buffers for steps whose inputs come from elsewhere
-        self.q_in = torch.empty((s, num_heads, d), dtype=k_cache.dtype, device=dev)
-        self.k_in = torch.empty((s, hkv, d), dtype=k_cache.dtype, device=dev)
-        self.v_in = torch.empty((s, hkv, d), dtype=k_cache.dtype, device=dev)
-        self.out = torch.empty((s, num_heads, d), dtype=k_cache.dtype, device=dev)
+        # staging buffers (one set per device buffer) for steps whose inputs
+        # come from elsewhere, and the streams/events of host transfers
+        # staging per device buffer: the step's new tokens packed as [q | k | v]
+        self._nq, self._nk = s * num_heads * d, s * hkv * d
+        self._stg = [torch.empty(self._nq + 2 * self._nk, dtype=k_cache.dtype, device=dev) for _ in range(2)]
+        self.q_in = [x[:self._nq].view(s, num_heads, d) for x in self._stg]
+        self.k_in = [x[self._nq:self._nq + self._nk].view(s, hkv, d) for x in self._stg]
+        self.v_in = [x[self._nq + self._nk:].view(s, hkv, d) for x in self._stg]
+        self.out = [torch.empty((s, num_heads, d), dtype=k_cache.dtype, device=dev) for _ in range(2)]
+        self.down_stream = torch.cuda.Stream(device=dev)
+        self._tok_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self._step_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self._out_read = [torch.cuda.Event(), torch.cuda.Event()]
         self._pool = None
 
     def _views(self, buf):
@@ -183,21 +191,26 @@ class ServingEngine:
         self._finish()
         return out
 
-    def capture(self, events=None, inputs=None) -> StepGraphs:
+    def capture(self, events=None, inputs=None, parity=None) -> StepGraphs:
         """Capture the main-stream part of a step (append, decode, merge) as
-        CUDA graphs, one per device buffer.  ``inputs`` = (q, k_new, v_new,
-        out) device tensors the graphs read and write (default: the
-        engine's staging buffers ``q_in, k_in, v_in, out``).  ``events``, if
-        given, are recorded around the decode at every replay (timing events
-        created with ``external``).  Call after at least one eager step."""
+        CUDA graphs, one per device buffer (or only for device buffer
+        ``parity``).  ``inputs`` = (q, k_new, v_new, out) device tensors the
+        graphs read and write (default: the engine's staging buffers of each
+        device buffer).  ``events``, if given, are recorded around the
+        decode at every replay (timing events created with ``external``).
+        Call after at least one eager step."""
         if not graphs_supported():
             raise RuntimeError("this torch cannot record events inside a CUDA graph")
-        q, kn, vn, out = inputs if inputs is not None else (self.q_in, self.k_in, self.v_in, self.out)
         if self._pool is None:
             self._pool = torch.cuda.graph_pool_handle()
         torch.cuda.synchronize()
         graphs = []
         for k in range(2):
+            if parity is not None and k != parity:
+                graphs.append(None)
+                continue
+            q, kn, vn, out = inputs if inputs is not None else (self.q_in[k], self.k_in[k], self.v_in[k],
+                                                                self.out[k])
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, pool=self._pool):
                 self._device(k, q, kn, vn, out, events)
@@ -205,31 +218,63 @@ class ServingEngine:
         torch.cuda.synchronize()
         return StepGraphs(graphs)
 
-    def replay(self, graphs: StepGraphs, q=None, k_new=None, v_new=None) -> torch.Tensor:
-        """One step through captured graphs.  New tokens given here are
-        copied into the staging buffers first (graphs captured on other
-        inputs need none)."""
-        self._prepare()
-        for src, dst in ((q, self.q_in), (k_new, self.k_in), (v_new, self.v_in)):
-            if src is not None and src.data_ptr() != dst.data_ptr():
-                dst.copy_(src, non_blocking=True)
-        graphs.graphs[self.k].replay()
-        self._finish()
-        return self.out
+    def pack_tokens(self, q, k_new, v_new, pin: bool = False) -> torch.Tensor:
+        """One step's new tokens packed as the staging layout [q | k | v]
+        (on the device, or in pinned host memory with ``pin``): a packed
+        step is staged with a single copy."""
+        flat = torch.cat([q.reshape(-1), k_new.reshape(-1), v_new.reshape(-1)])
+        return flat.pin_memory() if pin else flat
 
-    def step_host(self, q_h: torch.Tensor, k_h: torch.Tensor, v_h: torch.Tensor, out_h: torch.Tensor,
-                  graphs: StepGraphs | None = None) -> torch.Tensor:
-        """Same step with host (pinned) inputs and output: the new tokens are
-        copied into the staging buffers, the output back to ``out_h``.
+    def _stage(self, k, q=None, k_new=None, v_new=None, packed=None) -> None:
+        """Copy the step's new tokens (device or pinned host tensors; one
+        packed tensor or three) into staging buffer k on the upload stream,
+        after the step's tables, and make the main stream wait for them: the
+        copies overlap the previous step's decode."""
+        with torch.cuda.stream(self.up_stream):
+            if packed is not None:
+                self._stg[k].copy_(packed, non_blocking=True)
+            for src, dst in ((q, self.q_in[k]), (k_new, self.k_in[k]), (v_new, self.v_in[k])):
+                if src is not None and src.data_ptr() != dst.data_ptr():
+                    dst.copy_(src, non_blocking=True)
+            self._tok_done[k].record(self.up_stream)
+        main = torch.cuda.current_stream()
+        main.wait_event(self._tok_done[k])
+        main.wait_event(self._out_read[k])  # the copy-out of the step that last wrote out[k]
+
+    def replay(self, graphs: StepGraphs, q=None, k_new=None, v_new=None, packed=None) -> torch.Tensor:
+        """One step through captured graphs, reading the new tokens from the
+        staging buffers (copied there first when given here, as three
+        tensors or one from :meth:`pack_tokens`).  Returns the output buffer
+        the graph wrote."""
+        if graphs.graphs[self.k] is None:
+            raise ValueError("these graphs were captured for the other device buffer")
+        self._prepare()
+        k = self.k
+        self._stage(k, q, k_new, v_new, packed)
+        graphs.graphs[k].replay()
+        self._finish()
+        return self.out[k]
+
+    def step_host(self, q_h=None, k_h=None, v_h=None, out_h: torch.Tensor | None = None,
+                  graphs: StepGraphs | None = None, packed=None) -> torch.Tensor:
+        """Same step with host (pinned) inputs and output: three tensors, or
+        one packed by :meth:`pack_tokens` (``pin=True``).  The new tokens are
+        copied on the upload stream after the step's tables, the output
+        back on a third stream once the step is done, so both transfers
+        overlap neighbouring steps; synchronize before reading ``out_h``.
         ``graphs`` must have been captured on the staging buffers."""
         self._prepare()
-        self.q_in.copy_(q_h, non_blocking=True)
-        self.k_in.copy_(k_h, non_blocking=True)
-        self.v_in.copy_(v_h, non_blocking=True)
+        k = self.k
+        self._stage(k, q_h, k_h, v_h, packed)
+        main = torch.cuda.current_stream()
         if graphs is None:
-            self._device(self.k, self.q_in, self.k_in, self.v_in, self.out)
+            self._device(k, self.q_in[k], self.k_in[k], self.v_in[k], self.out[k])
         else:
-            graphs.graphs[self.k].replay()
+            graphs.graphs[k].replay()
         self._finish()
-        out_h.copy_(self.out, non_blocking=True)
+        self._step_done[k].record(main)
+        self.down_stream.wait_event(self._step_done[k])
+        with torch.cuda.stream(self.down_stream):
+            out_h.copy_(self.out[k], non_blocking=True)
+            self._out_read[k].record(self.down_stream)
         return out_h

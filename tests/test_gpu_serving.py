@@ -143,7 +143,7 @@ def test_serving_graph_replay_matches_oracle(pa):
     ncow = 0
     for step in range(steps):
         q, k, v = serving_step_tokens(w, step)
-        out = eng.replay(graph, to_dev(q), to_dev(k), to_dev(v))
+        out = eng.replay(graph, to_dev(q), to_dev(k), to_dev(v)).clone()
         slots, pairs, ref = orc.step(q, k, v, eng.width)
         ncow += len(pairs)
         torch.cuda.synchronize()
@@ -153,4 +153,40 @@ def test_serving_graph_replay_matches_oracle(pa):
         assert np.array_equal(to_bits(eng.v_cache), orc.v_cache)
         assert_close(out, ref, "bf16", f"graph step {step}")
     assert ncow == 1
+    assert pa.get_status() == 0
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_serving_host_buffers_match_oracle(pa, use_graph):
+    """Steps driven from pinned host buffers (tokens uploaded on the side
+    stream, output copied back on a third) give the oracle's outputs."""
+    from paged_kv_cache_216_gb300.serving import graphs_supported
+
+    if use_graph and not graphs_supported():
+        pytest.skip("this torch cannot record events inside a CUDA graph")
+    w = WORKLOADS["serving_bf16_b16"].replace(num_seqs=5, num_heads=16, num_kv_heads=4, ctx_mean=300.0,
+                                              ctx_hi=1200)
+    steps = 5
+    eng, orc = _engine_and_oracle(pa, w, steps + 1)  # + the eager first step
+    q0, k0, v0 = serving_step_tokens(w, 99)
+    eng.step(to_dev(q0), to_dev(k0), to_dev(v0))  # an eager step first
+    orc.step(q0, k0, v0, eng.width, seqs=[])
+    graphs = eng.capture() if use_graph else None
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    outs, refs = [], []
+    for step in range(steps):
+        q, k, v = serving_step_tokens(w, step)
+        out_h = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16).pin_memory()
+        if use_graph:  # one packed host buffer per step
+            eng.step_host(out_h=out_h, graphs=graphs, packed=eng.pack_tokens(pinned(q), pinned(k), pinned(v), pin=True))
+        else:
+            eng.step_host(pinned(q), pinned(k), pinned(v), out_h, graphs=graphs)
+        outs.append(out_h)
+        refs.append(orc.step(q, k, v, eng.width)[2])
+    torch.cuda.synchronize()
+    for step, (o, r) in enumerate(zip(outs, refs)):
+        assert_close(o, r, "bf16", f"host step {step}")
     assert pa.get_status() == 0

@@ -12,7 +12,7 @@
 //  * Persistent CTAs, two per SM.  Work items are (sequence, partition, KV
 //    head) triples taken from a longest-first work list (decode_plan.cu)
 //    through an atomic counter, the dynamic work queue of the same page's
-//    section 3.2; the producer claims items two ahead of use.
+//    section 3.2; the producer claims the next item as it starts one.
 //  * Warp 4 is the producer.  For each item it writes the item's descriptor
 //    and bulk-copies its g query rows into a 2-slot Q ring, then streams the item's keys and values
 //    32 tokens at a time into a ring of shared-memory stages: per cache block
@@ -130,26 +130,22 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
   pdl_wait_primary();  // the work list is complete and visible from here on
   const int total = __ldcg(&p.hdr->num_pairs) * p.Hkv;
   unsigned* counter = &p.hdr->counter;
-  // Lane 0 claims work items two ahead of use, so that the atomic and the
-  // read of the list entry are off the critical path.
-  int cur_idx = total, nxt_idx = total;
+  // Lane 0 claims the next work item when it starts the current one and
+  // reads that item's list entry once the current item's first chunk is on
+  // its way, so the atomic and the read overlap the copies.  Holding only
+  // one item ahead keeps the tail of the queue balanced across CTAs.
+  int cur_idx = total;
   int2 cur_pr = make_int2(0, -1);
   if (lane == 0) {
     cur_idx = (int)atomicAdd(counter, 1u);
-    if (cur_idx < total) {
-      cur_pr = __ldcg(p.plan + cur_idx / p.Hkv);
-      nxt_idx = (int)atomicAdd(counter, 1u);
-    }
+    if (cur_idx < total) cur_pr = __ldcg(p.plan + cur_idx / p.Hkv);
   }
   uint32_t kseq = 0, nq = 0;
   bool ok = true;
   for (uint32_t n = 0;; ++n) {
     int2 nxt_pr = make_int2(0, -1);
-    int nn_idx = total;
-    if (lane == 0 && nxt_idx < total) {
-      nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
-      nn_idx = (int)atomicAdd(counter, 1u);
-    }
+    int nxt_idx = total;
+    if (lane == 0 && cur_idx < total) nxt_idx = (int)atomicAdd(counter, 1u);
     const int idx = __shfl_sync(kFull, cur_idx, 0);
     const int prx = __shfl_sync(kFull, cur_pr.x, 0);
     const int ctx = __shfl_sync(kFull, cur_pr.y, 0);
@@ -218,11 +214,12 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
           }
         }
       }
+      if (ch == 0 && lane == 0 && nxt_idx < total) nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
     }
     if (!ok) break;
+    if (nch == 0 && lane == 0 && nxt_idx < total) nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
     cur_idx = nxt_idx;
     cur_pr = nxt_pr;
-    nxt_idx = nn_idx;
   }
   if (!ok) {
     give_up(p, abort);

@@ -44,8 +44,16 @@ METRIC = "paged-decode KV-read GB/s"
 UNIT = "GB/s"
 
 
-def kv_bytes(ctx: np.ndarray, w) -> int:
-    return int(np.asarray(ctx, dtype=np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
+def kv_bytes(ctx: np.ndarray, w, groups=None, partition_size: int = 0) -> int:
+    """Algorithmic KV bytes of one decode step: every context token's key and
+    value row per KV head; with prefix groups, the tokens of a group's shared
+    partitions once for the whole group."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    tokens = int(ctx.sum())
+    for first, count, prefix in (groups or ()):
+        shared = np.minimum(ctx[first:first + count], prefix // partition_size * partition_size)
+        tokens -= int(shared.sum()) - int(shared.max())
+    return tokens * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
 
 
 DECODE_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_tc.cu", "paged_kv_cache_216_gb300/csrc/device_common.cuh",
@@ -224,8 +232,19 @@ def run_ours(args, rank, world, local):
     if len(pairs):
         pa.copy_blocks(k_cache, v_cache, to_dev(pairs))
     seq_ids = np.arange(w.num_seqs)
+    # the forked sequences share the prefix's whole blocks (its last, partly
+    # filled block was copied by each one's first append)
+    groups = None
+    if w.prefix_share and not args.no_prefix_groups:
+        groups = [(0, w.prefix_share, w.prefix_len // w.block_size * w.block_size)]
     eng = pa.ServingEngine(k_cache, v_cache, alloc, seq_ids, w.num_heads, w.scale,
-                           int(ctx0.max()) + total_steps, w.partition_size)
+                           int(ctx0.max()) + total_steps, w.partition_size, prefix_groups=groups)
+    if not eng.split:
+        groups = None  # one partition per context: no shared partitions
+
+    def step_bytes(ctx):
+        return kv_bytes(ctx, w, groups, eng.partition_size)
+
     toks = _host_tokens(w, total_steps)
     n_dev = W + 2 + K + Kp + K
     dev_toks = [tuple(to_dev(x) for x in t) for t in toks[:n_dev]]
@@ -267,7 +286,7 @@ def run_ours(args, rank, world, local):
         step += 1
     torch.cuda.synchronize()
     T0 = step
-    bytes_steps = [kv_bytes(ctx0 + T0 + i + 1, w) for i in range(K)]
+    bytes_steps = [step_bytes(ctx0 + T0 + i + 1) for i in range(K)]
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     launches0 = eng.launches
     clocks = ClockSampler(local)
@@ -320,7 +339,7 @@ def run_ours(args, rank, world, local):
             run_step(step + i)
     step += Kp
     R0 = step
-    dec_bytes = sum(kv_bytes(ctx0 + R0 + i + 1, w) for i in range(K)) / K
+    dec_bytes = sum(step_bytes(ctx0 + R0 + i + 1) for i in range(K)) / K
     torch.cuda.synchronize()
     for i in range(K):
         run_step(R0 + i, gsteps[i], events=dec_ev[i])
@@ -336,7 +355,7 @@ def run_ours(args, rank, world, local):
     pin = [eng.pack_tokens(*(host(x) for x in t), pin=True) for t in toks[step:step + K]]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()  # every step's output lands here
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_bytes = sum(kv_bytes(ctx0 + step + i + 1, w) for i in range(K))
+    e2e_bytes = sum(step_bytes(ctx0 + step + i + 1) for i in range(K))
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
@@ -374,6 +393,8 @@ def run_ours(args, rank, world, local):
             "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": eng.partition_size,
             "context_start_mean": float(ctx0.mean()), "context_start_max": int(ctx0.max()),
             "kv_bytes_per_step": int(local_bytes / K),
+            "prefix_groups": groups,
+            "kv_bytes_per_step_logical": int(sum(kv_bytes(ctx0 + T0 + i + 1, w) for i in range(K)) / K),
             "l2": ("flushed before every step" if flush is not None else
                    f"inputs larger than L2 ({local_bytes / K / 1e9:.2f} GB KV per step vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}",
@@ -387,7 +408,8 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode_tc_kernel + lse_merge_kernel",
+                     "kernel": ("paged_decode_tc_kernel (with shared-prefix items) + lse_merge_kernel" if groups
+                                else "paged_decode_tc_kernel + lse_merge_kernel"),
                      "peak_source": f"{peak_src} hbm_gbs", "decode_ms": round(dec_avg * 1e3, 4),
                      "timing": f"CUDA events inside each step's graph, {K} steps after the timed run"},
         "clocks": clk,
@@ -466,6 +488,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0, help="seconds of oracle time in the reference arm")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--eager", action="store_true", help="launch every step's kernels eagerly (no CUDA graph)")
+    ap.add_argument("--no-prefix-groups", action="store_true",
+                    help="decode prefix-sharing sequences one by one (no shared-prefix kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

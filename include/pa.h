@@ -195,6 +195,63 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache,
                       void* stream);
 
 /*
+ * Shared-prefix decode [Day6 paragraph 5: sequences forked from one prompt
+ * share its cache blocks].  The same result as pa_decode (and, with a plan,
+ * pa_decode_planned), but each block a group of sequences shares is read
+ * once per kMaxGroup / g members (8 query rows; 8 members for g = 1, 2 for
+ * g = 4) instead of once per member.
+ *   groups      host, [num_groups][3] int32: first sequence, number of
+ *               sequences, shared prefix length in tokens.  Group i is
+ *               sequences first .. first + count - 1 of the batch; the
+ *               ranges are ascending and disjoint; sequences in no group
+ *               are decoded as by pa_decode.  0 <= num_groups <=
+ *               PA_MAX_PREFIX_GROUPS; groups may be NULL when num_groups is 0.
+ * The caller guarantees that the first `prefix` tokens of every member are
+ * stored in the same physical blocks, listed in the table of the group's
+ * first sequence, and that prefix <= max_context_len.  The whole partitions
+ * of the prefix (floor(prefix / P) * P tokens, P the partition size) become
+ * shared work items of the decode kernel, each attending one partition for
+ * several members at once and storing their split-K partials; the members'
+ * other partitions are decoded as usual and the log-sum-exp merge combines
+ * them.  A member whose context ends inside the shared part is masked to
+ * its own length.  Groups whose prefix is shorter than one partition, and
+ * calls where no context spans two partitions, fall back to plain decode
+ * for those sequences.  bf16 only; the workspace is sized as for pa_decode.
+ */
+#define PA_MAX_PREFIX_GROUPS 64
+int pa_decode_shared_prefix(const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context_len,
+                            float scale, void* out, int num_seqs,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks,
+                            int partition_size, const int32_t* groups,
+                            int num_groups, void* workspace,
+                            size_t workspace_bytes, int dtype, void* stream);
+
+/* Host work list for pa_decode_planned_shared_prefix: the list of
+ * pa_decode_plan_host with the groups' shared partitions as shared items
+ * (same groups, head counts, partition size and lengths as the decode
+ * call). */
+int pa_decode_plan_host_shared_prefix(const int32_t* context_lens,
+                                      int num_seqs, int max_context_len,
+                                      int partition_size, int num_heads,
+                                      int num_kv_heads, const int32_t* groups,
+                                      int num_groups, void* plan);
+
+/* pa_decode_planned for prefix groups; `plan` from
+ * pa_decode_plan_host_shared_prefix with the same groups. */
+int pa_decode_planned_shared_prefix(
+    const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len, float scale, void* out,
+    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int partition_size, const int32_t* groups,
+    int num_groups, const void* plan, void* workspace, size_t workspace_bytes,
+    int dtype, void* stream);
+
+/*
  * Paged decode that allocates nothing: the same computation and arguments as
  * pa_decode, but the split-K scratch is a fixed device array inside this
  * library, so the caller passes no workspace.  The pages have no counterpart;
@@ -322,6 +379,14 @@ void pa_stepper_destroy(pa_stepper* st);
 int pa_stepper_prepare(pa_stepper* st, void* upload_stream, void* main_stream,
                        int* buffer_index, int* num_cow);
 int pa_stepper_finish(pa_stepper* st, void* main_stream);
+/* Prefix groups of the stepper's batch (as for pa_decode_shared_prefix,
+ * positions in seq_ids; copied) and the decode's head counts: work lists
+ * built by later prepare calls are those of
+ * pa_decode_plan_host_shared_prefix, for pa_decode_planned_shared_prefix.
+ * num_groups = 0 removes them. */
+int pa_stepper_set_prefix_groups(pa_stepper* st, const int32_t* groups,
+                                 int num_groups, int num_heads,
+                                 int num_kv_heads);
 
 #ifdef __cplusplus
 }

@@ -15,6 +15,7 @@ from .ops import (  # noqa: F401
     decode_workspace_bytes,
     get_status,
     paged_decode,
+    paged_decode_shared_prefix,
     paged_decode_static_workspace,
 )
 from .serving import ServingEngine  # noqa: F401

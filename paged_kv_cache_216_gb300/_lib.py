@@ -24,6 +24,9 @@ PA_STATUS_TIMEOUT = 8
 # Size of the library's fixed decode scratch array (pa_decode_static_workspace).
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
+# Most prefix groups one shared-prefix decode call takes.
+PA_MAX_PREFIX_GROUPS = 64
+
 _c_int, _c_i64, _c_sz, _c_f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 _vp = ctypes.c_void_p
 _pi32 = ctypes.POINTER(ctypes.c_int32)
@@ -46,6 +49,13 @@ SIGNATURES = {
                                    _c_int, _c_int, _c_int, _vp, _vp, _c_sz, _c_int, _vp]),
     "pa_decode_static_workspace": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
+    "pa_decode_shared_prefix": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
+                                         _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _c_sz, _c_int,
+                                         _vp]),
+    "pa_decode_plan_host_shared_prefix": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp]),
+    "pa_decode_planned_shared_prefix": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int,
+                                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
+                                                 _vp, _c_sz, _c_int, _vp]),
     "pa_alloc_create": (_c_int, [_c_int, _c_int, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_num_free": (_c_int, [_vp]),
@@ -64,6 +74,7 @@ SIGNATURES = {
     "pa_stepper_destroy": (None, [_vp]),
     "pa_stepper_prepare": (_c_int, [_vp, _vp, _vp, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "pa_stepper_finish": (_c_int, [_vp, _vp]),
+    "pa_stepper_set_prefix_groups": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int]),
 }
 
 ERRORS = {-1: "PA_ERR_INVALID", -2: "PA_ERR_UNSUPPORTED", -3: "PA_ERR_OOM", -4: "PA_ERR_STATE", -5: "PA_ERR_CUDA"}

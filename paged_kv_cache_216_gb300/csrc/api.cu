@@ -215,8 +215,8 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int 
 static int decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
                        void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                       int num_blocks, int partition_size, const void* plan, void* workspace,
-                       size_t workspace_bytes, int dtype, void* stream) {
+                       int num_blocks, int partition_size, const void* plan, const int32_t* groups,
+                       int num_groups, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
   const int es = elem_bytes(dtype);
   if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_context_len < 1 ||
@@ -248,6 +248,10 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   if (!aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace not 256-byte aligned");
   if (plan && dtype != PA_BF16) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_planned: bf16 only");
   if (plan && !aligned(plan, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode_planned: plan not 256-byte aligned");
+  if (num_groups != 0 && dtype != PA_BF16) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix: bf16 only");
+  pa::PrefixGroups pg;
+  int rc = pa_prefix_groups(groups, num_groups, num_seqs, max_context_len, P, &pg, "pa_decode_shared_prefix");
+  if (rc) return rc;
 
   pa::DecodeArgs a{};
   a.q = q;
@@ -264,7 +268,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     a.ws_o = reinterpret_cast<float*>(ws + wl.o);
     a.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   }
-  int rc = status_ptr(&a.status);
+  rc = status_ptr(&a.status);
   if (rc) return rc;
   a.S = num_seqs;
   a.H = num_heads;
@@ -278,6 +282,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   a.P = P;
   a.max_parts = (int)parts;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+  a.shared_items = pg.n > 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -289,7 +294,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
     rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
     if (rc) return rc;
     if (!plan) {
-      e = pa::launch_decode_plan(a, st);
+      e = pa::launch_decode_plan(a, pg, st);
       if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");
     }
     e = pa::launch_decode_tc(a, kmap, vmap, st);
@@ -298,7 +303,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   }
   if (e != cudaSuccess) return cuda_fail(e, "pa_decode launch");
   if (parts > 1) {
-    e = pa::launch_lse_merge(a, dtype, st);
+    e = pa::launch_lse_merge(a, pg, dtype, st);
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode merge launch");
   }
   return PA_OK;
@@ -313,7 +318,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
               int partition_size, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
   return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
                      out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
-                     nullptr, workspace, workspace_bytes, dtype, stream);
+                     nullptr, nullptr, 0, workspace, workspace_bytes, dtype, stream);
 }
 
 int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -324,7 +329,30 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache, c
   if (!plan) return pa_fail(PA_ERR_INVALID, "pa_decode_planned: null plan");
   return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
                      out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
-                     plan, workspace, workspace_bytes, dtype, stream);
+                     plan, nullptr, 0, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
+                            void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, int partition_size, const int32_t* groups, int num_groups,
+                            void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                     out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
+                     nullptr, groups, num_groups, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_planned_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context_len, float scale, void* out,
+                                    int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, int partition_size, const int32_t* groups, int num_groups,
+                                    const void* plan, void* workspace, size_t workspace_bytes, int dtype,
+                                    void* stream) {
+  if (!plan) return pa_fail(PA_ERR_INVALID, "pa_decode_planned_shared_prefix: null plan");
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                     out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
+                     plan, groups, num_groups, workspace, workspace_bytes, dtype, stream);
 }
 
 }  // extern "C"

@@ -8,6 +8,10 @@
 // the longest to the shortest, so that the last items handed out are the
 // shortest and no CTA is left with a long item at the end.
 //
+// Shared partitions of prefix groups (kernels.h) come first, as
+// shared-prefix items that each cover several members; the members' own
+// items for those partitions are left out.
+//
 // One CTA of 1024 threads.  It also validates the context lengths (status
 // bit, clamping); an empty context gets one entry of length 0 at the end of
 // the list, for which the decode kernel writes a zero output row.  It lets
@@ -53,7 +57,8 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t* __restrict__ context_lens, int S,
                                                                    int P, int max_ctx, PlanHeader* hdr, int2* plan,
-                                                                   unsigned* status) {
+                                                                   unsigned* status, int g,
+                                                                   const __grid_constant__ PrefixGroups pg) {
   pdl_launch_dependents();
   __shared__ int scratch[32];
   __shared__ int bucket_count[kBuckets];
@@ -71,16 +76,21 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
       raise_status(status, PA_STATUS_BAD_CONTEXT);
       c = c < 1 ? 0 : max_ctx;
     }
-    nfull += c / P;
+    const int skip = prefix_parts_of(pg, s);
+    nfull += max(0, c / P - skip);
     nempty += c == 0;
     const int rem = c % P;
-    if (rem) atomicAdd(&bucket_count[(int)((long long)(rem - 1) * kBuckets / P)], 1);
+    if (rem && c / P >= skip) atomicAdd(&bucket_count[(int)((long long)(rem - 1) * kBuckets / P)], 1);
   }
+  // Shared-prefix items: full partitions, at the head of the list.
+  const int npre = prefix_entries(pg, g);
+  for (int e = tid; e < npre; e += kPlanThreads) plan[e] = prefix_entry_at(pg, g, e);
   int total_full = 0;
-  int pos = block_exclusive_scan(nfull, scratch, &total_full);
+  int pos = npre + block_exclusive_scan(nfull, scratch, &total_full);
+  total_full += npre;
   for (int s = s0; s < s1; ++s) {
     int c = min(max(context_lens[s], 0), max_ctx);
-    for (int p = 0; p < c / P; ++p) plan[pos++] = make_int2(s | (p << 16), c);
+    for (int p = prefix_parts_of(pg, s); p < c / P; ++p) plan[pos++] = make_int2(s | (p << 16), c);
   }
   // Partial partitions: buckets from the longest remainder down.
   int total_partial = 0;
@@ -97,7 +107,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
       continue;
     }
     const int rem = c % P;
-    if (!rem) continue;
+    if (!rem || c / P < prefix_parts_of(pg, s)) continue;
     const int at = atomicAdd(&bucket_cursor[(int)((long long)(rem - 1) * kBuckets / P)], 1);
     plan[at] = make_int2(s | ((c / P) << 16), c);
   }
@@ -109,9 +119,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const int32_t
 
 }  // namespace
 
-cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_plan(const DecodeArgs& a, const PrefixGroups& pg, cudaStream_t stream) {
   decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.context_lens, a.S, a.P, a.max_ctx, a.hdr,
-                                                     const_cast<int2*>(a.plan), a.status);
+                                                     const_cast<int2*>(a.plan), a.status, a.g, pg);
   return cudaGetLastError();
 }
 

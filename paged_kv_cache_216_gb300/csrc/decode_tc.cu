@@ -115,7 +115,7 @@ __device__ __forceinline__ int stage_line(int t, int half) {
   return kInter ? 2 * t + half : half * kChunk + t;
 }
 
-template <int D, bool kInter>
+template <int D, bool kInter, bool kShared>
 __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& p, uint8_t* base,
                          volatile int* abort) {
   using C = TcCfg<D>;
@@ -148,7 +148,7 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
     if (lane == 0 && cur_idx < total) nxt_idx = (int)atomicAdd(counter, 1u);
     const int idx = __shfl_sync(kFull, cur_idx, 0);
     const int prx = __shfl_sync(kFull, cur_pr.x, 0);
-    const int ctx = __shfl_sync(kFull, cur_pr.y, 0);
+    const int ctx = __shfl_sync(kFull, cur_pr.y, 0);  // < 0: a shared-prefix item
     const int slot = n & 1;
     if (!mbar_wait(&bar.qempty[slot], ((n >> 1) & 1) ^ 1, abort)) {
       ok = false;
@@ -161,17 +161,26 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
       }
       break;
     }
-    const int s = prx & 0xffff, part = prx >> 16, kvh = idx % p.Hkv;
-    const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
+    // Table row ts; query rows of nm sequences s0 .. s0 + nm - 1 (one for
+    // ordinary items; a shared-prefix item covers a whole partition).
+    const bool shared = kShared && ctx < 0;
+    const int ts = prx & 0xffff, part = prx >> 16, kvh = idx % p.Hkv;
+    const int s0 = shared ? (ctx >> 4) & 0xffff : ts;
+    const int nm = shared ? ctx & 15 : 1;
+    const int t0 = part * p.P, t1 = shared ? t0 + p.P : min(ctx, t0 + p.P);
     if (lane == 0) {
-      desc[slot] = make_int4(s, part, kvh, ctx);
-      mbar_arrive_expect_tx(&bar.qfull[slot], qbytes);
-      const __nv_bfloat16* src =
-          static_cast<const __nv_bfloat16*>(p.q) + ((size_t)s * p.H + (size_t)kvh * p.g) * D;
-      bulk_load(base + C::kOffQ + slot * C::kQSlot, src, qbytes, &bar.qfull[slot]);
+      // a shared item's descriptor also carries its member count and a flag
+      const int dy = kShared ? part | (nm << 16) | (shared ? 1 << 20 : 0) : part;
+      desc[slot] = make_int4(s0, dy, kvh, shared ? t1 : ctx);
+      mbar_arrive_expect_tx(&bar.qfull[slot], (uint32_t)nm * qbytes);
+      for (int i = 0; i < nm; ++i) {
+        const __nv_bfloat16* src =
+            static_cast<const __nv_bfloat16*>(p.q) + ((size_t)(s0 + i) * p.H + (size_t)kvh * p.g) * D;
+        bulk_load(base + C::kOffQ + slot * C::kQSlot + i * qbytes, src, qbytes, &bar.qfull[slot]);
+      }
     }
     ++nq;
-    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq + t0 / p.B;
+    const int32_t* row = p.block_tables + (size_t)ts * p.max_blocks_per_seq + t0 / p.B;
     const int nblk = (t1 - t0 + p.B - 1) / p.B;
     int cur = load_block_id(row, lane, nblk);
     int nxt = load_block_id(row, 32 + lane, nblk);
@@ -231,7 +240,7 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
   }
 }
 
-template <int D, bool kInter>
+template <int D, bool kInter, bool kShared>
 __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort) {
   using C = TcCfg<D>;
   constexpr int KS = D / 16;  // k-steps of the Q·Kᵀ product
@@ -255,17 +264,22 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     }
     const int4 d = desc[slot];
     if (d.w < 0) return;  // no work left
-    const int s = d.x, part = d.y, kvh = d.z, ctx = d.w;
+    const int s0 = d.x, kvh = d.z, ctx = d.w;
+    const int part = kShared ? d.y & 0xffff : d.y, nm = kShared ? (d.y >> 16) & 15 : 1;
+    const bool shared = kShared && ((d.y >> 20) & 1);
     const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
     const int nch = (t1 - t0 + kChunk - 1) / kChunk;
-    const int np = (ctx + p.P - 1) / p.P;
+    const int np = shared ? 2 : (ctx + p.P - 1) / p.P;  // a shared item always leaves a partial
+    const int nrow = nm * p.g;                           // rows of S: (sequence, query head) pairs
+    // Tokens row gq attends: its own sequence's length on a shared item.
+    const int lim = !shared ? ctx : gq < nrow ? min(max(__ldg(p.context_lens + s0 + gq / p.g), 0), p.max_ctx) : 0;
     uint32_t qa[KS][2];
     {
       const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(base + C::kOffQ + slot * C::kQSlot);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qa[ks][0] = gq < p.g ? *reinterpret_cast<const uint32_t*>(sq + gq * D + ks * 16 + 2 * tq) : 0u;
-        qa[ks][1] = gq < p.g ? *reinterpret_cast<const uint32_t*>(sq + gq * D + ks * 16 + 8 + 2 * tq) : 0u;
+        qa[ks][0] = gq < nrow ? *reinterpret_cast<const uint32_t*>(sq + gq * D + ks * 16 + 2 * tq) : 0u;
+        qa[ks][1] = gq < nrow ? *reinterpret_cast<const uint32_t*>(sq + gq * D + ks * 16 + 8 + 2 * tq) : 0u;
       }
     }
     __syncwarp();
@@ -319,13 +333,15 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         }
       }
       // Online softmax (log2 domain) for head row gq over this chunk.
+      // tokens of the chunk row gq may attend
+      const int left = kShared ? min(nv, lim - (t0 + ch * kChunk)) : nv;
       float mx = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int tok = nt * 8 + 2 * tq + e;
-          const float v = tok < nv ? sc[nt][e] * p.scale_log2 : -INFINITY;
+          const float v = tok < left ? sc[nt][e] * p.scale_log2 : -INFINITY;
           sc[nt][e] = v;
           mx = fmaxf(mx, v);
         }
@@ -333,12 +349,14 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
       const float m_new = fmaxf(m_run, mx);
-      const float alpha = exp2f(m_run - m_new);
+      // A row with no token yet (shared items only) keeps weight 0.
+      const float m_use = (kShared && m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = exp2f(m_run - m_use);
       float ls = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        sc[nt][0] = exp2f(sc[nt][0] - m_new);
-        sc[nt][1] = exp2f(sc[nt][1] - m_new);
+        sc[nt][0] = exp2f(sc[nt][0] - m_use);
+        sc[nt][1] = exp2f(sc[nt][1] - m_use);
         ls += sc[nt][0] + sc[nt][1];
       }
       l_run = l_run * alpha + ls;
@@ -381,17 +399,17 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     float l = l_run;
     l += __shfl_xor_sync(kFull, l, 1);
     l += __shfl_xor_sync(kFull, l, 2);
-    if (tq == 0 && gq < p.g) sML[warp * kMaxGroup + gq] = make_float2(m_run, l);
+    if (tq == 0 && gq < nrow) sML[warp * kMaxGroup + gq] = make_float2(m_run, l);
     float* ob = sO + warp * kMaxGroup * C::kOStride;
     const int h0 = 2 * tq, h1 = 2 * tq + 1;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const int dd = 16 * mt + gq;
-      if (h0 < p.g) {
+      if (h0 < nrow) {
         ob[h0 * C::kOStride + dd] = o[mt][0];
         ob[h0 * C::kOStride + dd + 8] = o[mt][2];
       }
-      if (h1 < p.g) {
+      if (h1 < nrow) {
         ob[h1 * C::kOStride + dd] = o[mt][1];
         ob[h1 * C::kOStride + dd + 8] = o[mt][3];
       }
@@ -402,7 +420,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
       give_up(p, abort);
       return;
     }
-    const int units = p.g * (D / 8);
+    const int units = nrow * (D / 8);
     for (int u = threadIdx.x; u < units; u += kConsumerWarps * 32) {
       const int h = u / (D / 8);
       const int d0 = (u % (D / 8)) * 8;
@@ -413,6 +431,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         mw[w] = sML[w * kMaxGroup + h].x;
         M = fmaxf(M, mw[w]);
       }
+      if (kShared && M == -INFINITY) M = 0.f;  // a shared-item row without tokens here: all weights 0
       float L = 0.f, acc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = 0.f;
@@ -431,7 +450,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         acc[6] += wt * x1.z;
         acc[7] += wt * x1.w;
       }
-      const int qh = kvh * p.g + h;
+      const int s = kShared ? s0 + h / p.g : s0;
+      const int qh = kShared ? kvh * p.g + h % p.g : kvh * p.g + h;
       if (np <= 1) {  // one partition, or an empty context (zero row)
         uint4 pk = make_uint4(0, 0, 0, 0);
         if (np == 1) {
@@ -456,7 +476,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
   }
 }
 
-template <int D, bool kInter>
+template <int D, bool kInter, bool kShared>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const DecodeArgs p) {
@@ -486,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    producer<D, kInter>(&kmap, &vmap, p, base, abort);
+    producer<D, kInter, kShared>(&kmap, &vmap, p, base, abort);
   } else {
-    consumer<D, kInter>(p, base, abort);
+    consumer<D, kInter, kShared>(p, base, abort);
   }
 }
 
@@ -502,8 +522,14 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
                              cudaStream_t stream) {
   const size_t smem = decode_tc_smem_bytes(a.D);
   const bool inter = decode_tc_interleaved(a.D, a.B);
-  auto kern = a.D == 128 ? (inter ? paged_decode_tc_kernel<128, true> : paged_decode_tc_kernel<128, false>)
-                         : paged_decode_tc_kernel<64, false>;
+  using Kern = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
+  // [shared items][D == 128 ? (inter ? 2 : 1) : 0]
+  static const Kern kernels[2][3] = {
+      {paged_decode_tc_kernel<64, false, false>, paged_decode_tc_kernel<128, false, false>,
+       paged_decode_tc_kernel<128, true, false>},
+      {paged_decode_tc_kernel<64, false, true>, paged_decode_tc_kernel<128, false, true>,
+       paged_decode_tc_kernel<128, true, true>}};
+  const Kern kern = kernels[a.shared_items ? 1 : 0][a.D == 128 ? (inter ? 2 : 1) : 0];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -518,21 +544,20 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
   std::call_once(once[dev], [&] {
     Shape sh;
     init_err = cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (init_err == cudaSuccess)
-      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<128, false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<128>::kBytes);
-    if (init_err == cudaSuccess)
-      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<128, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<128>::kBytes);
-    if (init_err == cudaSuccess)
-      init_err = cudaFuncSetAttribute(paged_decode_tc_kernel<64, false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<64>::kBytes);
-    if (init_err == cudaSuccess)
-      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm128, paged_decode_tc_kernel<128, false>,
-                                                               kThreads, TcCfg<128>::kBytes);
-    if (init_err == cudaSuccess)
-      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm64, paged_decode_tc_kernel<64, false>,
-                                                               kThreads, TcCfg<64>::kBytes);
+    for (int v = 0; v < 2 && init_err == cudaSuccess; ++v)
+      for (int k = 0; k < 3 && init_err == cudaSuccess; ++k)
+        init_err = cudaFuncSetAttribute(kernels[v][k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(k ? TcCfg<128>::kBytes : TcCfg<64>::kBytes));
+    // The variants share one launch shape; take the smallest occupancy.
+    sh.per_sm128 = sh.per_sm64 = 1 << 30;
+    for (int v = 0; v < 2 && init_err == cudaSuccess; ++v)
+      for (int k = 0; k < 3 && init_err == cudaSuccess; ++k) {
+        int n = 0;
+        init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernels[v][k], kThreads,
+                                                                 k ? TcCfg<128>::kBytes : TcCfg<64>::kBytes);
+        int& per = k ? sh.per_sm128 : sh.per_sm64;
+        per = std::min(per, n);
+      }
     shapes[dev] = sh;
   });
   if (init_err != cudaSuccess) return init_err;

@@ -27,16 +27,62 @@ struct DecodeArgs {
   float* ws_o;                  // [S][max_parts][H][D] split-K partial outputs
   float2* ws_ml;                // [S][max_parts][H] (max, sum), log2 domain
   PlanHeader* hdr;              // work counter + list length
-  const int2* plan;             // [S * max_parts] {s | part << 16, clamped ctx}; ctx 0 = empty context
+  const int2* plan;             // [S * max_parts] {s | part << 16, clamped ctx}; ctx 0 = empty context;
+                                // shared-prefix items: prefix_entry()
   unsigned* status;             // device status word
   int S, H, Hkv, g, D, B;
   int num_blocks, max_blocks_per_seq, max_ctx;
   int P;                        // partition size in tokens (multiple of 32)
   int max_parts;                // ceil(max_ctx / P)
   float scale_log2;             // scale * log2(e)
+  int shared_items;             // the work list may hold shared-prefix items
 };
 
 constexpr int kMaxGroup = 8;
+
+// Groups of sequences whose contexts start with the same tokens in the same
+// cache blocks (prefix sharing, "Day 6/90 of Inference Engineering",
+// PagedAttention notes, paragraph 5).  Group i is sequences
+// first[i] .. first[i] + count[i] - 1; its first parts[i] partitions
+// (parts[i] * P tokens) are shared.  The work list attends each shared
+// partition with shared-prefix items, each covering the query rows of up to
+// kMaxGroup / g members at once, and leaves the members' own items for those
+// partitions out.
+constexpr int kMaxPrefixGroups = 64;
+
+struct PrefixGroups {
+  int n;                         // groups with at least one shared partition
+  int first[kMaxPrefixGroups];   // ascending, ranges disjoint
+  int count[kMaxPrefixGroups];
+  int parts[kMaxPrefixGroups];
+};
+
+// Members per shared-prefix item: their g query rows each fill the
+// kMaxGroup rows a work item has.
+__host__ __device__ inline int prefix_members_per_item(int g) { return g >= kMaxGroup ? 1 : kMaxGroup / g; }
+
+// Work-list entry of a shared-prefix item: the table of sequence `table_seq`
+// (the group's first), partition `part`, query rows of sequences s0 .. s0 +
+// nm - 1.  The second word is negative, which tells it from an ordinary
+// entry {s | part << 16, context length}.
+__host__ __device__ inline int2 prefix_entry(int table_seq, int part, int s0, int nm) {
+  return make_int2(table_seq | (part << 16), (int)(0x80000000u | ((unsigned)s0 << 4) | (unsigned)nm));
+}
+
+// Shared partitions of sequence s (0 if it is in no group).
+__host__ __device__ inline int prefix_parts_of(const PrefixGroups& pg, int s) {
+  int lo = 0, hi = pg.n - 1, at = -1;
+  while (lo <= hi) {  // last group whose first sequence is <= s
+    const int mid = (lo + hi) >> 1;
+    if (pg.first[mid] <= s) {
+      at = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  return (at >= 0 && s < pg.first[at] + pg.count[at]) ? pg.parts[at] : 0;
+}
 
 // bf16, tensor cores; grid = persistent CTAs.
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -51,13 +97,37 @@ bool decode_tc_interleaved(int D, int B);
 // Work list (longest items first) for the tensor-core kernel, built on the
 // device from a.context_lens into a.hdr / a.plan.  Must precede
 // launch_decode_tc on the stream.
-cudaError_t launch_decode_plan(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_plan(const DecodeArgs& a, const PrefixGroups& pg, cudaStream_t stream);
+
+// Shared-prefix entries of the work list (the same on host and device):
+// for each group, partition p < parts and chunk of prefix_members_per_item(g)
+// consecutive members.
+__host__ __device__ inline int prefix_entries(const PrefixGroups& pg, int g) {
+  const int nm = prefix_members_per_item(g);
+  int n = 0;
+  for (int i = 0; i < pg.n; ++i) n += pg.parts[i] * ((pg.count[i] + nm - 1) / nm);
+  return n;
+}
+__host__ __device__ inline int2 prefix_entry_at(const PrefixGroups& pg, int g, int e) {
+  const int nm = prefix_members_per_item(g);
+  for (int i = 0;; ++i) {
+    const int chunks = (pg.count[i] + nm - 1) / nm;
+    if (e < pg.parts[i] * chunks) {
+      const int part = e / chunks, s0 = pg.first[i] + (e % chunks) * nm;
+      const int left = pg.first[i] + pg.count[i] - s0;
+      return prefix_entry(pg.first[i], part, s0, left < nm ? left : nm);
+    }
+    e -= pg.parts[i] * chunks;
+  }
+}
 
 // fp32, CUDA cores; one CTA per (sequence, partition, KV head).
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
 
 // Log-sum-exp merge of split-K partials into `out` (dtype PA_F32/PA_BF16).
-cudaError_t launch_lse_merge(const DecodeArgs& a, int dtype, cudaStream_t stream);
+// Members of a prefix group always go through the merge (their shared
+// partitions were written as partials).
+cudaError_t launch_lse_merge(const DecodeArgs& a, const PrefixGroups& pg, int dtype, cudaStream_t stream);
 
 cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
                                 void* v_cache, int num_blocks, int Hkv, int D, int B, int elem_bytes,

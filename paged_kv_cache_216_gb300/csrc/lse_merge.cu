@@ -14,7 +14,8 @@
 // (max, sum, O) with online rescaling, lanes holding D/32 consecutive dims
 // so each partial row is one coalesced 4*D-byte line, and the group's warps
 // are combined through shared memory.  Sequences that fit one partition were written by the decode
-// kernel and are skipped.  Launched with programmatic dependent launch: the
+// kernel and are skipped, unless they belong to a prefix group: there even a
+// single partition is a partial written by the shared-prefix kernel.  Launched with programmatic dependent launch: the
 // CTAs may start while the decode kernel drains and wait for its results
 // with griddepcontrol.wait.
 
@@ -32,7 +33,8 @@ namespace {
 constexpr int kMaxWarps = 8;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeArgs p, int wpr) {
+__global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeArgs p, int wpr,
+                                                                    const __grid_constant__ PrefixGroups pg) {
   constexpr int E = D / 32;
   __shared__ float s_m[kMaxWarps], s_l[kMaxWarps];
   __shared__ __align__(16) float s_o[kMaxWarps][D];
@@ -40,17 +42,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long sh = (long long)blockIdx.x * (kMaxWarps / wpr) + warp / wpr;
   const int wg = warp % wpr;  // warp within its (sequence, head) group
-  int s = 0, h = 0, np = 0;
+  int s = 0, h = 0, np = 0, first = 2;  // merge when np >= first
   if (sh < (long long)p.S * p.H) {
     s = (int)(sh / p.H);
     h = (int)(sh - (long long)s * p.H);
     const int ctx = min(max(p.context_lens[s], 0), p.max_ctx);
     np = (ctx + p.P - 1) / p.P;
+    if (pg.n > 0 && prefix_parts_of(pg, s) > 0) first = 1;
   }
   float m = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  if (np > 1) {
+  if (np >= first) {
     const size_t base = (size_t)s * p.max_parts * p.H + h;  // row of partition 0
 #pragma unroll 4
     for (int pp = wg; pp < np; pp += wpr) {
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
 #pragma unroll
     for (int e = 0; e < E; ++e) s_o[warp][lane * E + e] = acc[e];
     __syncthreads();
-    if (wg != 0 || np <= 1) return;
+    if (wg != 0 || np < first) return;
     float M = -INFINITY;
     for (int w = warp; w < warp + wpr; ++w) M = fmaxf(M, s_m[w]);
     l = 0.f;
@@ -92,7 +95,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] += wt * s_o[w][lane * E + e];
     }
-  } else if (np <= 1) {
+  } else if (np < first) {
     return;
   }
   const float inv = 1.f / l;
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
 }
 
 template <typename T, int D>
-cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_typed(const DecodeArgs& a, const PrefixGroups& pg, cudaStream_t stream) {
   // Warps per (sequence, head): enough to keep several partial rows in
   // flight for the longest context without idling warps on short ones.
   const int wpr = a.max_parts >= 32 ? 8 : 1;
@@ -123,16 +126,17 @@ cudaError_t launch_typed(const DecodeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a, wpr);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a, wpr, pg);
 }
 
 }  // namespace
 
-cudaError_t launch_lse_merge(const DecodeArgs& a, int dtype, cudaStream_t stream) {
+cudaError_t launch_lse_merge(const DecodeArgs& a, const PrefixGroups& pg, int dtype, cudaStream_t stream) {
   if ((long long)a.S * a.H <= 0) return cudaSuccess;
   if (dtype == PA_BF16)
-    return a.D == 128 ? launch_typed<__nv_bfloat16, 128>(a, stream) : launch_typed<__nv_bfloat16, 64>(a, stream);
-  return a.D == 128 ? launch_typed<float, 128>(a, stream) : launch_typed<float, 64>(a, stream);
+    return a.D == 128 ? launch_typed<__nv_bfloat16, 128>(a, pg, stream)
+                      : launch_typed<__nv_bfloat16, 64>(a, pg, stream);
+  return a.D == 128 ? launch_typed<float, 128>(a, pg, stream) : launch_typed<float, 64>(a, pg, stream);
 }
 
 }  // namespace pa

@@ -24,6 +24,7 @@
 #include <new>
 #include <vector>
 
+#include "kernels.h"
 #include "pa.h"
 #include "pa_internal.h"
 
@@ -40,6 +41,8 @@ struct pa_stepper {
   cudaEvent_t uploaded[2] = {nullptr, nullptr};
   cudaEvent_t consumed[2] = {nullptr, nullptr};
   int k = 0;
+  std::vector<int32_t> groups;  // prefix groups, [n][3]
+  int num_heads = 1, num_kv_heads = 1;
 };
 
 namespace {
@@ -125,6 +128,29 @@ void pa_stepper_destroy(pa_stepper* st) {
   delete st;
 }
 
+int pa_stepper_set_prefix_groups(pa_stepper* st, const int32_t* groups, int num_groups, int num_heads,
+                                 int num_kv_heads) {
+  if (!st) return pa_fail(PA_ERR_INVALID, "pa_stepper_set_prefix_groups: null stepper");
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
+    return pa_fail(PA_ERR_INVALID, "pa_stepper_set_prefix_groups: head counts");
+  if (st->partition_size == 0 && num_groups != 0)
+    return pa_fail(PA_ERR_INVALID, "pa_stepper_set_prefix_groups: the stepper builds no work list");
+  if (num_groups != 0) {
+    pa::PrefixGroups pg;
+    int rc = pa_prefix_groups(groups, num_groups, (int)st->seq_ids.size(), st->max_context_len, st->partition_size,
+                              &pg, "pa_stepper_set_prefix_groups");
+    if (rc) return rc;
+  }
+  try {
+    st->groups.assign(groups, groups + 3 * (size_t)num_groups);
+    st->num_heads = num_heads;
+    st->num_kv_heads = num_kv_heads;
+  } catch (...) {
+    return pa_fail(PA_ERR_OOM, "pa_stepper_set_prefix_groups: host allocation failed");
+  }
+  return PA_OK;
+}
+
 int pa_stepper_prepare(pa_stepper* st, void* upload_stream, void* main_stream, int* buffer_index, int* num_cow) {
   if (!st || !buffer_index || !num_cow) return pa_fail(PA_ERR_INVALID, "pa_stepper_prepare: null argument");
   const int k = st->k;
@@ -139,8 +165,10 @@ int pa_stepper_prepare(pa_stepper* st, void* upload_stream, void* main_stream, i
                                 reinterpret_cast<int32_t*>(st->host + st->off[2]));
   if (rc) return rc;
   if (st->partition_size) {
-    rc = pa_decode_plan_host(reinterpret_cast<const int32_t*>(st->host + st->off[2]), n, st->max_context_len,
-                             st->partition_size, st->host + st->off[0]);
+    rc = pa_decode_plan_host_shared_prefix(reinterpret_cast<const int32_t*>(st->host + st->off[2]), n,
+                                           st->max_context_len, st->partition_size, st->num_heads,
+                                           st->num_kv_heads, st->groups.empty() ? nullptr : st->groups.data(),
+                                           (int)(st->groups.size() / 3), st->host + st->off[0]);
     if (rc) return rc;
   }
   cudaStream_t up = static_cast<cudaStream_t>(upload_stream);

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 
+import numpy as np
 import torch
 
 from ._lib import PA_BF16, PA_F32, check, lib
@@ -116,28 +117,91 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_le
     return out
 
 
+def prefix_groups_array(groups):
+    """Prefix groups as the C ABI takes them: a C-contiguous int32 array
+    ``[n, 3]`` of (first sequence, number of sequences, shared prefix
+    tokens), or None for no groups."""
+    if groups is None:
+        return None
+    g = np.ascontiguousarray(np.asarray(groups, dtype=np.int32).reshape(-1, 3))
+    return g if g.shape[0] else None
+
+
+def _groups_args(groups):
+    g = prefix_groups_array(groups)
+    return (ctypes.c_void_p(g.ctypes.data) if g is not None else None), (0 if g is None else g.shape[0]), g
+
+
+def paged_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                               prefix_groups, out=None, partition_size: int = 0, workspace=None, stream=None):
+    """:func:`paged_decode` for batches where groups of sequences share the
+    blocks of a prefix: ``prefix_groups`` rows (first sequence, number of
+    sequences, shared prefix tokens).  The whole partitions of each prefix
+    are attended by work items that cover several members at once; the
+    result is that of :func:`paged_decode`.  bf16 only."""
+    _cuda_contig(q, k_cache, v_cache, block_tables, context_lens)
+    _need(q.dtype == k_cache.dtype == v_cache.dtype, "q and caches must share a dtype")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+          "block_tables and context_lens must be int32")
+    s, h, d = q.shape
+    n, hkv, b, d2 = k_cache.shape
+    _need(d == d2 and v_cache.shape == k_cache.shape, "head_dim mismatch")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == s and context_lens.shape == (s,),
+          "block_tables [S, max_blocks], context_lens [S]")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig(out)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = decode_workspace(s, h, hkv, d, max_context_len, partition_size, q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    gp, gn, _keep = _groups_args(prefix_groups)
+    check(lib().pa_decode_shared_prefix(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+                                        float(scale), _ptr(out), s, h, hkv, d, b, n, int(partition_size), gp, gn,
+                                        _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream)))
+    return out
+
+
 def decode_plan_bytes(num_seqs: int, max_context_len: int, partition_size: int) -> int:
     return int(lib().pa_decode_plan_bytes(num_seqs, max_context_len, partition_size))
 
 
-def decode_plan_host(context_lens, max_context_len: int, partition_size: int, plan) -> None:
+def decode_plan_host(context_lens, max_context_len: int, partition_size: int, plan, prefix_groups=None,
+                     num_heads: int = 1, num_kv_heads: int = 1) -> None:
     """Build the decode work list on the host into ``plan`` (a host buffer
     of decode_plan_bytes(...) bytes, numpy or a CPU tensor) from the int32
-    host array ``context_lens``."""
+    host array ``context_lens``; with ``prefix_groups`` (and the decode's
+    head counts), the list for :func:`paged_decode_planned` with the same
+    groups."""
     ptr = plan.ctypes.data if hasattr(plan, "ctypes") else plan.data_ptr()
     cptr = context_lens.ctypes.data if hasattr(context_lens, "ctypes") else context_lens.data_ptr()
-    check(lib().pa_decode_plan_host(ctypes.c_void_p(cptr), len(context_lens), int(max_context_len),
-                                    int(partition_size), ctypes.c_void_p(ptr)))
+    gp, gn, _keep = _groups_args(prefix_groups)
+    if gn:
+        check(lib().pa_decode_plan_host_shared_prefix(ctypes.c_void_p(cptr), len(context_lens),
+                                                      int(max_context_len), int(partition_size), int(num_heads),
+                                                      int(num_kv_heads), gp, gn, ctypes.c_void_p(ptr)))
+    else:
+        check(lib().pa_decode_plan_host(ctypes.c_void_p(cptr), len(context_lens), int(max_context_len),
+                                        int(partition_size), ctypes.c_void_p(ptr)))
 
 
 def paged_decode_planned(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
-                         out, plan, workspace, partition_size: int, stream=None):
+                         out, plan, workspace, partition_size: int, stream=None, prefix_groups=None):
     """:func:`paged_decode` with a work list built by :func:`decode_plan_host`
     and copied to the device (``plan``, uint8, counter at 0; consumed by the
-    call)."""
+    call).  With ``prefix_groups`` (the groups the list was built with) it
+    is :func:`paged_decode_shared_prefix`."""
     s, h, d = q.shape
     n, hkv, b, _ = k_cache.shape
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    gp, gn, _keep = _groups_args(prefix_groups)
+    if gn:
+        check(lib().pa_decode_planned_shared_prefix(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            int(max_context_len), float(scale), _ptr(out), s, h, hkv, d, b, n, int(partition_size), gp, gn,
+            _ptr(plan), _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream)))
+        return out
     check(lib().pa_decode_planned(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
                                   _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), s, h, hkv, d, b,
                                   n, int(partition_size), _ptr(plan), _ptr(workspace), ws_bytes, _dtype_code(q),

@@ -66,7 +66,7 @@ class StepGraphs:
 
 class ServingEngine:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, allocator: BlockAllocator, seq_ids,
-                 num_heads: int, scale: float, max_context_len: int, partition_size: int = 0):
+                 num_heads: int, scale: float, max_context_len: int, partition_size: int = 0, prefix_groups=None):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.alloc = allocator
         self.num_heads = num_heads
@@ -96,6 +96,16 @@ class ServingEngine:
                                       self.max_context_len, b, plan_p, ctypes.c_void_p(self._up_h.data_ptr()),
                                       ctypes.c_void_p(self._up_d[0].data_ptr()),
                                       ctypes.c_void_p(self._up_d[1].data_ptr()), nbytes, ctypes.byref(self._st)))
+        # Groups of the batch that share a prefix's blocks (rows: first
+        # position, count, prefix tokens): their shared partitions are
+        # attended by work items covering several members each (bf16).
+        self.prefix_groups = ops.prefix_groups_array(prefix_groups)
+        if self.prefix_groups is not None:
+            if not self.bf16:
+                raise ValueError("prefix groups need bf16 caches")
+            g = self.prefix_groups
+            check(lib().pa_stepper_set_prefix_groups(self._st, ctypes.c_void_p(g.ctypes.data), g.shape[0],
+                                                     num_heads, hkv))
         self.workspace = ops.decode_workspace(s, num_heads, hkv, d, self.max_context_len, self.partition_size, dev)
         self.up_stream = torch.cuda.Stream(device=dev)
         self._up_ptr = ctypes.c_void_p(self.up_stream.cuda_stream)
@@ -171,7 +181,8 @@ class ServingEngine:
             events[0].record()
         if self.bf16:
             out = ops.paged_decode_planned(q, self.k_cache, self.v_cache, tables, ctx, self.max_context_len,
-                                           self.scale, out, plan, self.workspace, self.partition_size)
+                                           self.scale, out, plan, self.workspace, self.partition_size,
+                                           prefix_groups=self.prefix_groups)
         else:
             out = ops.paged_decode(q, self.k_cache, self.v_cache, tables, ctx, self.max_context_len, self.scale,
                                    out=out, partition_size=self.partition_size, workspace=self.workspace)

@@ -57,3 +57,105 @@ def test_plan_rejects_bad_arguments(ops):
         ops.decode_plan_host(np.array([5, 900], dtype=np.int32), 800, 64, buf)  # longer than the bound
     with pytest.raises(PAError):
         ops.decode_plan_host(np.array([5, 9], dtype=np.int32), 800, 48, buf)  # not a multiple of 32
+
+
+def _skip_of(groups, n, P, max_ctx):
+    """Shared partitions of each sequence: whole partitions of its group's
+    prefix, none when no context can span two partitions."""
+    skip = np.zeros(n, dtype=np.int64)
+    if -(-max_ctx // P) > 1:
+        for first, count, prefix in groups:
+            skip[first:first + count] = prefix // P
+    return skip
+
+
+def _parse_shared(buf):
+    """(ordinary entries (s, part, ctx), shared entries (table seq, part, s0, nm))."""
+    hdr = buf[:256].view(np.int32)
+    n = int(hdr[1])
+    ent = buf[256:256 + 8 * n].view(np.int32).reshape(n, 2)
+    sh = ent[:, 1] < 0
+    nsh = int(sh.sum())
+    assert sh[:nsh].all() and not sh[nsh:].any()  # shared items head the list
+    x, y = ent[:nsh, 0], ent[:nsh, 1]
+    shared = [(int(a & 0xFFFF), int(a >> 16), int((b >> 4) & 0xFFFF), int(b & 15)) for a, b in zip(x, y)]
+    o = ent[nsh:]
+    return int(hdr[0]), o[:, 0] & 0xFFFF, o[:, 0] >> 16, o[:, 1], shared
+
+
+@pytest.mark.parametrize("P,g", [(32, 4), (64, 1), (64, 8)])
+def test_plan_shares_prefix_partitions(ops, P, g):
+    """With prefix groups the list starts with one shared item per (group,
+    shared partition, run of 8/g consecutive members), then holds every
+    other (sequence, partition) pair exactly once, longest first."""
+    rng = np.random.default_rng(100 + P + g)
+    ctx = rng.integers(150, 900, size=23).astype(np.int32)
+    ctx[1] = 3 * P  # ends exactly at its group's shared part
+    ctx[6] = 0  # an empty member
+    ctx[9] = P // 2  # a member shorter than its group's shared part
+    groups = [(0, 4, 3 * P + 5), (5, 6, 2 * P), (12, 1, P - 1), (14, 3, 200)]
+    mx = int(ctx.max())
+    buf = np.full(ops.decode_plan_bytes(len(ctx), mx, P), 0xCD, dtype=np.uint8)
+    ops.decode_plan_host(ctx, mx, P, buf, prefix_groups=groups, num_heads=8 * g, num_kv_heads=8)
+    counter, s, part, c, shared = _parse_shared(buf)
+    assert counter == 0
+    skip = _skip_of(groups, len(ctx), P, mx)
+    nm = 8 // g
+    want_shared = set()
+    for first, count, prefix in groups:
+        for p in range(prefix // P):
+            for s0 in range(first, first + count, nm):
+                want_shared.add((first, p, s0, min(nm, first + count - s0)))
+    assert len(shared) == len(want_shared) and set(shared) == want_shared
+    want = {(i, p) for i in range(len(ctx)) for p in range(int(skip[i]), -(-int(ctx[i]) // P))}
+    want |= {(i, 0) for i in range(len(ctx)) if ctx[i] == 0}
+    got = list(zip(s.tolist(), part.tolist()))
+    assert len(got) == len(want) and set(got) == want
+    assert not any(i == 1 for i, _ in got)  # all of its partitions are shared
+    assert np.array_equal(c, ctx[s])
+    size = np.where(c == 0, -1, np.minimum(c - part * P, P))
+    nf = int((size == P).sum())
+    assert (size[:nf] == P).all() and np.all(size[nf:-1] >= size[nf + 1:])
+    # no groups: the plain list
+    buf2 = np.full_like(buf, 0xCD)
+    ops.decode_plan_host(ctx, mx, P, buf2, prefix_groups=[])
+    plain = np.full_like(buf, 0xCD)
+    ops.decode_plan_host(ctx, mx, P, plain)
+    assert np.array_equal(buf2, plain)
+
+
+def test_plan_with_one_partition_shares_nothing(ops):
+    """When no context spans two partitions there are no partial slots for
+    shared partitions: groups change nothing."""
+    ctx = np.array([40, 64, 10], dtype=np.int32)
+    a = np.zeros(ops.decode_plan_bytes(3, 64, 64), dtype=np.uint8)
+    b = np.zeros_like(a)
+    ops.decode_plan_host(ctx, 64, 64, a, prefix_groups=[(0, 3, 64)], num_heads=8, num_kv_heads=2)
+    ops.decode_plan_host(ctx, 64, 64, b)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("groups", [
+    [(0, 3, 100), (2, 2, 100)],  # overlapping
+    [(3, 2, 100), (0, 2, 100)],  # not ascending
+    [(0, 0, 100)],  # empty
+    [(8, 3, 100)],  # past the batch
+    [(0, 2, 5000)],  # prefix longer than the length bound
+    [(0, 2, -1)],
+])
+def test_plan_rejects_bad_prefix_groups(ops, groups):
+    from paged_kv_cache_216_gb300._lib import PAError
+
+    buf = np.zeros(ops.decode_plan_bytes(10, 1000, 64), dtype=np.uint8)
+    with pytest.raises(PAError):
+        ops.decode_plan_host(np.full(10, 500, dtype=np.int32), 1000, 64, buf, prefix_groups=groups)
+
+
+def test_plan_rejects_too_many_prefix_groups(ops):
+    from paged_kv_cache_216_gb300._lib import PA_MAX_PREFIX_GROUPS, PAError
+
+    n = PA_MAX_PREFIX_GROUPS + 1
+    groups = [(i, 1, 64) for i in range(n)]
+    buf = np.zeros(ops.decode_plan_bytes(n, 1000, 64), dtype=np.uint8)
+    with pytest.raises(PAError, match="UNSUPPORTED|more than"):
+        ops.decode_plan_host(np.full(n, 500, dtype=np.int32), 1000, 64, buf, prefix_groups=groups)

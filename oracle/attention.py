@@ -69,15 +69,26 @@ def decode_one(q_heads: np.ndarray, k_rows: np.ndarray, v_rows: np.ndarray,
 
 def paged_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                  block_tables: np.ndarray, context_lens: np.ndarray,
-                 scale: float, dtype: str, seqs=None) -> np.ndarray:
+                 scale: float, dtype: str, seqs=None, cache_dtype: str | None = None,
+                 k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
     """Decode output ``[len(seqs), H, D]`` (fp64) for the listed sequences
     (all by default).
 
     q ``[S, H, D]``; k_cache, v_cache ``[N, Hkv, B, D]``; block_tables
     ``[S, max_blocks]`` (entries past a sequence's last block are ignored);
     context_lens ``[S]`` (each >= 1).  ``dtype`` is the storage type of q and
-    of the caches ("bf16" bit patterns or "f32").
+    of the caches ("bf16" bit patterns or "f32"); ``cache_dtype="fp8"``
+    takes the caches as E4M3 codes read as decode(code) · k_scale (or
+    v_scale), see ``oracle.fp8``.
     """
+    if cache_dtype == "fp8":
+        from .fp8 import decode as fp8_decode
+
+        def kv_f64(rows, which):
+            return fp8_decode(rows) * (k_scale if which == "k" else v_scale)
+    else:
+        def kv_f64(rows, which):
+            return to_f64(rows, dtype)
     s_all, h, d = q.shape
     hkv = k_cache.shape[1]
     assert h % hkv == 0 and k_cache.shape[3] == d
@@ -89,7 +100,7 @@ def paged_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
         assert n >= 1
         qs = to_f64(q[s], dtype)
         for kv in range(hkv):
-            k_rows = to_f64(gather_sequence(k_cache, block_tables[s], n, kv), dtype)
-            v_rows = to_f64(gather_sequence(v_cache, block_tables[s], n, kv), dtype)
+            k_rows = kv_f64(gather_sequence(k_cache, block_tables[s], n, kv), "k")
+            v_rows = kv_f64(gather_sequence(v_cache, block_tables[s], n, kv), "v")
             out[i, kv * g:(kv + 1) * g] = decode_one(qs[kv * g:(kv + 1) * g], k_rows, v_rows, scale)
     return out

@@ -44,35 +44,38 @@ METRIC = "paged-decode KV-read GB/s"
 UNIT = "GB/s"
 
 
-def kv_bytes(ctx: np.ndarray, w, groups=None, partition_size: int = 0) -> int:
+def kv_bytes(ctx: np.ndarray, w, groups=None, partition_size: int = 0, elem_bytes: int | None = None) -> int:
     """Algorithmic KV bytes of one decode step: every context token's key and
-    value row per KV head; with prefix groups, the tokens of a group's shared
+    value row per KV head (``elem_bytes`` per element: the workload's, or 1
+    for an E4M3 cache); with prefix groups, the tokens of a group's shared
     partitions once for the whole group."""
     ctx = np.asarray(ctx, dtype=np.int64)
     tokens = int(ctx.sum())
     for first, count, prefix in (groups or ()):
         shared = np.minimum(ctx[first:first + count], prefix // partition_size * partition_size)
         tokens -= int(shared.sum()) - int(shared.max())
-    return tokens * w.num_kv_heads * w.head_dim * 2 * w.elem_bytes
+    return tokens * w.num_kv_heads * w.head_dim * 2 * (w.elem_bytes if elem_bytes is None else elem_bytes)
 
 
 DECODE_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_tc.cu", "paged_kv_cache_216_gb300/csrc/device_common.cuh",
                   "paged_kv_cache_216_gb300/csrc/kernels.h")
+DECODE_FP8_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_fp8.cu", "paged_kv_cache_216_gb300/csrc/device_common.cuh",
+                      "paged_kv_cache_216_gb300/csrc/kernels.h")
 
 
-def decode_kernel_hash() -> str:
+def decode_kernel_hash(sources=DECODE_SOURCES) -> str:
     """Hash of the decode kernel's sources: DRAM counters taken on another
     version of the kernel are not reported."""
     import hashlib
 
     h = hashlib.sha256()
-    for rel in DECODE_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def decode_traffic(workload: str):
+def decode_traffic(workload: str, fp8: bool = False):
     """DRAM bytes (read + write) of one decode-kernel launch on this workload
     from the committed ncu summary profiles/decode_dram_traffic.txt (lines:
     workload read_bytes write_bytes source_hash), or None if absent or taken
@@ -80,7 +83,9 @@ def decode_traffic(workload: str):
     p = os.path.join(ROOT, "profiles", "decode_dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    cur = decode_kernel_hash()
+    cur = decode_kernel_hash(DECODE_FP8_SOURCES if fp8 else DECODE_SOURCES)
+    if fp8:
+        workload = workload + "/fp8"
     with open(p) as f:
         for line in f:
             parts = line.split("#", 1)[0].split()
@@ -227,6 +232,25 @@ def run_ours(args, rank, world, local):
 
     k_cache = to_dev(random_pool(w, nb, "k"))
     v_cache = to_dev(random_pool(w, nb, "v"))
+    fp8 = args.kv_dtype == "fp8"
+    kv_scales = None
+    if fp8:
+        # E4M3 caches: the pools are stored through the append kernel, one
+        # slot per token row; new tokens are quantized the same way each step
+        kv_scales = (w.std / 32.0, w.std / 32.0)
+        n_, h_, b_, d_ = k_cache.shape
+        slots = torch.arange(n_ * b_, dtype=torch.int64, device=dev)
+        codes = []
+        for src in (k_cache, v_cache):
+            dst = torch.zeros(src.shape, dtype=torch.uint8, device=dev)
+            codes.append(dst)
+        pa.cache_append_fp8(k_cache.permute(0, 2, 1, 3).reshape(n_ * b_, h_, d_).contiguous(),
+                            v_cache.permute(0, 2, 1, 3).reshape(n_ * b_, h_, d_).contiguous(), slots, codes[0],
+                            codes[1], *kv_scales)
+        torch.cuda.synchronize()
+        del k_cache, v_cache, slots
+        torch.cuda.empty_cache()
+        k_cache, v_cache = codes
     alloc = pa.BlockAllocator(nb, w.block_size, order)
     pairs = populate(alloc, ctx0, w.prefix_len, w.prefix_share)
     if len(pairs):
@@ -237,23 +261,27 @@ def run_ours(args, rank, world, local):
     groups = None
     if w.prefix_share and not args.no_prefix_groups:
         groups = [(0, w.prefix_share, w.prefix_len // w.block_size * w.block_size)]
+    if fp8:
+        groups = None  # prefix groups are not supported with E4M3 caches
     eng = pa.ServingEngine(k_cache, v_cache, alloc, seq_ids, w.num_heads, w.scale,
-                           int(ctx0.max()) + total_steps, w.partition_size, prefix_groups=groups)
+                           int(ctx0.max()) + total_steps, w.partition_size, prefix_groups=groups,
+                           kv_scales=kv_scales)
     if not eng.split:
         groups = None  # one partition per context: no shared partitions
 
     def step_bytes(ctx):
-        return kv_bytes(ctx, w, groups, eng.partition_size)
+        return kv_bytes(ctx, w, groups, eng.partition_size, 1 if fp8 else None)
 
     toks = _host_tokens(w, total_steps)
     n_dev = W + 2 + K + Kp + K
     dev_toks = [tuple(to_dev(x) for x in t) for t in toks[:n_dev]]
     packed = [eng.pack_tokens(*t) for t in dev_toks]  # each step's new tokens, resident in HBM
-    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=k_cache.dtype, device=dev)
+    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16 if fp8 else k_cache.dtype,
+                      device=dev)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
-    if kv_bytes(ctx0, w) < 2 * l2:
+    if step_bytes(ctx0) < 2 * l2:
         flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device=dev)
     step = 0  # steps done so far; step j decodes contexts ctx0 + j + 1
 
@@ -379,7 +407,7 @@ def run_ours(args, rank, world, local):
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     achieved = dec_bytes / dec_avg / 1e9
-    traffic = decode_traffic(args.workload)
+    traffic = decode_traffic(args.workload, fp8)
     status = pa.get_status()
     if status:
         raise RuntimeError(f"device status word {status:#x} after the benchmark")
@@ -387,17 +415,20 @@ def run_ours(args, rank, world, local):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(t_max / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if fp8 else w.dtype, "data": "synthetic",
         "config": {
             "workload": w.name, "batch": w.num_seqs, "query_heads": w.num_heads, "kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "partition_size": eng.partition_size,
             "context_start_mean": float(ctx0.mean()), "context_start_max": int(ctx0.max()),
             "kv_bytes_per_step": int(local_bytes / K),
             "prefix_groups": groups,
-            "kv_bytes_per_step_logical": int(sum(kv_bytes(ctx0 + T0 + i + 1, w) for i in range(K)) / K),
+            "kv_bytes_per_step_logical": int(sum(kv_bytes(ctx0 + T0 + i + 1, w, elem_bytes=1 if fp8 else None)
+                                                 for i in range(K)) / K),
             "l2": ("flushed before every step" if flush is not None else
                    f"inputs larger than L2 ({local_bytes / K / 1e9:.2f} GB KV per step vs {l2 / 1e6:.0f} MB L2)"),
             "parallelism": f"replicas x{world}",
+            "kv_storage": ("E4M3 codes, one scale per cache; f16 tensor-core products, f32 accumulation, bf16 q/out"
+                           if fp8 else w.dtype),
             "launch": ("tables and new tokens uploaded on a side stream; append+decode+merge replayed as a "
                        "CUDA graph per device buffer" if use_graphs else "uploads on a side stream; eager launches"),
         },
@@ -408,7 +439,8 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("paged_decode_tc_kernel (with shared-prefix items) + lse_merge_kernel" if groups
+                     "kernel": ("paged_decode_fp8_kernel + lse_merge_kernel" if fp8 else
+                                "paged_decode_tc_kernel (with shared-prefix items) + lse_merge_kernel" if groups
                                 else "paged_decode_tc_kernel + lse_merge_kernel"),
                      "peak_source": f"{peak_src} hbm_gbs", "decode_ms": round(dec_avg * 1e3, 4),
                      "timing": f"CUDA events inside each step's graph, {K} steps after the timed run"},
@@ -488,6 +520,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0, help="seconds of oracle time in the reference arm")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--eager", action="store_true", help="launch every step's kernels eagerly (no CUDA graph)")
+    ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",
+                    help="store the KV cache as the workload's type or as E4M3 codes")
     ap.add_argument("--no-prefix-groups", action="store_true",
                     help="decode prefix-sharing sequences one by one (no shared-prefix kernel)")
     args = ap.parse_args()

@@ -36,7 +36,8 @@
  *   physical block block_tables[seq][t / block_size], row t % block_size.
  *   Slot s = block * block_size + row.
  *
- * Supported set: dtype PA_BF16 or PA_F32; head_dim 64 or 128; block_size 8,
+ * Supported set: dtype PA_BF16 or PA_F32 (PA_FP8_E4M3 caches through the
+ * _fp8 entry points, head_dim 128); head_dim 64 or 128; block_size 8,
  * 16 or 32; g = num_heads / num_kv_heads in {1, 2, 4, 8}.  Anything else
  * returns PA_ERR_UNSUPPORTED.  Decode in bf16 runs on tensor cores with fp32
  * accumulation; fp32 decode runs on CUDA cores in fp32.
@@ -62,6 +63,8 @@ extern "C" {
 /* Element types of q, k, v, caches and out (all the same in one call). */
 #define PA_F32 0
 #define PA_BF16 1
+/* E4M3 8-bit floats (caches only; q, k, v inputs and out are then bf16). */
+#define PA_FP8_E4M3 2
 
 /* Bits of the device status word. */
 #define PA_STATUS_BAD_SLOT 1u    /* append: slot >= num_blocks*block_size */
@@ -97,6 +100,23 @@ int pa_cache_append(const void* k, const void* v, const int64_t* slot_mapping,
                     int num_tokens, void* k_cache, void* v_cache, int num_blocks,
                     int num_kv_heads, int head_dim, int block_size, int dtype,
                     void* stream);
+
+/*
+ * KV append into an FP8 cache: the same scatter as pa_cache_append, of the
+ * bf16 tokens k, v ([num_tokens][num_kv_heads][head_dim]) stored as E4M3
+ * codes: code = round-to-nearest-even(x / scale) in E4M3 (bias 7, largest
+ * finite 448; no infinities), the quotient an IEEE fp32 division; finite
+ * quotients beyond ±448 and infinities store ±448, NaN stores a NaN code.
+ * k_scale, v_scale: finite, > 0, one per cache.  The pages ask for fewer
+ * bytes moved (memory notes, "Core Ideas" 1; [PAK section 6]: FP16
+ * compute, FP32 accumulation); one byte per element is this library's
+ * reading.  k_cache, v_cache: cache layout above with 1-byte elements.
+ */
+int pa_cache_append_fp8(const void* k, const void* v,
+                        const int64_t* slot_mapping, int num_tokens,
+                        void* k_cache, void* v_cache, int num_blocks,
+                        int num_kv_heads, int head_dim, int block_size,
+                        float k_scale, float v_scale, void* stream);
 
 /*
  * Block copy for copy-on-write [Day6 paragraph 5]: for each pair
@@ -193,6 +213,24 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache,
                       int num_blocks, int partition_size, const void* plan,
                       void* workspace, size_t workspace_bytes, int dtype,
                       void* stream);
+
+/*
+ * Paged decode over FP8 caches written by pa_cache_append_fp8: the result of
+ * pa_decode with K = e4m3(code) * k_scale and V = e4m3(code) * v_scale.  q
+ * and out are bf16; head_dim 128; products in FP16 on tensor cores, sums in
+ * FP32 [PAK section 6].  q must be finite with |q| < 65504 (it is taken to
+ * FP16).  plan: NULL to build the work list on the device, else a list from
+ * pa_decode_plan_host (as for pa_decode_planned).  Workspace as pa_decode.
+ * Prefix groups are not supported with FP8 caches.
+ */
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int max_blocks_per_seq,
+                  const int32_t* context_lens, int max_context_len,
+                  float scale, float k_scale, float v_scale, void* out,
+                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                  int block_size, int num_blocks, int partition_size,
+                  const void* plan, void* workspace, size_t workspace_bytes,
+                  void* stream);
 
 /*
  * Shared-prefix decode [Day6 paragraph 5: sequences forked from one prompt

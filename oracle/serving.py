@@ -25,7 +25,8 @@ import numpy as np
 
 from .allocator import BlockAllocator
 from .attention import paged_decode
-from .cache import cache_append_inplace, copy_blocks
+from .cache import bf16_to_f32, cache_append_inplace, copy_blocks
+from .fp8 import quantize
 
 
 def tables_array(alloc: BlockAllocator, seq_ids, width: int) -> np.ndarray:
@@ -66,7 +67,11 @@ class ServingOracle:
     context lengths."""
 
     def __init__(self, alloc: BlockAllocator, k_cache: np.ndarray,
-                 v_cache: np.ndarray, num_seqs: int, dtype: str, scale: float):
+                 v_cache: np.ndarray, num_seqs: int, dtype: str, scale: float,
+                 fp8_scales=None):
+        """``fp8_scales = (k_scale, v_scale)``: the caches hold E4M3 codes and
+        new bf16 tokens are stored quantized (``oracle.fp8``)."""
+        self.fp8_scales = fp8_scales
         self.alloc = alloc
         self.k_cache = k_cache
         self.v_cache = v_cache
@@ -91,7 +96,14 @@ class ServingOracle:
             if src >= 0:
                 pairs.append((src, dst))
         copy_blocks(self.k_cache, self.v_cache, pairs)
-        cache_append_inplace(self.k_cache, self.v_cache, k_new, v_new, slots)
-        out = paged_decode(q, self.k_cache, self.v_cache, self.tables(width),
-                           self.context_lens(), self.scale, self.dtype, seqs)
+        if self.fp8_scales is None:
+            cache_append_inplace(self.k_cache, self.v_cache, k_new, v_new, slots)
+            out = paged_decode(q, self.k_cache, self.v_cache, self.tables(width),
+                               self.context_lens(), self.scale, self.dtype, seqs)
+            return slots, pairs, out
+        ks, vs = self.fp8_scales
+        cache_append_inplace(self.k_cache, self.v_cache, quantize(bf16_to_f32(k_new), ks),
+                             quantize(bf16_to_f32(v_new), vs), slots)
+        out = paged_decode(q, self.k_cache, self.v_cache, self.tables(width), self.context_lens(),
+                           self.scale, "bf16", seqs, cache_dtype="fp8", k_scale=ks, v_scale=vs)
         return slots, pairs, out

@@ -9,12 +9,14 @@ from ._lib import PAError, OutOfBlocks, lib  # noqa: F401
 from .allocator import BlockAllocator  # noqa: F401
 from .ops import (  # noqa: F401
     cache_append,
+    cache_append_fp8,
     copy_blocks,
     decode_partition_size,
     decode_workspace,
     decode_workspace_bytes,
     get_status,
     paged_decode,
+    paged_decode_fp8,
     paged_decode_shared_prefix,
     paged_decode_static_workspace,
 )

@@ -15,6 +15,7 @@ from .build import LIB
 
 PA_F32 = 0
 PA_BF16 = 1
+PA_FP8_E4M3 = 2
 
 PA_STATUS_BAD_SLOT = 1
 PA_STATUS_BAD_BLOCK = 2
@@ -49,6 +50,10 @@ SIGNATURES = {
                                    _c_int, _c_int, _c_int, _vp, _vp, _c_sz, _c_int, _vp]),
     "pa_decode_static_workspace": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
+    "pa_cache_append_fp8": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_f, _c_f,
+                                     _vp]),
+    "pa_decode_fp8": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _c_f, _c_f, _vp, _c_int, _c_int,
+                               _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_sz, _vp]),
     "pa_decode_shared_prefix": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _c_sz, _c_int,
                                          _vp]),

@@ -67,6 +67,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // array [N*Hkv*B rows][D] read in boxes of B rows x 64 dims, or (interleaved)
 // [N*Hkv*B*2 lines][64] read in boxes of 2B lines, one (block, head) slab per
 // box; 128-byte swizzle in both.
+// Tensor map over an E4M3 cache (head_dim 128): [N*Hkv*B rows][128 bytes],
+// one box of B rows per (block, head) slab, 128-byte swizzle.
+int make_cache_map_fp8(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B) {
+  auto fn = encode_fn();
+  if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {128u, (cuuint64_t)num_blocks * Hkv * B};
+  cuuint64_t strides[1] = {128u};
+  cuuint32_t box[2] = {128u, (cuuint32_t)B};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  return PA_OK;
+}
+
 int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D, bool inter) {
   auto fn = encode_fn();
   if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
@@ -86,7 +102,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool supported_shape(int D, int B) { return (D == 64 || D == 128) && (B == 8 || B == 16 || B == 32); }
 
-int elem_bytes(int dtype) { return dtype == PA_BF16 ? 2 : dtype == PA_F32 ? 4 : 0; }
+int elem_bytes(int dtype) { return dtype == PA_BF16 ? 2 : dtype == PA_F32 ? 4 : dtype == PA_FP8_E4M3 ? 1 : 0; }
+
+bool good_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
 // Work items (sequence x partition x KV head) below which the library
 // splits contexts into smaller partitions; about four per resident CTA.
@@ -146,7 +164,8 @@ int pa_cache_append(const void* k, const void* v, const int64_t* slot_mapping, i
                     void* v_cache, int num_blocks, int num_kv_heads, int head_dim, int block_size, int dtype,
                     void* stream) {
   const int es = elem_bytes(dtype);
-  if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_cache_append: dtype");
+  if (es == 0 || dtype == PA_FP8_E4M3)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_cache_append: dtype (FP8 caches: pa_cache_append_fp8)");
   if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0)
     return pa_fail(PA_ERR_INVALID, "pa_cache_append: sizes");
   if (!supported_shape(head_dim, block_size)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_cache_append: head_dim/block_size");
@@ -162,6 +181,31 @@ int pa_cache_append(const void* k, const void* v, const int64_t* slot_mapping, i
                                           num_kv_heads, head_dim, block_size, es, status,
                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "pa_cache_append launch");
+  return PA_OK;
+}
+
+int pa_cache_append_fp8(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens, void* k_cache,
+                        void* v_cache, int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                        float k_scale, float v_scale, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_cache_append_fp8: sizes");
+  if (!supported_shape(head_dim, block_size))
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_cache_append_fp8: head_dim/block_size");
+  if (!good_scale(k_scale) || !good_scale(v_scale))
+    return pa_fail(PA_ERR_INVALID, "pa_cache_append_fp8: scales must be finite and > 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return pa_fail(PA_ERR_INVALID, "pa_cache_append_fp8: null pointer");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return pa_fail(PA_ERR_INVALID, "pa_cache_append_fp8: misaligned pointer");
+  unsigned* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  cudaError_t e = pa::launch_cache_append_fp8(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                                              num_kv_heads, head_dim, block_size, k_scale, v_scale, status,
+                                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pa_cache_append_fp8 launch");
   return PA_OK;
 }
 
@@ -216,9 +260,16 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
                        void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                        int num_blocks, int partition_size, const void* plan, const int32_t* groups,
-                       int num_groups, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+                       int num_groups, void* workspace, size_t workspace_bytes, int dtype, void* stream,
+                       float k_scale = 1.f, float v_scale = 1.f) {
+  // dtype is the caches' type; with PA_FP8_E4M3 q and out are bf16.
   const int es = elem_bytes(dtype);
   if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
+  const bool fp8 = dtype == PA_FP8_E4M3;
+  if (fp8 && head_dim != 128) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: head_dim 128 only");
+  if (fp8 && (!good_scale(k_scale) || !good_scale(v_scale)))
+    return pa_fail(PA_ERR_INVALID, "pa_decode_fp8: scales must be finite and > 0");
+  if (fp8 && num_groups != 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: no prefix groups");
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_context_len < 1 ||
       max_blocks_per_seq <= 0 || !std::isfinite(scale))
     return pa_fail(PA_ERR_INVALID, "pa_decode: sizes");
@@ -246,7 +297,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   ws_layout(num_seqs, num_heads, head_dim, max_context_len, P, &wl);
   if (!workspace || workspace_bytes < wl.total) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace too small");
   if (!aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode: workspace not 256-byte aligned");
-  if (plan && dtype != PA_BF16) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_planned: bf16 only");
+  if (plan && dtype == PA_F32) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_planned: bf16 or FP8 caches only");
   if (plan && !aligned(plan, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode_planned: plan not 256-byte aligned");
   if (num_groups != 0 && dtype != PA_BF16) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_shared_prefix: bf16 only");
   pa::PrefixGroups pg;
@@ -281,8 +332,9 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   a.max_ctx = max_context_len;
   a.P = P;
   a.max_parts = (int)parts;
-  a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+  a.scale_log2 = (float)((double)scale * (fp8 ? (double)k_scale : 1.0) * 1.4426950408889634);  // log2(e)
   a.shared_items = pg.n > 0;
+  a.v_scale = fp8 ? v_scale : 1.f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -298,12 +350,23 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
       if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");
     }
     e = pa::launch_decode_tc(a, kmap, vmap, st);
+  } else if (fp8) {
+    CUtensorMap kmap, vmap;
+    rc = make_cache_map_fp8(&kmap, k_cache, num_blocks, num_kv_heads, block_size);
+    if (rc) return rc;
+    rc = make_cache_map_fp8(&vmap, v_cache, num_blocks, num_kv_heads, block_size);
+    if (rc) return rc;
+    if (!plan) {
+      e = pa::launch_decode_plan(a, pg, st);
+      if (e != cudaSuccess) return cuda_fail(e, "pa_decode plan launch");
+    }
+    e = pa::launch_decode_fp8(a, kmap, vmap, st);
   } else {
     e = pa::launch_decode_simt(a, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "pa_decode launch");
   if (parts > 1) {
-    e = pa::launch_lse_merge(a, pg, dtype, st);
+    e = pa::launch_lse_merge(a, pg, fp8 ? PA_BF16 : dtype, st);
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode merge launch");
   }
   return PA_OK;
@@ -316,6 +379,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
               int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale, void* out,
               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
               int partition_size, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+  if (dtype == PA_FP8_E4M3) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: FP8 caches need pa_decode_fp8");
   return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
                      out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
                      nullptr, nullptr, 0, workspace, workspace_bytes, dtype, stream);
@@ -327,9 +391,20 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache, c
                       int num_blocks, int partition_size, const void* plan, void* workspace,
                       size_t workspace_bytes, int dtype, void* stream) {
   if (!plan) return pa_fail(PA_ERR_INVALID, "pa_decode_planned: null plan");
+  if (dtype == PA_FP8_E4M3) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_planned: FP8 caches need pa_decode_fp8");
   return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
                      out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
                      plan, nullptr, 0, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                  int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
+                  float k_scale, float v_scale, void* out, int num_seqs, int num_heads, int num_kv_heads,
+                  int head_dim, int block_size, int num_blocks, int partition_size, const void* plan,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                     out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size, plan,
+                     nullptr, 0, workspace, workspace_bytes, PA_FP8_E4M3, stream, k_scale, v_scale);
 }
 
 int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

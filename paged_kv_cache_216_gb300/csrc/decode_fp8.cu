@@ -1,0 +1,540 @@
+// Paged decode attention over an FP8 (E4M3) KV cache: bf16 queries and
+// output, FP16 tensor-core products, FP32 accumulation (the mixed-precision
+// recipe of "PagedAttention Kernel：大模型推理优化的显存管理革新" section 6:
+// compute in FP16, accumulate in FP32), on keys and values stored as one
+// byte each -- half the bytes of bf16 to move, the memory notes' measure
+// ("Core Ideas" 1).  Stored code c of a cache with scale s reads as
+// e4m3(c) * s.
+//
+// Same schedule as the bf16 kernel (decode_tc.cu): persistent CTAs take
+// (sequence, partition, KV head) items from the longest-first work list
+// through an atomic counter; warp 4 loads each item's g query rows and
+// streams its blocks by TMA into a 4-stage shared-memory ring (one box of
+// [B tokens x 128 bytes] per block for keys and one for values, 128-byte
+// swizzle), 64 tokens per stage; warps 0-3 take the stages in turn and
+// merge their (max, sum, O) states at the end of the item.  Head dim 128.
+//
+// The consumer never widens a whole stage: it reads codes with ldmatrix and
+// converts them in registers (cvt e4m3x2 -> f16x2, exact), so each code
+// crosses shared memory once.
+//  * S = Q Kᵀ (mma.m16n8k16 f16, query heads as rows of A): a 16-bit
+//    ldmatrix of a K row gives a thread four consecutive dims of one token,
+//    so the k order of each 16-dim step is permuted -- k 2t, 2t+1 are dims
+//    4t, 4t+1 and k 2t+8, 2t+9 are dims 4t+2, 4t+3 -- and Q's fragments are
+//    built in the same order (a dot product does not depend on it).
+//  * Oᵀ = Vᵀ Pᵀ: the 8-bit transposing ldmatrix (m16n16) of a 16-token x
+//    16-dim V tile gives a thread one dim of four consecutive tokens, so the
+//    token order of each 16-token step is permuted the same way (k 2t, 2t+1
+//    are tokens 4t, 4t+1 and k 2t+8, 2t+9 tokens 4t+2, 4t+3).  To let P
+//    come straight from the S accumulators, the 8 tokens of S tile 2j are
+//    tokens {0,1,4,5,8,9,12,13} of step j and those of tile 2j+1 tokens
+//    {2,3,6,7,10,11,14,15} (the K ldmatrix gathers its rows in that order).
+// Every wait is bounded (device_common.cuh); a time-out raises
+// PA_STATUS_TIMEOUT and the CTA winds down.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace pa {
+namespace {
+
+constexpr int kD = 128;                      // head_dim
+constexpr int kChunk = 64;                   // tokens per pipeline stage
+constexpr int kRegion = kChunk * kD;         // 8 KB: the keys (or values) of a stage
+constexpr int kStage = 2 * kRegion;
+constexpr int kStages = 4;
+constexpr int NTILES = kChunk / 8;           // 8-token tiles of S per stage
+constexpr int KSTEPS = kChunk / 16;          // 16-token steps of P·V per stage
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr unsigned kFull = 0xffffffffu;
+// chunk k goes to consumer warp k % 4 and stage k % kStages: a multiple, so
+// every stage always belongs to one warp
+static_assert(kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
+constexpr int kQSlot = kMaxGroup * kD * 2;   // bf16 query rows of one item
+constexpr int kOStride = kD + 4;
+constexpr int kOBuf = kConsumerWarps * kMaxGroup * kOStride * 4;
+constexpr int kML = kConsumerWarps * kMaxGroup * 8;
+constexpr int kBars = (2 * kStages + 6) * 8;  // full, empty, qfull[2], qempty[2], epi_full, epi_done
+constexpr int kOffQ = kStages * kStage;
+constexpr int kOffO = kOffQ + 2 * kQSlot;
+constexpr int kOffML = kOffO + kOBuf;
+constexpr int kOffDesc = kOffML + kML;
+constexpr int kOffBar = kOffDesc + 2 * 16;
+constexpr int kOffAbort = kOffBar + kBars;
+constexpr size_t kBytes = 1024 + kOffAbort + 16;
+
+struct Bars {
+  uint64_t *full, *empty, *qfull, *qempty, *epi_full, *epi_done;
+};
+
+__device__ __forceinline__ Bars bars_at(uint8_t* base) {
+  Bars b;
+  b.full = reinterpret_cast<uint64_t*>(base + kOffBar);
+  b.empty = b.full + kStages;
+  b.qfull = b.empty + kStages;
+  b.qempty = b.qfull + 2;
+  b.epi_full = b.qempty + 2;
+  b.epi_done = b.epi_full + 1;
+  return b;
+}
+
+// Thread (g, t) of the warp receives bytes [4t .. 4t+3] of row g (tokens
+// 4t..4t+3) at column g and g + 8 of a 16 x 16 byte tile, transposed:
+// d0 byte j = tile[4t + j][g], d1 byte j = tile[4t + j][g + 8].  Lanes 0-15
+// give the addresses of rows 0-15.
+__device__ __forceinline__ void ldmatrix_b8_trans(uint32_t addr, uint32_t& d0, uint32_t& d1) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];" : "=r"(d0), "=r"(d1) : "r"(addr));
+}
+
+// Two E4M3 codes (low byte first) -> two f16 (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)two));
+  return r;
+}
+
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two bf16 (one 32-bit word) -> two f16; exact for |x| in [2^-14, 65504].
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ int load_block_id(const int32_t* row, int rel, int nblk) {
+  return rel < nblk ? __ldg(row + rel) : 0;
+}
+
+__device__ __forceinline__ void give_up(const DecodeArgs& p, volatile int* abort) {
+  *abort = 1;
+  raise_status(p.status, PA_STATUS_TIMEOUT);
+}
+
+__device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& p, uint8_t* base,
+                         volatile int* abort) {
+  const int lane = threadIdx.x & 31;
+  const Bars bar = bars_at(base);
+  int4* desc = reinterpret_cast<int4*>(base + kOffDesc);
+  const uint64_t policy = policy_evict_first();
+  const int bpc = kChunk / p.B;  // cache blocks per chunk
+  const uint32_t qbytes = (uint32_t)(p.g * kD * 2);
+  const uint32_t block_bytes = (uint32_t)(p.B * kD * 2);  // keys + values of one block
+
+  pdl_wait_primary();  // the work list is complete and visible from here on
+  const int total = __ldcg(&p.hdr->num_pairs) * p.Hkv;
+  unsigned* counter = &p.hdr->counter;
+  // The next item is claimed when the current one starts and its list
+  // entry read once the current item's first chunk is issued.
+  int cur_idx = total;
+  int2 cur_pr = make_int2(0, -1);
+  if (lane == 0) {
+    cur_idx = (int)atomicAdd(counter, 1u);
+    if (cur_idx < total) cur_pr = __ldcg(p.plan + cur_idx / p.Hkv);
+  }
+  uint32_t kseq = 0, nq = 0;
+  bool ok = true;
+  for (uint32_t n = 0;; ++n) {
+    int2 nxt_pr = make_int2(0, -1);
+    int nxt_idx = total;
+    if (lane == 0 && cur_idx < total) nxt_idx = (int)atomicAdd(counter, 1u);
+    const int idx = __shfl_sync(kFull, cur_idx, 0);
+    const int prx = __shfl_sync(kFull, cur_pr.x, 0);
+    const int ctx = __shfl_sync(kFull, cur_pr.y, 0);
+    const int slot = n & 1;
+    if (!mbar_wait(&bar.qempty[slot], ((n >> 1) & 1) ^ 1, abort)) {
+      ok = false;
+      break;
+    }
+    if (idx >= total) {  // no work left: tell the consumers
+      if (lane == 0) {
+        desc[slot] = make_int4(0, 0, 0, -1);
+        mbar_arrive(&bar.qfull[slot]);
+      }
+      break;
+    }
+    const int s = prx & 0xffff, part = prx >> 16, kvh = idx % p.Hkv;
+    const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
+    if (lane == 0) {
+      desc[slot] = make_int4(s, part, kvh, ctx);
+      mbar_arrive_expect_tx(&bar.qfull[slot], qbytes);
+      const __nv_bfloat16* src =
+          static_cast<const __nv_bfloat16*>(p.q) + ((size_t)s * p.H + (size_t)kvh * p.g) * kD;
+      bulk_load(base + kOffQ + slot * kQSlot, src, qbytes, &bar.qfull[slot]);
+    }
+    ++nq;
+    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq + t0 / p.B;
+    const int nblk = (t1 - t0 + p.B - 1) / p.B;
+    int cur = load_block_id(row, lane, nblk);
+    int nxt = load_block_id(row, 32 + lane, nblk);
+    int wbase = 0;
+    const int nch = (t1 - t0 + kChunk - 1) / kChunk;
+    for (int ch = 0; ch < nch; ++ch, ++kseq) {
+      const int jb = ch * bpc;
+      if (jb >= wbase + 32) {
+        cur = nxt;
+        wbase += 32;
+        nxt = load_block_id(row, wbase + 32 + lane, nblk);
+      }
+      const int nv = min(kChunk, t1 - (t0 + ch * kChunk));
+      const int nb = (nv + p.B - 1) / p.B;
+      int id = __shfl_sync(kFull, cur, (jb - wbase + lane) & 31);
+      if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
+        raise_status(p.status, PA_STATUS_BAD_BLOCK);
+        id = 0;
+      }
+      const int stage = kseq % kStages;
+      if (!mbar_wait(&bar.empty[stage], ((kseq / kStages) & 1) ^ 1, abort)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * block_bytes);
+      __syncwarp();
+      if (lane < nb) {
+        const int y = (id * p.Hkv + kvh) * p.B;
+        uint8_t* sk = base + stage * kStage + lane * p.B * kD;
+        tma_load_2d(sk, kmap, &bar.full[stage], 0, y, policy);
+        tma_load_2d(sk + kRegion, vmap, &bar.full[stage], 0, y, policy);
+      }
+      if (ch == 0 && lane == 0 && nxt_idx < total) nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
+    }
+    if (!ok) break;
+    if (nch == 0 && lane == 0 && nxt_idx < total) nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
+    cur_idx = nxt_idx;
+    cur_pr = nxt_pr;
+  }
+  if (!ok) {
+    give_up(p, abort);
+    // Let copies already issued land before the CTA's shared memory goes away.
+    const volatile int never = 0;
+    for (uint32_t k = (kseq > (uint32_t)kStages ? kseq - kStages : 0); k < kseq; ++k)
+      mbar_wait(&bar.full[k % kStages], (k / kStages) & 1, &never);
+    for (uint32_t k = (nq > 2 ? nq - 2 : 0); k < nq; ++k) mbar_wait(&bar.qfull[k & 1], (k >> 1) & 1, &never);
+  }
+}
+
+// Byte offset of 16-byte piece c of token row r of a stage region (TMA's
+// 128-byte swizzle: pieces XOR-permuted by the row's low three bits).
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * kD + ((c ^ (r & 7)) << 4)); }
+
+__device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort) {
+  constexpr int KS = kD / 16;  // 16-dim steps of Q·Kᵀ
+  constexpr int MT = kD / 16;  // 16-dim tiles of Oᵀ = Vᵀ Pᵀ
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gq = lane >> 2;  // mma group id
+  const int tq = lane & 3;   // thread in group
+  const Bars bar = bars_at(base);
+  const int4* desc = reinterpret_cast<const int4*>(base + kOffDesc);
+  float* sO = reinterpret_cast<float*>(base + kOffO);
+  float2* sML = reinterpret_cast<float2*>(base + kOffML);
+  const uint32_t base_addr = smem_addr(base);
+  // Row of this lane's K ldmatrix address within a 16-token step: S tile
+  // 2j + h holds tokens 4(r / 2) + 2h + (r % 2), r = 0..7.
+  const int krow = 4 * ((lane & 7) >> 1) + (lane & 1);
+  uint32_t kseq = 0;
+
+  for (uint32_t n = 0;; ++n) {
+    const int slot = n & 1;
+    if (!mbar_wait(&bar.qfull[slot], (n >> 1) & 1, abort)) {
+      give_up(p, abort);
+      return;
+    }
+    const int4 d = desc[slot];
+    if (d.w < 0) return;  // no work left
+    const int s = d.x, part = d.y, kvh = d.z, ctx = d.w;
+    const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
+    const int nch = (t1 - t0 + kChunk - 1) / kChunk;
+    const int np = (ctx + p.P - 1) / p.P;
+    // Q fragments in f16, dims of each 16-dim step in the permuted order.
+    uint32_t qa[KS][2];
+    {
+      const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(base + kOffQ + slot * kQSlot);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const __nv_bfloat16* r = sq + gq * kD + ks * 16 + 4 * tq;
+        qa[ks][0] = gq < p.g ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(r)) : 0u;
+        qa[ks][1] = gq < p.g ? bf16x2_to_f16x2(*reinterpret_cast<const uint32_t*>(r + 2)) : 0u;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.qempty[slot]);
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    for (int ch = 0; ch < nch; ++ch, ++kseq) {
+      if ((int)(kseq & (kConsumerWarps - 1)) != warp) continue;
+      const int stage = kseq % kStages;
+      if (!mbar_wait(&bar.full[stage], (kseq / kStages) & 1, abort)) {
+        give_up(p, abort);
+        return;
+      }
+      const int nv = min(kChunk, t1 - (t0 + ch * kChunk));
+      const uint32_t sk = base_addr + stage * kStage;
+      const uint32_t sv = sk + kRegion;
+      if (nv < kChunk) {
+        // Rows past the context hold stale or unwritten codes (possibly
+        // NaN): zero their values; their scores are masked below.
+        uint8_t* vrow = base + stage * kStage + kRegion;
+        for (int u = lane; u < (kChunk - nv) * 8; u += 32)
+          *reinterpret_cast<uint4*>(vrow + (nv + u / 8) * kD + (u % 8) * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // S = Q Kᵀ : tiles of 8 tokens (rows = heads; only c0, c1 are real).
+      float sc[NTILES][4];
+#pragma unroll
+      for (int nt = 0; nt < NTILES; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NTILES; ++nt) {
+        const int r = 16 * (nt >> 1) + 2 * (nt & 1) + krow;
+#pragma unroll
+        for (int kb = 0; kb < KS / 4; ++kb) {
+          uint32_t w[4];
+          ldmatrix_x4(sk + swz(r, 4 * kb + (lane >> 3)), w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int ks = 4 * kb + m;
+            mma_f16_16816(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w[m]), e4m3x2_to_f16x2(w[m] >> 16));
+          }
+        }
+      }
+      // Online softmax (log2 domain) for head row gq over this chunk.
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < NTILES; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = 16 * (nt >> 1) + 4 * tq + 2 * (nt & 1) + e;
+          const float v = tok < nv ? sc[nt][e] * p.scale_log2 : -INFINITY;
+          sc[nt][e] = v;
+          mx = fmaxf(mx, v);
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = exp2f(m_run - m_new);
+      float ls = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NTILES; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - m_new);
+        sc[nt][1] = exp2f(sc[nt][1] - m_new);
+        ls += sc[nt][0] + sc[nt][1];
+      }
+      l_run = l_run * alpha + ls;
+      m_run = m_new;
+      const float a_lo = __shfl_sync(kFull, alpha, 8 * tq);
+      const float a_hi = __shfl_sync(kFull, alpha, 8 * tq + 4);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= a_lo;
+        o[mt][1] *= a_hi;
+        o[mt][2] *= a_lo;
+        o[mt][3] *= a_hi;
+      }
+      // Oᵀ += Vᵀ Pᵀ : 16 tokens per step, 16 dims per tile.
+#pragma unroll
+      for (int kt = 0; kt < KSTEPS; ++kt) {
+        const uint32_t pb0 = pack_f16x2(sc[2 * kt][0], sc[2 * kt][1]);          // tokens 4t, 4t+1
+        const uint32_t pb1 = pack_f16x2(sc[2 * kt + 1][0], sc[2 * kt + 1][1]);  // tokens 4t+2, 4t+3
+        const int r = 16 * kt + (lane & 15);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t d0, d1;
+          ldmatrix_b8_trans(sv + swz(r, mt), d0, d1);
+          mma_f16_16816(o[mt], e4m3x2_to_f16x2(d0), e4m3x2_to_f16x2(d1), e4m3x2_to_f16x2(d0 >> 16),
+                        e4m3x2_to_f16x2(d1 >> 16), pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.empty[stage]);
+    }
+
+    // ---- item epilogue: merge the four warps' states ----
+    if (n > 0 && !mbar_wait(bar.epi_done, (n - 1) & 1, abort)) {
+      give_up(p, abort);
+      return;
+    }
+    float l = l_run;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (tq == 0 && gq < p.g) sML[warp * kMaxGroup + gq] = make_float2(m_run, l);
+    float* ob = sO + warp * kMaxGroup * kOStride;
+    const int h0 = 2 * tq, h1 = 2 * tq + 1;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int dd = 16 * mt + gq;
+      if (h0 < p.g) {
+        ob[h0 * kOStride + dd] = o[mt][0];
+        ob[h0 * kOStride + dd + 8] = o[mt][2];
+      }
+      if (h1 < p.g) {
+        ob[h1 * kOStride + dd] = o[mt][1];
+        ob[h1 * kOStride + dd + 8] = o[mt][3];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.epi_full);
+    if (!mbar_wait(bar.epi_full, n & 1, abort)) {
+      give_up(p, abort);
+      return;
+    }
+    const int units = p.g * (kD / 8);
+    for (int u = threadIdx.x; u < units; u += kConsumerWarps * 32) {
+      const int h = u / (kD / 8);
+      const int d0 = (u % (kD / 8)) * 8;
+      float mw[kConsumerWarps];
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        mw[w] = sML[w * kMaxGroup + h].x;
+        M = fmaxf(M, mw[w]);
+      }
+      float L = 0.f, acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float wt = exp2f(mw[w] - M);
+        L += wt * sML[w * kMaxGroup + h].y;
+        const float4* src = reinterpret_cast<const float4*>(sO + (w * kMaxGroup + h) * kOStride + d0);
+        const float4 x0 = src[0], x1 = src[1];
+        acc[0] += wt * x0.x;
+        acc[1] += wt * x0.y;
+        acc[2] += wt * x0.z;
+        acc[3] += wt * x0.w;
+        acc[4] += wt * x1.x;
+        acc[5] += wt * x1.y;
+        acc[6] += wt * x1.z;
+        acc[7] += wt * x1.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] *= p.v_scale;  // codes -> values
+      const int qh = kvh * p.g + h;
+      if (np <= 1) {  // one partition, or an empty context (zero row)
+        uint4 pk = make_uint4(0, 0, 0, 0);
+        if (np == 1) {
+          const float inv = 1.f / L;
+          pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+          pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+          pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+          pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        }
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + ((size_t)s * p.H + qh) * kD + d0;
+        *reinterpret_cast<uint4*>(dst) = pk;
+      } else {
+        const size_t wi = ((size_t)s * p.max_parts + part) * p.H + qh;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + wi * kD + d0);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        if (d0 == 0) p.ws_ml[wi] = make_float2(M, L);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.epi_done);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                            const DecodeArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  volatile int* abort = reinterpret_cast<volatile int*>(base + kOffAbort);
+  if (threadIdx.x == 0) {
+    const Bars b = bars_at(base);
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(&b.full[k], 1);
+      mbar_init(&b.empty[k], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&b.qfull[k], 1);
+      mbar_init(&b.qempty[k], kConsumerWarps);
+    }
+    mbar_init(b.epi_full, kConsumerWarps);
+    mbar_init(b.epi_done, kConsumerWarps);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if ((threadIdx.x >> 5) == kConsumerWarps) {
+    if ((threadIdx.x & 31) == 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+    }
+    producer(&kmap, &vmap, p, base, abort);
+  } else {
+    consumer(p, base, abort);
+  }
+}
+
+}  // namespace
+
+size_t decode_fp8_smem_bytes() { return kBytes; }
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Shape {
+    int sms = 0, per_sm = 0;
+  };
+  static Shape shapes[64];
+  static std::once_flag once[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t init_err = cudaSuccess;
+  std::call_once(once[dev], [&] {
+    Shape sh;
+    init_err = cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (init_err == cudaSuccess)
+      init_err = cudaFuncSetAttribute(paged_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kBytes);
+    if (init_err == cudaSuccess)
+      init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm, paged_decode_fp8_kernel, kThreads, kBytes);
+    shapes[dev] = sh;
+  });
+  if (init_err != cudaSuccess) return init_err;
+  const Shape& sh = shapes[dev];
+  if (sh.per_sm < 1 || sh.sms < 1) return cudaErrorInvalidConfiguration;
+  const long long total = (long long)a.max_parts * a.S * a.Hkv;  // upper bound of the work items
+  const int grid = (int)std::min<long long>(total, (long long)sh.sms * sh.per_sm);
+  if (grid <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_decode_fp8_kernel, kmap, vmap, a);
+}
+
+}  // namespace pa

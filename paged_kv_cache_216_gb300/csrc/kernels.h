@@ -36,6 +36,7 @@ struct DecodeArgs {
   int max_parts;                // ceil(max_ctx / P)
   float scale_log2;             // scale * log2(e)
   int shared_items;             // the work list may hold shared-prefix items
+  float v_scale;                // FP8 caches: value of a V code = e4m3(code) * v_scale (1 otherwise)
 };
 
 constexpr int kMaxGroup = 8;
@@ -94,6 +95,12 @@ size_t decode_tc_smem_bytes(int D);
 // cache tensor maps must be made to match.
 bool decode_tc_interleaved(int D, int B);
 
+// FP8 (E4M3) caches, head_dim 128, bf16 q/out; same work list, workspace and
+// merge as the bf16 kernel.  scale_log2 must include the K scale.
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream);
+size_t decode_fp8_smem_bytes();
+
 // Work list (longest items first) for the tensor-core kernel, built on the
 // device from a.context_lens into a.hdr / a.plan.  Must precede
 // launch_decode_tc on the stream.
@@ -132,6 +139,11 @@ cudaError_t launch_lse_merge(const DecodeArgs& a, const PrefixGroups& pg, int dt
 cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
                                 void* v_cache, int num_blocks, int Hkv, int D, int B, int elem_bytes,
                                 unsigned* status, cudaStream_t stream);
+
+// bf16 tokens quantized into an E4M3 cache (codes = RNE(x / scale), saturating).
+cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
+                                    void* v_cache, int num_blocks, int Hkv, int D, int B, float k_scale,
+                                    float v_scale, unsigned* status, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* pairs, int num_pairs,
                                int num_blocks, size_t block_bytes, unsigned* status, cudaStream_t stream);

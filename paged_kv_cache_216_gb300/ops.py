@@ -12,16 +12,24 @@ import ctypes
 import numpy as np
 import torch
 
-from ._lib import PA_BF16, PA_F32, check, lib
+from ._lib import PA_BF16, PA_F32, PA_FP8_E4M3, check, lib
 
-_DTYPES = {torch.bfloat16: PA_BF16, torch.float32: PA_F32}
+_DTYPES = {torch.bfloat16: PA_BF16, torch.float32: PA_F32, torch.uint8: PA_FP8_E4M3}
+_FP8 = getattr(torch, "float8_e4m3fn", None)
+if _FP8 is not None:
+    _DTYPES[_FP8] = PA_FP8_E4M3
+
+
+def is_fp8(t: torch.Tensor) -> bool:
+    """Whether ``t`` holds E4M3 codes (float8_e4m3fn, or uint8 codes)."""
+    return _DTYPES.get(t.dtype) == PA_FP8_E4M3
 
 
 def _dtype_code(t: torch.Tensor) -> int:
     try:
         return _DTYPES[t.dtype]
     except KeyError:
-        raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32") from None
+        raise TypeError(f"unsupported dtype {t.dtype}: bfloat16, float32 or E4M3 codes") from None
 
 
 def _ptr(t):
@@ -56,6 +64,22 @@ def cache_append(k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
     _need(tuple(k.shape) == (t, hkv, d) and tuple(v.shape) == (t, hkv, d), "k, v must be [T, Hkv, D]")
     check(lib().pa_cache_append(_ptr(k), _ptr(v), _ptr(slot_mapping), t, _ptr(k_cache), _ptr(v_cache),
                                 n, hkv, d, b, _dtype_code(k_cache), _stream(stream)))
+
+
+def cache_append_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: float, stream=None) -> None:
+    """:func:`cache_append` into E4M3 caches (float8_e4m3fn or uint8
+    ``[N, Hkv, B, D]``): the bf16 tokens are stored as round-to-nearest-even
+    E4M3 codes of x / scale, saturating at ±448."""
+    _cuda_contig(k, v, slot_mapping, k_cache, v_cache)
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    _need(k.dtype == v.dtype == torch.bfloat16, "k and v must be bfloat16")
+    _need(is_fp8(k_cache) and is_fp8(v_cache), "caches must hold E4M3 codes")
+    n, hkv, b, d = k_cache.shape
+    _need(v_cache.shape == k_cache.shape, "k_cache and v_cache shapes differ")
+    t = slot_mapping.shape[0]
+    _need(tuple(k.shape) == (t, hkv, d) and tuple(v.shape) == (t, hkv, d), "k, v must be [T, Hkv, D]")
+    check(lib().pa_cache_append_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), t, _ptr(k_cache), _ptr(v_cache), n, hkv,
+                                    d, b, float(k_scale), float(v_scale), _stream(stream)))
 
 
 def copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
@@ -130,6 +154,36 @@ def prefix_groups_array(groups):
 def _groups_args(groups):
     g = prefix_groups_array(groups)
     return (ctypes.c_void_p(g.ctypes.data) if g is not None else None), (0 if g is None else g.shape[0]), g
+
+
+def paged_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                     k_scale: float, v_scale: float, out=None, partition_size: int = 0, workspace=None, plan=None,
+                     stream=None):
+    """:func:`paged_decode` over E4M3 caches written by
+    :func:`cache_append_fp8`: keys read as code · k_scale, values as
+    code · v_scale; q and out bf16, head_dim 128.  ``plan``: a work list
+    from :func:`decode_plan_host` copied to the device (counter at 0), or
+    None to build it on the device."""
+    _cuda_contig(q, k_cache, v_cache, block_tables, context_lens)
+    _need(q.dtype == torch.bfloat16, "q must be bfloat16")
+    _need(is_fp8(k_cache) and is_fp8(v_cache), "caches must hold E4M3 codes")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+          "block_tables and context_lens must be int32")
+    s, h, d = q.shape
+    n, hkv, b, d2 = k_cache.shape
+    _need(d == d2 and v_cache.shape == k_cache.shape, "head_dim mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig(out)
+    _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = decode_workspace(s, h, hkv, d, max_context_len, partition_size, q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    check(lib().pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                              _ptr(context_lens), int(max_context_len), float(scale), float(k_scale),
+                              float(v_scale), _ptr(out), s, h, hkv, d, b, n, int(partition_size), _ptr(plan),
+                              _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
 
 
 def paged_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,

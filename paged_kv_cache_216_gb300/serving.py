@@ -66,7 +66,8 @@ class StepGraphs:
 
 class ServingEngine:
     def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor, allocator: BlockAllocator, seq_ids,
-                 num_heads: int, scale: float, max_context_len: int, partition_size: int = 0, prefix_groups=None):
+                 num_heads: int, scale: float, max_context_len: int, partition_size: int = 0, prefix_groups=None,
+                 kv_scales=None):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.alloc = allocator
         self.num_heads = num_heads
@@ -81,7 +82,15 @@ class ServingEngine:
         self.width = -(-self.max_context_len // b)
         self.partition_size = ops.decode_partition_size(s, hkv, self.max_context_len, partition_size)
         self.bf16 = k_cache.dtype == torch.bfloat16
-        plan_p = self.partition_size if self.bf16 else 0
+        # E4M3 caches: new tokens arrive in bf16 and are stored as codes of
+        # x / scale; kv_scales = (k_scale, v_scale).
+        self.fp8 = ops.is_fp8(k_cache)
+        if self.fp8:
+            if kv_scales is None:
+                raise ValueError("E4M3 caches need kv_scales=(k_scale, v_scale)")
+            self.k_scale, self.v_scale = (float(x) for x in kv_scales)
+        tok_dtype = torch.bfloat16 if self.fp8 else k_cache.dtype
+        plan_p = self.partition_size if (self.bf16 or self.fp8) else 0
         offs = (ctypes.c_size_t * 5)()
         total = ctypes.c_size_t(0)
         check(lib().pa_stepper_layout(s, self.max_context_len, b, plan_p, offs, ctypes.byref(total)))
@@ -119,11 +128,11 @@ class ServingEngine:
         # come from elsewhere, and the streams/events of host transfers
         # staging per device buffer: the step's new tokens packed as [q | k | v]
         self._nq, self._nk = s * num_heads * d, s * hkv * d
-        self._stg = [torch.empty(self._nq + 2 * self._nk, dtype=k_cache.dtype, device=dev) for _ in range(2)]
+        self._stg = [torch.empty(self._nq + 2 * self._nk, dtype=tok_dtype, device=dev) for _ in range(2)]
         self.q_in = [x[:self._nq].view(s, num_heads, d) for x in self._stg]
         self.k_in = [x[self._nq:self._nq + self._nk].view(s, hkv, d) for x in self._stg]
         self.v_in = [x[self._nq + self._nk:].view(s, hkv, d) for x in self._stg]
-        self.out = [torch.empty((s, num_heads, d), dtype=k_cache.dtype, device=dev) for _ in range(2)]
+        self.out = [torch.empty((s, num_heads, d), dtype=tok_dtype, device=dev) for _ in range(2)]
         self.down_stream = torch.cuda.Stream(device=dev)
         self._tok_done = [torch.cuda.Event(), torch.cuda.Event()]
         self._step_done = [torch.cuda.Event(), torch.cuda.Event()]
@@ -176,10 +185,17 @@ class ServingEngine:
     # -- main-stream part (capturable) ---------------------------------------
     def _device(self, k, q, k_new, v_new, out, events=None):
         plan, slots, ctx, _, tables = self._dv[k]
-        ops.cache_append(k_new, v_new, slots, self.k_cache, self.v_cache)
+        if self.fp8:
+            ops.cache_append_fp8(k_new, v_new, slots, self.k_cache, self.v_cache, self.k_scale, self.v_scale)
+        else:
+            ops.cache_append(k_new, v_new, slots, self.k_cache, self.v_cache)
         if events is not None:
             events[0].record()
-        if self.bf16:
+        if self.fp8:
+            out = ops.paged_decode_fp8(q, self.k_cache, self.v_cache, tables, ctx, self.max_context_len, self.scale,
+                                       self.k_scale, self.v_scale, out=out, partition_size=self.partition_size,
+                                       workspace=self.workspace, plan=plan)
+        elif self.bf16:
             out = ops.paged_decode_planned(q, self.k_cache, self.v_cache, tables, ctx, self.max_context_len,
                                            self.scale, out, plan, self.workspace, self.partition_size,
                                            prefix_groups=self.prefix_groups)

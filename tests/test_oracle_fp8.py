@@ -172,3 +172,41 @@ def test_planted_codec_mistakes_are_caught(monkeypatch, bad):
         except AssertionError:
             failed += 1
     assert failed >= 1
+
+
+def test_fp8_serving_loop_equals_attention_over_dequantized_history():
+    """Serving steps with an E4M3 cache: every output equals dense attention
+    (scipy softmax) over each sequence's token history, each token read back
+    as decode(quantize(x)) · scale and kept contiguously by the test."""
+    import scipy.special
+
+    from oracle.serving import ServingOracle, initial_state
+
+    rng = np.random.default_rng(24)
+    b, hkv, d, h, s = 4, 2, 8, 4, 3
+    ctx = np.array([5, 9, 2], dtype=np.int32)
+    nblk, ks, vs = 20, 0.02, 0.3
+    alloc, pairs = initial_state(s, b, ctx, nblk, rng.permutation(nblk))
+    kc = fp8.quantize(rng.standard_normal((nblk, hkv, b, d)).astype(np.float32), ks)
+    vc = fp8.quantize(rng.standard_normal((nblk, hkv, b, d)).astype(np.float32), vs)
+    hist_k, hist_v = [], []
+    for i in range(s):
+        t = alloc.block_table(i)
+        n = alloc.num_tokens(i)
+        hist_k.append(fp8.decode(kc[t]).transpose(1, 0, 2, 3).reshape(hkv, -1, d)[:, :n] * ks)
+        hist_v.append(fp8.decode(vc[t]).transpose(1, 0, 2, 3).reshape(hkv, -1, d)[:, :n] * vs)
+    srv = ServingOracle(alloc, kc, vc, s, "bf16", 0.4, fp8_scales=(ks, vs))
+    for step in range(5):
+        q = bf16_bits(rng.standard_normal((s, h, d)).astype(np.float32))
+        kn = bf16_bits(rng.standard_normal((s, hkv, d)).astype(np.float32))
+        vn = bf16_bits(rng.standard_normal((s, hkv, d)).astype(np.float32))
+        _, _, out = srv.step(q, kn, vn, width=8)
+        qf = bf16_to_f32(q).astype(np.float64)
+        for i in range(s):
+            hist_k[i] = np.concatenate([hist_k[i], (fp8.decode(fp8.quantize(bf16_to_f32(kn[i]), ks)) * ks)[:, None]],
+                                       axis=1)
+            hist_v[i] = np.concatenate([hist_v[i], (fp8.decode(fp8.quantize(bf16_to_f32(vn[i]), vs)) * vs)[:, None]],
+                                       axis=1)
+            for hh in range(h):
+                p = scipy.special.softmax(0.4 * hist_k[i][hh // 2] @ qf[i, hh])
+                np.testing.assert_allclose(out[i, hh], hist_v[i][hh // 2].T @ p, rtol=0, atol=1e-12)

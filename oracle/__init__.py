@@ -21,6 +21,7 @@ Modules:
   attention  decode output by the plain definition softmax(scale·q·Kᵀ)·V
   cache      KV append (scatter into slots, also into an FP8 cache) and block copy
   fp8        E4M3 codes: quantize with a scale, decode
+  prefill    append a prompt's tokens, then causal attention of each of them
   allocator  block allocator: free list, ref-counted sharing, copy-on-write
   serving    the serving loop (allocate, append, decode) built from the above
 

@@ -37,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from workloads import WORKLOADS, context_lens, free_order, pool_blocks, queries, random_pool  # noqa: E402
-from workloads import serving_step_tokens  # noqa: E402
+from workloads import normal, serving_step_tokens  # noqa: E402
 
 DEFAULT_WORKLOAD = "mha_bf16"
 METRIC = "paged-decode KV-read GB/s"
@@ -510,6 +510,154 @@ def run_reference(args, rank, world):
     return res
 
 
+PREFILL_SHAPE = dict(num_seqs=8, cached=512, new=512, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16)
+
+
+def prefill_batch(seed: int = 11, **shape):
+    """Seeded synthetic prefill batch: every sequence has `cached` tokens in
+    the pool and `new` prompt tokens to append and attend; shuffled tables."""
+    sh = dict(PREFILL_SHAPE, **shape)
+    S, c, n, H, Hkv, D, B = (sh[k] for k in ("num_seqs", "cached", "new", "num_heads", "num_kv_heads", "head_dim",
+                                            "block_size"))
+    rng = np.random.default_rng(seed)
+    nb_seq = -(-(c + n) // B)
+    N = S * nb_seq + 8
+    perm = rng.permutation(N).astype(np.int32)
+    tables = perm[:S * nb_seq].reshape(S, nb_seq)
+    pos = c + np.arange(n)
+    slots = (tables[:, pos // B] * B + pos % B).reshape(-1).astype(np.int64)
+    T = S * n
+    return dict(q=normal((T, H, D), 1.0, "bf16", seed, 31), k=normal((T, Hkv, D), 1.0, "bf16", seed, 32),
+                v=normal((T, Hkv, D), 1.0, "bf16", seed, 33), kc=normal((N, Hkv, B, D), 1.0, "bf16", seed, 34),
+                vc=normal((N, Hkv, B, D), 1.0, "bf16", seed, 35), slots=slots, tables=tables,
+                qs=(np.arange(S + 1) * n).astype(np.int32), ctx=np.full(S, c + n, dtype=np.int32), shape=sh,
+                scale=1.0 / np.sqrt(D))
+
+
+def prefill_flops(b) -> float:
+    """Attention FLOPs of a prefill call: each new token's query head does
+    2·D flops per key for Q·Kᵀ and 2·D for P·V over its keys 0..p."""
+    sh = b["shape"]
+    keys = sum(sh["cached"] + i + 1 for i in range(sh["new"]))
+    return float(keys) * sh["num_seqs"] * sh["num_heads"] * sh["head_dim"] * 4
+
+
+def run_prefill(args, rank, world, local):
+    """One prefill call per step (append of every sequence's prompt plus its
+    causal attention) on the synthetic batch; L2 flushed between steps."""
+    import torch
+
+    import paged_kv_cache_216_gb300 as pa
+    from paged_kv_cache_216_gb300 import build
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    b = prefill_batch(seed=11 + rank)
+    sh = b["shape"]
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, k, v, kc, vc = (to_dev(b[x]) for x in ("q", "k", "v", "kc", "vc"))
+    slots, qs, ctx, tables = (to_dev(b[x]) for x in ("slots", "qs", "ctx", "tables"))
+    out = torch.empty_like(q)
+    mql, mctx = sh["new"], sh["cached"] + sh["new"]
+
+    def call(qq=q, kk=k, vv=v, oo=out):
+        pa.prefill(qq, kk, vv, slots, qs, ctx, tables, mql, mctx, b["scale"], kc, vc, out=oo)
+
+    K, W = args.steps, args.warmup
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(4 * l2 // 4, dtype=torch.int32, device=dev)
+    for _ in range(W):
+        flush.add_(1)
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.add_(1)
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    t_dev = allreduce_max(sum(a.elapsed_time(z) for a, z in ev) / 1e3, world)
+    flops = prefill_flops(b)
+    value = allreduce_sum(flops * K, world) / t_dev / 1e12
+    # end to end: inputs from pinned host memory, output back, every step
+    def pin(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    hq, hk, hv = pin(b["q"]), pin(b["k"]), pin(b["v"])
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        flush.add_(1)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        call()
+        hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
+    status = pa.get_status()
+    if status:
+        raise RuntimeError(f"device status word {status:#x} after the benchmark")
+    peaks = measured_peaks()
+    peak = peaks.get("bf16_tflops") or 1900.0
+    achieved = flops * K / t_dev / 1e12  # one GPU's calls over the slowest rank's time
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    res = {
+        "metric": "prefill attention TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(t_dev / K * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill_bf16", **sh, "tokens_per_step": sh["num_seqs"] * sh["new"],
+                   "flops_per_step": flops, "l2": "flushed before every step", "parallelism": f"replicas x{world}"},
+        "prefill_tokens_per_s": round(allreduce_sum(float(sh["num_seqs"] * sh["new"] * K), world) / t_dev, 1),
+        "e2e": {"value": round(allreduce_sum(flops * K, world) / t_e2e / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size())},
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "cache_append_kernel + prefill_kernel",
+                     "peak_source": ("measured bf16_tflops" if peaks.get("bf16_tflops") else "fallback")},
+        "clocks": clk,
+    }
+    return res
+
+
+def prefill_oracle_sample(budget_s: float):
+    """Oracle prefill on whole sequences of the bench batch for a bounded
+    time: TFLOP/s of the sample."""
+    from oracle.prefill import prefill as oracle_prefill
+
+    b = prefill_batch()
+    sh = b["shape"]
+    n = sh["new"]
+    t0 = time.perf_counter()
+    done = 0
+    while time.perf_counter() - t0 < budget_s and done < sh["num_seqs"]:
+        rows = slice(done * n, (done + 1) * n)
+        oracle_prefill(b["q"][rows], b["k"][rows], b["v"][rows], b["slots"][rows], np.array([0, n], np.int32),
+                       b["ctx"][done:done + 1], b["tables"][done:done + 1], b["kc"], b["vc"], b["scale"], "bf16")
+        done += 1
+    t = time.perf_counter() - t0
+    flops = prefill_flops(b) / sh["num_seqs"] * done
+    return flops / t / 1e12, f"oracle prefill of {done} of the {sh['num_seqs']} sequences in {t:.1f} s"
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,6 +670,8 @@ def main():
     ap.add_argument("--eager", action="store_true", help="launch every step's kernels eagerly (no CUDA graph)")
     ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",
                     help="store the KV cache as the workload's type or as E4M3 codes")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time prefill (append + causal attention of 8 x 512 new tokens after 512 cached)")
     ap.add_argument("--no-prefix-groups", action="store_true",
                     help="decode prefix-sharing sequences one by one (no shared-prefix kernel)")
     args = ap.parse_args()
@@ -531,6 +681,14 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if args.prefill:
+        res = run_prefill(args, rank, world, local)
+        if rank == 0:
+            val, desc = prefill_oracle_sample(min(args.cpu_budget, 15.0))
+            res["cpu_baseline"] = {"value": round(val, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                                   "sample": desc}
             print(json.dumps(res), flush=True)
         return
     res, eng, w = run_ours(args, rank, world, local)

@@ -215,6 +215,32 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache,
                       void* stream);
 
 /*
+ * Prefill [Day6 paragraph 2; PAK section 3.1]: append the new tokens of
+ * every sequence (a prompt, or several tokens at once), then causal
+ * attention of each of them.  Sequence s owns rows query_start[s] ..
+ * query_start[s+1]-1 of q, k, v (device int32 [num_seqs + 1], ascending,
+ * query_start[num_seqs] <= num_tokens) and has context_lens[s] tokens after
+ * the append (device int32, n_s <= context_lens[s] <= max_context_len);
+ * its new token i sits at position p = context_lens[s] - n_s + i and gets
+ *     out[row][h] = softmax(scale * K_s[0..p] q[row][h]) V_s[0..p]
+ * (K_s, V_s gathered through block_tables[s] after the append, kv = h / g).
+ *   q, out      device, [num_tokens][num_heads][head_dim] bf16
+ *   k, v        device, [num_tokens][num_kv_heads][head_dim] bf16
+ *   slot_mapping  device, [num_tokens] int64, as for pa_cache_append
+ *   max_query_len  host bound of every n_s
+ * bf16 only.  Lengths or offsets out of range set PA_STATUS_BAD_CONTEXT and
+ * that sequence's rows are left unwritten.
+ */
+int pa_prefill(const void* q, const void* k, const void* v,
+               const int64_t* slot_mapping, int num_tokens,
+               const int32_t* query_start, const int32_t* context_lens,
+               const int32_t* block_tables, int max_blocks_per_seq,
+               int max_query_len, int max_context_len, float scale,
+               void* k_cache, void* v_cache, void* out, int num_seqs,
+               int num_heads, int num_kv_heads, int head_dim, int block_size,
+               int num_blocks, int dtype, void* stream);
+
+/*
  * Paged decode over FP8 caches written by pa_cache_append_fp8: the result of
  * pa_decode with K = e4m3(code) * k_scale and V = e4m3(code) * v_scale.  q
  * and out are bf16; head_dim 128; products in FP16 on tensor cores, sums in

@@ -19,5 +19,6 @@ from .ops import (  # noqa: F401
     paged_decode_fp8,
     paged_decode_shared_prefix,
     paged_decode_static_workspace,
+    prefill,
 )
 from .serving import ServingEngine  # noqa: F401

@@ -52,6 +52,8 @@ SIGNATURES = {
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_cache_append_fp8": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_f, _c_f,
                                      _vp]),
+    "pa_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_f, _vp, _vp, _vp,
+                            _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_decode_fp8": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _c_f, _c_f, _vp, _c_int, _c_int,
                                _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_sz, _vp]),
     "pa_decode_shared_prefix": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,

@@ -397,6 +397,64 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache, c
                      plan, nullptr, 0, workspace, workspace_bytes, dtype, stream);
 }
 
+int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+               const int32_t* query_start, const int32_t* context_lens, const int32_t* block_tables,
+               int max_blocks_per_seq, int max_query_len, int max_context_len, float scale, void* k_cache,
+               void* v_cache, void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+               int block_size, int num_blocks, int dtype, void* stream) {
+  if (dtype != PA_BF16) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: bf16 only");
+  if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0 || max_query_len < 0 || max_context_len < 1 || !std::isfinite(scale))
+    return pa_fail(PA_ERR_INVALID, "pa_prefill: sizes");
+  if (num_heads % num_kv_heads) return pa_fail(PA_ERR_INVALID, "pa_prefill: num_heads % num_kv_heads != 0");
+  const int g = num_heads / num_kv_heads;
+  if (!(g == 1 || g == 2 || g == 4 || g == 8)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: heads per KV head");
+  if (!supported_shape(head_dim, block_size)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: head_dim/block_size");
+  if (cdiv(max_context_len, block_size) > max_blocks_per_seq)
+    return pa_fail(PA_ERR_INVALID, "pa_prefill: max_blocks_per_seq < ceil(max_context_len / block_size)");
+  if (max_query_len > max_context_len) return pa_fail(PA_ERR_INVALID, "pa_prefill: max_query_len > max_context_len");
+  if (num_seqs > 65535 || num_kv_heads > 65535) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: more than 65535 sequences");
+  if ((long long)max_query_len * g > (1LL << 30)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: prompt too long");
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!q || !k || !v || !slot_mapping || !query_start || !context_lens || !block_tables || !k_cache || !v_cache ||
+      !out)
+    return pa_fail(PA_ERR_INVALID, "pa_prefill: null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(out, 16) || !aligned(slot_mapping, 8) || !aligned(query_start, 4) || !aligned(context_lens, 4) ||
+      !aligned(block_tables, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_prefill: misaligned pointer");
+  pa::PrefillArgs a{};
+  int rc = status_ptr(&a.status);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The prompt's keys and values first; the attention kernel waits for them.
+  cudaError_t e = pa::launch_cache_append(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                                          num_kv_heads, head_dim, block_size, 2, a.status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_prefill append launch");
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.query_start = query_start;
+  a.context_lens = context_lens;
+  a.S = num_seqs;
+  a.T = num_tokens;
+  a.H = num_heads;
+  a.Hkv = num_kv_heads;
+  a.g = g;
+  a.D = head_dim;
+  a.B = block_size;
+  a.num_blocks = num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_ctx = max_context_len;
+  a.max_query_len = max_query_len;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  e = pa::launch_prefill(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_prefill launch");
+  return PA_OK;
+}
+
 int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
                   float k_scale, float v_scale, void* out, int num_seqs, int num_heads, int num_kv_heads,

@@ -136,6 +136,22 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
 // partitions were written as partials).
 cudaError_t launch_lse_merge(const DecodeArgs& a, const PrefixGroups& pg, int dtype, cudaStream_t stream);
 
+// Prefill: causal attention of the new tokens of each sequence.
+struct PrefillArgs {
+  const void* q;                // [T][H][D] bf16, the new tokens of all sequences one after another
+  const void* k_cache;          // [N][Hkv][B][D] bf16, the new tokens already appended
+  const void* v_cache;
+  void* out;                    // [T][H][D] bf16
+  const int32_t* block_tables;  // [S][max_blocks_per_seq]
+  const int32_t* query_start;   // [S + 1] rows of q owned by each sequence
+  const int32_t* context_lens;  // [S] tokens after the append
+  unsigned* status;
+  int S, T, H, Hkv, g, D, B;
+  int num_blocks, max_blocks_per_seq, max_ctx, max_query_len;
+  float scale_log2;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
 cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
                                 void* v_cache, int num_blocks, int Hkv, int D, int B, int elem_bytes,
                                 unsigned* status, cudaStream_t stream);

@@ -156,6 +156,33 @@ def _groups_args(groups):
     return (ctypes.c_void_p(g.ctypes.data) if g is not None else None), (0 if g is None else g.shape[0]), g
 
 
+def prefill(q, k, v, slot_mapping, query_start, context_lens, block_tables, max_query_len: int,
+            max_context_len: int, scale: float, k_cache, v_cache, out=None, stream=None):
+    """Append the new tokens ``k, v [T, Hkv, D]`` at ``slot_mapping`` and
+    return causal attention ``[T, H, D]`` of their queries ``q``: sequence s
+    owns rows ``query_start[s] .. query_start[s+1]-1`` (int32, device) and
+    has ``context_lens[s]`` tokens after the append; each new token attends
+    the sequence's tokens up to its own position.  bf16."""
+    _cuda_contig(q, k, v, slot_mapping, query_start, context_lens, block_tables, k_cache, v_cache)
+    _need(q.dtype == k.dtype == v.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16, "bf16 only")
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    _need(query_start.dtype == context_lens.dtype == block_tables.dtype == torch.int32,
+          "query_start, context_lens and block_tables must be int32")
+    t, h, d = q.shape
+    n, hkv, b, d2 = k_cache.shape
+    _need(d == d2 and tuple(k.shape) == (t, hkv, d) and v.shape == k.shape, "shapes")
+    s = context_lens.shape[0]
+    _need(query_start.shape == (s + 1,) and block_tables.shape[0] == s, "query_start [S+1], block_tables [S, ...]")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig(out)
+    check(lib().pa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping), t, _ptr(query_start), _ptr(context_lens),
+                           _ptr(block_tables), block_tables.shape[1], int(max_query_len), int(max_context_len),
+                           float(scale), _ptr(k_cache), _ptr(v_cache), _ptr(out), s, h, hkv, d, b, n, PA_BF16,
+                           _stream(stream)))
+    return out
+
+
 def paged_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
                      k_scale: float, v_scale: float, out=None, partition_size: int = 0, workspace=None, plan=None,
                      stream=None):

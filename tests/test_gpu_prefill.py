@@ -1,0 +1,145 @@
+"""Prefill on the GPU against the oracle: the appended cache bit for bit,
+the causal attention of every new token within the bf16 tolerance
+(|gpu - ref| <= 2e-2 + 1e-2 |ref|)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.attention import decode_one, gather_sequence, to_f64
+from oracle.cache import cache_append
+from oracle.prefill import prefill as oracle_prefill
+from tests._cases import assert_close, to_bits, to_dev
+from tests._lib_fixture import ensure_built
+from workloads import normal
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    ensure_built()
+    import paged_kv_cache_216_gb300 as pa
+
+    return pa
+
+
+def _batch(seed, prev, new, H, Hkv, D, B):
+    """Seeded bf16 batch: sequence s has prev[s] cached tokens and new[s]
+    new ones; tables over a shuffled pool; slots of the new tokens."""
+    rng = np.random.default_rng(seed)
+    S = len(prev)
+    ctx = np.array([p + n for p, n in zip(prev, new)], dtype=np.int32)
+    need = sum(-(-int(c) // B) for c in ctx)
+    N = need + 7
+    perm = rng.permutation(N)
+    width = max(-(-int(c) // B) for c in ctx)
+    tables = np.full((S, width), -1, dtype=np.int32)
+    it = iter(perm.tolist())
+    for s in range(S):
+        nb = -(-int(ctx[s]) // B)
+        tables[s, :nb] = [next(it) for _ in range(nb)]
+    qs = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    T = int(qs[-1])
+    slots = np.empty(T, dtype=np.int64)
+    for s in range(S):
+        for j in range(new[s]):
+            pos = prev[s] + j
+            slots[qs[s] + j] = tables[s, pos // B] * B + pos % B
+    kc = normal((N, Hkv, B, D), 1.0, "bf16", seed, 21)
+    vc = normal((N, Hkv, B, D), 1.0, "bf16", seed, 22)
+    q = normal((T, H, D), 1.0, "bf16", seed, 23)
+    k = normal((T, Hkv, D), 1.0, "bf16", seed, 24)
+    v = normal((T, Hkv, D), 1.0, "bf16", seed, 25)
+    return dict(q=q, k=k, v=v, slots=slots, qs=qs, ctx=ctx, tables=tables, kc=kc, vc=vc, scale=1.0 / np.sqrt(D))
+
+
+def _run(pa, b, max_query_len=None):
+    kc, vc = to_dev(b["kc"]), to_dev(b["vc"])
+    out = pa.prefill(to_dev(b["q"]), to_dev(b["k"]), to_dev(b["v"]), torch.from_numpy(b["slots"]).cuda(),
+                     torch.from_numpy(b["qs"]).cuda(), torch.from_numpy(b["ctx"]).cuda(),
+                     torch.from_numpy(b["tables"]).cuda(),
+                     int(np.diff(b["qs"]).max()) if max_query_len is None else max_query_len, int(b["ctx"].max()),
+                     b["scale"], kc, vc)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+CASES = {
+    # (prev cached tokens, new tokens, H, Hkv, D, B)
+    "g4_d128_b16": ([0, 5, 100, 1000], [1, 37, 64, 130], 16, 4, 128, 16),
+    "g1_d64_b32": ([0, 33], [200, 65], 4, 4, 64, 32),
+    "g8_d128_b8": ([7, 0, 300], [9, 17, 1], 16, 2, 128, 8),
+    "g2_long_prompt": ([2000], [700], 8, 4, 128, 16),
+    "g4_fresh_prompts": ([0, 0, 0], [1, 2, 63], 8, 2, 128, 32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_matches_oracle(pa, name):
+    prev, new, H, Hkv, D, B = CASES[name]
+    b = _batch(sum(new) + len(prev), prev, new, H, Hkv, D, B)
+    out, kc, vc = _run(pa, b)
+    kc_o, vc_o, ref = oracle_prefill(b["q"], b["k"], b["v"], b["slots"], b["qs"], b["ctx"], b["tables"], b["kc"],
+                                     b["vc"], b["scale"], "bf16")
+    assert np.array_equal(to_bits(kc), kc_o) and np.array_equal(to_bits(vc), vc_o)
+    assert_close(out, ref, "bf16", name)
+    assert pa.get_status() == 0
+
+
+def test_prefill_of_one_token_per_sequence_is_decode(pa):
+    """n_s = 1 everywhere: the rows equal paged decode over the appended
+    cache (both within tolerance of the same oracle values)."""
+    prev, new = [10, 77, 0, 300], [1, 1, 1, 1]
+    b = _batch(91, prev, new, 16, 4, 128, 16)
+    out, kc, vc = _run(pa, b)
+    dec = pa.paged_decode(to_dev(b["q"]), kc, vc, torch.from_numpy(b["tables"]).cuda(),
+                          torch.from_numpy(b["ctx"]).cuda(), int(b["ctx"].max()), b["scale"])
+    torch.cuda.synchronize()
+    _, _, ref = oracle_prefill(b["q"], b["k"], b["v"], b["slots"], b["qs"], b["ctx"], b["tables"], b["kc"], b["vc"],
+                               b["scale"], "bf16")
+    assert_close(out, ref, "bf16", "prefill")
+    assert_close(dec, ref, "bf16", "decode")
+
+
+def test_prefill_larger_max_query_len_and_bad_lengths(pa):
+    """A host bound above the longest prompt changes nothing; a sequence whose
+    lengths are inconsistent (more new tokens than context) is skipped with
+    PA_STATUS_BAD_CONTEXT while the others are computed."""
+    prev, new, H, Hkv, D, B = CASES["g4_d128_b16"]
+    b = _batch(7, prev, new, H, Hkv, D, B)
+    out, _, _ = _run(pa, b, max_query_len=512)
+    _, _, ref = oracle_prefill(b["q"], b["k"], b["v"], b["slots"], b["qs"], b["ctx"], b["tables"], b["kc"], b["vc"],
+                               b["scale"], "bf16")
+    assert_close(out, ref, "bf16", "max_query_len 512")
+    assert pa.get_status() == 0
+    bad = dict(b)
+    bad["ctx"] = b["ctx"].copy()
+    bad["ctx"][1] = 10  # 37 new tokens cannot fit in a context of 10
+    out2, _, _ = _run(pa, bad)
+    assert pa.get_status() == pa._lib.PA_STATUS_BAD_CONTEXT
+    rows = np.r_[b["qs"][0]:b["qs"][1], b["qs"][2]:b["qs"][4]]
+    assert_close(out2[rows], ref[rows], "bf16", "other sequences")
+
+
+def test_prefill_bench_shape_sampled(pa):
+    """The benchmark's prefill batch (8 sequences, 512 cached + 512 new
+    tokens, 32/8 heads): sampled tokens (first, last, random) of every
+    sequence against the oracle's per-token definition."""
+    S, prev_n, new_n, H, Hkv, D, B = 8, 512, 512, 32, 8, 128, 16
+    b = _batch(5, [prev_n] * S, [new_n] * S, H, Hkv, D, B)
+    out, kc, vc = _run(pa, b)
+    kc_o, vc_o = cache_append(b["kc"], b["vc"], b["k"], b["v"], b["slots"])
+    assert np.array_equal(to_bits(kc), kc_o)
+    rng = np.random.default_rng(6)
+    g = H // Hkv
+    for s in range(S):
+        for i in sorted({0, new_n - 1, int(rng.integers(new_n))}):
+            row = int(b["qs"][s]) + i
+            p = prev_n + i
+            for kv in range(Hkv):
+                kr = to_f64(gather_sequence(kc_o, b["tables"][s], p + 1, kv), "bf16")
+                vr = to_f64(gather_sequence(vc_o, b["tables"][s], p + 1, kv), "bf16")
+                ref = decode_one(to_f64(b["q"][row, kv * g:(kv + 1) * g], "bf16"), kr, vr, b["scale"])
+                assert_close(out[row, kv * g:(kv + 1) * g], ref, "bf16", f"s{s} i{i} kv{kv}")
+    assert pa.get_status() == 0

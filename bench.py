@@ -631,7 +631,7 @@ def run_prefill(args, rank, world, local):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size())},
         "gpu_launches": 2 * K,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "cache_append_kernel + prefill_kernel",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "cache_append_kernel + prefill_tc_kernel (tcgen05)",
                      "peak_source": ("measured bf16_tflops" if peaks.get("bf16_tflops") else "fallback")},
         "clocks": clk,
     }

@@ -414,6 +414,8 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
     return pa_fail(PA_ERR_INVALID, "pa_prefill: max_blocks_per_seq < ceil(max_context_len / block_size)");
   if (max_query_len > max_context_len) return pa_fail(PA_ERR_INVALID, "pa_prefill: max_query_len > max_context_len");
   if (num_seqs > 65535 || num_kv_heads > 65535) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: more than 65535 sequences");
+  if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: pool rows exceed 2^31 (TMA coordinates are 32-bit)");
   if ((long long)max_query_len * g > (1LL << 30)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: prompt too long");
   if (num_seqs == 0 || num_tokens == 0) return PA_OK;
   if (!q || !k || !v || !slot_mapping || !query_start || !context_lens || !block_tables || !k_cache || !v_cache ||
@@ -450,7 +452,16 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
   a.max_ctx = max_context_len;
   a.max_query_len = max_query_len;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  e = pa::launch_prefill(a, st);
+  if (head_dim == 128) {  // tensor-core generation 5 (tcgen05) path
+    CUtensorMap kmap, vmap;
+    rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
+    if (rc) return rc;
+    rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
+    if (rc) return rc;
+    e = pa::launch_prefill_tc(a, kmap, vmap, st);
+  } else {
+    e = pa::launch_prefill(a, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "pa_prefill launch");
   return PA_OK;
 }

@@ -151,6 +151,10 @@ struct PrefillArgs {
   float scale_log2;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// head_dim 128 on tcgen05; kmap/vmap: the bf16 cache maps with boxes of
+// [B rows x 64 dims] (not the interleaved form).
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaStream_t stream);
 
 cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
                                 void* v_cache, int num_blocks, int Hkv, int D, int B, int elem_bytes,

@@ -13,11 +13,13 @@
 //    values a tile attends, 64 tokens per stage of a 2-stage ring, as 2D TMA
 //    boxes of [B tokens x 64 dims] with 128-byte swizzle (the K-major UMMA
 //    layout);
-//  * warp 5 (MMA): per stage, S = Q Kᵀ (M 128, N 64, K 128: eight
-//    tcgen05.mma kind::f16 from shared-memory descriptors) into tensor
-//    memory, then -- once the softmax warps have written P -- O += P V
+//  * warp 5 (MMA): S = Q Kᵀ (M 128, N 64, K 128: eight tcgen05.mma
+//    kind::f16 from shared-memory descriptors) into one of two S buffers in
+//    tensor memory as soon as a stage's keys have landed, and O += P V
 //    (M 128, N 128, K 64: P read from tensor memory, V an MN-major operand
-//    in shared memory); tcgen05.commit signals the mbarriers;
+//    in shared memory) as soon as the softmax warps have written P, polling
+//    both conditions without blocking; S of the next chunk thus overlaps the
+//    softmax of this one; tcgen05.commit signals the mbarriers;
 //  * warps 0-3 (softmax): thread t owns query row t (tensor-memory lane t):
 //    it reads its 64 scores (tcgen05.ld), masks keys past its position,
 //    keeps the running max and sum, writes P as bf16 back to tensor memory
@@ -25,7 +27,9 @@
 //    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
 //    exact enough and O and the sum use the same max); at the end it reads
 //    its row of O, divides by the sum and stores it.
-// Tensor memory: O at columns 0-127, S at 128-191, P at 192-223 (256
+// Tensor memory: O at columns 0-127 and two S buffers (128-191, 192-255)
+// so that S of the next chunk is computed while the softmax works on this
+// one; P is written over the first half of its own S buffer (256 columns
 // allocated; two CTAs per SM).  Rows past the tile's valid keys are zeroed
 // in shared memory before P·V so stale cache rows cannot turn 0 x NaN into
 // NaN.  Every wait is bounded; on a time-out the kernel raises
@@ -46,19 +50,24 @@ namespace {
 constexpr int kM = 128;                 // query rows per CTA (one tensor-memory lane each)
 constexpr int kN = 64;                  // keys per stage
 constexpr int kDh = 128;                // head_dim
+// Two stages of 64 keys (four of 32 in the same shared memory measured
+// slower: the per-stage barrier round trips cost more than the deeper ring
+// saves).
 constexpr int kStagesT = 2;
 constexpr int kSoftWarps = 4;
 constexpr int kProducerWarp = kSoftWarps;
 constexpr int kMmaWarp = kSoftWarps + 1;
 constexpr int kThreadsT = (kSoftWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 0, kColS = 128, kColP = 192;
+// O at columns 0-127; S of chunk c in buffer c % 2 (columns 128-191 or
+// 192-255), and P of chunk c written over the first 32 columns of that buffer.
+constexpr uint32_t kColO = 0, kColS = 128;
 constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of the query tile
 constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of K (or V) of a stage
 constexpr int kStageT = 4 * kKVHalf;     // K half 0, K half 1, V half 0, V half 1
 constexpr int kOffStages = 2 * kQHalf;
-constexpr int kOffBars = kOffStages + kStagesT * kStageT;  // full[2], empty[2], s_full, p_full, o_final
-constexpr int kOffMisc = kOffBars + 8 * 8;                  // tensor-memory address, abort flag
+constexpr int kOffBars = kOffStages + kStagesT * kStageT;  // full[], empty[], s_full[2], p_full, o_done, o_final
+constexpr int kOffMisc = kOffBars + (2 * kStagesT + 5) * 8; // tensor-memory address, abort flag
 constexpr size_t kBytesT = 1024 + kOffMisc + 16;
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
 
@@ -113,6 +122,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t addr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// Same without waiting: several loads in flight, then one tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t addr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(addr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -120,6 +138,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&r)[16]
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// Non-blocking test of an mbarrier phase (try_wait may suspend the thread;
+// the MMA warp polls two barriers and must not sleep on either).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -158,9 +190,10 @@ __global__ void __launch_bounds__(kThreadsT, 2)
 
   uint64_t* full = reinterpret_cast<uint64_t*>(base + kOffBars);
   uint64_t* empty = full + kStagesT;
-  uint64_t* s_full = empty + kStagesT;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* o_final = p_full + 1;
+  uint64_t* s_full = empty + kStagesT;  // [2]: S of chunk c is in buffer c % 2
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 1;        // one phase per P·V
+  uint64_t* o_final = o_done + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
@@ -170,8 +203,10 @@ __global__ void __launch_bounds__(kThreadsT, 2)
       mbar_init(&full[k], 1);
       mbar_init(&empty[k], 1);
     }
-    mbar_init(s_full, 1);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(p_full, kSoftWarps * 32);
+    mbar_init(o_done, 1);
     mbar_init(o_final, 1);
     *abort = 0;
     fence_barrier_init();
@@ -207,8 +242,8 @@ __global__ void __launch_bounds__(kThreadsT, 2)
       const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
       const uint64_t policy = policy_evict_first();
       for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        if (!mbar_wait(&empty[st], ((c >> 1) & 1) ^ 1, abort)) {
+        const int st = c % kStagesT;
+        if (!mbar_wait(&empty[st], ((c / kStagesT) & 1) ^ 1, abort)) {
           *abort = 1;
           raise_status(p.status, PA_STATUS_TIMEOUT);
           break;
@@ -234,54 +269,81 @@ __global__ void __launch_bounds__(kThreadsT, 2)
       }
     }
   } else if (warp == kMmaWarp) {
+    // S(c) and P·V(c) are issued as soon as each is ready -- S(c) when its
+    // keys have landed and its buffer is free (P·V(c - 2) issued), P·V(c)
+    // when the softmax has written P(c) -- so S of the next chunk overlaps
+    // the softmax of this one without holding P·V back.  The tensor cores
+    // run one thread's MMAs in order: S(c + 2) overwrites buffer c % 2 only
+    // after P·V(c) has read P(c) from it, and the commit that releases
+    // S(c + 1) to the softmax also covers P·V(c - 1).
     const uint32_t id_s = instr_desc(kM, kN, false);
     const uint32_t id_o = instr_desc(kM, kDh, true);
-    for (int c = 0; c < nch; ++c) {
-      const int st = c & 1;
-      if (!mbar_wait(&full[st], (c >> 1) & 1, abort)) {
-        *abort = 1;
-        raise_status(p.status, PA_STATUS_TIMEOUT);
-        break;
-      }
-      uint8_t* stage = base + kOffStages + st * kStageT;
-      const int nv = min(kN, t_end - c * kN);
-      if (nv < kN) {  // rows past the tile's keys: zero values (keys are masked)
-        for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
-          const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
-          *reinterpret_cast<uint4*>(stage + (2 + hlf) * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      const uint32_t sst = sbase + kOffStages + st * kStageT;
+    int ns = 0, npv = 0;  // next S and next P·V to issue
+    bool ok = true;
+    const unsigned long long t_start = global_timer_ns();
+    unsigned spins = 0;
+    while (npv < nch) {
+      int what = 0;  // 1: issue S(ns), 2: issue P·V(npv)
       if (lane == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kDh / 16; ++kk) {
-          const int hlf = kk >> 2, w = kk & 3;
-          const uint64_t a = smem_desc(sbase + hlf * kQHalf + w * 32, 16, 1024);
-          const uint64_t b = smem_desc(sst + hlf * kKVHalf + w * 32, 16, 1024);
-          mma_ss(tmem + kColS, a, b, id_s, kk > 0);
+        if (npv < ns && mbar_test(p_full, npv & 1))
+          what = 2;
+        else if (ns < nch && ns <= npv + 1 && mbar_test(&full[ns % kStagesT], (ns / kStagesT) & 1))
+          what = 1;
+      }
+      what = __shfl_sync(0xffffffffu, what, 0);
+      if (what == 1) {
+        const int c = ns++;
+        uint8_t* stage = base + kOffStages + (c % kStagesT) * kStageT;
+        const int nv = min(kN, t_end - c * kN);
+        if (nv < kN) {  // rows past the tile's keys: zero values (keys are masked)
+          for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
+            const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
+            *reinterpret_cast<uint4*>(stage + (2 + hlf) * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
         }
-        mma_commit(s_full);
-      }
-      __syncwarp();
-      if (!mbar_wait(p_full, c & 1, abort)) {
-        *abort = 1;
-        raise_status(p.status, PA_STATUS_TIMEOUT);
-        break;
-      }
-      if (lane == 0) {
-        tc_fence_after();
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sst = sbase + kOffStages + (c % kStagesT) * kStageT;
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint64_t b = smem_desc(sst + 2 * kKVHalf + kk * 16 * 128, kKVHalf, 1024);
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, b, id_o, c > 0 || kk > 0);
+          for (int kk = 0; kk < kDh / 16; ++kk) {
+            const int hlf = kk >> 2, w = kk & 3;
+            const uint64_t a = smem_desc(sbase + hlf * kQHalf + w * 32, 16, 1024);
+            const uint64_t b = smem_desc(sst + hlf * kKVHalf + w * 32, 16, 1024);
+            mma_ss(tmem + kColS + (uint32_t)(c & 1) * kN, a, b, id_s, kk > 0);
+          }
+          mma_commit(&s_full[c & 1]);
         }
-        mma_commit(&empty[st]);
+        __syncwarp();
+        spins = 0;
+      } else if (what == 2) {
+        const int c = npv++;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sst = sbase + kOffStages + (c % kStagesT) * kStageT;
+          const uint32_t p_cols = tmem + kColS + (uint32_t)(c & 1) * kN;
+#pragma unroll
+          for (int kk = 0; kk < kN / 16; ++kk) {
+            const uint64_t b = smem_desc(sst + 2 * kKVHalf + kk * 16 * 128, kKVHalf, 1024);
+            mma_ts(tmem + kColO, p_cols + kk * 8, b, id_o, c > 0 || kk > 0);
+          }
+          mma_commit(o_done);
+          mma_commit(&empty[c % kStagesT]);
+        }
+        __syncwarp();
+        spins = 0;
+      } else if ((++spins & 63u) == 0) {
+        if (*abort || global_timer_ns() - t_start > kWaitLimitNs * 8) {
+          ok = false;
+          break;
+        }
       }
-      __syncwarp();
+    }
+    if (!ok) {
+      *abort = 1;
+      raise_status(p.status, PA_STATUS_TIMEOUT);
     }
     if (lane == 0) mma_commit(o_final);
   } else {
@@ -292,27 +354,35 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
-      if (!mbar_wait(s_full, c & 1, abort)) {
+      if (!mbar_wait(&s_full[c & 1], (c >> 1) & 1, abort)) {
         ok = false;
         break;
       }
+      const uint32_t s_cols = lane_base + kColS + (uint32_t)(c & 1) * kN;
       tc_fence_after();
+      uint32_t raw[kN];
+#pragma unroll
+      for (int i = 0; i < kN / 16; ++i) tmem_ld16_nowait(s_cols + 16 * i, raw + 16 * i);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       float sc[kN];
 #pragma unroll
-      for (int i = 0; i < kN / 16; ++i) {
-        float v[16];
-        tmem_ld16(lane_base + kColS + 16 * i, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sc[16 * i + j] = v[j];
-      }
+      for (int j = 0; j < kN; ++j) sc[j] = __uint_as_float(raw[j]);
+      // Keys t0 .. t0 + nvalid - 1 of this chunk are at or before the row's
+      // position; masking is needed only in chunks that cross it.
       const int t0 = c * kN;
-      float mx = -INFINITY;
+      const int nvalid = min(kN, pos - t0 + 1);
+      float mxr = -INFINITY;  // max of the raw (unscaled) valid scores
+      if (nvalid >= kN) {
 #pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        const float x = t0 + j <= pos ? sc[j] * p.scale_log2 : -INFINITY;
-        sc[j] = x;
-        mx = fmaxf(mx, x);
+        for (int j = 0; j < kN; ++j) mxr = fmaxf(mxr, sc[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kN; ++j) {
+          sc[j] = j < nvalid ? sc[j] : -INFINITY;
+          mxr = fmaxf(mxr, sc[j]);
+        }
       }
+      const float mx = mxr * p.scale_log2;  // scale > 0: the max of the scaled scores
       // Raise the running max (and rescale O) only when it grows past the
       // threshold; the decision is made per warp because tensor-memory
       // loads and stores are warp-wide.
@@ -320,6 +390,12 @@ __global__ void __launch_bounds__(kThreadsT, 2)
       const float m_new = grow ? mx : m_run;
       const float alpha = grow ? exp2f(m_run - m_new) : 1.f;  // m_run = -inf: alpha 0
       if (c > 0 && __any_sync(0xffffffffu, grow && m_run != -INFINITY)) {
+        // O must hold P·V(c - 1) before it is rescaled
+        if (!mbar_wait(o_done, (c - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll 1
         for (int i = 0; i < kDh / 16; ++i) {
           float v[16];
@@ -336,8 +412,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
       uint32_t pk[kN / 2];
       float ls = 0.f;
 #pragma unroll
-      for (int j = 0; j < kN / 2; ++j) {
-        const float e0 = exp2f(sc[2 * j] - base_m), e1 = exp2f(sc[2 * j + 1] - base_m);
+      for (int j = 0; j < kN / 2; ++j) {  // exp2(s * scale - max): one FMA per score
+        const float e0 = exp2f(fmaf(sc[2 * j], p.scale_log2, -base_m));
+        const float e1 = exp2f(fmaf(sc[2 * j + 1], p.scale_log2, -base_m));
         ls += e0 + e1;
         pk[j] = pack_bf16x2(e0, e1);
       }
@@ -347,7 +424,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) w[j] = pk[16 * i + j];
-        tmem_st16(lane_base + kColP + 16 * i, w);
+        tmem_st16(s_cols + 16 * i, w);  // P over the first 32 columns of its S buffer
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();

@@ -217,6 +217,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = workload_for(args.workload, rank)
+    if args.partition_size is not None:
+        w = w.replace(partition_size=args.partition_size)
     K, W = args.steps, args.warmup
     Kp = K + (K % 2)  # untimed pass that launches every per-step graph once (even: same buffer parity)
     # warm-up, graph warm-up, timed run, roofline warm-up, roofline run, end-to-end run
@@ -670,6 +672,8 @@ def main():
     ap.add_argument("--eager", action="store_true", help="launch every step's kernels eagerly (no CUDA graph)")
     ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",
                     help="store the KV cache as the workload's type or as E4M3 codes")
+    ap.add_argument("--partition-size", type=int, default=None,
+                    help="split-K partition size in tokens (default: the workload's, 0 = library choice)")
     ap.add_argument("--prefill", action="store_true",
                     help="time prefill (append + causal attention of 8 x 512 new tokens after 512 cached)")
     ap.add_argument("--no-prefix-groups", action="store_true",

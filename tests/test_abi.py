@@ -97,7 +97,11 @@ def test_append_and_copy_reject_bad_arguments(L):
 def test_partition_and_workspace_sizing(L):
     # explicit partition sizes pass through; auto sizing is a multiple of 32
     assert L.pa_decode_partition_size(8, 8, 131072, 512) == 512
-    assert L.pa_decode_partition_size(256, 8, 4116, 0) == 512
+    # a wide batch: one partition per context up to 4096 tokens, else 4096
+    assert L.pa_decode_partition_size(256, 8, 4116, 0) == 4096
+    assert L.pa_decode_partition_size(32, 32, 2068, 0) == 2080
+    # a narrow one keeps 512-token partitions (or smaller, for enough items)
+    assert L.pa_decode_partition_size(64, 8, 8200, 0) == 512
     p = L.pa_decode_partition_size(1, 1, 5000, 0)
     assert p % 32 == 0 and 64 <= p < 512
     assert L.pa_decode_partition_size(1, 1, 100, 33) == -1

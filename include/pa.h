@@ -228,7 +228,9 @@ int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache,
  *   k, v        device, [num_tokens][num_kv_heads][head_dim] bf16
  *   slot_mapping  device, [num_tokens] int64, as for pa_cache_append
  *   max_query_len  host bound of every n_s
- * bf16 only.  Lengths or offsets out of range set PA_STATUS_BAD_CONTEXT and
+ * bf16 only; heads per KV head 1, 2, 4 or 8; up to 65535 sequences and,
+ * for head_dim 128, ceil(max_query_len * g / 128) <= 65535 (PA_ERR_UNSUPPORTED
+ * beyond).  Lengths or offsets out of range set PA_STATUS_BAD_CONTEXT and
  * that sequence's rows are left unwritten.
  */
 int pa_prefill(const void* q, const void* k, const void* v,

@@ -427,6 +427,8 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
   if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
     return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: pool rows exceed 2^31 (TMA coordinates are 32-bit)");
   if ((long long)max_query_len * g > (1LL << 30)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: prompt too long");
+  if (head_dim == 128 && cdiv(max_query_len * g, 128) > 65535)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: more than 65535 query tiles of 128 rows");
   if (num_seqs == 0 || num_tokens == 0) return PA_OK;
   if (!q || !k || !v || !slot_mapping || !query_start || !context_lens || !block_tables || !k_cache || !v_cache ||
       !out)

@@ -121,10 +121,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-__device__ __forceinline__ int load_block_id(const int32_t* row, int rel, int nblk) {
-  return rel < nblk ? __ldg(row + rel) : 0;
-}
-
 __device__ __forceinline__ void give_up(const DecodeArgs& p, volatile int* abort) {
   *abort = 1;
   raise_status(p.status, PA_STATUS_TIMEOUT);

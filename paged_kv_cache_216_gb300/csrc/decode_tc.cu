@@ -95,10 +95,6 @@ __device__ __forceinline__ Bars bars_at(uint8_t* base) {
   return b;
 }
 
-__device__ __forceinline__ int load_block_id(const int32_t* row, int rel, int nblk) {
-  return rel < nblk ? __ldg(row + rel) : 0;
-}
-
 __device__ __forceinline__ void give_up(const DecodeArgs& p, volatile int* abort) {
   *abort = 1;
   raise_status(p.status, PA_STATUS_TIMEOUT);

@@ -150,6 +150,12 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Entry `rel` of a block-table row of `nblk` valid entries (0 past the end):
+// producer warps load 32 entries at once, one per lane.
+__device__ __forceinline__ int load_block_id(const int32_t* row, int rel, int nblk) {
+  return rel < nblk ? __ldg(row + rel) : 0;
+}
+
 __device__ __forceinline__ void raise_status(unsigned* status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }

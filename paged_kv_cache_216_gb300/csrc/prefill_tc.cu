@@ -12,7 +12,9 @@
 //  * warp 4 (producer): after griddepcontrol.wait, streams the keys and
 //    values a tile attends, 64 tokens per stage of a 2-stage ring, as 2D TMA
 //    boxes of [B tokens x 64 dims] with 128-byte swizzle (the K-major UMMA
-//    layout);
+//    layout), lane b issuing block b of a chunk from block-table entries
+//    fetched 32 at a time; keys and values have separate barriers and keys
+//    run a chunk ahead, released as soon as S has read them;
 //  * warp 5 (MMA): S = Q Kᵀ (M 128, N 64, K 128: eight tcgen05.mma
 //    kind::f16 from shared-memory descriptors) into one of two S buffers in
 //    tensor memory as soon as a stage's keys have landed, and O += P V
@@ -66,8 +68,9 @@ constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of the quer
 constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of K (or V) of a stage
 constexpr int kStageT = 4 * kKVHalf;     // K half 0, K half 1, V half 0, V half 1
 constexpr int kOffStages = 2 * kQHalf;
-constexpr int kOffBars = kOffStages + kStagesT * kStageT;  // full[], empty[], s_full[2], p_full, o_done, o_final
-constexpr int kOffMisc = kOffBars + (2 * kStagesT + 5) * 8; // tensor-memory address, abort flag
+// full_k[], full_v[], empty_k[], empty_v[], s_full[2], p_full[2], o_done, o_final, q_full
+constexpr int kOffBars = kOffStages + kStagesT * kStageT;
+constexpr int kOffMisc = kOffBars + (4 * kStagesT + 7) * 8; // tensor-memory address, abort flag
 constexpr size_t kBytesT = 1024 + kOffMisc + 16;
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
 
@@ -170,8 +173,10 @@ __global__ void __launch_bounds__(kThreadsT, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = blockIdx.z, kvh = blockIdx.y;
-  const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest first
+  // The tile index is the slowest grid dimension and runs backwards, so the
+  // tiles with the most keys start first across all sequences and heads.
+  const int kvh = blockIdx.x, s = blockIdx.y;
+  const int tile = (int)gridDim.z - 1 - (int)blockIdx.z;
 
   const int q0 = __ldg(p.query_start + s), q1 = __ldg(p.query_start + s + 1);
   const int ctx = __ldg(p.context_lens + s);
@@ -188,24 +193,33 @@ __global__ void __launch_bounds__(kThreadsT, 2)
   const int t_end = first_pos + last_row / p.g + 1;  // keys the tile attends
   const int nch = (t_end + kN - 1) / kN;
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + kOffBars);
-  uint64_t* empty = full + kStagesT;
-  uint64_t* s_full = empty + kStagesT;  // [2]: S of chunk c is in buffer c % 2
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 1;        // one phase per P·V
+  // Keys and values of a stage have their own barriers: the keys of chunk c
+  // are released when S(c) completes, the values when P·V(c) does.
+  uint64_t* full_k = reinterpret_cast<uint64_t*>(base + kOffBars);
+  uint64_t* full_v = full_k + kStagesT;
+  uint64_t* empty_k = full_v + kStagesT;
+  uint64_t* empty_v = empty_k + kStagesT;
+  uint64_t* s_full = empty_v + kStagesT;  // [2]: S of chunk c is in buffer c % 2
+  uint64_t* p_full = s_full + 2;          // [2]: P of chunk c is in S buffer c % 2
+  uint64_t* o_done = p_full + 2;          // one phase per P·V
   uint64_t* o_final = o_done + 1;
+  uint64_t* q_full = o_final + 1;         // the query tile is in shared memory
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
 
   if (tid == 0) {
     for (int k = 0; k < kStagesT; ++k) {
-      mbar_init(&full[k], 1);
-      mbar_init(&empty[k], 1);
+      mbar_init(&full_k[k], 1);
+      mbar_init(&full_v[k], 1);
+      mbar_init(&empty_k[k], 1);
+      mbar_init(&empty_v[k], 1);
     }
+    mbar_init(q_full, kSoftWarps * 32);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, kSoftWarps * 32);
+    mbar_init(&p_full[0], kSoftWarps * 32);
+    mbar_init(&p_full[1], kSoftWarps * 32);
     mbar_init(o_done, 1);
     mbar_init(o_final, 1);
     *abort = 0;
@@ -216,57 +230,75 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // Query tile (an input, not written by the append), K-major with swizzle.
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  for (int i = tid; i < kM * 16; i += kThreadsT) {
-    const int r = i >> 4, u = i & 15;
-    const int gr = row0 + r;
-    const uint32_t off = kmajor_off(r, u, kM);
-    if (gr < rows) {
-      const int h = kvh * p.g + gr % p.g;
-      cp_async16(sbase + off, q + ((size_t)(q0 + gr / p.g) * p.H + h) * kDh + u * 8);
-    } else {
-      *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
-    }
-  }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  fence_proxy_async_smem();  // the query tile is read by the tensor cores (async proxy)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
   if (warp == kProducerWarp) {
-    if (lane == 0) {
-      pdl_wait_primary();  // the prompt's keys and values are in the cache from here on
-      const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-      const uint64_t policy = policy_evict_first();
-      for (int c = 0; c < nch; ++c) {
-        const int st = c % kStagesT;
-        if (!mbar_wait(&empty[st], ((c / kStagesT) & 1) ^ 1, abort)) {
-          *abort = 1;
-          raise_status(p.status, PA_STATUS_TIMEOUT);
-          break;
+    // The whole warp: lane b loads block b of a chunk.  Block-table entries
+    // are fetched 32 at a time, one per lane, a window ahead, so no TMA
+    // issue waits on a dependent table load.
+    pdl_wait_primary();  // the prompt's keys and values are in the cache from here on
+    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+    const int nblk = (t_end + p.B - 1) / p.B;
+    const int bpc = kN / p.B;  // blocks per chunk (block sizes 8, 16, 32)
+    const uint64_t policy = policy_evict_first();
+    int cur = load_block_id(row, lane, nblk);
+    int nxt = load_block_id(row, 32 + lane, nblk);
+    int wbase = 0, id_prev = 0;
+    bool alive = true;
+    // Keys run one chunk ahead of values: K(j) waits for S(j - 2) and
+    // V(j - 1) for P·V(j - 3), and the tensor pipe completes S(j - 2),
+    // P·V(j - 3), S(j - 1), ... in that order, so neither wait holds the
+    // other back.
+    for (int j = 0; j <= nch && alive; ++j) {
+      int id = 0;
+      if (j < nch) {
+        const int jb = j * bpc;
+        if (jb >= wbase + 32) {
+          cur = nxt;
+          wbase += 32;
+          nxt = load_block_id(row, wbase + 32 + lane, nblk);
         }
-        const int t0 = c * kN;
-        const int nv = min(kN, t_end - t0);
-        const int nb = (nv + p.B - 1) / p.B;
-        mbar_arrive_expect_tx(&full[st], (uint32_t)(nb * p.B * 128 * 4));
-        uint8_t* dst = base + kOffStages + st * kStageT;
-        for (int j = 0; j < nb; ++j) {
-          int blk = __ldg(table + t0 / p.B + j);
-          if ((unsigned)blk >= (unsigned)p.num_blocks) {
-            raise_status(p.status, PA_STATUS_BAD_BLOCK);
-            blk = 0;
-          }
-          const int y = (blk * p.Hkv + kvh) * p.B;
-          uint8_t* d = dst + j * p.B * 128;
-          tma_load_2d(d, &kmap, &full[st], 0, y, policy);
-          tma_load_2d(d + kKVHalf, &kmap, &full[st], 64, y, policy);
-          tma_load_2d(d + 2 * kKVHalf, &vmap, &full[st], 0, y, policy);
-          tma_load_2d(d + 3 * kKVHalf, &vmap, &full[st], 64, y, policy);
+        id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
+        const int nb = (min(kN, t_end - j * kN) + p.B - 1) / p.B;
+        if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
+          raise_status(p.status, PA_STATUS_BAD_BLOCK);
+          id = 0;
         }
       }
+#pragma unroll 1
+      for (int kv = 0; kv < 2; ++kv) {
+        const int c = j - kv;
+        if (c < 0 || c >= nch) continue;
+        const int st = c % kStagesT;
+        const int nb = (min(kN, t_end - c * kN) + p.B - 1) / p.B;
+        uint64_t* fb = kv == 0 ? &full_k[st] : &full_v[st];
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(kv == 0 ? &empty_k[st] : &empty_v[st], ((c / kStagesT) & 1) ^ 1, abort);
+          if (ok) {
+            mbar_arrive_expect_tx(fb, (uint32_t)(nb * p.B * 128 * 2));
+          } else {
+            *abort = 1;
+            raise_status(p.status, PA_STATUS_TIMEOUT);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          alive = false;
+          break;
+        }
+        __syncwarp();  // the expected byte count is set before any copy can land
+        if (lane < nb) {
+          const int y = ((kv == 0 ? id : id_prev) * p.Hkv + kvh) * p.B;
+          uint8_t* d = base + kOffStages + st * kStageT + kv * 2 * kKVHalf + lane * p.B * 128;
+          const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
+          tma_load_2d(d, map, fb, 0, y, policy);
+          tma_load_2d(d + kKVHalf, map, fb, 64, y, policy);
+        }
+      }
+      id_prev = id;
     }
   } else if (warp == kMmaWarp) {
     // S(c) and P·V(c) are issued as soon as each is ready -- S(c) when its
@@ -275,35 +307,29 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     // the softmax of this one without holding P·V back.  The tensor cores
     // run one thread's MMAs in order: S(c + 2) overwrites buffer c % 2 only
     // after P·V(c) has read P(c) from it, and the commit that releases
-    // S(c + 1) to the softmax also covers P·V(c - 1).
+    // S(c + 1) to the softmax also covers P·V(c - 1).  P(c) is signalled on
+    // p_full[c % 2]: the softmax can finish P(c + 1) before this warp has
+    // seen P(c), but not P(c + 2), which needs S(c + 2), so neither barrier
+    // runs a phase ahead of the poll.
     const uint32_t id_s = instr_desc(kM, kN, false);
     const uint32_t id_o = instr_desc(kM, kDh, true);
     int ns = 0, npv = 0;  // next S and next P·V to issue
-    bool ok = true;
+    bool ok = true, q_ready = false;
     const unsigned long long t_start = global_timer_ns();
     unsigned spins = 0;
     while (npv < nch) {
       int what = 0;  // 1: issue S(ns), 2: issue P·V(npv)
       if (lane == 0) {
-        if (npv < ns && mbar_test(p_full, npv & 1))
+        if (npv < ns && mbar_test(&p_full[npv & 1], (npv >> 1) & 1) &&
+            mbar_test(&full_v[npv % kStagesT], (npv / kStagesT) & 1))
           what = 2;
-        else if (ns < nch && ns <= npv + 1 && mbar_test(&full[ns % kStagesT], (ns / kStagesT) & 1))
+        else if (ns < nch && ns <= npv + 1 && (q_ready || (q_ready = mbar_test(q_full, 0))) &&
+                 mbar_test(&full_k[ns % kStagesT], (ns / kStagesT) & 1))
           what = 1;
       }
       what = __shfl_sync(0xffffffffu, what, 0);
       if (what == 1) {
         const int c = ns++;
-        uint8_t* stage = base + kOffStages + (c % kStagesT) * kStageT;
-        const int nv = min(kN, t_end - c * kN);
-        if (nv < kN) {  // rows past the tile's keys: zero values (keys are masked)
-          for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
-            const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
-            *reinterpret_cast<uint4*>(stage + (2 + hlf) * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
         if (lane == 0) {
           tc_fence_after();
           const uint32_t sst = sbase + kOffStages + (c % kStagesT) * kStageT;
@@ -315,11 +341,23 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             mma_ss(tmem + kColS + (uint32_t)(c & 1) * kN, a, b, id_s, kk > 0);
           }
           mma_commit(&s_full[c & 1]);
+          mma_commit(&empty_k[c % kStagesT]);
         }
         __syncwarp();
         spins = 0;
       } else if (what == 2) {
         const int c = npv++;
+        uint8_t* stage = base + kOffStages + (c % kStagesT) * kStageT;
+        const int nv = min(kN, t_end - c * kN);
+        if (nv < kN) {  // value rows past the tile's keys: zeros (their keys are masked)
+          for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
+            const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
+            *reinterpret_cast<uint4*>(stage + (2 + hlf) * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
         if (lane == 0) {
           tc_fence_after();
           const uint32_t sst = sbase + kOffStages + (c % kStagesT) * kStageT;
@@ -330,7 +368,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
             mma_ts(tmem + kColO, p_cols + kk * 8, b, id_o, c > 0 || kk > 0);
           }
           mma_commit(o_done);
-          mma_commit(&empty[c % kStagesT]);
+          mma_commit(&empty_v[c % kStagesT]);
         }
         __syncwarp();
         spins = 0;
@@ -347,6 +385,23 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     }
     if (lane == 0) mma_commit(o_final);
   } else {
+    // Query tile (an input, not written by the append), K-major with
+    // 128-byte swizzle; loaded here so that it overlaps the first stages.
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    for (int i = tid; i < kM * 16; i += kSoftWarps * 32) {
+      const int rr = i >> 4, u = i & 15;
+      const int gr = row0 + rr;
+      const uint32_t off = kmajor_off(rr, u, kM);
+      if (gr < rows) {
+        const int h = kvh * p.g + gr % p.g;
+        cp_async16(sbase + off, q + ((size_t)(q0 + gr / p.g) * p.H + h) * kDh + u * 8);
+      } else {
+        *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();  // the query tile is read by the tensor cores (async proxy)
+    mbar_arrive(q_full);
     // softmax: thread tid owns row tid (tensor-memory lane tid)
     const int r = row0 + tid;
     const int pos = r < rows ? first_pos + r / p.g : -1;  // keys 0 .. pos
@@ -428,7 +483,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[c & 1]);
     }
     if (ok && mbar_wait(o_final, 0, abort)) {
       tc_fence_after();
@@ -474,6 +529,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
                               cudaStream_t stream) {
   const int tiles = (a.max_query_len * a.g + kM - 1) / kM;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
+  if (tiles > 65535 || a.S > 65535 || a.Hkv > 65535) return cudaErrorInvalidConfiguration;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -485,7 +541,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
   });
   if (init_err != cudaSuccess) return init_err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.Hkv, (unsigned)a.S);
+  cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)a.S, (unsigned)tiles);
   cfg.blockDim = dim3(kThreadsT);
   cfg.dynamicSmemBytes = kBytesT;
   cfg.stream = stream;

@@ -94,6 +94,35 @@ def test_append_and_copy_reject_bad_arguments(L):
     assert L.pa_copy_blocks(f, f, f, 0, 10, 2, 128, 16, 1, None) == 0
 
 
+def _prefill_args(**over):
+    f = ctypes.c_void_p(0x100000)
+    a = dict(q=f, k=f, v=f, slots=f, T=64, qs=f, ctx=f, bt=f, mb=8, mql=64, maxctx=128, scale=0.1, kc=f, vc=f,
+             out=f, S=1, H=8, Hkv=2, D=128, B=16, N=16, dtype=1, stream=None)
+    a.update(over)
+    return [a[k] for k in ("q", "k", "v", "slots", "T", "qs", "ctx", "bt", "mb", "mql", "maxctx", "scale", "kc",
+                           "vc", "out", "S", "H", "Hkv", "D", "B", "N", "dtype", "stream")]
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H=12, Hkv=4), -2),              # g = 3
+    (dict(H=32, Hkv=2), -2),              # g = 16
+    (dict(D=96), -2),
+    (dict(dtype=2), -2),                  # FP8 caches are decode-only
+    (dict(dtype=0), -2),                  # fp16
+    (dict(mql=200), -1),                  # longer than the context
+    (dict(mb=4), -1),                     # 4 blocks of 16 < 128 tokens
+    (dict(S=70000), -2),
+    # 8 heads per KV head x 1.1M prompt tokens = 68750 query tiles of 128 rows
+    (dict(H=16, Hkv=2, mql=1_100_000, maxctx=1_100_000, mb=70_000), -2),
+    (dict(q=ctypes.c_void_p(0)), -1),
+    (dict(q=ctypes.c_void_p(0x100004)), -1),  # misaligned
+])
+def test_prefill_rejects_bad_arguments_without_a_launch(L, over, code):
+    rc = L.pa_prefill(*_prefill_args(**over))
+    assert rc == code
+    assert L.pa_last_error()
+
+
 def test_partition_and_workspace_sizing(L):
     # explicit partition sizes pass through; auto sizing is a multiple of 32
     assert L.pa_decode_partition_size(8, 8, 131072, 512) == 512

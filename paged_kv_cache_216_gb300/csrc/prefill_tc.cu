@@ -7,35 +7,38 @@
 // and values were appended into their blocks first, "Day 6/90 of Inference
 // Engineering", PagedAttention notes, paragraph 2).
 //
-// One CTA per (sequence, KV head, tile of 128 query rows), the rows being
-// (new token, query head) pairs, token-major; tiles longest first.  Roles:
-//  * warp 4 (producer): after griddepcontrol.wait, streams the keys and
-//    values a tile attends, 64 tokens per stage of a 2-stage ring, as 2D TMA
-//    boxes of [B tokens x 64 dims] with 128-byte swizzle (the K-major UMMA
-//    layout), lane b issuing block b of a chunk from block-table entries
-//    fetched 32 at a time; keys and values have separate barriers and keys
-//    run a chunk ahead, released as soon as S has read them;
-//  * warp 5 (MMA): S = Q Kᵀ (M 128, N 64, K 128: eight tcgen05.mma
-//    kind::f16 from shared-memory descriptors) into one of two S buffers in
-//    tensor memory as soon as a stage's keys have landed, and O += P V
-//    (M 128, N 128, K 64: P read from tensor memory, V an MN-major operand
-//    in shared memory) as soon as the softmax warps have written P, polling
-//    both conditions without blocking; S of the next chunk thus overlaps the
-//    softmax of this one; tcgen05.commit signals the mbarriers;
-//  * warps 0-3 (softmax): thread t owns query row t (tensor-memory lane t):
-//    it reads its 64 scores (tcgen05.ld), masks keys past its position,
-//    keeps the running max and sum, writes P as bf16 back to tensor memory
+// One CTA per (sequence, KV head, pair of adjacent tiles of 128 query rows),
+// the rows being (new token, query head) pairs, token-major; pairs with the
+// most keys first.  Both tiles read every stage of keys and values, so each
+// TMA box feeds 256 rows.  Roles (352 threads, one CTA per SM):
+//  * warps 8 and 9 (producers): after griddepcontrol.wait, stream the keys
+//    (warp 8) and values (warp 9) the pair attends, 128 tokens per stage,
+//    into rings of their own (3 stages of keys, 2 of values), as 2D TMA boxes of [B tokens x 64 dims]
+//    with 128-byte swizzle (the K-major UMMA layout); lane b issues block b
+//    of a chunk from block-table entries fetched 32 at a time; a stage of
+//    keys is released as soon as both tiles' S have read it;
+//  * warp 10 (MMA): one thread issues, per tile, S = Q Kᵀ (M 128, N 128,
+//    K 128: eight tcgen05.mma kind::f16 from shared-memory descriptors)
+//    into the tile's S and O += P V (M 128, N 128, K 128: eight MMAs, P read
+//    from tensor memory, V an MN-major operand in shared memory), in a fixed
+//    order -- per chunk c and tile, P·V(c) and then S(c + 1) -- waiting for
+//    one barrier at a time, so the tensor cores work for one tile while the
+//    other tile's softmax runs (ping-pong); tcgen05.commit signals the
+//    mbarriers;
+//  * warps 0-3 and 4-7 (softmax, one warpgroup per tile): thread t of a
+//    warpgroup owns query row t of its tile (tensor-memory lane t): it
+//    reads its 128 scores (tcgen05.ld), masks keys past its position, keeps
+//    the running max and sum, writes P as bf16 back to tensor memory
 //    (tcgen05.st) and rescales its row of O only when its max grows by more
 //    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
 //    exact enough and O and the sum use the same max); at the end it reads
-//    its row of O, divides by the sum and stores it.
-// Tensor memory: O at columns 0-127 and two S buffers (128-191, 192-255)
-// so that S of the next chunk is computed while the softmax works on this
-// one; P is written over the first half of its own S buffer (256 columns
-// allocated; two CTAs per SM).  Rows past the tile's valid keys are zeroed
-// in shared memory before P·V so stale cache rows cannot turn 0 x NaN into
-// NaN.  Every wait is bounded; on a time-out the kernel raises
-// PA_STATUS_TIMEOUT and stops issuing work.
+//    its row of O, divides by the sum and stores it.  Each warpgroup loads
+//    its own query tile while the first stages land.
+// Tensor memory (all 512 columns): O of tile t at columns 128t..128t+127 and
+// its S at 256 + 128t; P is written over the first half of its S.  Value rows past the pair's keys are zeroed in
+// shared memory before the first P·V of that stage so stale cache rows
+// cannot turn 0 x NaN into NaN.  Every wait is bounded; on a time-out the
+// kernel raises PA_STATUS_TIMEOUT and stops issuing work.
 
 #include <cuda_bf16.h>
 
@@ -49,29 +52,33 @@
 namespace pa {
 namespace {
 
-constexpr int kM = 128;                 // query rows per CTA (one tensor-memory lane each)
-constexpr int kN = 64;                  // keys per stage
+constexpr int kM = 128;                 // query rows per tile (one tensor-memory lane each)
+constexpr int kTiles = 2;               // query tiles per CTA, sharing every stage
+constexpr int kN = 128;                 // keys per stage (the N of S = Q Kᵀ)
 constexpr int kDh = 128;                // head_dim
-// Two stages of 64 keys (four of 32 in the same shared memory measured
-// slower: the per-stage barrier round trips cost more than the deeper ring
-// saves).
-constexpr int kStagesT = 2;
-constexpr int kSoftWarps = 4;
-constexpr int kProducerWarp = kSoftWarps;
-constexpr int kMmaWarp = kSoftWarps + 1;
-constexpr int kThreadsT = (kSoftWarps + 2) * 32;
-constexpr uint32_t kTmemCols = 256;
-// O at columns 0-127; S of chunk c in buffer c % 2 (columns 128-191 or
-// 192-255), and P of chunk c written over the first 32 columns of that buffer.
-constexpr uint32_t kColO = 0, kColS = 128;
-constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of the query tile
-constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of K (or V) of a stage
-constexpr int kStageT = 4 * kKVHalf;     // K half 0, K half 1, V half 0, V half 1
-constexpr int kOffStages = 2 * kQHalf;
-// full_k[], full_v[], empty_k[], empty_v[], s_full[2], p_full[2], o_done, o_final, q_full
-constexpr int kOffBars = kOffStages + kStagesT * kStageT;
-constexpr int kOffMisc = kOffBars + (4 * kStagesT + 7) * 8; // tensor-memory address, abort flag
+constexpr int kStagesK = 3;             // stages in the key ring
+constexpr int kStagesV = 2;             // stages in the value ring
+constexpr int kSoftWarps = 4;           // per tile
+constexpr int kProducerWarp = kTiles * kSoftWarps;  // keys; the next warp streams values
+constexpr int kMmaWarp = kProducerWarp + 2;
+constexpr int kThreadsT = (kTiles * kSoftWarps + 3) * 32;
+constexpr uint32_t kTmemCols = 512;
+// O of tile t at columns 128t..128t+127, S of tile t at 256 + 128t, and P
+// (bf16 pairs) written over the first 64 columns of its S.
+constexpr uint32_t kColO = 0, kColS = 256;
+constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of a query tile
+constexpr int kQTile = 2 * kQHalf;
+constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage of K (or V)
+constexpr int kKVStage = 2 * kKVHalf;
+constexpr int kOffK = kTiles * kQTile;
+constexpr int kOffV = kOffK + kStagesK * kKVStage;
+constexpr int kOffBars = kOffV + kStagesV * kKVStage;
+// full_k[], empty_k[], full_v[], empty_v[]; per tile s_full, p_full,
+// o_final, q_full
+constexpr int kTileBars = 4;
+constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars) * 8; // tensor-memory address, abort flag
 constexpr size_t kBytesT = 1024 + kOffMisc + 16;
+static_assert(kBytesT <= 227 * 1024, "shared memory of one CTA");
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -143,20 +150,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&r)[16]
       : "memory");
 }
 
-// Non-blocking test of an mbarrier phase (try_wait may suspend the thread;
-// the MMA warp polls two barriers and must not sleep on either).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -167,61 +160,67 @@ __device__ __forceinline__ uint32_t kmajor_off(int r, int u, int rows) {
   return (uint32_t)((u >> 3) * rows * 128 + r * 128 + (((u & 7) ^ (r & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kThreadsT, 2)
+__global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const PrefillArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // The tile index is the slowest grid dimension and runs backwards, so the
-  // tiles with the most keys start first across all sequences and heads.
+  // The pair index is the slowest grid dimension and runs backwards, so the
+  // pairs with the most keys start first across all sequences and heads.
   const int kvh = blockIdx.x, s = blockIdx.y;
-  const int tile = (int)gridDim.z - 1 - (int)blockIdx.z;
+  const int pair = (int)gridDim.z - 1 - (int)blockIdx.z;
 
   const int q0 = __ldg(p.query_start + s), q1 = __ldg(p.query_start + s + 1);
   const int ctx = __ldg(p.context_lens + s);
   const int n_new = q1 - q0;
   const int rows = n_new * p.g;
   if (q0 < 0 || n_new < 0 || n_new > p.max_query_len || ctx < n_new || ctx > p.max_ctx || q1 > p.T) {
-    if (tile == 0 && kvh == 0 && tid == 0) raise_status(p.status, PA_STATUS_BAD_CONTEXT);
+    if (pair == 0 && kvh == 0 && tid == 0) raise_status(p.status, PA_STATUS_BAD_CONTEXT);
     return;
   }
-  const int row0 = tile * kM;
-  if (row0 >= rows) return;
   const int first_pos = ctx - n_new;
-  const int last_row = min(rows, row0 + kM) - 1;
-  const int t_end = first_pos + last_row / p.g + 1;  // keys the tile attends
-  const int nch = (t_end + kN - 1) / kN;
+  // Keys each tile attends (0 for a tile past the sequence's rows) and the
+  // 64-key chunks that hold them; tile 1 is the later one, so it attends
+  // at least as many keys as tile 0.
+  const int row00 = pair * kTiles * kM, row01 = row00 + kM;
+  if (row00 >= rows) return;
+  const int t_end0 = first_pos + (min(rows, row00 + kM) - 1) / p.g + 1;
+  const int t_end1 = row01 < rows ? first_pos + (min(rows, row01 + kM) - 1) / p.g + 1 : 0;
+  const int nch0 = (t_end0 + kN - 1) / kN, nch1 = (t_end1 + kN - 1) / kN;
+  const int t_end = max(t_end0, t_end1);
+  const int nch = max(nch0, nch1);
 
-  // Keys and values of a stage have their own barriers: the keys of chunk c
-  // are released when S(c) completes, the values when P·V(c) does.
   uint64_t* full_k = reinterpret_cast<uint64_t*>(base + kOffBars);
-  uint64_t* full_v = full_k + kStagesT;
-  uint64_t* empty_k = full_v + kStagesT;
-  uint64_t* empty_v = empty_k + kStagesT;
-  uint64_t* s_full = empty_v + kStagesT;  // [2]: S of chunk c is in buffer c % 2
-  uint64_t* p_full = s_full + 2;          // [2]: P of chunk c is in S buffer c % 2
-  uint64_t* o_done = p_full + 2;          // one phase per P·V
-  uint64_t* o_final = o_done + 1;
-  uint64_t* q_full = o_final + 1;         // the query tile is in shared memory
+  uint64_t* empty_k = full_k + kStagesK;
+  uint64_t* full_v = empty_k + kStagesK;
+  uint64_t* empty_v = full_v + kStagesV;
+  uint64_t* tile_bars = empty_v + kStagesV;  // kTileBars per tile
+  // per tile: [0] S of a chunk is in, [1] P of a chunk is in, [2] the last
+  // P·V is done, [3] the query tile is in
+  auto s_full = [&](int t) { return tile_bars + t * kTileBars; };
+  auto p_full = [&](int t) { return tile_bars + t * kTileBars + 1; };
+  auto o_final = [&](int t) { return tile_bars + t * kTileBars + 2; };
+  auto q_full = [&](int t) { return tile_bars + t * kTileBars + 3; };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
 
   if (tid == 0) {
-    for (int k = 0; k < kStagesT; ++k) {
+    for (int k = 0; k < kStagesK; ++k) {
       mbar_init(&full_k[k], 1);
-      mbar_init(&full_v[k], 1);
       mbar_init(&empty_k[k], 1);
+    }
+    for (int k = 0; k < kStagesV; ++k) {
+      mbar_init(&full_v[k], 1);
       mbar_init(&empty_v[k], 1);
     }
-    mbar_init(q_full, kSoftWarps * 32);
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&p_full[0], kSoftWarps * 32);
-    mbar_init(&p_full[1], kSoftWarps * 32);
-    mbar_init(o_done, 1);
-    mbar_init(o_final, 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), kSoftWarps * 32);
+      mbar_init(o_final(t), 1);
+      mbar_init(q_full(t), kSoftWarps * 32);
+    }
     *abort = 0;
     fence_barrier_init();
   }
@@ -235,283 +234,278 @@ __global__ void __launch_bounds__(kThreadsT, 2)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == kProducerWarp) {
-    // The whole warp: lane b loads block b of a chunk.  Block-table entries
-    // are fetched 32 at a time, one per lane, a window ahead, so no TMA
-    // issue waits on a dependent table load.
+  if (warp == kProducerWarp || warp == kProducerWarp + 1) {
+    // One warp streams the keys, the next the values, each into its own
+    // ring, so neither waits behind the other's release.  Lane b loads
+    // block b of a chunk; block-table entries are fetched 32 at a time, one
+    // per lane, a window ahead, so no TMA issue waits on a dependent load.
+    const int kv = warp - kProducerWarp;  // 0 keys, 1 values
     pdl_wait_primary();  // the prompt's keys and values are in the cache from here on
     const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     const int nblk = (t_end + p.B - 1) / p.B;
-    const int bpc = kN / p.B;  // blocks per chunk (block sizes 8, 16, 32)
+    const int bpc = kN / p.B;  // blocks per chunk (block sizes 8, 16, 32: 16, 8 or 4, dividing 32)
     const uint64_t policy = policy_evict_first();
+    const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
+    uint64_t* fulls = kv == 0 ? full_k : full_v;
+    uint64_t* empties = kv == 0 ? empty_k : empty_v;
+    const int stages = kv == 0 ? kStagesK : kStagesV;
     int cur = load_block_id(row, lane, nblk);
     int nxt = load_block_id(row, 32 + lane, nblk);
-    int wbase = 0, id_prev = 0;
-    bool alive = true;
-    // Keys run one chunk ahead of values: K(j) waits for S(j - 2) and
-    // V(j - 1) for P·V(j - 3), and the tensor pipe completes S(j - 2),
-    // P·V(j - 3), S(j - 1), ... in that order, so neither wait holds the
-    // other back.
-    for (int j = 0; j <= nch && alive; ++j) {
-      int id = 0;
-      if (j < nch) {
-        const int jb = j * bpc;
-        if (jb >= wbase + 32) {
-          cur = nxt;
-          wbase += 32;
-          nxt = load_block_id(row, wbase + 32 + lane, nblk);
-        }
-        id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
-        const int nb = (min(kN, t_end - j * kN) + p.B - 1) / p.B;
-        if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
-          raise_status(p.status, PA_STATUS_BAD_BLOCK);
-          id = 0;
+    int wbase = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int jb = c * bpc;
+      if (jb >= wbase + 32) {
+        cur = nxt;
+        wbase += 32;
+        nxt = load_block_id(row, wbase + 32 + lane, nblk);
+      }
+      int id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
+      const int nb = (min(kN, t_end - c * kN) + p.B - 1) / p.B;
+      if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
+        raise_status(p.status, PA_STATUS_BAD_BLOCK);
+        id = 0;
+      }
+      const int st = c % stages;
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(&empties[st], ((c / stages) & 1) ^ 1, abort);
+        if (ok) {
+          mbar_arrive_expect_tx(&fulls[st], (uint32_t)(nb * p.B * 128 * 2));
+        } else {
+          *abort = 1;
+          raise_status(p.status, PA_STATUS_TIMEOUT);
         }
       }
-#pragma unroll 1
-      for (int kv = 0; kv < 2; ++kv) {
-        const int c = j - kv;
-        if (c < 0 || c >= nch) continue;
-        const int st = c % kStagesT;
-        const int nb = (min(kN, t_end - c * kN) + p.B - 1) / p.B;
-        uint64_t* fb = kv == 0 ? &full_k[st] : &full_v[st];
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(kv == 0 ? &empty_k[st] : &empty_v[st], ((c / kStagesT) & 1) ^ 1, abort);
-          if (ok) {
-            mbar_arrive_expect_tx(fb, (uint32_t)(nb * p.B * 128 * 2));
-          } else {
-            *abort = 1;
-            raise_status(p.status, PA_STATUS_TIMEOUT);
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          alive = false;
-          break;
-        }
-        __syncwarp();  // the expected byte count is set before any copy can land
-        if (lane < nb) {
-          const int y = ((kv == 0 ? id : id_prev) * p.Hkv + kvh) * p.B;
-          uint8_t* d = base + kOffStages + st * kStageT + kv * 2 * kKVHalf + lane * p.B * 128;
-          const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
-          tma_load_2d(d, map, fb, 0, y, policy);
-          tma_load_2d(d + kKVHalf, map, fb, 64, y, policy);
-        }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      __syncwarp();  // the expected byte count is set before any copy can land
+      if (lane < nb) {
+        const int y = (id * p.Hkv + kvh) * p.B;
+        uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
+        tma_load_2d(d, map, &fulls[st], 0, y, policy);
+        tma_load_2d(d + kKVHalf, map, &fulls[st], 64, y, policy);
       }
-      id_prev = id;
     }
   } else if (warp == kMmaWarp) {
-    // S(c) and P·V(c) are issued as soon as each is ready -- S(c) when its
-    // keys have landed and its buffer is free (P·V(c - 2) issued), P·V(c)
-    // when the softmax has written P(c) -- so S of the next chunk overlaps
-    // the softmax of this one without holding P·V back.  The tensor cores
-    // run one thread's MMAs in order: S(c + 2) overwrites buffer c % 2 only
-    // after P·V(c) has read P(c) from it, and the commit that releases
-    // S(c + 1) to the softmax also covers P·V(c - 1).  P(c) is signalled on
-    // p_full[c % 2]: the softmax can finish P(c + 1) before this warp has
-    // seen P(c), but not P(c + 2), which needs S(c + 2), so neither barrier
-    // runs a phase ahead of the poll.
+    // One thread issues every MMA in a fixed order, waiting (bounded
+    // try_wait) for one barrier at a time: S of both tiles for chunk 0,
+    // then per chunk c and tile t: P·V(c) as soon as the tile's P(c) is in,
+    // and right behind it S(c + 1) of that tile.  Each tile has one S
+    // buffer, so its softmax and its products alternate, and the tensor
+    // cores work for one tile while the other tile's softmax runs.  The
+    // tensor cores run one thread's MMAs in order: S(c + 1) overwrites P(c)
+    // only after P·V(c) has read it, and the commit that releases S(c + 1)
+    // to the softmax also covers P·V(c), so the softmax may rescale O at
+    // once.  A stage is released by a commit after the last MMA that reads
+    // it.
     const uint32_t id_s = instr_desc(kM, kN, false);
     const uint32_t id_o = instr_desc(kM, kDh, true);
-    int ns = 0, npv = 0;  // next S and next P·V to issue
-    bool ok = true, q_ready = false;
-    const unsigned long long t_start = global_timer_ns();
-    unsigned spins = 0;
-    while (npv < nch) {
-      int what = 0;  // 1: issue S(ns), 2: issue P·V(npv)
+    bool ok = true;
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+      int r = 1;
+      if (lane == 0) r = mbar_wait(bar, parity, abort);
+      ok = ok && __shfl_sync(0xffffffffu, r, 0);
+      return ok;
+    };
+    auto issue_s = [&](int t, int c) {  // lane 0; the keys of chunk c have landed
+      tc_fence_after();
+      const uint32_t kst = sbase + kOffK + (c % kStagesK) * kKVStage;
+      const uint32_t qt = sbase + t * kQTile;
+      const uint32_t d = tmem + kColS + (uint32_t)t * 128;
+#pragma unroll
+      for (int kk = 0; kk < kDh / 16; ++kk) {
+        const int hlf = kk >> 2, w = kk & 3;
+        const uint64_t a = smem_desc(qt + hlf * kQHalf + w * 32, 16, 1024);
+        const uint64_t b = smem_desc(kst + hlf * kKVHalf + w * 32, 16, 1024);
+        mma_ss(d, a, b, id_s, kk > 0);
+      }
+      mma_commit(s_full(t));
+    };
+    auto issue_pv = [&](int t, int c) {  // lane 0; P(c) and the values of chunk c are in
+      tc_fence_after();
+      const uint32_t vst = sbase + kOffV + (c % kStagesV) * kKVStage;
+      const uint32_t p_cols = tmem + kColS + (uint32_t)t * 128;
+      const uint32_t d = tmem + kColO + (uint32_t)t * 128;
+#pragma unroll
+      for (int kk = 0; kk < kN / 16; ++kk) {
+        const uint64_t b = smem_desc(vst + kk * 16 * 128, kKVHalf, 1024);
+        mma_ts(d, p_cols + kk * 8, b, id_o, c > 0 || kk > 0);
+      }
+      if (c + 1 == (t == 0 ? nch0 : nch1)) mma_commit(o_final(t));
+    };
+    if (wait_bar(q_full(0), 0) && (nch1 == 0 || wait_bar(q_full(1), 0)) && wait_bar(&full_k[0], 0)) {
       if (lane == 0) {
-        if (npv < ns && mbar_test(&p_full[npv & 1], (npv >> 1) & 1) &&
-            mbar_test(&full_v[npv % kStagesT], (npv / kStagesT) & 1))
-          what = 2;
-        else if (ns < nch && ns <= npv + 1 && (q_ready || (q_ready = mbar_test(q_full, 0))) &&
-                 mbar_test(&full_k[ns % kStagesT], (ns / kStagesT) & 1))
-          what = 1;
+        issue_s(0, 0);
+        if (nch1 > 0) issue_s(1, 0);
+        mma_commit(&empty_k[0]);
       }
-      what = __shfl_sync(0xffffffffu, what, 0);
-      if (what == 1) {
-        const int c = ns++;
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t sst = sbase + kOffStages + (c % kStagesT) * kStageT;
-#pragma unroll
-          for (int kk = 0; kk < kDh / 16; ++kk) {
-            const int hlf = kk >> 2, w = kk & 3;
-            const uint64_t a = smem_desc(sbase + hlf * kQHalf + w * 32, 16, 1024);
-            const uint64_t b = smem_desc(sst + hlf * kKVHalf + w * 32, 16, 1024);
-            mma_ss(tmem + kColS + (uint32_t)(c & 1) * kN, a, b, id_s, kk > 0);
-          }
-          mma_commit(&s_full[c & 1]);
-          mma_commit(&empty_k[c % kStagesT]);
+      __syncwarp();
+    }
+    for (int c = 0; c < nch && ok; ++c) {
+      if (!wait_bar(&full_v[c % kStagesV], (c / kStagesV) & 1)) break;
+      const int nv = min(kN, t_end - c * kN);
+      if (nv < kN) {  // value rows past the pair's keys: zeros (their keys are masked)
+        uint8_t* vs = base + kOffV + (c % kStagesV) * kKVStage;
+        for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
+          const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
+          *reinterpret_cast<uint4*>(vs + hlf * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      bool k_next = false;  // the keys of chunk c + 1 have landed
+#pragma unroll 1
+      for (int t = 0; t < kTiles; ++t) {
+        const int nch_t = t == 0 ? nch0 : nch1;
+        if (c >= nch_t) continue;
+        if (!wait_bar(p_full(t), c & 1)) break;
+        if (lane == 0) issue_pv(t, c);
         __syncwarp();
-        spins = 0;
-      } else if (what == 2) {
-        const int c = npv++;
-        uint8_t* stage = base + kOffStages + (c % kStagesT) * kStageT;
-        const int nv = min(kN, t_end - c * kN);
-        if (nv < kN) {  // value rows past the tile's keys: zeros (their keys are masked)
-          for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
-            const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
-            *reinterpret_cast<uint4*>(stage + (2 + hlf) * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
+        if (c + 1 < nch_t) {
+          if (!k_next && !(k_next = wait_bar(&full_k[(c + 1) % kStagesK], ((c + 1) / kStagesK) & 1))) break;
+          if (lane == 0) {
+            issue_s(t, c + 1);
+            // the last tile that reads the keys of chunk c + 1
+            if (t == kTiles - 1 || c + 1 >= nch1) mma_commit(&empty_k[(c + 1) % kStagesK]);
           }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t sst = sbase + kOffStages + (c % kStagesT) * kStageT;
-          const uint32_t p_cols = tmem + kColS + (uint32_t)(c & 1) * kN;
-#pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk) {
-            const uint64_t b = smem_desc(sst + 2 * kKVHalf + kk * 16 * 128, kKVHalf, 1024);
-            mma_ts(tmem + kColO, p_cols + kk * 8, b, id_o, c > 0 || kk > 0);
-          }
-          mma_commit(o_done);
-          mma_commit(&empty_v[c % kStagesT]);
-        }
-        __syncwarp();
-        spins = 0;
-      } else if ((++spins & 63u) == 0) {
-        if (*abort || global_timer_ns() - t_start > kWaitLimitNs * 8) {
-          ok = false;
-          break;
+          __syncwarp();
         }
       }
+      if (ok && lane == 0) mma_commit(&empty_v[c % kStagesV]);
+      __syncwarp();
     }
     if (!ok) {
       *abort = 1;
       raise_status(p.status, PA_STATUS_TIMEOUT);
     }
-    if (lane == 0) mma_commit(o_final);
-  } else {
-    // Query tile (an input, not written by the append), K-major with
-    // 128-byte swizzle; loaded here so that it overlaps the first stages.
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    for (int i = tid; i < kM * 16; i += kSoftWarps * 32) {
-      const int rr = i >> 4, u = i & 15;
-      const int gr = row0 + rr;
-      const uint32_t off = kmajor_off(rr, u, kM);
-      if (gr < rows) {
-        const int h = kvh * p.g + gr % p.g;
-        cp_async16(sbase + off, q + ((size_t)(q0 + gr / p.g) * p.H + h) * kDh + u * 8);
-      } else {
-        *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    fence_proxy_async_smem();  // the query tile is read by the tensor cores (async proxy)
-    mbar_arrive(q_full);
-    // softmax: thread tid owns row tid (tensor-memory lane tid)
-    const int r = row0 + tid;
-    const int pos = r < rows ? first_pos + r / p.g : -1;  // keys 0 .. pos
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int c = 0; c < nch; ++c) {
-      if (!mbar_wait(&s_full[c & 1], (c >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      const uint32_t s_cols = lane_base + kColS + (uint32_t)(c & 1) * kN;
-      tc_fence_after();
-      uint32_t raw[kN];
-#pragma unroll
-      for (int i = 0; i < kN / 16; ++i) tmem_ld16_nowait(s_cols + 16 * i, raw + 16 * i);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      float sc[kN];
-#pragma unroll
-      for (int j = 0; j < kN; ++j) sc[j] = __uint_as_float(raw[j]);
-      // Keys t0 .. t0 + nvalid - 1 of this chunk are at or before the row's
-      // position; masking is needed only in chunks that cross it.
-      const int t0 = c * kN;
-      const int nvalid = min(kN, pos - t0 + 1);
-      float mxr = -INFINITY;  // max of the raw (unscaled) valid scores
-      if (nvalid >= kN) {
-#pragma unroll
-        for (int j = 0; j < kN; ++j) mxr = fmaxf(mxr, sc[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < kN; ++j) {
-          sc[j] = j < nvalid ? sc[j] : -INFINITY;
-          mxr = fmaxf(mxr, sc[j]);
+  } else if (warp < kProducerWarp) {
+    // softmax warpgroup t: thread lt owns row lt of tile t (tensor-memory lane lt)
+    const int t = warp / kSoftWarps, lt = tid - t * kM;
+    const int row0 = row00 + t * kM;
+    const int nch_t = t == 0 ? nch0 : nch1;
+    if (nch_t > 0) {
+      // Query tile (an input, not written by the append), K-major with
+      // 128-byte swizzle; loaded here so that it overlaps the first stages.
+      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+      const uint32_t qt = sbase + t * kQTile;
+      for (int i = lt; i < kM * 16; i += kSoftWarps * 32) {
+        const int rr = i >> 4, u = i & 15;
+        const int gr = row0 + rr;
+        const uint32_t off = kmajor_off(rr, u, kM);
+        if (gr < rows) {
+          const int h = kvh * p.g + gr % p.g;
+          cp_async16(qt + off, q + ((size_t)(q0 + gr / p.g) * p.H + h) * kDh + u * 8);
+        } else {
+          *reinterpret_cast<uint4*>(base + t * kQTile + off) = make_uint4(0, 0, 0, 0);
         }
       }
-      const float mx = mxr * p.scale_log2;  // scale > 0: the max of the scaled scores
-      // Raise the running max (and rescale O) only when it grows past the
-      // threshold; the decision is made per warp because tensor-memory
-      // loads and stores are warp-wide.
-      const bool grow = mx > m_run + kRescaleLog2 || (m_run == -INFINITY && mx != -INFINITY);
-      const float m_new = grow ? mx : m_run;
-      const float alpha = grow ? exp2f(m_run - m_new) : 1.f;  // m_run = -inf: alpha 0
-      if (c > 0 && __any_sync(0xffffffffu, grow && m_run != -INFINITY)) {
-        // O must hold P·V(c - 1) before it is rescaled
-        if (!mbar_wait(o_done, (c - 1) & 1, abort)) {
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+      fence_proxy_async_smem();  // the query tile is read by the tensor cores (async proxy)
+      mbar_arrive(q_full(t));
+
+      const int r = row0 + lt;
+      const int pos = r < rows ? first_pos + r / p.g : -1;  // keys 0 .. pos
+      const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
+      const uint32_t o_cols = lane_base + kColO + (uint32_t)t * 128;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int c = 0; c < nch_t; ++c) {
+        if (!mbar_wait(s_full(t), c & 1, abort)) {
           ok = false;
           break;
         }
+        const uint32_t s_cols = lane_base + kColS + (uint32_t)t * 128;
         tc_fence_after();
+        uint32_t raw[kN];
+#pragma unroll
+        for (int i = 0; i < kN / 16; ++i) tmem_ld16_nowait(s_cols + 16 * i, raw + 16 * i);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        float sc[kN];
+#pragma unroll
+        for (int j = 0; j < kN; ++j) sc[j] = __uint_as_float(raw[j]);
+        // Keys t0 .. t0 + nvalid - 1 of this chunk are at or before the row's
+        // position; masking is needed only in chunks that cross it.
+        const int t0 = c * kN;
+        const int nvalid = min(kN, pos - t0 + 1);
+        float mxr = -INFINITY;  // max of the raw (unscaled) valid scores
+        if (nvalid >= kN) {
+#pragma unroll
+          for (int j = 0; j < kN; ++j) mxr = fmaxf(mxr, sc[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kN; ++j) {
+            sc[j] = j < nvalid ? sc[j] : -INFINITY;
+            mxr = fmaxf(mxr, sc[j]);
+          }
+        }
+        const float mx = mxr * p.scale_log2;  // scale > 0: the max of the scaled scores
+        // Raise the running max (and rescale O) only when it grows past the
+        // threshold; the decision is made per warp because tensor-memory
+        // loads and stores are warp-wide.
+        const bool grow = mx > m_run + kRescaleLog2 || (m_run == -INFINITY && mx != -INFINITY);
+        const float m_new = grow ? mx : m_run;
+        const float alpha = grow ? exp2f(m_run - m_new) : 1.f;  // m_run = -inf: alpha 0
+        if (c > 0 && __any_sync(0xffffffffu, grow && m_run != -INFINITY)) {
+          // O holds P·V(c - 1): the commit that released S(c) covers it
+#pragma unroll 1
+          for (int i = 0; i < kDh / 16; ++i) {
+            float v[16];
+            tmem_ld16(o_cols + 16 * i, v);
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(v[j] * alpha);
+            tmem_st16(o_cols + 16 * i, w);
+          }
+        }
+        l_run *= alpha;
+        m_run = m_new;
+        const float base_m = m_run == -INFINITY ? 0.f : m_run;
+        float ls = 0.f;
+#pragma unroll
+        for (int i = 0; i < kN / 32; ++i) {  // exp2(s * scale - max): one FMA per score
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float e0 = exp2f(fmaf(sc[32 * i + 2 * j], p.scale_log2, -base_m));
+            const float e1 = exp2f(fmaf(sc[32 * i + 2 * j + 1], p.scale_log2, -base_m));
+            ls += e0 + e1;
+            w[j] = pack_bf16x2(e0, e1);
+          }
+          tmem_st16(s_cols + 16 * i, w);  // P over the first 64 columns of its S
+        }
+        l_run += ls;
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(p_full(t));
+      }
+      if (ok && mbar_wait(o_final(t), 0, abort)) {
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16* dst =
+            r < rows ? static_cast<__nv_bfloat16*>(p.out) + ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * kDh
+                     : nullptr;
 #pragma unroll 1
         for (int i = 0; i < kDh / 16; ++i) {
           float v[16];
-          tmem_ld16(lane_base + kColO + 16 * i, v);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(v[j] * alpha);
-          tmem_st16(lane_base + kColO + 16 * i, w);
+          tmem_ld16(o_cols + 16 * i, v);
+          if (dst) {
+            uint4 a, b2;
+            a.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+            a.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+            a.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+            a.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+            b2.x = pack_bf16x2(v[8] * inv, v[9] * inv);
+            b2.y = pack_bf16x2(v[10] * inv, v[11] * inv);
+            b2.z = pack_bf16x2(v[12] * inv, v[13] * inv);
+            b2.w = pack_bf16x2(v[14] * inv, v[15] * inv);
+            reinterpret_cast<uint4*>(dst + 16 * i)[0] = a;
+            reinterpret_cast<uint4*>(dst + 16 * i)[1] = b2;
+          }
         }
+      } else {
+        *abort = 1;
+        raise_status(p.status, PA_STATUS_TIMEOUT);
       }
-      l_run *= alpha;
-      m_run = m_new;
-      const float base_m = m_run == -INFINITY ? 0.f : m_run;
-      uint32_t pk[kN / 2];
-      float ls = 0.f;
-#pragma unroll
-      for (int j = 0; j < kN / 2; ++j) {  // exp2(s * scale - max): one FMA per score
-        const float e0 = exp2f(fmaf(sc[2 * j], p.scale_log2, -base_m));
-        const float e1 = exp2f(fmaf(sc[2 * j + 1], p.scale_log2, -base_m));
-        ls += e0 + e1;
-        pk[j] = pack_bf16x2(e0, e1);
-      }
-      l_run += ls;
-#pragma unroll
-      for (int i = 0; i < kN / 32; ++i) {
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = pk[16 * i + j];
-        tmem_st16(s_cols + 16 * i, w);  // P over the first 32 columns of its S buffer
-      }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      mbar_arrive(&p_full[c & 1]);
-    }
-    if (ok && mbar_wait(o_final, 0, abort)) {
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* dst =
-          r < rows ? static_cast<__nv_bfloat16*>(p.out) + ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * kDh
-                   : nullptr;
-#pragma unroll 1
-      for (int i = 0; i < kDh / 16; ++i) {
-        float v[16];
-        tmem_ld16(lane_base + kColO + 16 * i, v);
-        if (dst) {
-          uint4 a, b2;
-          a.x = pack_bf16x2(v[0] * inv, v[1] * inv);
-          a.y = pack_bf16x2(v[2] * inv, v[3] * inv);
-          a.z = pack_bf16x2(v[4] * inv, v[5] * inv);
-          a.w = pack_bf16x2(v[6] * inv, v[7] * inv);
-          b2.x = pack_bf16x2(v[8] * inv, v[9] * inv);
-          b2.y = pack_bf16x2(v[10] * inv, v[11] * inv);
-          b2.z = pack_bf16x2(v[12] * inv, v[13] * inv);
-          b2.w = pack_bf16x2(v[14] * inv, v[15] * inv);
-          reinterpret_cast<uint4*>(dst + 16 * i)[0] = a;
-          reinterpret_cast<uint4*>(dst + 16 * i)[1] = b2;
-        }
-      }
-    } else {
-      *abort = 1;
-      raise_status(p.status, PA_STATUS_TIMEOUT);
     }
   }
 
@@ -528,8 +522,9 @@ __global__ void __launch_bounds__(kThreadsT, 2)
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaStream_t stream) {
   const int tiles = (a.max_query_len * a.g + kM - 1) / kM;
+  const int pairs = (tiles + kTiles - 1) / kTiles;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
-  if (tiles > 65535 || a.S > 65535 || a.Hkv > 65535) return cudaErrorInvalidConfiguration;
+  if (pairs > 65535 || a.S > 65535 || a.Hkv > 65535) return cudaErrorInvalidConfiguration;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -541,7 +536,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
   });
   if (init_err != cudaSuccess) return init_err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)a.S, (unsigned)tiles);
+  cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)a.S, (unsigned)pairs);
   cfg.blockDim = dim3(kThreadsT);
   cfg.dynamicSmemBytes = kBytesT;
   cfg.stream = stream;

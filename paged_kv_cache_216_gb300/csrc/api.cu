@@ -98,6 +98,23 @@ int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, 
   return PA_OK;
 }
 
+// Query rows of one KV head for the tcgen05 prefill: q [T][H][128] bf16 as a
+// 3D tensor (dims, head, token); a box of 64 dims x g heads x 128 / g tokens
+// lands as 128 rows of 128 bytes, row = token * g + head, 128-byte swizzle.
+int make_query_map(CUtensorMap* map, const void* q, int T, int H, int g) {
+  auto fn = encode_fn();
+  if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {128u, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {256u, (cuuint64_t)H * 256u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)g, (cuuint32_t)(128 / g)};
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  return PA_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool supported_shape(int D, int B) { return (D == 64 || D == 128) && (B == 8 || B == 16 || B == 32); }
@@ -470,7 +487,10 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
     if (rc) return rc;
     rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
     if (rc) return rc;
-    e = pa::launch_prefill_tc(a, kmap, vmap, st);
+    CUtensorMap qmap;
+    rc = make_query_map(&qmap, q, num_tokens, num_heads, g);
+    if (rc) return rc;
+    e = pa::launch_prefill_tc(a, kmap, vmap, qmap, st);
   } else {
     e = pa::launch_prefill(a, st);
   }

@@ -21,7 +21,7 @@
 //    K 128: eight tcgen05.mma kind::f16 from shared-memory descriptors)
 //    into the tile's S and O += P V (M 128, N 128, K 128: eight MMAs, P read
 //    from tensor memory, V an MN-major operand in shared memory), in a fixed
-//    order -- per chunk c and tile, P·V(c) and then S(c + 1) -- waiting for
+//    order -- per chunk c and tile, P·V(c) and then S(c + 1) -- spinning on
 //    one barrier at a time, so the tensor cores work for one tile while the
 //    other tile's softmax runs (ping-pong); tcgen05.commit signals the
 //    mbarriers;
@@ -32,8 +32,9 @@
 //    (tcgen05.st) and rescales its row of O only when its max grows by more
 //    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
 //    exact enough and O and the sum use the same max); at the end it reads
-//    its row of O, divides by the sum and stores it.  Each warpgroup loads
-//    its own query tile while the first stages land.
+//    its row of O, divides by the sum and stores it.  The key producer
+//    loads both query tiles first, one 3D TMA box per 64-dim half, so they
+//    land with the first stage of keys.
 // Tensor memory (all 512 columns): O of tile t at columns 128t..128t+127 and
 // its S at 256 + 128t; P is written over the first half of its S.  Value rows past the pair's keys are zeroed in
 // shared memory before the first P·V of that stage so stale cache rows
@@ -150,19 +151,35 @@ __device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&r)[16]
       : "memory");
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
-// Byte offset of 16-byte piece u (0..15) of row r in a K-major tile of
-// `rows` rows stored as two 64-dim halves with 128-byte swizzle.
-__device__ __forceinline__ uint32_t kmajor_off(int r, int u, int rows) {
-  return (uint32_t)((u >> 3) * rows * 128 + r * 128 + (((u & 7) ^ (r & 7)) << 4));
+// Wait for a phase by spinning on test_wait (bounded like mbar_wait): a
+// thread suspended in try_wait resumed several hundred cycles after the
+// phase completed, which the MMA thread cannot afford on its critical path.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (unsigned i = 0; i < kWaitLimitIters; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 255u && (*abort || global_timer_ns() - t0 > kWaitLimitNs)) return false;
+  }
+  return false;
 }
 
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const PrefillArgs p) {
+                      const __grid_constant__ CUtensorMap qmap, const PrefillArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -219,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), kSoftWarps * 32);
       mbar_init(o_final(t), 1);
-      mbar_init(q_full(t), kSoftWarps * 32);
+      mbar_init(q_full(t), 1);
     }
     *abort = 0;
     fence_barrier_init();
@@ -240,6 +257,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     // block b of a chunk; block-table entries are fetched 32 at a time, one
     // per lane, a window ahead, so no TMA issue waits on a dependent load.
     const int kv = warp - kProducerWarp;  // 0 keys, 1 values
+    if (kv == 0 && lane == 0) {
+      // The query tiles (an input the append does not write), one box per
+      // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past the
+      // sequence read the next sequence's queries (or zeros past the last
+      // token); their scores are all masked and their rows never stored.
+      const uint64_t qpol = policy_evict_first();
+#pragma unroll 1
+      for (int t = 0; t < kTiles; ++t) {
+        if ((t == 0 ? nch0 : nch1) == 0) continue;
+        const int z = q0 + (row00 + t * kM) / p.g;
+        mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
+        tma_load_3d(base + t * kQTile, &qmap, q_full(t), 0, kvh * p.g, z, qpol);
+        tma_load_3d(base + t * kQTile + kQHalf, &qmap, q_full(t), 64, kvh * p.g, z, qpol);
+      }
+    }
     pdl_wait_primary();  // the prompt's keys and values are in the cache from here on
     const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     const int nblk = (t_end + p.B - 1) / p.B;
@@ -302,34 +334,34 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     bool ok = true;
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
       int r = 1;
-      if (lane == 0) r = mbar_wait(bar, parity, abort);
+      if (lane == 0) r = mbar_spin(bar, parity, abort);
       ok = ok && __shfl_sync(0xffffffffu, r, 0);
       return ok;
     };
+    // Descriptors are built once per group; a k-step adds its byte offset
+    // / 16 to the address field (every shared address is below 256 KB, so
+    // the 14-bit field never carries).  This thread shares its scheduler
+    // with two softmax warps, so fewer instructions per MMA matter.
     auto issue_s = [&](int t, int c) {  // lane 0; the keys of chunk c have landed
       tc_fence_after();
-      const uint32_t kst = sbase + kOffK + (c % kStagesK) * kKVStage;
-      const uint32_t qt = sbase + t * kQTile;
+      const uint64_t a0 = smem_desc(sbase + t * kQTile, 16, 1024);
+      const uint64_t b0 = smem_desc(sbase + kOffK + (c % kStagesK) * kKVStage, 16, 1024);
       const uint32_t d = tmem + kColS + (uint32_t)t * 128;
 #pragma unroll
       for (int kk = 0; kk < kDh / 16; ++kk) {
         const int hlf = kk >> 2, w = kk & 3;
-        const uint64_t a = smem_desc(qt + hlf * kQHalf + w * 32, 16, 1024);
-        const uint64_t b = smem_desc(kst + hlf * kKVHalf + w * 32, 16, 1024);
-        mma_ss(d, a, b, id_s, kk > 0);
+        mma_ss(d, a0 + (uint64_t)((hlf * kQHalf + w * 32) >> 4), b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4), id_s,
+               kk > 0);
       }
       mma_commit(s_full(t));
     };
     auto issue_pv = [&](int t, int c) {  // lane 0; P(c) and the values of chunk c are in
       tc_fence_after();
-      const uint32_t vst = sbase + kOffV + (c % kStagesV) * kKVStage;
+      const uint64_t b0 = smem_desc(sbase + kOffV + (c % kStagesV) * kKVStage, kKVHalf, 1024);
       const uint32_t p_cols = tmem + kColS + (uint32_t)t * 128;
       const uint32_t d = tmem + kColO + (uint32_t)t * 128;
 #pragma unroll
-      for (int kk = 0; kk < kN / 16; ++kk) {
-        const uint64_t b = smem_desc(vst + kk * 16 * 128, kKVHalf, 1024);
-        mma_ts(d, p_cols + kk * 8, b, id_o, c > 0 || kk > 0);
-      }
+      for (int kk = 0; kk < kN / 16; ++kk) mma_ts(d, p_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, c > 0 || kk > 0);
       if (c + 1 == (t == 0 ? nch0 : nch1)) mma_commit(o_final(t));
     };
     if (wait_bar(q_full(0), 0) && (nch1 == 0 || wait_bar(q_full(1), 0)) && wait_bar(&full_k[0], 0)) {
@@ -384,25 +416,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const int row0 = row00 + t * kM;
     const int nch_t = t == 0 ? nch0 : nch1;
     if (nch_t > 0) {
-      // Query tile (an input, not written by the append), K-major with
-      // 128-byte swizzle; loaded here so that it overlaps the first stages.
-      const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-      const uint32_t qt = sbase + t * kQTile;
-      for (int i = lt; i < kM * 16; i += kSoftWarps * 32) {
-        const int rr = i >> 4, u = i & 15;
-        const int gr = row0 + rr;
-        const uint32_t off = kmajor_off(rr, u, kM);
-        if (gr < rows) {
-          const int h = kvh * p.g + gr % p.g;
-          cp_async16(qt + off, q + ((size_t)(q0 + gr / p.g) * p.H + h) * kDh + u * 8);
-        } else {
-          *reinterpret_cast<uint4*>(base + t * kQTile + off) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-      fence_proxy_async_smem();  // the query tile is read by the tensor cores (async proxy)
-      mbar_arrive(q_full(t));
-
       const int r = row0 + lt;
       const int pos = r < rows ? first_pos + r / p.g : -1;  // keys 0 .. pos
       const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
@@ -427,17 +440,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         // position; masking is needed only in chunks that cross it.
         const int t0 = c * kN;
         const int nvalid = min(kN, pos - t0 + 1);
-        float mxr = -INFINITY;  // max of the raw (unscaled) valid scores
+        // max of the raw (unscaled) valid scores, four chains at a time
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (nvalid >= kN) {
 #pragma unroll
-          for (int j = 0; j < kN; ++j) mxr = fmaxf(mxr, sc[j]);
+          for (int j = 0; j < kN; ++j) m4[j & 3] = fmaxf(m4[j & 3], sc[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < kN; ++j) {
             sc[j] = j < nvalid ? sc[j] : -INFINITY;
-            mxr = fmaxf(mxr, sc[j]);
+            m4[j & 3] = fmaxf(m4[j & 3], sc[j]);
           }
         }
+        const float mxr = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         const float mx = mxr * p.scale_log2;  // scale > 0: the max of the scaled scores
         // Raise the running max (and rescale O) only when it grows past the
         // threshold; the decision is made per warp because tensor-memory
@@ -460,7 +475,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         l_run *= alpha;
         m_run = m_new;
         const float base_m = m_run == -INFINITY ? 0.f : m_run;
-        float ls = 0.f;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < kN / 32; ++i) {  // exp2(s * scale - max): one FMA per score
           uint32_t w[16];
@@ -468,12 +483,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           for (int j = 0; j < 16; ++j) {
             const float e0 = exp2f(fmaf(sc[32 * i + 2 * j], p.scale_log2, -base_m));
             const float e1 = exp2f(fmaf(sc[32 * i + 2 * j + 1], p.scale_log2, -base_m));
-            ls += e0 + e1;
+            l4[j & 3] += e0 + e1;
             w[j] = pack_bf16x2(e0, e1);
           }
           tmem_st16(s_cols + 16 * i, w);  // P over the first 64 columns of its S
         }
-        l_run += ls;
+        l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         mbar_arrive(p_full(t));
@@ -520,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              cudaStream_t stream) {
+                              const CUtensorMap& qmap, cudaStream_t stream) {
   const int tiles = (a.max_query_len * a.g + kM - 1) / kM;
   const int pairs = (tiles + kTiles - 1) / kTiles;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
@@ -545,7 +560,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, kmap, vmap, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, kmap, vmap, qmap, a);
 }
 
 }  // namespace pa

@@ -487,10 +487,12 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
     if (rc) return rc;
     rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
     if (rc) return rc;
-    CUtensorMap qmap;
+    CUtensorMap qmap, omap;
     rc = make_query_map(&qmap, q, num_tokens, num_heads, g);
     if (rc) return rc;
-    e = pa::launch_prefill_tc(a, kmap, vmap, qmap, st);
+    rc = make_query_map(&omap, out, num_tokens, num_heads, g);
+    if (rc) return rc;
+    e = pa::launch_prefill_tc(a, kmap, vmap, qmap, omap, st);
   } else {
     e = pa::launch_prefill(a, st);
   }

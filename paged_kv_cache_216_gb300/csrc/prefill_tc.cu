@@ -32,7 +32,9 @@
 //    (tcgen05.st) and rescales its row of O only when its max grows by more
 //    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
 //    exact enough and O and the sum use the same max); at the end it reads
-//    its row of O, divides by the sum and stores it.  The key producer
+//    its row of O, divides by the sum and stores it (a full tile through
+//    its query buffer and two TMA boxes, the sequence's last tile row by
+//    row).  The key producer
 //    loads both query tiles first, one 3D TMA box per 64-dim half, so they
 //    land with the first stage of keys.
 // Tensor memory (all 512 columns): O of tile t at columns 128t..128t+127 and
@@ -179,7 +181,8 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const 
 
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap qmap, const PrefillArgs p) {
+                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                      const PrefillArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -423,7 +426,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int c = 0; c < nch_t; ++c) {
-        if (!mbar_wait(s_full(t), c & 1, abort)) {
+        // the warp leaves together (warp-wide votes follow)
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(t), c & 1, abort))) {
           ok = false;
           break;
         }
@@ -493,29 +497,43 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         tc_fence_before();
         mbar_arrive(p_full(t));
       }
-      if (ok && mbar_wait(o_final(t), 0, abort)) {
+      // One outcome for the whole warpgroup: the full-tile store below syncs it.
+      if (named_barrier_and(1 + t, kSoftWarps * 32, ok && mbar_wait(o_final(t), 0, abort))) {
         tc_fence_after();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        __nv_bfloat16* dst =
-            r < rows ? static_cast<__nv_bfloat16*>(p.out) + ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * kDh
-                     : nullptr;
-#pragma unroll 1
-        for (int i = 0; i < kDh / 16; ++i) {
-          float v[16];
-          tmem_ld16(o_cols + 16 * i, v);
-          if (dst) {
-            uint4 a, b2;
-            a.x = pack_bf16x2(v[0] * inv, v[1] * inv);
-            a.y = pack_bf16x2(v[2] * inv, v[3] * inv);
-            a.z = pack_bf16x2(v[4] * inv, v[5] * inv);
-            a.w = pack_bf16x2(v[6] * inv, v[7] * inv);
-            b2.x = pack_bf16x2(v[8] * inv, v[9] * inv);
-            b2.y = pack_bf16x2(v[10] * inv, v[11] * inv);
-            b2.z = pack_bf16x2(v[12] * inv, v[13] * inv);
-            b2.w = pack_bf16x2(v[14] * inv, v[15] * inv);
-            reinterpret_cast<uint4*>(dst + 16 * i)[0] = a;
-            reinterpret_cast<uint4*>(dst + 16 * i)[1] = b2;
+        uint32_t o[kDh];  // the row of O, all loads in flight at once
+#pragma unroll
+        for (int i = 0; i < kDh / 16; ++i) tmem_ld16_nowait(o_cols + 16 * i, o + 16 * i);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        auto piece = [&](int u) {  // dims 8u .. 8u + 7 of the row, normalized, as bf16
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[8 * u]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+          return w;
+        };
+        if (row0 + kM <= rows) {
+          // A full tile: stage the rows in this tile's query buffer (its last
+          // S has completed) in the layout the query boxes arrived in, then
+          // store them with two TMA boxes through the same geometry.
+          uint8_t* qt = base + t * kQTile;
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            *reinterpret_cast<uint4*>(qt + (u >> 3) * kQHalf + lt * 128 + (((u & 7) ^ (lt & 7)) << 4)) = piece(u);
+          fence_proxy_async_smem();
+          named_barrier_sync(1 + t, kSoftWarps * 32);
+          if (lt == 0) {
+            const int z = q0 + row0 / p.g;
+            tma_store_3d(&omap, qt, 0, kvh * p.g, z);
+            tma_store_3d(&omap, qt + kQHalf, 64, kvh * p.g, z);
+            bulk_store_drain();
           }
+        } else if (r < rows) {  // the sequence's last tile: only its own rows
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * kDh);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) dst[u] = piece(u);
         }
       } else {
         *abort = 1;
@@ -535,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, cudaStream_t stream) {
+                              const CUtensorMap& qmap, const CUtensorMap& omap, cudaStream_t stream) {
   const int tiles = (a.max_query_len * a.g + kM - 1) / kM;
   const int pairs = (tiles + kTiles - 1) / kTiles;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
@@ -560,7 +578,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, kmap, vmap, qmap, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, kmap, vmap, qmap, omap, a);
 }
 
 }  // namespace pa

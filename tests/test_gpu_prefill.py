@@ -72,6 +72,10 @@ CASES = {
     "g8_d128_b8": ([7, 0, 300], [9, 17, 1], 16, 2, 128, 8),
     "g2_long_prompt": ([2000], [700], 8, 4, 128, 16),
     "g4_fresh_prompts": ([0, 0, 0], [1, 2, 63], 8, 2, 128, 32),
+    # one query head per KV head on the tcgen05 path (query boxes of 128 tokens x 1 head)
+    "g1_d128_b32": ([0, 100], [150, 33], 4, 4, 128, 32),
+    # a sequence with no new tokens between two that have some
+    "g4_no_new_tokens": ([12, 40, 0], [3, 0, 70], 8, 2, 128, 16),
 }
 
 

@@ -11,12 +11,13 @@
 // the rows being (new token, query head) pairs, token-major; pairs with the
 // most keys first.  Both tiles read every stage of keys and values, so each
 // TMA box feeds 256 rows.  Roles (352 threads, one CTA per SM):
-//  * warps 8 and 9 (producers): after griddepcontrol.wait, stream the keys
-//    (warp 8) and values (warp 9) the pair attends, 128 tokens per stage,
-//    into rings of their own (3 stages of keys, 2 of values), as 2D TMA boxes of [B tokens x 64 dims]
-//    with 128-byte swizzle (the K-major UMMA layout); lane b issues block b
-//    of a chunk from block-table entries fetched 32 at a time; a stage of
-//    keys is released as soon as both tiles' S have read it;
+//  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
+//    the pair attends, 128 tokens per stage, into rings of their own (3
+//    stages of keys, 2 of values), as 2D TMA boxes of [B tokens x 64 dims]
+//    with 128-byte swizzle (the K-major UMMA layout), after
+//    griddepcontrol.wait; lane b issues block b of a chunk from block-table
+//    entries fetched 32 at a time.  Warp 8 first loads both query tiles,
+//    one 3D box per 64-dim half, so they land with the first keys;
 //  * warp 10 (MMA): one thread issues, per tile, S = Q Kᵀ (M 128, N 128,
 //    K 128: eight tcgen05.mma kind::f16 from shared-memory descriptors)
 //    into the tile's S and O += P V (M 128, N 128, K 128: eight MMAs, P read
@@ -24,7 +25,7 @@
 //    order -- per chunk c and tile, P·V(c) and then S(c + 1) -- spinning on
 //    one barrier at a time, so the tensor cores work for one tile while the
 //    other tile's softmax runs (ping-pong); tcgen05.commit signals the
-//    mbarriers;
+//    mbarriers and releases each stage after the last MMA that reads it;
 //  * warps 0-3 and 4-7 (softmax, one warpgroup per tile): thread t of a
 //    warpgroup owns query row t of its tile (tensor-memory lane t): it
 //    reads its 128 scores (tcgen05.ld), masks keys past its position, keeps
@@ -34,14 +35,13 @@
 //    exact enough and O and the sum use the same max); at the end it reads
 //    its row of O, divides by the sum and stores it (a full tile through
 //    its query buffer and two TMA boxes, the sequence's last tile row by
-//    row).  The key producer
-//    loads both query tiles first, one 3D TMA box per 64-dim half, so they
-//    land with the first stage of keys.
+//    row).
 // Tensor memory (all 512 columns): O of tile t at columns 128t..128t+127 and
-// its S at 256 + 128t; P is written over the first half of its S.  Value rows past the pair's keys are zeroed in
-// shared memory before the first P·V of that stage so stale cache rows
-// cannot turn 0 x NaN into NaN.  Every wait is bounded; on a time-out the
-// kernel raises PA_STATUS_TIMEOUT and stops issuing work.
+// its S at 256 + 128t; P is written over the first half of its S.  Value
+// rows past the pair's keys are zeroed in shared memory before the first
+// P·V of that stage so stale cache rows cannot turn 0 x NaN into NaN.  Every
+// wait is bounded; on a time-out the kernel raises PA_STATUS_TIMEOUT and
+// stops issuing work.
 
 #include <cuda_bf16.h>
 

@@ -1,0 +1,137 @@
+"""The synchronisation protocol of the bf16 decode kernel
+(csrc/decode_tc.cu), checked on the CPU by a randomised discrete-event
+model (tests/_event_sim.py): no deadlock, every mbarrier wait sees exactly
+the phase it means, and every buffer holds the right data when it is read.
+
+The model follows the kernel's roles:
+  * the producer warp, per work item n: wait until every consumer warp has
+    read the query slot n % 2 last used by item n - 2, write the item's
+    descriptor, copy its query rows into the slot, then stream its chunks,
+    chunk k (counted over all items) into ring stage k % S once that
+    stage's previous chunk has been consumed; after the last item it
+    signals the end through the next slot;
+  * four consumer warps: per item, wait for the slot, read the descriptor
+    and the query, release the slot; warp w consumes the item's chunks
+    with k % 4 == w and releases each stage; then the item epilogue: wait
+    until every warp has finished combining the previous item, store its
+    state, wait until all four have, combine, and arrive.
+With S a multiple of four every stage always belongs to the same warp, so
+a warp never tests a stage whose earlier phase is still pending for
+another warp.  With S = 5 or 6 a warp running ahead passes the parity test
+on a phase two behind, which is why the kernel asserts the multiple (and
+why these checks are shown to fire for 5 and 6)."""
+
+import pytest
+
+from tests._event_sim import Bar, EventSim
+
+WARPS = 4
+END = "end"
+
+
+class DecodeSim(EventSim):
+    def __init__(self, items, stages, seed):
+        super().__init__(seed)
+        self.items = items  # chunks of each work item (0 for an empty context)
+        self.S = stages
+        self.full = [Bar(f"full{i}", 1) for i in range(stages)]
+        self.empty = [Bar(f"empty{i}", 1) for i in range(stages)]
+        self.qfull = [Bar(f"qfull{i}", 1) for i in range(2)]
+        self.qempty = [Bar(f"qempty{i}", WARPS) for i in range(2)]
+        self.epi_full = Bar("epi_full", WARPS)
+        self.epi_done = Bar("epi_done", WARPS)
+        self.stage = [None] * stages  # chunk held by each stage
+        self.desc = [None, None]  # item described by each slot
+        self.q = [None, None]  # item whose query rows each slot holds
+        self.state = [None] * WARPS  # item whose partial state each warp has stored
+        self.combined = {}  # item -> warps that finished its combine
+
+    def run(self):
+        roles = [self.producer()] + [self.consumer(w) for w in range(WARPS)]
+        return self.run_roles(roles, {"producer"} | {f"w{w}" for w in range(WARPS)})
+
+    def producer(self):
+        k = 0
+        for n in range(len(self.items) + 1):
+            slot = n & 1
+            yield ("wait", self.qempty[slot], ((n >> 1) & 1) ^ 1, n >> 1, f"producer q slot for item {n}")
+            if n == len(self.items):
+                self.desc[slot] = END
+                self.arrive(self.qfull[slot])
+                break
+            self.desc[slot] = n
+            self.expect_tx(self.qfull[slot], 1)
+            self.copy(self.qfull[slot], 1, lambda slot=slot, n=n: self.q.__setitem__(slot, n))
+            for _ in range(self.items[n]):
+                st = k % self.S
+                yield ("wait", self.empty[st], ((k // self.S) & 1) ^ 1, k // self.S, f"producer chunk {k}")
+                self.expect_tx(self.full[st], 1)
+                self.copy(self.full[st], 1, lambda st=st, k=k: self.stage.__setitem__(st, k))
+                k += 1
+                yield ("delay", self.rng.uniform(0.0, 0.4))
+        self.done.add("producer")
+
+    def consumer(self, w):
+        k = 0
+        n = 0
+        while True:
+            slot = n & 1
+            yield ("wait", self.qfull[slot], (n >> 1) & 1, (n >> 1) + 1, f"warp {w} q slot for item {n}")
+            if self.desc[slot] == END:
+                self.done.add(f"w{w}")
+                return
+            if self.desc[slot] != n or self.q[slot] != n:
+                self.fail(f"warp {w} item {n}: slot holds descriptor {self.desc[slot]}, query {self.q[slot]}")
+            yield ("delay", self.rng.uniform(0.0, 0.5))
+            if self.q[slot] != n:
+                self.fail(f"warp {w} item {n}: query overwritten while read")
+            self.arrive(self.qempty[slot])
+            for _ in range(self.items[n]):
+                if k % WARPS == w:
+                    st = k % self.S
+                    yield ("wait", self.full[st], (k // self.S) & 1, k // self.S + 1, f"warp {w} chunk {k}")
+                    if self.stage[st] != k:
+                        self.fail(f"warp {w} reads chunk {self.stage[st]} from stage {st}, wanted {k}")
+                    yield ("delay", self.rng.uniform(0.2, 3.0))
+                    if self.stage[st] != k:
+                        self.fail(f"warp {w}: stage {st} overwritten while chunk {k} was read")
+                    self.arrive(self.empty[st])
+                k += 1
+            # item epilogue
+            if n > 0:
+                yield ("wait", self.epi_done, (n - 1) & 1, n, f"warp {w} epilogue {n} (previous combine)")
+                if len(self.combined.get(n - 1, ())) != WARPS:
+                    self.fail(f"warp {w} stores item {n} before item {n - 1} is combined")
+            self.state[w] = n
+            self.arrive(self.epi_full)
+            yield ("wait", self.epi_full, n & 1, n + 1, f"warp {w} epilogue {n} (states)")
+            if any(s != n for s in self.state):
+                self.fail(f"warp {w} combines item {n} from states {self.state}")
+            yield ("delay", self.rng.uniform(0.1, 1.0))
+            if any(s != n for s in self.state):
+                self.fail(f"warp {w}: a state was overwritten during the combine of item {n}")
+            self.combined.setdefault(n, set()).add(w)
+            self.arrive(self.epi_done)
+            n += 1
+
+
+def _items(rng):
+    return [rng.choice([0, 1, 2, 3, 5, 8, 13]) for _ in range(rng.randint(1, 9))]
+
+
+@pytest.mark.parametrize("stages", [4, 8, 12])
+def test_decode_protocol_is_race_free(stages):
+    import random
+
+    for seed in range(150):
+        items = _items(random.Random(1000 + seed))
+        v = DecodeSim(items, stages, seed).run()
+        assert not v, f"seed {seed}, items {items}: {v[:3]}"
+
+
+@pytest.mark.parametrize("stages", [5, 6])
+def test_stage_counts_not_a_multiple_of_the_warps_are_caught(stages):
+    import random
+
+    caught = sum(bool(DecodeSim(_items(random.Random(1000 + seed)), stages, seed).run()) for seed in range(150))
+    assert caught > 0

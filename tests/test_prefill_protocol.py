@@ -23,37 +23,19 @@ reads the buffer it overwrites, an epilogue without its wait, a producer
 waiting on the wrong parity) show that the checks catch each kind of
 failure: stale data, a deadlock."""
 
-import heapq
-import random
-
 import pytest
+
+from tests._event_sim import Bar, EventSim
 
 K_STAGES, V_STAGES = 3, 2
 
 
-class Bar:
-    """mbarrier: a phase completes when its arrivals and transaction bytes
-    are all in; a parity test passes when the phase of the other parity
-    is the last completed one."""
-
-    def __init__(self, name, count):
-        self.name, self.count, self.pending, self.tx, self.completed = name, count, count, 0, 0
-
-    def test(self, parity):
-        return (self.completed & 1) != parity
-
-
-class Sim:
+class Sim(EventSim):
     def __init__(self, nch, seed, mutate=None):
-        self.rng = random.Random(seed)
+        super().__init__(seed)
         self.nch = nch  # chunks each tile attends (0: no such tile)
         self.n = max(nch)
         self.mutate = mutate
-        self.now = 0.0
-        self.events = []
-        self.seq = 0
-        self.waiting = []  # (bar, parity, gen, intended count, site)
-        self.violations = []
         self.full_k = [Bar(f"full_k{i}", 1) for i in range(K_STAGES)]
         self.empty_k = [Bar(f"empty_k{i}", 1) for i in range(K_STAGES)]
         self.full_v = [Bar(f"full_v{i}", 1) for i in range(V_STAGES)]
@@ -69,84 +51,13 @@ class Sim:
         self.s_buf = [None, None]  # ("S", c) or ("P", c)
         self.o_last = [-1, -1]  # last chunk accumulated into O_t
         self.pipe_free = 0.0
-        self.done = set()
-
-    # --- engine ---
-    def at(self, t, fn):
-        self.seq += 1
-        heapq.heappush(self.events, (t, self.seq, fn))
-
-    def fail(self, msg):
-        self.violations.append(f"t={self.now:.2f}: {msg}")
-
-    def arrive(self, bar, n=1):
-        bar.pending -= n
-        self._maybe_complete(bar)
-
-    def expect_tx(self, bar, nbytes):
-        bar.tx += nbytes
-        self.arrive(bar)
-
-    def complete_tx(self, bar, nbytes):
-        bar.tx -= nbytes
-        self._maybe_complete(bar)
-
-    def _maybe_complete(self, bar):
-        if bar.pending == 0 and bar.tx == 0:
-            bar.completed += 1
-            bar.pending = bar.count
-            still = []
-            for w in self.waiting:
-                if w[0] is bar and bar.test(w[1]):
-                    self.at(self.now, lambda w=w: self._resume_wait(w))
-                else:
-                    still.append(w)
-            self.waiting = still
-
-    def _resume_wait(self, w):
-        bar, parity, gen, intended, site = w
-        if bar.completed != intended:
-            self.fail(f"{site}: {bar.name} has completed {bar.completed} phases, wanted {intended}")
-        self.step(gen)
-
-    def step(self, gen, value=None):
-        try:
-            req = gen.send(value)
-        except StopIteration:
-            return
-        kind = req[0]
-        if kind == "delay":
-            self.at(self.now + req[1], lambda: self.step(gen))
-        elif kind == "wait":
-            _, bar, parity, intended, site = req
-            if bar.test(parity):
-                if bar.completed != intended:
-                    self.fail(f"{site}: {bar.name} has completed {bar.completed} phases, wanted {intended}")
-                self.at(self.now, lambda: self.step(gen))
-            else:
-                self.waiting.append((bar, parity, gen, intended, site))
 
     def run(self):
         roles = [self.key_producer(), self.value_producer(), self.mma()]
         roles += [self.softmax(t) for t in range(2) if self.nch[t] > 0]
-        for g in roles:
-            self.at(0.0, lambda g=g: self.step(g))
-        while self.events:
-            self.now, _, fn = heapq.heappop(self.events)
-            fn()
-        expect = {"kp", "vp", "mma"} | {f"sm{t}" for t in range(2) if self.nch[t] > 0}
-        if self.done != expect:
-            self.fail(f"deadlock: finished {sorted(self.done)}, waiting on "
-                      f"{sorted(w[0].name for w in self.waiting)}")
-        return self.violations
+        return self.run_roles(roles, {"kp", "vp", "mma"} | {f"sm{t}" for t in range(2) if self.nch[t] > 0})
 
     # --- copies and the tensor pipe ---
-    def tma(self, bar, nbytes, land):
-        def fin():
-            land()
-            self.complete_tx(bar, nbytes)
-        self.at(self.now + self.rng.uniform(0.5, 6.0), fin)
-
     def pipe(self, duration, start, end):
         t0 = max(self.now, self.pipe_free)
         self.pipe_free = t0 + duration
@@ -161,13 +72,13 @@ class Sim:
         for t in range(2):
             if self.nch[t]:
                 self.expect_tx(self.q_full[t], 2)
-                self.tma(self.q_full[t], 2, lambda t=t: self.q_tile.__setitem__(t, True))
+                self.copy(self.q_full[t], 2, lambda t=t: self.q_tile.__setitem__(t, True))
         for c in range(self.n):
             st = c % K_STAGES
             flip = 0 if self.mutate == "producer_parity" else 1
             yield ("wait", self.empty_k[st], ((c // K_STAGES) & 1) ^ flip, c // K_STAGES, f"key producer c{c}")
             self.expect_tx(self.full_k[st], 1)
-            self.tma(self.full_k[st], 1, lambda st=st, c=c: self.k_stage.__setitem__(st, c))
+            self.copy(self.full_k[st], 1, lambda st=st, c=c: self.k_stage.__setitem__(st, c))
             yield ("delay", self.rng.uniform(0.0, 0.5))
         self.done.add("kp")
 
@@ -176,7 +87,7 @@ class Sim:
             st = c % V_STAGES
             yield ("wait", self.empty_v[st], ((c // V_STAGES) & 1) ^ 1, c // V_STAGES, f"value producer c{c}")
             self.expect_tx(self.full_v[st], 1)
-            self.tma(self.full_v[st], 1, lambda st=st, c=c: self.v_stage.__setitem__(st, c))
+            self.copy(self.full_v[st], 1, lambda st=st, c=c: self.v_stage.__setitem__(st, c))
             yield ("delay", self.rng.uniform(0.0, 0.5))
         self.done.add("vp")
 

@@ -98,14 +98,14 @@ int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, 
   return PA_OK;
 }
 
-// Query rows of one KV head for the tcgen05 prefill: q [T][H][128] bf16 as a
+// Query rows of one KV head for the tcgen05 prefill: q [T][H][D] bf16 as a
 // 3D tensor (dims, head, token); a box of 64 dims x g heads x 128 / g tokens
 // lands as 128 rows of 128 bytes, row = token * g + head, 128-byte swizzle.
-int make_query_map(CUtensorMap* map, const void* q, int T, int H, int g) {
+int make_query_map(CUtensorMap* map, const void* q, int T, int H, int g, int D) {
   auto fn = encode_fn();
   if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t dims[3] = {128u, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {256u, (cuuint64_t)H * 256u};
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2u, (cuuint64_t)H * D * 2u};
   cuuint32_t box[3] = {64u, (cuuint32_t)g, (cuuint32_t)(128 / g)};
   cuuint32_t elem_strides[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, elem_strides,
@@ -444,7 +444,7 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
   if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31))
     return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: pool rows exceed 2^31 (TMA coordinates are 32-bit)");
   if ((long long)max_query_len * g > (1LL << 30)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: prompt too long");
-  if (head_dim == 128 && cdiv(max_query_len * g, 128) > 65535)
+  if (cdiv(max_query_len * g, 128) > 65535)
     return pa_fail(PA_ERR_UNSUPPORTED, "pa_prefill: more than 65535 query tiles of 128 rows");
   if (num_seqs == 0 || num_tokens == 0) return PA_OK;
   if (!q || !k || !v || !slot_mapping || !query_start || !context_lens || !block_tables || !k_cache || !v_cache ||
@@ -481,21 +481,17 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
   a.max_ctx = max_context_len;
   a.max_query_len = max_query_len;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-  if (head_dim == 128) {  // tensor-core generation 5 (tcgen05) path
-    CUtensorMap kmap, vmap;
-    rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
-    if (rc) return rc;
-    rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
-    if (rc) return rc;
-    CUtensorMap qmap, omap;
-    rc = make_query_map(&qmap, q, num_tokens, num_heads, g);
-    if (rc) return rc;
-    rc = make_query_map(&omap, out, num_tokens, num_heads, g);
-    if (rc) return rc;
-    e = pa::launch_prefill_tc(a, kmap, vmap, qmap, omap, st);
-  } else {
-    e = pa::launch_prefill(a, st);
-  }
+  // 5th-generation tensor cores (tcgen05) for head_dim 64 and 128
+  CUtensorMap kmap, vmap, qmap, omap;
+  rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
+  if (rc) return rc;
+  rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
+  if (rc) return rc;
+  rc = make_query_map(&qmap, q, num_tokens, num_heads, g, head_dim);
+  if (rc) return rc;
+  rc = make_query_map(&omap, out, num_tokens, num_heads, g, head_dim);
+  if (rc) return rc;
+  e = pa::launch_prefill_tc(a, kmap, vmap, qmap, omap, st);
   if (e != cudaSuccess) return cuda_fail(e, "pa_prefill launch");
   return PA_OK;
 }

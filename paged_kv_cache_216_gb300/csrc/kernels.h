@@ -150,8 +150,7 @@ struct PrefillArgs {
   int num_blocks, max_blocks_per_seq, max_ctx, max_query_len;
   float scale_log2;
 };
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
-// head_dim 128 on tcgen05; kmap/vmap: the bf16 cache maps with boxes of
+// Prefill on tcgen05, head_dim 64 or 128; kmap/vmap: the bf16 cache maps with boxes of
 // [B rows x 64 dims] (not the interleaved form); qmap: q as (dims, head,
 // token) with boxes of [64 dims x g heads x 128 / g tokens]; omap: out with
 // the same geometry.

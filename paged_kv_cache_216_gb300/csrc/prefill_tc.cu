@@ -1,11 +1,11 @@
 // Prefill on the 5th-generation tensor cores (tcgen05, accumulators in
-// tensor memory), head_dim 128, bf16 storage, fp32 accumulation.
+// tensor memory), head_dim 64 or 128, bf16 storage, fp32 accumulation.
 //
-// Same result as prefill.cu: every new token of a sequence attends the
-// sequence's tokens up to its own position ("PagedAttention Kernel：大模型
-// 推理优化的显存管理革新" section 3.1 with a causal limit; the prompt's keys
-// and values were appended into their blocks first, "Day 6/90 of Inference
-// Engineering", PagedAttention notes, paragraph 2).
+// Every new token of a sequence attends the sequence's tokens up to its own
+// position ("PagedAttention Kernel：大模型推理优化的显存管理革新" section 3.1
+// with a causal limit; the prompt's keys and values were appended into their
+// blocks first, "Day 6/90 of Inference Engineering", PagedAttention notes,
+// paragraph 2).
 //
 // One CTA per (sequence, KV head, pair of adjacent tiles of 128 query rows),
 // the rows being (new token, query head) pairs, token-major; pairs with the
@@ -58,7 +58,6 @@ namespace {
 constexpr int kM = 128;                 // query rows per tile (one tensor-memory lane each)
 constexpr int kTiles = 2;               // query tiles per CTA, sharing every stage
 constexpr int kN = 128;                 // keys per stage (the N of S = Q Kᵀ)
-constexpr int kDh = 128;                // head_dim
 constexpr int kStagesK = 3;             // stages in the key ring
 constexpr int kStagesV = 2;             // stages in the value ring
 constexpr int kSoftWarps = 4;           // per tile
@@ -66,22 +65,30 @@ constexpr int kProducerWarp = kTiles * kSoftWarps;  // keys; the next warp strea
 constexpr int kMmaWarp = kProducerWarp + 2;
 constexpr int kThreadsT = (kTiles * kSoftWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
-// O of tile t at columns 128t..128t+127, S of tile t at 256 + 128t, and P
-// (bf16 pairs) written over the first 64 columns of its S.
-constexpr uint32_t kColO = 0, kColS = 256;
 constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of a query tile
-constexpr int kQTile = 2 * kQHalf;
 constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage of K (or V)
-constexpr int kKVStage = 2 * kKVHalf;
-constexpr int kOffK = kTiles * kQTile;
-constexpr int kOffV = kOffK + kStagesK * kKVStage;
-constexpr int kOffBars = kOffV + kStagesV * kKVStage;
 // full_k[], empty_k[], full_v[], empty_v[]; per tile s_full, p_full,
 // o_final, q_full
 constexpr int kTileBars = 4;
-constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars) * 8; // tensor-memory address, abort flag
-constexpr size_t kBytesT = 1024 + kOffMisc + 16;
-static_assert(kBytesT <= 227 * 1024, "shared memory of one CTA");
+
+// Layout for head_dim DH (64 or 128): tiles and stages hold DH / 64 halves
+// of 64 dims; O of tile t at columns DH·t .. DH·t + DH - 1, S of tile t at
+// 2·DH + 128t (128 columns), P (bf16 pairs) over the first 64 columns of S.
+template <int DH>
+struct PfCfg {
+  static constexpr int kHalves = DH / 64;
+  static constexpr int kQTile = kHalves * kQHalf;
+  static constexpr int kKVStage = kHalves * kKVHalf;
+  static constexpr int kOffK = kTiles * kQTile;
+  static constexpr int kOffV = kOffK + kStagesK * kKVStage;
+  static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars) * 8;  // tensor-memory address, abort flag
+  static constexpr size_t kBytes = 1024 + kOffMisc + 16;
+  static constexpr uint32_t kColO = 0, kColS = 2 * DH;
+  static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
+  static_assert(kBytes <= 227 * 1024, "shared memory of one CTA");
+  static_assert(kColS + kTiles * 128 <= kTmemCols, "tensor-memory columns");
+};
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -179,10 +186,14 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const 
   return false;
 }
 
+template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
                       const PrefillArgs p) {
+  using C = PfCfg<DH>;
+  constexpr int kQTile = C::kQTile, kKVStage = C::kKVStage, kOffK = C::kOffK, kOffV = C::kOffV;
+  constexpr uint32_t kColO = C::kColO, kColS = C::kColS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int t_end = max(t_end0, t_end1);
   const int nch = max(nch0, nch1);
 
-  uint64_t* full_k = reinterpret_cast<uint64_t*>(base + kOffBars);
+  uint64_t* full_k = reinterpret_cast<uint64_t*>(base + C::kOffBars);
   uint64_t* empty_k = full_k + kStagesK;
   uint64_t* full_v = empty_k + kStagesK;
   uint64_t* empty_v = full_v + kStagesV;
@@ -222,8 +233,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   auto p_full = [&](int t) { return tile_bars + t * kTileBars + 1; };
   auto o_final = [&](int t) { return tile_bars + t * kTileBars + 2; };
   auto q_full = [&](int t) { return tile_bars + t * kTileBars + 3; };
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kOffMisc);
-  volatile int* abort = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
 
   if (tid == 0) {
@@ -271,8 +282,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if ((t == 0 ? nch0 : nch1) == 0) continue;
         const int z = q0 + (row00 + t * kM) / p.g;
         mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
-        tma_load_3d(base + t * kQTile, &qmap, q_full(t), 0, kvh * p.g, z, qpol);
-        tma_load_3d(base + t * kQTile + kQHalf, &qmap, q_full(t), 64, kvh * p.g, z, qpol);
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, kvh * p.g, z, qpol);
       }
     }
     pdl_wait_primary();  // the prompt's keys and values are in the cache from here on
@@ -305,7 +317,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (lane == 0) {
         ok = mbar_wait(&empties[st], ((c / stages) & 1) ^ 1, abort);
         if (ok) {
-          mbar_arrive_expect_tx(&fulls[st], (uint32_t)(nb * p.B * 128 * 2));
+          mbar_arrive_expect_tx(&fulls[st], (uint32_t)(nb * p.B * 128 * C::kHalves));
         } else {
           *abort = 1;
           raise_status(p.status, PA_STATUS_TIMEOUT);
@@ -316,8 +328,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (lane < nb) {
         const int y = (id * p.Hkv + kvh) * p.B;
         uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
-        tma_load_2d(d, map, &fulls[st], 0, y, policy);
-        tma_load_2d(d + kKVHalf, map, &fulls[st], 64, y, policy);
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h) tma_load_2d(d + h * kKVHalf, map, &fulls[st], 64 * h, y, policy);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     // once.  A stage is released by a commit after the last MMA that reads
     // it.
     const uint32_t id_s = instr_desc(kM, kN, false);
-    const uint32_t id_o = instr_desc(kM, kDh, true);
+    const uint32_t id_o = instr_desc(kM, DH, true);
     bool ok = true;
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
       int r = 1;
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       const uint64_t b0 = smem_desc(sbase + kOffK + (c % kStagesK) * kKVStage, 16, 1024);
       const uint32_t d = tmem + kColS + (uint32_t)t * 128;
 #pragma unroll
-      for (int kk = 0; kk < kDh / 16; ++kk) {
+      for (int kk = 0; kk < DH / 16; ++kk) {
         const int hlf = kk >> 2, w = kk & 3;
         mma_ss(d, a0 + (uint64_t)((hlf * kQHalf + w * 32) >> 4), b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4), id_s,
                kk > 0);
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       tc_fence_after();
       const uint64_t b0 = smem_desc(sbase + kOffV + (c % kStagesV) * kKVStage, kKVHalf, 1024);
       const uint32_t p_cols = tmem + kColS + (uint32_t)t * 128;
-      const uint32_t d = tmem + kColO + (uint32_t)t * 128;
+      const uint32_t d = tmem + kColO + (uint32_t)t * DH;
 #pragma unroll
       for (int kk = 0; kk < kN / 16; ++kk) mma_ts(d, p_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, c > 0 || kk > 0);
       if (c + 1 == (t == 0 ? nch0 : nch1)) mma_commit(o_final(t));
@@ -380,7 +392,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       const int nv = min(kN, t_end - c * kN);
       if (nv < kN) {  // value rows past the pair's keys: zeros (their keys are masked)
         uint8_t* vs = base + kOffV + (c % kStagesV) * kKVStage;
-        for (int u = lane; u < (kN - nv) * 8 * 2; u += 32) {
+        for (int u = lane; u < (kN - nv) * 8 * C::kHalves; u += 32) {
           const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
           *reinterpret_cast<uint4*>(vs + hlf * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       const int r = row0 + lt;
       const int pos = r < rows ? first_pos + r / p.g : -1;  // keys 0 .. pos
       const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
-      const uint32_t o_cols = lane_base + kColO + (uint32_t)t * 128;
+      const uint32_t o_cols = lane_base + kColO + (uint32_t)t * DH;
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int c = 0; c < nch_t; ++c) {
@@ -467,7 +479,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (c > 0 && __any_sync(0xffffffffu, grow && m_run != -INFINITY)) {
           // O holds P·V(c - 1): the commit that released S(c) covers it
 #pragma unroll 1
-          for (int i = 0; i < kDh / 16; ++i) {
+          for (int i = 0; i < DH / 16; ++i) {
             float v[16];
             tmem_ld16(o_cols + 16 * i, v);
             uint32_t w[16];
@@ -501,9 +513,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (named_barrier_and(1 + t, kSoftWarps * 32, ok && mbar_wait(o_final(t), 0, abort))) {
         tc_fence_after();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint32_t o[kDh];  // the row of O, all loads in flight at once
+        uint32_t o[DH];  // the row of O, all loads in flight at once
 #pragma unroll
-        for (int i = 0; i < kDh / 16; ++i) tmem_ld16_nowait(o_cols + 16 * i, o + 16 * i);
+        for (int i = 0; i < DH / 16; ++i) tmem_ld16_nowait(o_cols + 16 * i, o + 16 * i);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         auto piece = [&](int u) {  // dims 8u .. 8u + 7 of the row, normalized, as bf16
           uint4 w;
@@ -519,21 +531,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           // store them with two TMA boxes through the same geometry.
           uint8_t* qt = base + t * kQTile;
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
+          for (int u = 0; u < DH / 8; ++u)
             *reinterpret_cast<uint4*>(qt + (u >> 3) * kQHalf + lt * 128 + (((u & 7) ^ (lt & 7)) << 4)) = piece(u);
           fence_proxy_async_smem();
           named_barrier_sync(1 + t, kSoftWarps * 32);
           if (lt == 0) {
             const int z = q0 + row0 / p.g;
-            tma_store_3d(&omap, qt, 0, kvh * p.g, z);
-            tma_store_3d(&omap, qt + kQHalf, 64, kvh * p.g, z);
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) tma_store_3d(&omap, qt + h * kQHalf, 64 * h, kvh * p.g, z);
             bulk_store_drain();
           }
         } else if (r < rows) {  // the sequence's last tile: only its own rows
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * kDh);
+                                                ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * DH);
 #pragma unroll
-          for (int u = 0; u < 16; ++u) dst[u] = piece(u);
+          for (int u = 0; u < DH / 8; ++u) dst[u] = piece(u);
         }
       } else {
         *abort = 1;
@@ -550,6 +562,33 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
 }
 
+template <int DH>
+cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const CUtensorMap& qmap, const CUtensorMap& omap, int pairs, cudaStream_t stream) {
+  constexpr size_t kBytes = PfCfg<DH>::kBytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::once_flag once[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t init_err = cudaSuccess;
+  std::call_once(once[dev], [&] {
+    init_err = cudaFuncSetAttribute(prefill_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBytes);
+  });
+  if (init_err != cudaSuccess) return init_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)a.S, (unsigned)pairs);
+  cfg.blockDim = dim3(kThreadsT);
+  cfg.dynamicSmemBytes = kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, omap, a);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -558,27 +597,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
   const int pairs = (tiles + kTiles - 1) / kTiles;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
   if (pairs > 65535 || a.S > 65535 || a.Hkv > 65535) return cudaErrorInvalidConfiguration;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  static std::once_flag once[64];
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  cudaError_t init_err = cudaSuccess;
-  std::call_once(once[dev], [&] {
-    init_err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBytesT);
-  });
-  if (init_err != cudaSuccess) return init_err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)a.S, (unsigned)pairs);
-  cfg.blockDim = dim3(kThreadsT);
-  cfg.dynamicSmemBytes = kBytesT;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, kmap, vmap, qmap, omap, a);
+  if (a.D == 128) return launch_prefill_tc_dh<128>(a, kmap, vmap, qmap, omap, pairs, stream);
+  if (a.D == 64) return launch_prefill_tc_dh<64>(a, kmap, vmap, qmap, omap, pairs, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

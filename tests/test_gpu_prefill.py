@@ -76,6 +76,8 @@ CASES = {
     "g1_d128_b32": ([0, 100], [150, 33], 4, 4, 128, 32),
     # a sequence with no new tokens between two that have some
     "g4_no_new_tokens": ([12, 40, 0], [3, 0, 70], 8, 2, 128, 16),
+    # head_dim 64 with grouped heads: ragged prompts, full and partial tiles, 8-token blocks
+    "g4_d64_b8": ([0, 77, 300], [70, 33, 129], 16, 4, 64, 8),
 }
 
 

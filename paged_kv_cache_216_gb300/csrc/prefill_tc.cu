@@ -19,13 +19,14 @@
 //    entries fetched 32 at a time.  Warp 8 first loads both query tiles,
 //    one 3D box per 64-dim half, so they land with the first keys;
 //  * warp 10 (MMA): one thread issues, per tile, S = Q Kᵀ (M 128, N 128,
-//    K 128: eight tcgen05.mma kind::f16 from shared-memory descriptors)
-//    into the tile's S and O += P V (M 128, N 128, K 128: eight MMAs, P read
-//    from tensor memory, V an MN-major operand in shared memory), in a fixed
-//    order -- per chunk c and tile, P·V(c) and then S(c + 1) -- spinning on
-//    one barrier at a time, so the tensor cores work for one tile while the
-//    other tile's softmax runs (ping-pong); tcgen05.commit signals the
-//    mbarriers and releases each stage after the last MMA that reads it;
+//    K = head_dim: head_dim / 16 tcgen05.mma kind::f16 from shared-memory
+//    descriptors) into the tile's S and O += P V (M 128, N = head_dim,
+//    K 128: eight MMAs, P read from tensor memory, V an MN-major operand in
+//    shared memory), in a fixed order -- per chunk c and tile, P·V(c) and
+//    then S(c + 1) -- spinning on one barrier at a time, so the tensor cores
+//    work for one tile while the other tile's softmax runs (ping-pong);
+//    tcgen05.commit signals the mbarriers and releases each stage after the
+//    last MMA that reads it;
 //  * warps 0-3 and 4-7 (softmax, one warpgroup per tile): thread t of a
 //    warpgroup owns query row t of its tile (tensor-memory lane t): it
 //    reads its 128 scores (tcgen05.ld), masks keys past its position, keeps
@@ -34,14 +35,14 @@
 //    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
 //    exact enough and O and the sum use the same max); at the end it reads
 //    its row of O, divides by the sum and stores it (a full tile through
-//    its query buffer and two TMA boxes, the sequence's last tile row by
-//    row).
-// Tensor memory (all 512 columns): O of tile t at columns 128t..128t+127 and
-// its S at 256 + 128t; P is written over the first half of its S.  Value
-// rows past the pair's keys are zeroed in shared memory before the first
-// P·V of that stage so stale cache rows cannot turn 0 x NaN into NaN.  Every
-// wait is bounded; on a time-out the kernel raises PA_STATUS_TIMEOUT and
-// stops issuing work.
+//    its query buffer and one TMA box per 64-dim half, the sequence's last
+//    tile row by row).
+// Tensor memory (512 columns allocated): O of tile t at columns DH·t ..
+// DH·t + DH - 1 and its S at 2·DH + 128t (DH = head_dim); P is written over
+// the first half of its S.  Value rows past the pair's keys are zeroed in
+// shared memory before the first P·V of that stage so stale cache rows
+// cannot turn 0 x NaN into NaN.  Every wait is bounded; on a time-out the
+// kernel raises PA_STATUS_TIMEOUT and stops issuing work.
 
 #include <cuda_bf16.h>
 

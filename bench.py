@@ -492,6 +492,8 @@ def host_cores() -> int:
 def run_reference(args, rank, world):
     if rank != 0:
         return None
+    if args.prefill:
+        return run_reference_prefill(args, world)
     w = WORKLOADS[args.workload]
     vals = []
     desc = ""
@@ -658,6 +660,27 @@ def prefill_oracle_sample(budget_s: float):
     t = time.perf_counter() - t0
     flops = prefill_flops(b) / sh["num_seqs"] * done
     return flops / t / 1e12, f"oracle prefill of {done} of the {sh['num_seqs']} sequences in {t:.1f} s"
+
+
+def run_reference_prefill(args, world):
+    """The reference arm of the prefill benchmark: the oracle on whole
+    sequences of the same batch, a bounded sample per step, with our arm's
+    metric, unit and workload."""
+    vals, desc = [], ""
+    for _ in range(args.steps):
+        v, desc = prefill_oracle_sample(max(0.5, args.ref_budget / max(1, args.steps)))
+        vals.append(v)
+    value = statistics.median(vals)
+    sh = dict(PREFILL_SHAPE)
+    return {
+        "metric": "prefill attention TFLOP/s", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "prefill_bf16", **sh},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
 
 
 def main():

@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 from workloads import WORKLOADS, context_lens, free_order, pool_blocks, queries, random_pool  # noqa: E402
 from workloads import normal, serving_step_tokens  # noqa: E402
 
-DEFAULT_WORKLOAD = "mha_bf16"
+DEFAULT_WORKLOAD = "long_bf16"
 METRIC = "paged-decode KV-read GB/s"
 UNIT = "GB/s"
 
@@ -102,6 +102,28 @@ def measured_peaks() -> dict:
     return {}
 
 
+def smi_gpu_id(device: int) -> str:
+    """The identifier nvidia-smi knows this process's CUDA device ``device``
+    by.  nvidia-smi numbers GPUs physically and ignores CUDA_VISIBLE_DEVICES,
+    so the CUDA ordinal is not it: use the device's UUID, else its PCI
+    address, else the ordinal mapped through CUDA_VISIBLE_DEVICES."""
+    try:
+        import torch
+
+        props = torch.cuda.get_device_properties(device)
+        uuid = str(getattr(props, "uuid", "") or "")
+        if uuid:
+            return uuid if uuid.startswith(("GPU-", "MIG-")) else "GPU-" + uuid
+        if hasattr(props, "pci_bus_id"):
+            return f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    except Exception:
+        pass
+    vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    if device < len(vis):
+        return vis[device]
+    return str(device)
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
 
@@ -109,15 +131,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, device: int):
         self.proc = None
         self.path = None
-        self.gpu = gpu_index
+        self.gpu = smi_gpu_id(device)
         exe = shutil.which("nvidia-smi")
         if exe:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
-            self.proc = subprocess.Popen([exe, "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+            self.proc = subprocess.Popen([exe, "-i", self.gpu, "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
@@ -445,9 +467,9 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("paged_decode_fp8_kernel + lse_merge_kernel" if fp8 else
-                                "paged_decode_tc_kernel (with shared-prefix items) + lse_merge_kernel" if groups
-                                else "paged_decode_tc_kernel + lse_merge_kernel"),
+                     "kernel": ("paged_decode_fp8_kernel" if fp8 else
+                                "paged_decode_tc_kernel (with shared-prefix items)" if groups
+                                else "paged_decode_tc_kernel") + (" + lse_merge_kernel" if eng.split else ""),
                      "peak_source": f"{peak_src} hbm_gbs", "decode_ms": round(dec_avg * 1e3, 4),
                      "timing": f"CUDA events inside each step's graph, {K} steps after the timed run"},
         "clocks": clk,

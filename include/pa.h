@@ -181,6 +181,35 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*
+ * Test hook for the decode kernel's time-out path; not for production use.
+ * The pages recommend defensive checks in the kernel [PAK section 5.1]:
+ * every pipeline wait of the bf16 decode kernel is bounded, and one that
+ * runs out raises PA_STATUS_TIMEOUT and stops the CTA instead of hanging.
+ * This call is pa_decode (bf16 caches, same arguments and workspace) with
+ * two changes that make such a wait run out on purpose, with no fault:
+ *   - every pipeline wait gives up after wait_limit_us microseconds
+ *     (1 .. 2000000) instead of 2 s;
+ *   - the copy warp of every persistent CTA never issues that CTA's chunk
+ *     number withheld_chunk (>= 0, counted over the CTA's work from 0): no
+ *     copy is in flight for it and its barrier is never armed, so the
+ *     consumer waiting for it runs out of time.
+ * A CTA that gives up raises PA_STATUS_TIMEOUT, waits (bounded the same
+ * way) for its own copies in flight, and exits; the other CTAs follow once
+ * they reach the chunk.  `out` is then undefined; the context stays usable
+ * and later calls are unaffected.  Read the status with pa_get_status.
+ */
+int pa_decode_test_withhold(const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context_len,
+                            float scale, void* out, int num_seqs,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, int partition_size,
+                            void* workspace, size_t workspace_bytes,
+                            int withheld_chunk, int wait_limit_us,
+                            void* stream);
+
+/*
  * Work list of the decode kernel built on the host, for callers that know
  * their context lengths there (a serving loop's allocator does) and can
  * upload it with their block tables, so that no planning kernel runs in the
@@ -328,7 +357,9 @@ int pa_decode_planned_shared_prefix(
  *     (pa_decode_workspace_bytes) exceeds it return PA_ERR_INVALID.
  *   - Every GPU that loads the library holds the array until the process
  *     exits.  The first call on a device looks up the array's address there
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress), and so does the first call after the device's
+ *     context was re-created (cudaDeviceReset); make that first call before
+ *     any stream capture.
  *   - All calls share the array and it keeps the last call's contents;
  *     nothing in it needs to start at zero.  Calls whose kernels overlap on
  *     the GPU (different streams or threads) race on it: serialise them.

@@ -44,6 +44,8 @@ SIGNATURES = {
     "pa_decode_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _vp]),
+    "pa_decode_test_withhold": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
+                                         _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _c_int, _vp]),
     "pa_decode_plan_bytes": (_c_sz, [_c_int, _c_int, _c_int]),
     "pa_decode_plan_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp]),
     "pa_decode_planned": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,

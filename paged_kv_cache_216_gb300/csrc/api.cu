@@ -30,23 +30,37 @@ int cuda_fail(cudaError_t e, const char* what) {
   return pa_fail(PA_ERR_CUDA, buf);
 }
 
-// Address of this device's status word (looked up once per device).
+// Address of this device's status word, looked up once per device and
+// context (again if the device's context was re-created since).
 int status_ptr(unsigned** out) {
   static unsigned* ptrs[kMaxDevices] = {};
+  static unsigned long long ctx_ids[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return pa_fail(PA_ERR_UNSUPPORTED, "device ordinal too large");
+  const unsigned long long ctx = pa_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (!ptrs[dev] || ctx == 0 || ctx != ctx_ids[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_status_word);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
     ptrs[dev] = static_cast<unsigned*>(p);
+    ctx_ids[dev] = pa_context_id();  // the lookup made the device's context current
   }
   *out = ptrs[dev];
   return PA_OK;
+}
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -168,6 +182,21 @@ bool ws_layout(int S, int H, int D, int max_ctx, int P, WsLayout* l) {
 
 }  // namespace
 
+unsigned long long pa_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent");
+    get_id = driver_fn<PFN_cuCtxGetId_v12000>("cuCtxGetId");
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 extern "C" {
 
 int pa_get_status(void* stream, uint32_t* status) {
@@ -288,7 +317,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
                        void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                        int num_blocks, int partition_size, const void* plan, const int32_t* groups,
                        int num_groups, void* workspace, size_t workspace_bytes, int dtype, void* stream,
-                       float k_scale = 1.f, float v_scale = 1.f) {
+                       float k_scale = 1.f, float v_scale = 1.f,
+                       unsigned long long wait_limit_ns = pa::kDefaultWaitLimitNs, int withhold_chunk = -1) {
   // dtype is the caches' type; with PA_FP8_E4M3 q and out are bf16.
   const int es = elem_bytes(dtype);
   if (es == 0) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
@@ -362,6 +392,8 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   a.scale_log2 = (float)((double)scale * (fp8 ? (double)k_scale : 1.0) * 1.4426950408889634);  // log2(e)
   a.shared_items = pg.n > 0;
   a.v_scale = fp8 ? v_scale : 1.f;
+  a.wait_limit_ns = wait_limit_ns;
+  a.withhold_chunk = withhold_chunk;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -410,6 +442,20 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
                      out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
                      nullptr, nullptr, 0, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_decode_test_withhold(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
+                            void* out, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, int partition_size, void* workspace, size_t workspace_bytes,
+                            int withheld_chunk, int wait_limit_us, void* stream) {
+  if (withheld_chunk < 0) return pa_fail(PA_ERR_INVALID, "pa_decode_test_withhold: withheld_chunk < 0");
+  if (wait_limit_us < 1 || wait_limit_us > 2000000)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_test_withhold: wait_limit_us outside [1, 2000000]");
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, max_context_len, scale,
+                     out, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, partition_size,
+                     nullptr, nullptr, 0, workspace, workspace_bytes, PA_BF16, stream, 1.f, 1.f,
+                     1000ull * (unsigned long long)wait_limit_us, withheld_chunk);
 }
 
 int pa_decode_planned(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

@@ -30,17 +30,21 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PA_STATIC_WORKSP
 constexpr int kMaxDevices = 64;
 
 // Device address of this device's copy of the array.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device, with that device current.
+// array's name is only a host-side stand-in, so the address is looked up
+// with the device current: once per device, on the first call there, and
+// again if the device's context was re-created since (cudaDeviceReset
+// unloads the library's module; the old address would then dangle).
 int scratch_address(void** out) {
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_ids[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return pa_fail(PA_ERR_CUDA, "pa_decode_static_workspace: cudaGetDevice failed");
   if (dev < 0 || dev >= kMaxDevices) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_static_workspace: device ordinal");
+  const unsigned long long ctx = pa_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx != ctx_ids[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || !p) {
@@ -50,6 +54,7 @@ int scratch_address(void** out) {
       return pa_fail(PA_ERR_CUDA, buf);
     }
     addr[dev] = p;
+    ctx_ids[dev] = pa_context_id();  // the lookup made the device's context current
   }
   *out = addr[dev];
   return PA_OK;

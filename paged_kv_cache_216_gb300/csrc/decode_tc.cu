@@ -146,7 +146,7 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
     const int prx = __shfl_sync(kFull, cur_pr.x, 0);
     const int ctx = __shfl_sync(kFull, cur_pr.y, 0);  // < 0: a shared-prefix item
     const int slot = n & 1;
-    if (!mbar_wait(&bar.qempty[slot], ((n >> 1) & 1) ^ 1, abort)) {
+    if (!mbar_wait(&bar.qempty[slot], ((n >> 1) & 1) ^ 1, abort, p.wait_limit_ns)) {
       ok = false;
       break;
     }
@@ -197,13 +197,16 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
         id = 0;
       }
       const int stage = kseq % C::kStages;
-      if (!mbar_wait(&bar.empty[stage], ((kseq / C::kStages) & 1) ^ 1, abort)) {
+      // Test hook: a withheld chunk is never issued (no copy in flight, no
+      // arrival), so the consumer's wait for it runs out.
+      const bool issue = kseq != (uint32_t)p.withhold_chunk;
+      if (issue && !mbar_wait(&bar.empty[stage], ((kseq / C::kStages) & 1) ^ 1, abort, p.wait_limit_ns)) {
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * chunk_block_bytes);
+      if (issue && lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * chunk_block_bytes);
       __syncwarp();
-      if (lane < nb) {
+      if (issue && lane < nb) {
         const int y = (id * p.Hkv + kvh) * p.B;
         if constexpr (kInter) {
           uint8_t* sk = base + stage * C::kStage + lane * p.B * 256;
@@ -231,8 +234,8 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
     // Let copies already issued land before the CTA's shared memory goes away.
     const volatile int never = 0;
     for (uint32_t k = (kseq > (uint32_t)C::kStages ? kseq - C::kStages : 0); k < kseq; ++k)
-      mbar_wait(&bar.full[k % C::kStages], (k / C::kStages) & 1, &never);
-    for (uint32_t k = (nq > 2 ? nq - 2 : 0); k < nq; ++k) mbar_wait(&bar.qfull[k & 1], (k >> 1) & 1, &never);
+      mbar_wait(&bar.full[k % C::kStages], (k / C::kStages) & 1, &never, p.wait_limit_ns);
+    for (uint32_t k = (nq > 2 ? nq - 2 : 0); k < nq; ++k) mbar_wait(&bar.qfull[k & 1], (k >> 1) & 1, &never, p.wait_limit_ns);
   }
 }
 
@@ -254,7 +257,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
 
   for (uint32_t n = 0;; ++n) {
     const int slot = n & 1;
-    if (!mbar_wait(&bar.qfull[slot], (n >> 1) & 1, abort)) {
+    if (!mbar_wait(&bar.qfull[slot], (n >> 1) & 1, abort, p.wait_limit_ns)) {
       give_up(p, abort);
       return;
     }
@@ -289,7 +292,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     for (int ch = 0; ch < nch; ++ch, ++kseq) {
       if ((int)(kseq & (kConsumerWarps - 1)) != warp) continue;
       const int stage = kseq % C::kStages;
-      if (!mbar_wait(&bar.full[stage], (kseq / C::kStages) & 1, abort)) {
+      if (!mbar_wait(&bar.full[stage], (kseq / C::kStages) & 1, abort, p.wait_limit_ns)) {
         give_up(p, abort);
         return;
       }
@@ -388,7 +391,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
 
     // ---- item epilogue: merge the four warps' states ----
     // The previous item's combine must be over before its buffers are reused.
-    if (n > 0 && !mbar_wait(bar.epi_done, (n - 1) & 1, abort)) {
+    if (n > 0 && !mbar_wait(bar.epi_done, (n - 1) & 1, abort, p.wait_limit_ns)) {
       give_up(p, abort);
       return;
     }
@@ -412,7 +415,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar.epi_full);
-    if (!mbar_wait(bar.epi_full, n & 1, abort)) {
+    if (!mbar_wait(bar.epi_full, n & 1, abort, p.wait_limit_ns)) {
       give_up(p, abort);
       return;
     }

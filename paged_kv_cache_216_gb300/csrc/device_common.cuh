@@ -13,7 +13,7 @@ namespace pa {
 
 // A pipeline wait that has not completed after this long is treated as a
 // fault: the kernel sets PA_STATUS_TIMEOUT and returns.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s (kDefaultWaitLimitNs of kernels.h)
 constexpr unsigned kWaitLimitIters = 1u << 30;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -64,16 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns
-// false if it did not within the time limit or if `abort` (shared flag) is
+// false if it did not within `limit_ns` or if `abort` (shared flag) is
 // raised by another warp meanwhile.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (unsigned i = 0; i < kWaitLimitIters; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 63u) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
   return false;

@@ -16,6 +16,10 @@ struct PlanHeader {
   int pad[62];
 };
 
+// Bound of a pipeline wait of the decode kernels unless a call says
+// otherwise (a wait this long means the pipeline is broken).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
 // Everything a decode launch needs besides the cache tensor maps.
 struct DecodeArgs {
   const void* q;                // [S][H][D]
@@ -37,6 +41,11 @@ struct DecodeArgs {
   float scale_log2;             // scale * log2(e)
   int shared_items;             // the work list may hold shared-prefix items
   float v_scale;                // FP8 caches: value of a V code = e4m3(code) * v_scale (1 otherwise)
+  // Bound of every pipeline wait of the bf16 kernel (2 s normally), and a
+  // test hook: the producer of each CTA never issues the CTA's chunk number
+  // `withhold_chunk` (-1: none), so that the wait for it runs out.
+  unsigned long long wait_limit_ns;
+  int withhold_chunk;
 };
 
 constexpr int kMaxGroup = 8;

@@ -11,6 +11,13 @@ void pa_clear_error();
 
 #define PA_ABI_VERSION 1
 
+// Identifier of the CUDA context current on the calling thread (unique
+// within the process; a device's primary context gets a new one when it is
+// re-created, e.g. after cudaDeviceReset), or 0 if none is current or it
+// cannot be read.  Device addresses the library caches per device are keyed
+// on it, so that they are looked up again in a new context.
+unsigned long long pa_context_id();
+
 namespace pa {
 struct PrefixGroups;
 }

@@ -1,15 +1,35 @@
 """The C ABI library loads, exports every symbol its header declares, and
-rejects bad host-side arguments before touching the GPU (no GPU needed)."""
+rejects bad host-side arguments before touching the GPU (no GPU needed).
 
-import ctypes
+The refusal cases pass made-up device addresses for the pointers they do not
+test.  They run in a child process that sees no GPU (tests/_abi_child.py):
+should a host-side check ever stop refusing one of them, the call fails with
+a CUDA "no device" error there instead of launching a kernel on the bogus
+address on whatever GPU this suite runs on."""
+
+import json
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
 from tests._lib_fixture import ensure_built
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = {"ptr": 0x100000}  # a made-up device address (only ever used where no GPU is visible)
+
+
+def run_without_gpu(calls):
+    """[(function, args)] -> [(rc, message)], made in a process with
+    CUDA_VISIBLE_DEVICES="" ."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "_abi_child.py")],
+                       input=json.dumps([[f, a] for f, a in calls]), capture_output=True, text=True, env=env,
+                       cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [tuple(x) for x in json.loads(r.stdout.strip().splitlines()[-1])]
 
 
 @pytest.fixture(scope="module")
@@ -54,15 +74,14 @@ def test_version(L):
 
 
 def _decode_args(**over):
-    fake = ctypes.c_void_p(0x100000)
-    a = dict(q=fake, k=fake, v=fake, bt=fake, mb=8, ctx=fake, maxctx=100, scale=0.1, out=fake, S=2, H=8, Hkv=2,
-             D=128, B=16, N=10, P=0, ws=fake, wsb=1 << 30, dtype=1, stream=None)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mb=8, ctx=FAKE, maxctx=100, scale=0.1, out=FAKE, S=2, H=8, Hkv=2,
+             D=128, B=16, N=10, P=0, ws=FAKE, wsb=1 << 30, dtype=1, stream=None)
     a.update(over)
     return [a[k] for k in ("q", "k", "v", "bt", "mb", "ctx", "maxctx", "scale", "out", "S", "H", "Hkv", "D", "B",
                            "N", "P", "ws", "wsb", "dtype", "stream")]
 
 
-@pytest.mark.parametrize("over,code", [
+DECODE_CASES = [
     (dict(H=12, Hkv=4), -2),              # g = 3
     (dict(H=32, Hkv=2), -2),              # g = 16
     (dict(H=8, Hkv=3), -1),               # not a multiple
@@ -72,38 +91,22 @@ def _decode_args(**over):
     (dict(maxctx=0), -1),
     (dict(mb=6), -1),                     # 6 blocks of 16 < 100 tokens
     (dict(P=48), -1),                     # not a multiple of 32
-    (dict(q=ctypes.c_void_p(0)), -1),
-    (dict(q=ctypes.c_void_p(0x100004)), -1),  # misaligned
+    (dict(q=None), -1),
+    (dict(q={"ptr": 0x100004}), -1),      # misaligned
     (dict(wsb=16), -1),                   # workspace too small
     (dict(scale=float("nan")), -1),
-])
-def test_decode_rejects_bad_arguments_without_a_launch(L, over, code):
-    rc = L.pa_decode(*_decode_args(**over))
-    assert rc == code
-    assert L.pa_last_error()
-
-
-def test_append_and_copy_reject_bad_arguments(L):
-    f = ctypes.c_void_p(0x100000)
-    assert L.pa_cache_append(f, f, f, 4, f, f, 10, 2, 96, 16, 1, None) == -2
-    assert L.pa_cache_append(f, f, f, -1, f, f, 10, 2, 128, 16, 1, None) == -1
-    assert L.pa_cache_append(None, f, f, 4, f, f, 10, 2, 128, 16, 1, None) == -1
-    assert L.pa_cache_append(f, f, f, 0, f, f, 10, 2, 128, 16, 1, None) == 0  # nothing to do
-    assert L.pa_copy_blocks(f, f, f, 3, 10, 2, 128, 12, 1, None) == -2
-    assert L.pa_copy_blocks(f, f, None, 3, 10, 2, 128, 16, 1, None) == -1
-    assert L.pa_copy_blocks(f, f, f, 0, 10, 2, 128, 16, 1, None) == 0
+]
 
 
 def _prefill_args(**over):
-    f = ctypes.c_void_p(0x100000)
-    a = dict(q=f, k=f, v=f, slots=f, T=64, qs=f, ctx=f, bt=f, mb=8, mql=64, maxctx=128, scale=0.1, kc=f, vc=f,
-             out=f, S=1, H=8, Hkv=2, D=128, B=16, N=16, dtype=1, stream=None)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, slots=FAKE, T=64, qs=FAKE, ctx=FAKE, bt=FAKE, mb=8, mql=64, maxctx=128,
+             scale=0.1, kc=FAKE, vc=FAKE, out=FAKE, S=1, H=8, Hkv=2, D=128, B=16, N=16, dtype=1, stream=None)
     a.update(over)
     return [a[k] for k in ("q", "k", "v", "slots", "T", "qs", "ctx", "bt", "mb", "mql", "maxctx", "scale", "kc",
                            "vc", "out", "S", "H", "Hkv", "D", "B", "N", "dtype", "stream")]
 
 
-@pytest.mark.parametrize("over,code", [
+PREFILL_CASES = [
     (dict(H=12, Hkv=4), -2),              # g = 3
     (dict(H=32, Hkv=2), -2),              # g = 16
     (dict(D=96), -2),
@@ -114,13 +117,50 @@ def _prefill_args(**over):
     (dict(S=70000), -2),
     # 8 heads per KV head x 1.1M prompt tokens = 68750 query tiles of 128 rows
     (dict(H=16, Hkv=2, mql=1_100_000, maxctx=1_100_000, mb=70_000), -2),
-    (dict(q=ctypes.c_void_p(0)), -1),
-    (dict(q=ctypes.c_void_p(0x100004)), -1),  # misaligned
-])
-def test_prefill_rejects_bad_arguments_without_a_launch(L, over, code):
-    rc = L.pa_prefill(*_prefill_args(**over))
-    assert rc == code
-    assert L.pa_last_error()
+    (dict(q=None), -1),
+    (dict(q={"ptr": 0x100004}), -1),      # misaligned
+]
+
+f = FAKE
+OTHER_CASES = [
+    ("pa_cache_append", [f, f, f, 4, f, f, 10, 2, 96, 16, 1, None], -2),
+    ("pa_cache_append", [f, f, f, -1, f, f, 10, 2, 128, 16, 1, None], -1),
+    ("pa_cache_append", [None, f, f, 4, f, f, 10, 2, 128, 16, 1, None], -1),
+    ("pa_cache_append", [f, f, f, 0, f, f, 10, 2, 128, 16, 1, None], 0),  # nothing to do
+    ("pa_copy_blocks", [f, f, f, 3, 10, 2, 128, 12, 1, None], -2),
+    ("pa_copy_blocks", [f, f, None, 3, 10, 2, 128, 16, 1, None], -1),
+    ("pa_copy_blocks", [f, f, f, 0, 10, 2, 128, 16, 1, None], 0),
+]
+del f
+
+
+@pytest.fixture(scope="module")
+def refusals(L):
+    calls = ([("pa_decode", _decode_args(**o)) for o, _ in DECODE_CASES] +
+             [("pa_prefill", _prefill_args(**o)) for o, _ in PREFILL_CASES] +
+             [(fn, a) for fn, a, _ in OTHER_CASES])
+    res = run_without_gpu(calls)
+    nd, npf = len(DECODE_CASES), len(PREFILL_CASES)
+    return res[:nd], res[nd:nd + npf], res[nd + npf:]
+
+
+@pytest.mark.parametrize("i", range(len(DECODE_CASES)))
+def test_decode_rejects_bad_arguments_without_a_launch(refusals, i):
+    rc, msg = refusals[0][i]
+    assert rc == DECODE_CASES[i][1], msg
+    assert msg
+
+
+@pytest.mark.parametrize("i", range(len(PREFILL_CASES)))
+def test_prefill_rejects_bad_arguments_without_a_launch(refusals, i):
+    rc, msg = refusals[1][i]
+    assert rc == PREFILL_CASES[i][1], msg
+    assert msg
+
+
+def test_append_and_copy_reject_bad_arguments(refusals):
+    for (fn, args, code), (rc, msg) in zip(OTHER_CASES, refusals[2]):
+        assert rc == code, (fn, args, msg)
 
 
 def test_partition_and_workspace_sizing(L):

@@ -159,12 +159,11 @@ struct PrefillArgs {
   int num_blocks, max_blocks_per_seq, max_ctx, max_query_len;
   float scale_log2;
 };
-// Prefill on tcgen05, head_dim 64 or 128; kmap/vmap: the bf16 cache maps with boxes of
-// [B rows x 64 dims] (not the interleaved form); qmap: q as (dims, head,
-// token) with boxes of [64 dims x g heads x 128 / g tokens]; omap: out with
-// the same geometry.
+// Prefill on tcgen05, head_dim 64 or 128: persistent CTAs, one per SM; kmap/vmap: the bf16 cache maps
+// with boxes of [B rows x 64 dims] (not the interleaved form); qmap: q as (dims, head, token) with
+// boxes of [64 dims x g heads x 128 / g tokens].
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, const CUtensorMap& omap, cudaStream_t stream);
+                              const CUtensorMap& qmap, cudaStream_t stream);
 
 cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
                                 void* v_cache, int num_blocks, int Hkv, int D, int B, int elem_bytes,

@@ -7,42 +7,58 @@
 // blocks first, "Day 6/90 of Inference Engineering", PagedAttention notes,
 // paragraph 2).
 //
-// One CTA per (sequence, KV head, pair of adjacent tiles of 128 query rows),
-// the rows being (new token, query head) pairs, token-major; pairs with the
-// most keys first.  Both tiles read every stage of keys and values, so each
-// TMA box feeds 256 rows.  Roles (352 threads, one CTA per SM):
+// Work items are (sequence, KV head, pair of adjacent tiles of 128 query
+// rows), the rows being (new token, query head) pairs, token-major; the
+// pairs with the most keys come first.  Both tiles of an item read every
+// stage of keys and values, so each TMA box feeds 256 rows.  The kernel is
+// persistent: one CTA per SM (384 threads) walks a fixed list of items --
+// rounds of one item per CTA, alternately in and against CTA order -- so the
+// set-up (barriers, tensor memory) is paid once per SM, there is no tail of
+// whole waves, and the next item's loads overlap the current item's last
+// products and epilogue.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
-//    the pair attends, 128 tokens per stage, into rings of their own (3
-//    stages of keys, 2 of values), as 2D TMA boxes of [B tokens x 64 dims]
-//    with 128-byte swizzle (the K-major UMMA layout), after
-//    griddepcontrol.wait; lane b issues block b of a chunk from block-table
-//    entries fetched 32 at a time.  Warp 8 first loads both query tiles,
-//    one 3D box per 64-dim half, so they land with the first keys;
-//  * warp 10 (MMA): one thread issues, per tile, S = Q Kᵀ (M 128, N 128,
-//    K = head_dim: head_dim / 16 tcgen05.mma kind::f16 from shared-memory
-//    descriptors) into the tile's S and O += P V (M 128, N = head_dim,
-//    K 128: eight MMAs, P read from tensor memory, V an MN-major operand in
-//    shared memory), in a fixed order -- per chunk c and tile, P·V(c) and
-//    then S(c + 1) -- spinning on one barrier at a time, so the tensor cores
-//    work for one tile while the other tile's softmax runs (ping-pong);
-//    tcgen05.commit signals the mbarriers and releases each stage after the
-//    last MMA that reads it;
+//    of each item, 128 tokens per stage, into rings of their own (2 stages
+//    of keys, 3 of values: values are needed a softmax later than keys)
+//    that run on across items, with an L2 policy that keeps them for the
+//    other pairs of the same sequence and head, as 2D TMA boxes of
+//    [B tokens x 64 dims] with 128-byte swizzle (the K-major UMMA layout),
+//    after griddepcontrol.wait; lane b issues block b of a chunk from
+//    block-table entries fetched 32 at a time.  Warp 8 first loads the
+//    item's query tiles, one 3D box per 64-dim half, once the previous
+//    item's last S has completed, and prefetches the next item's into L2;
+//  * warps 10 and 11 (MMA, one per tile): one thread issues the tile's
+//    S = Q Kᵀ (M 128, N 128, K = head_dim: head_dim / 16 tcgen05.mma
+//    kind::f16 from shared-memory descriptors) and O += P V (M 128,
+//    N = head_dim, K 128: eight MMAs, P read from tensor memory, V an
+//    MN-major operand in shared memory), per chunk c P·V(c) then S(c + 1),
+//    spinning on one barrier at a time.  A thread issues about one MMA per
+//    64 cycles, about what one takes, so one thread for both tiles would
+//    leave the tensor cores idle half the time; with one each, one tile's
+//    products run while the other tile's softmax does (ping-pong).
+//    tcgen05.commit signals the mbarriers and releases each stage right
+//    after the tile's last MMA that reads it (a stage is free once both
+//    tiles have released it), and the query tiles after the item's last S;
 //  * warps 0-3 and 4-7 (softmax, one warpgroup per tile): thread t of a
 //    warpgroup owns query row t of its tile (tensor-memory lane t): it
 //    reads its 128 scores (tcgen05.ld), masks keys past its position, keeps
 //    the running max and sum, writes P as bf16 back to tensor memory
 //    (tcgen05.st) and rescales its row of O only when its max grows by more
 //    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
-//    exact enough and O and the sum use the same max); at the end it reads
-//    its row of O, divides by the sum and stores it (a full tile through
-//    its query buffer and one TMA box per 64-dim half, the sequence's last
-//    tile row by row).
-// Tensor memory (512 columns allocated): O of tile t at columns DH·t ..
-// DH·t + DH - 1 and its S at 2·DH + 128t (DH = head_dim); P is written over
-// the first half of its S.  Value rows past the pair's keys are zeroed in
-// shared memory before the first P·V of that stage so stale cache rows
-// cannot turn 0 x NaN into NaN.  Every wait is bounded; on a time-out the
-// kernel raises PA_STATUS_TIMEOUT and stops issuing work.
+//    exact enough and O and the sum use the same max); at the end of the
+//    item it reads its row of O, divides by the sum and stores it.  The
+//    exponentials are one packed FMA per two scores (scale and max) and one
+//    ex2 each; the max is taken three operands at a time.  The two
+//    warpgroups take strict turns, chunk by chunk, so that one tile's
+//    softmax runs while the other tile's products do;
+// Both tiles attend all of the item's chunks (the earlier tile's keys past
+// its rows' positions are masked), which keeps the two MMA warps' releases
+// symmetric.  Tensor memory (512 columns allocated once per CTA): O of tile
+// t at columns DH·t .. DH·t + DH - 1 and its S at 2·DH + 128t (DH =
+// head_dim); P is written over the first half of its S.  Value rows past the
+// pair's keys are zeroed in shared memory before the first P·V of that stage
+// so stale cache rows cannot turn 0 x NaN into NaN.  Every wait is bounded;
+// on a time-out the kernel raises PA_STATUS_TIMEOUT, stops issuing work,
+// lets its copies and products in flight finish, and exits.
 
 #include <cuda_bf16.h>
 
@@ -59,12 +75,12 @@ namespace {
 constexpr int kM = 128;                 // query rows per tile (one tensor-memory lane each)
 constexpr int kTiles = 2;               // query tiles per CTA, sharing every stage
 constexpr int kN = 128;                 // keys per stage (the N of S = Q Kᵀ)
-constexpr int kStagesK = 3;             // stages in the key ring
-constexpr int kStagesV = 2;             // stages in the value ring
+constexpr int kStagesK = 2;             // stages in the key ring
+constexpr int kStagesV = 3;             // stages in the value ring (values are needed later than keys)
 constexpr int kSoftWarps = 4;           // per tile
 constexpr int kProducerWarp = kTiles * kSoftWarps;  // keys; the next warp streams values
-constexpr int kMmaWarp = kProducerWarp + 2;
-constexpr int kThreadsT = (kTiles * kSoftWarps + 3) * 32;
+constexpr int kMmaWarp = kProducerWarp + 2;         // tile 0's MMAs; the next warp issues tile 1's
+constexpr int kThreadsT = (kTiles * kSoftWarps + 2 + kTiles) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of a query tile
 constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage of K (or V)
@@ -83,7 +99,8 @@ struct PfCfg {
   static constexpr int kOffK = kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars) * 8;  // tensor-memory address, abort flag
+  // barriers: the rings, kTileBars per tile, q_empty, drained per MMA warp, softmax turn per tile
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 1 + 2 * kTiles) * 8;  // tensor-memory address, abort flag
   static constexpr size_t kBytes = 1024 + kOffMisc + 16;
   static constexpr uint32_t kColO = 0, kColS = 2 * DH;
   static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
@@ -91,6 +108,21 @@ struct PfCfg {
   static_assert(kColS + kTiles * 128 <= kTmemCols, "tensor-memory columns");
 };
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x on the special-function unit (subnormal results flushed to zero,
+// which a softmax weight below 2^-126 does not notice).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -187,71 +219,102 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const 
   return false;
 }
 
+// Work item j of S * Hkv * pairs: pair of query tiles pairs - 1 - j / (S * Hkv)
+// (the pairs with the most keys first), sequence (j / Hkv) % S, KV head
+// j % Hkv.  Every role of a CTA walks the same items in the same order and
+// derives the same chunk counts from them, so they need no messages beyond
+// the pipeline's barriers.
+struct PfItem {
+  int s, kvh, pair, q0, rows, first_pos, row00;
+  int nch, t_end;              // chunks of keys the pair attends, and its keys
+  int state;                   // 0: work; 1: no rows of the sequence in this pair; 2: inconsistent lengths
+};
+
+__device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs) {
+  PfItem it{};
+  const int per = p.S * p.Hkv;
+  it.pair = pairs - 1 - j / per;
+  it.s = (j % per) / p.Hkv;
+  it.kvh = j % p.Hkv;
+  const int q0 = __ldg(p.query_start + it.s), q1 = __ldg(p.query_start + it.s + 1);
+  const int ctx = __ldg(p.context_lens + it.s);
+  const int n_new = q1 - q0;
+  if (q0 < 0 || n_new < 0 || n_new > p.max_query_len || ctx < n_new || ctx > p.max_ctx || q1 > p.T) {
+    it.state = 2;
+    return it;
+  }
+  it.q0 = q0;
+  it.rows = n_new * p.g;
+  it.first_pos = ctx - n_new;
+  it.row00 = it.pair * kTiles * kM;
+  if (it.row00 >= it.rows) {
+    it.state = 1;
+    return it;
+  }
+  // Keys the pair attends: up to the position of its last row (tile 1 is
+  // the later one).  Both tiles run over all of them; a tile's rows mask
+  // the keys past their positions.
+  it.t_end = it.first_pos + (min(it.rows, it.row00 + kTiles * kM) - 1) / p.g + 1;
+  it.nch = (it.t_end + kN - 1) / kN;
+  return it;
+}
+
+// The r-th item of CTA b of G: rounds of G items, alternately in and against
+// CTA order, so that a CTA given one of the costliest items of a round gets
+// one of the cheapest of the next.
+__device__ __forceinline__ int pf_item_index(int r, int b, int G) { return r * G + ((r & 1) ? G - 1 - b : b); }
+
 template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                      const PrefillArgs p) {
+                      const __grid_constant__ CUtensorMap qmap, const PrefillArgs p, int pairs, int num_items) {
   using C = PfCfg<DH>;
   constexpr int kQTile = C::kQTile, kKVStage = C::kKVStage, kOffK = C::kOffK, kOffV = C::kOffV;
   constexpr uint32_t kColO = C::kColO, kColS = C::kColS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // The pair index is the slowest grid dimension and runs backwards, so the
-  // pairs with the most keys start first across all sequences and heads.
-  const int kvh = blockIdx.x, s = blockIdx.y;
-  const int pair = (int)gridDim.z - 1 - (int)blockIdx.z;
-
-  const int q0 = __ldg(p.query_start + s), q1 = __ldg(p.query_start + s + 1);
-  const int ctx = __ldg(p.context_lens + s);
-  const int n_new = q1 - q0;
-  const int rows = n_new * p.g;
-  if (q0 < 0 || n_new < 0 || n_new > p.max_query_len || ctx < n_new || ctx > p.max_ctx || q1 > p.T) {
-    if (pair == 0 && kvh == 0 && tid == 0) raise_status(p.status, PA_STATUS_BAD_CONTEXT);
-    return;
-  }
-  const int first_pos = ctx - n_new;
-  // Keys each tile attends (0 for a tile past the sequence's rows) and the
-  // 64-key chunks that hold them; tile 1 is the later one, so it attends
-  // at least as many keys as tile 0.
-  const int row00 = pair * kTiles * kM, row01 = row00 + kM;
-  if (row00 >= rows) return;
-  const int t_end0 = first_pos + (min(rows, row00 + kM) - 1) / p.g + 1;
-  const int t_end1 = row01 < rows ? first_pos + (min(rows, row01 + kM) - 1) / p.g + 1 : 0;
-  const int nch0 = (t_end0 + kN - 1) / kN, nch1 = (t_end1 + kN - 1) / kN;
-  const int t_end = max(t_end0, t_end1);
-  const int nch = max(nch0, nch1);
+  const int G = (int)gridDim.x, b = (int)blockIdx.x;
 
   uint64_t* full_k = reinterpret_cast<uint64_t*>(base + C::kOffBars);
   uint64_t* empty_k = full_k + kStagesK;
   uint64_t* full_v = empty_k + kStagesK;
   uint64_t* empty_v = full_v + kStagesV;
   uint64_t* tile_bars = empty_v + kStagesV;  // kTileBars per tile
-  // per tile: [0] S of a chunk is in, [1] P of a chunk is in, [2] the last
-  // P·V is done, [3] the query tile is in
+  // per tile: [0] S of a chunk is in, [1] P of a chunk is in, [2] the item's
+  // last P·V is done, [3] the item's query tile is in
   auto s_full = [&](int t) { return tile_bars + t * kTileBars; };
   auto p_full = [&](int t) { return tile_bars + t * kTileBars + 1; };
   auto o_final = [&](int t) { return tile_bars + t * kTileBars + 2; };
   auto q_full = [&](int t) { return tile_bars + t * kTileBars + 3; };
+  uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // the item's last S of both tiles is done: the query tiles are free
+  uint64_t* drained = q_empty + 1;                     // per MMA warp: every MMA it issued is done
+  uint64_t* turn = drained + kTiles;                   // per tile: the other warpgroup has passed it the turn
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
 
   if (tid == 0) {
+    // a stage (and the query tiles) is free once both tiles' MMA warps
+    // have released it
     for (int k = 0; k < kStagesK; ++k) {
       mbar_init(&full_k[k], 1);
-      mbar_init(&empty_k[k], 1);
+      mbar_init(&empty_k[k], kTiles);
     }
     for (int k = 0; k < kStagesV; ++k) {
       mbar_init(&full_v[k], 1);
-      mbar_init(&empty_v[k], 1);
+      mbar_init(&empty_v[k], kTiles);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), kSoftWarps * 32);
       mbar_init(o_final(t), 1);
       mbar_init(q_full(t), 1);
+    }
+    mbar_init(q_empty, kTiles);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(drained + t, 1);
+      mbar_init(turn + t, kSoftWarps);
     }
     *abort = 0;
     fence_barrier_init();
@@ -271,80 +334,136 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     // ring, so neither waits behind the other's release.  Lane b loads
     // block b of a chunk; block-table entries are fetched 32 at a time, one
     // per lane, a window ahead, so no TMA issue waits on a dependent load.
+    // The key warp also loads each item's query tiles, once the previous
+    // item's last S has completed.
     const int kv = warp - kProducerWarp;  // 0 keys, 1 values
-    if (kv == 0 && lane == 0) {
-      // The query tiles (an input the append does not write), one box per
-      // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past the
-      // sequence read the next sequence's queries (or zeros past the last
-      // token); their scores are all masked and their rows never stored.
-      const uint64_t qpol = policy_evict_first();
-#pragma unroll 1
-      for (int t = 0; t < kTiles; ++t) {
-        if ((t == 0 ? nch0 : nch1) == 0) continue;
-        const int z = q0 + (row00 + t * kM) / p.g;
-        mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
-#pragma unroll
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, kvh * p.g, z, qpol);
-      }
-    }
-    pdl_wait_primary();  // the prompt's keys and values are in the cache from here on
-    const int32_t* row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-    const int nblk = (t_end + p.B - 1) / p.B;
-    const int bpc = kN / p.B;  // blocks per chunk (block sizes 8, 16, 32: 16, 8 or 4, dividing 32)
-    const uint64_t policy = policy_evict_first();
+    const int bpc = kN / p.B;             // blocks per chunk (block sizes 8, 16, 32: 16, 8 or 4, dividing 32)
+    // The other pairs of the same sequence and KV head read the same keys
+    // and values: keep them in L2.
+    const uint64_t policy = policy_evict_last();
     const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
     uint64_t* fulls = kv == 0 ? full_k : full_v;
     uint64_t* empties = kv == 0 ? empty_k : empty_v;
     const int stages = kv == 0 ? kStagesK : kStagesV;
-    int cur = load_block_id(row, lane, nblk);
-    int nxt = load_block_id(row, 32 + lane, nblk);
-    int wbase = 0;
-    for (int c = 0; c < nch; ++c) {
-      const int jb = c * bpc;
-      if (jb >= wbase + 32) {
-        cur = nxt;
-        wbase += 32;
-        nxt = load_block_id(row, wbase + 32 + lane, nblk);
+    uint32_t k = 0;                // chunks issued into this ring over the CTA's items
+    uint32_t qi = 0, qn[kTiles] = {0, 0};  // items whose query tiles were issued; loads per tile
+    bool waited = false, ok = true;
+    for (int r = 0; ok; ++r) {
+      const int j = pf_item_index(r, b, G);
+      if (j >= num_items) break;
+      const PfItem it = pf_item(p, j, pairs);
+      if (it.state) continue;
+      if (kv == 0) {
+        // The query tiles (an input the append does not write), one box per
+        // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past
+        // the sequence read the next sequence's queries (or zeros past the
+        // last token); their scores are all masked and their rows never stored.
+        int okq = 1;
+        if (lane == 0) {
+          if (qi > 0) okq = mbar_wait(q_empty, (qi - 1) & 1, abort);
+          if (okq) {
+            const uint64_t qpol = policy_evict_first();
+#pragma unroll 1
+            for (int t = 0; t < kTiles; ++t) {
+              const int z = it.q0 + (it.row00 + t * kM) / p.g;
+              mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
+#pragma unroll
+              for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, it.kvh * p.g, z, qpol);
+              ++qn[t];
+            }
+            // The next item's query tiles into L2, so that their load at the
+            // item boundary does not wait on HBM.
+            const int jn = pf_item_index(r + 1, b, G);
+            if (jn < num_items) {
+              const PfItem nx = pf_item(p, jn, pairs);
+              if (!nx.state)
+                for (int t = 0; t < kTiles; ++t) {
+                  const int z = nx.q0 + (nx.row00 + t * kM) / p.g;
+                  for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(&qmap, 64 * h, nx.kvh * p.g, z);
+                }
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, okq, 0)) {
+          ok = false;
+          break;
+        }
+        ++qi;
       }
-      int id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
-      const int nb = (min(kN, t_end - c * kN) + p.B - 1) / p.B;
-      if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
-        raise_status(p.status, PA_STATUS_BAD_BLOCK);
-        id = 0;
+      if (!waited) {
+        pdl_wait_primary();  // the prompts' keys and values are in the cache from here on
+        waited = true;
       }
-      const int st = c % stages;
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait(&empties[st], ((c / stages) & 1) ^ 1, abort);
-        if (ok) {
-          mbar_arrive_expect_tx(&fulls[st], (uint32_t)(nb * p.B * 128 * C::kHalves));
-        } else {
-          *abort = 1;
-          raise_status(p.status, PA_STATUS_TIMEOUT);
+      const int32_t* row = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+      const int nblk = (it.t_end + p.B - 1) / p.B;
+      int cur = load_block_id(row, lane, nblk);
+      int nxt = load_block_id(row, 32 + lane, nblk);
+      int wbase = 0;
+      for (int c = 0; c < it.nch; ++c, ++k) {
+        const int jb = c * bpc;
+        if (jb >= wbase + 32) {
+          cur = nxt;
+          wbase += 32;
+          nxt = load_block_id(row, wbase + 32 + lane, nblk);
+        }
+        int id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
+        const int nb = (min(kN, it.t_end - c * kN) + p.B - 1) / p.B;
+        if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
+          raise_status(p.status, PA_STATUS_BAD_BLOCK);
+          id = 0;
+        }
+        const int st = (int)(k % (uint32_t)stages);
+        int okc = 1;
+        if (lane == 0) {
+          okc = mbar_wait(&empties[st], ((k / stages) & 1) ^ 1, abort);
+          if (okc) mbar_arrive_expect_tx(&fulls[st], (uint32_t)(nb * p.B * 128 * C::kHalves));
+        }
+        if (!__shfl_sync(0xffffffffu, okc, 0)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();  // the expected byte count is set before any copy can land
+        if (lane < nb) {
+          const int y = (id * p.Hkv + it.kvh) * p.B;
+          uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) tma_load_2d(d + h * kKVHalf, map, &fulls[st], 64 * h, y, policy);
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      __syncwarp();  // the expected byte count is set before any copy can land
-      if (lane < nb) {
-        const int y = (id * p.Hkv + kvh) * p.B;
-        uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
-#pragma unroll
-        for (int h = 0; h < C::kHalves; ++h) tma_load_2d(d + h * kKVHalf, map, &fulls[st], 64 * h, y, policy);
-      }
     }
-  } else if (warp == kMmaWarp) {
-    // One thread issues every MMA in a fixed order, waiting (bounded
-    // try_wait) for one barrier at a time: S of both tiles for chunk 0,
-    // then per chunk c and tile t: P·V(c) as soon as the tile's P(c) is in,
-    // and right behind it S(c + 1) of that tile.  Each tile has one S
-    // buffer, so its softmax and its products alternate, and the tensor
-    // cores work for one tile while the other tile's softmax runs.  The
-    // tensor cores run one thread's MMAs in order: S(c + 1) overwrites P(c)
-    // only after P·V(c) has read it, and the commit that releases S(c + 1)
-    // to the softmax also covers P·V(c), so the softmax may rescale O at
-    // once.  A stage is released by a commit after the last MMA that reads
-    // it.
+    if (!ok) {
+      if (lane == 0) {
+        *abort = 1;
+        raise_status(p.status, PA_STATUS_TIMEOUT);
+        // Let copies already issued land before the CTA's shared memory goes away.
+        const volatile int never = 0;
+        for (uint32_t c = (k > (uint32_t)stages ? k - stages : 0); c < k; ++c)
+          mbar_wait(&fulls[c % stages], (c / stages) & 1, &never);
+        for (int t = 0; t < kTiles; ++t)
+          if (qn[t] > 0) mbar_wait(q_full(t), (qn[t] - 1) & 1, &never);
+      }
+      __syncwarp();
+    }
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // MMA warp of tile t: one thread issues the tile's MMAs in a fixed
+    // order, waiting for one barrier at a time: per item S(0), then per
+    // chunk c P·V(c) as soon as P(c) is in and right behind it S(c + 1).
+    // One thread issues at most about one tcgen05.mma every 64 cycles, about
+    // the time an M 128 N 128 K 16 MMA takes, so each tile has its own
+    // issuing warp and the tensor cores interleave the two tiles' work: one
+    // tile's products run while the other tile's softmax does.  The tile's
+    // MMAs run in issue order: S(c + 1) overwrites P(c) only after P·V(c)
+    // has read it, and the commit that releases S(c + 1) to the softmax also
+    // covers P·V(c), so the softmax may rescale O at once.  The first P·V of
+    // an item overwrites O without a barrier of its own: it waits for P(0),
+    // which the warpgroup writes only after it has read the previous item's
+    // O.  Both tiles attend every chunk of the item (keys past a row's
+    // position are masked), so the stage releases are symmetric: a commit
+    // from each tile's warp after its last MMA that reads the stage (values
+    // right after P·V, keys after S), and one after its item's last S for
+    // the query tiles.
+    const int t = warp - kMmaWarp;
     const uint32_t id_s = instr_desc(kM, kN, false);
     const uint32_t id_o = instr_desc(kM, DH, true);
     bool ok = true;
@@ -356,95 +475,134 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     };
     // Descriptors are built once per group; a k-step adds its byte offset
     // / 16 to the address field (every shared address is below 256 KB, so
-    // the 14-bit field never carries).  This thread shares its scheduler
-    // with two softmax warps, so fewer instructions per MMA matter.
-    auto issue_s = [&](int t, int c) {  // lane 0; the keys of chunk c have landed
+    // the 14-bit field never carries).
+    const uint64_t a_q = smem_desc(sbase + t * kQTile, 16, 1024);
+    const uint32_t s_cols = tmem + kColS + (uint32_t)t * 128;
+    const uint32_t o_cols = tmem + kColO + (uint32_t)t * DH;
+    auto issue_s = [&](int kst) {  // lane 0; the keys in stage kst have landed
       tc_fence_after();
-      const uint64_t a0 = smem_desc(sbase + t * kQTile, 16, 1024);
-      const uint64_t b0 = smem_desc(sbase + kOffK + (c % kStagesK) * kKVStage, 16, 1024);
-      const uint32_t d = tmem + kColS + (uint32_t)t * 128;
+      const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk) {
         const int hlf = kk >> 2, w = kk & 3;
-        mma_ss(d, a0 + (uint64_t)((hlf * kQHalf + w * 32) >> 4), b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4), id_s,
-               kk > 0);
+        mma_ss(s_cols, a_q + (uint64_t)((hlf * kQHalf + w * 32) >> 4), b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4),
+               id_s, kk > 0);
       }
       mma_commit(s_full(t));
     };
-    auto issue_pv = [&](int t, int c) {  // lane 0; P(c) and the values of chunk c are in
+    auto issue_pv = [&](int vst, bool acc) {  // lane 0; P and the values in stage vst are in
       tc_fence_after();
-      const uint64_t b0 = smem_desc(sbase + kOffV + (c % kStagesV) * kKVStage, kKVHalf, 1024);
-      const uint32_t p_cols = tmem + kColS + (uint32_t)t * 128;
-      const uint32_t d = tmem + kColO + (uint32_t)t * DH;
+      const uint64_t b0 = smem_desc(sbase + kOffV + vst * kKVStage, kKVHalf, 1024);
 #pragma unroll
-      for (int kk = 0; kk < kN / 16; ++kk) mma_ts(d, p_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, c > 0 || kk > 0);
-      if (c + 1 == (t == 0 ? nch0 : nch1)) mma_commit(o_final(t));
+      for (int kk = 0; kk < kN / 16; ++kk)
+        mma_ts(o_cols, s_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, acc || kk > 0);
     };
-    if (wait_bar(q_full(0), 0) && (nch1 == 0 || wait_bar(q_full(1), 0)) && wait_bar(&full_k[0], 0)) {
+    uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
+    for (int r = 0; ok; ++r) {
+      const int j = pf_item_index(r, b, G);
+      if (j >= num_items) break;
+      const PfItem it = pf_item(p, j, pairs);
+      if (it.state) continue;
+      if (!wait_bar(q_full(t), nit & 1)) break;
+      if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
       if (lane == 0) {
-        issue_s(0, 0);
-        if (nch1 > 0) issue_s(1, 0);
-        mma_commit(&empty_k[0]);
+        issue_s((int)(kq % kStagesK));
+        mma_commit(&empty_k[kq % kStagesK]);
+        if (it.nch == 1) mma_commit(q_empty);
       }
       __syncwarp();
-    }
-    for (int c = 0; c < nch && ok; ++c) {
-      if (!wait_bar(&full_v[c % kStagesV], (c / kStagesV) & 1)) break;
-      const int nv = min(kN, t_end - c * kN);
-      if (nv < kN) {  // value rows past the pair's keys: zeros (their keys are masked)
-        uint8_t* vs = base + kOffV + (c % kStagesV) * kKVStage;
-        for (int u = lane; u < (kN - nv) * 8 * C::kHalves; u += 32) {
-          const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
-          *reinterpret_cast<uint4*>(vs + hlf * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
+      ++kq;
+      for (int c = 0; c < it.nch; ++c) {
+        const int vst = (int)(vq % kStagesV);
+        if (!wait_bar(&full_v[vst], (vq / kStagesV) & 1)) break;
+        const int nv = min(kN, it.t_end - c * kN);
+        if (nv < kN) {
+          // Value rows past the pair's keys: zeros (their keys are masked).
+          // Both tiles' warps write the same zeros; each orders its own
+          // writes before its own P·V.
+          uint8_t* vs = base + kOffV + vst * kKVStage;
+          for (int u = lane; u < (kN - nv) * 8 * C::kHalves; u += 32) {
+            const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
+            *reinterpret_cast<uint4*>(vs + hlf * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      bool k_next = false;  // the keys of chunk c + 1 have landed
-#pragma unroll 1
-      for (int t = 0; t < kTiles; ++t) {
-        const int nch_t = t == 0 ? nch0 : nch1;
-        if (c >= nch_t) continue;
-        if (!wait_bar(p_full(t), c & 1)) break;
-        if (lane == 0) issue_pv(t, c);
         __syncwarp();
-        if (c + 1 < nch_t) {
-          if (!k_next && !(k_next = wait_bar(&full_k[(c + 1) % kStagesK], ((c + 1) / kStagesK) & 1))) break;
+        if (!wait_bar(p_full(t), sp & 1)) break;
+        ++sp;
+        if (lane == 0) {
+          issue_pv(vst, c > 0);
+          if (c + 1 == it.nch) mma_commit(o_final(t));
+          mma_commit(&empty_v[vst]);
+        }
+        __syncwarp();
+        ++vq;
+        if (c + 1 < it.nch) {
+          if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
           if (lane == 0) {
-            issue_s(t, c + 1);
-            // the last tile that reads the keys of chunk c + 1
-            if (t == kTiles - 1 || c + 1 >= nch1) mma_commit(&empty_k[(c + 1) % kStagesK]);
+            issue_s((int)(kq % kStagesK));
+            mma_commit(&empty_k[kq % kStagesK]);
+            if (c + 2 == it.nch) mma_commit(q_empty);
           }
           __syncwarp();
+          ++kq;
         }
       }
-      if (ok && lane == 0) mma_commit(&empty_v[c % kStagesV]);
-      __syncwarp();
+      ++nit;
     }
     if (!ok) {
       *abort = 1;
       raise_status(p.status, PA_STATUS_TIMEOUT);
     }
+    // Every MMA this warp issued has completed before tensor memory is released.
+    if (lane == 0) {
+      mma_commit(drained + t);
+      const volatile int never = 0;
+      mbar_wait(drained + t, 0, &never);
+    }
+    __syncwarp();
   } else if (warp < kProducerWarp) {
-    // softmax warpgroup t: thread lt owns row lt of tile t (tensor-memory lane lt)
+    // softmax warpgroup t: thread lt owns row lt of its tile (tensor-memory lane lt)
     const int t = warp / kSoftWarps, lt = tid - t * kM;
-    const int row0 = row00 + t * kM;
-    const int nch_t = t == 0 ? nch0 : nch1;
-    if (nch_t > 0) {
-      const int r = row0 + lt;
-      const int pos = r < rows ? first_pos + r / p.g : -1;  // keys 0 .. pos
-      const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
-      const uint32_t o_cols = lane_base + kColO + (uint32_t)t * DH;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
+    const uint32_t o_cols = lane_base + kColO + (uint32_t)t * DH;
+    const uint32_t s_cols = lane_base + kColS + (uint32_t)t * 128;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    uint32_t sc_n = 0, ot = 0;  // S phases consumed, items finished by this tile
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int j = pf_item_index(r, b, G);
+      if (j >= num_items) break;
+      const PfItem it = pf_item(p, j, pairs);
+      if (it.state == 2) {
+        if (t == 0 && lt == 0 && it.pair == 0 && it.kvh == 0) raise_status(p.status, PA_STATUS_BAD_CONTEXT);
+        continue;
+      }
+      if (it.state) continue;
+      const int nch_t = it.nch;  // both tiles attend every chunk of the item
+      const int row0 = it.row00 + t * kM;
+      const int rr = row0 + lt;
+      const int pos = rr < it.rows ? it.first_pos + rr / p.g : -1;  // keys 0 .. pos
       float m_run = -INFINITY, l_run = 0.f;
-      bool ok = true;
       for (int c = 0; c < nch_t; ++c) {
-        // the warp leaves together (warp-wide votes follow)
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full(t), c & 1, abort))) {
+        // the warp leaves together (warp-wide tensor-memory accesses follow)
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full(t), sc_n & 1, abort))) {
           ok = false;
           break;
         }
-        const uint32_t s_cols = lane_base + kColS + (uint32_t)t * 128;
+        // Strict turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk
+        // k + 1, ...: one warpgroup's softmax runs while the other tile's
+        // products do, and the two never contend for the exp2 unit.  Each
+        // warpgroup is one turn behind the other at most, so a barrier is
+        // never two phases ahead of its waiter.
+        const bool my_turn = t == 0 ? (sc_n == 0 || mbar_wait(turn, (sc_n - 1) & 1, abort))
+                                    : mbar_wait(turn + 1, sc_n & 1, abort);
+        if (!__all_sync(0xffffffffu, my_turn)) {
+          ok = false;
+          break;
+        }
+        ++sc_n;
         tc_fence_after();
         uint32_t raw[kN];
 #pragma unroll
@@ -452,23 +610,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         float sc[kN];
 #pragma unroll
-        for (int j = 0; j < kN; ++j) sc[j] = __uint_as_float(raw[j]);
+        for (int q = 0; q < kN; ++q) sc[q] = __uint_as_float(raw[q]);
         // Keys t0 .. t0 + nvalid - 1 of this chunk are at or before the row's
         // position; masking is needed only in chunks that cross it.
         const int t0 = c * kN;
         const int nvalid = min(kN, pos - t0 + 1);
-        // max of the raw (unscaled) valid scores, four chains at a time
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (nvalid >= kN) {
+        if (nvalid < kN) {
 #pragma unroll
-          for (int j = 0; j < kN; ++j) m4[j & 3] = fmaxf(m4[j & 3], sc[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kN; ++j) {
-            sc[j] = j < nvalid ? sc[j] : -INFINITY;
-            m4[j & 3] = fmaxf(m4[j & 3], sc[j]);
-          }
+          for (int q = 0; q < kN; ++q) sc[q] = q < nvalid ? sc[q] : -INFINITY;
         }
+        // max of the raw (unscaled) scores: three-input max, four chains
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int q = 0; q < kN / 2; ++q) m4[q & 3] = fmax3(m4[q & 3], sc[2 * q], sc[2 * q + 1]);
         const float mxr = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         const float mx = mxr * p.scale_log2;  // scale > 0: the max of the scaled scores
         // Raise the running max (and rescale O) only when it grows past the
@@ -485,73 +639,67 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             tmem_ld16(o_cols + 16 * i, v);
             uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(v[j] * alpha);
+            for (int q = 0; q < 16; ++q) w[q] = __float_as_uint(v[q] * alpha);
             tmem_st16(o_cols + 16 * i, w);
           }
         }
         l_run *= alpha;
         m_run = m_new;
         const float base_m = m_run == -INFINITY ? 0.f : m_run;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        const float2 nb2 = make_float2(-base_m, -base_m);
+        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int i = 0; i < kN / 32; ++i) {  // exp2(s * scale - max): one FMA per score
+        for (int i = 0; i < kN / 32; ++i) {  // exp2(s * scale - max): one packed FMA per two scores
           uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float e0 = exp2f(fmaf(sc[32 * i + 2 * j], p.scale_log2, -base_m));
-            const float e1 = exp2f(fmaf(sc[32 * i + 2 * j + 1], p.scale_log2, -base_m));
-            l4[j & 3] += e0 + e1;
-            w[j] = pack_bf16x2(e0, e1);
+          for (int q = 0; q < 16; ++q) {
+            const float2 x = __ffma2_rn(make_float2(sc[32 * i + 2 * q], sc[32 * i + 2 * q + 1]), sl2, nb2);
+            const float2 e = make_float2(ex2_ftz(x.x), ex2_ftz(x.y));
+            l2[q & 1] = __fadd2_rn(l2[q & 1], e);
+            w[q] = pack_bf16x2(e.x, e.y);
           }
           tmem_st16(s_cols + 16 * i, w);  // P over the first 64 columns of its S
         }
-        l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         mbar_arrive(p_full(t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(turn + (1 - t));  // the other tile's turn
       }
-      // One outcome for the whole warpgroup: the full-tile store below syncs it.
-      if (named_barrier_and(1 + t, kSoftWarps * 32, ok && mbar_wait(o_final(t), 0, abort))) {
-        tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint32_t o[DH];  // the row of O, all loads in flight at once
+      if (!ok) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(o_final(t), ot & 1, abort))) {
+        ok = false;
+        break;
+      }
+      ++ot;
+      // Read the row of O (all loads in flight at once).  The next item's
+      // first P·V overwrites it only after this warpgroup's next P(0),
+      // which comes after these loads have completed.
+      tc_fence_after();
+      uint32_t o[DH];
 #pragma unroll
-        for (int i = 0; i < DH / 16; ++i) tmem_ld16_nowait(o_cols + 16 * i, o + 16 * i);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        auto piece = [&](int u) {  // dims 8u .. 8u + 7 of the row, normalized, as bf16
+      for (int i = 0; i < DH / 16; ++i) tmem_ld16_nowait(o_cols + 16 * i, o + 16 * i);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      if (rr < it.rows) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                              ((size_t)(it.q0 + rr / p.g) * p.H + it.kvh * p.g + rr % p.g) * DH);
+#pragma unroll
+        for (int u = 0; u < DH / 8; ++u) {  // dims 8u .. 8u + 7 of the row, normalized, as bf16
           uint4 w;
           w.x = pack_bf16x2(__uint_as_float(o[8 * u]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
           w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
           w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
           w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
-          return w;
-        };
-        if (row0 + kM <= rows) {
-          // A full tile: stage the rows in this tile's query buffer (its last
-          // S has completed) in the layout the query boxes arrived in, then
-          // store them with two TMA boxes through the same geometry.
-          uint8_t* qt = base + t * kQTile;
-#pragma unroll
-          for (int u = 0; u < DH / 8; ++u)
-            *reinterpret_cast<uint4*>(qt + (u >> 3) * kQHalf + lt * 128 + (((u & 7) ^ (lt & 7)) << 4)) = piece(u);
-          fence_proxy_async_smem();
-          named_barrier_sync(1 + t, kSoftWarps * 32);
-          if (lt == 0) {
-            const int z = q0 + row0 / p.g;
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h) tma_store_3d(&omap, qt + h * kQHalf, 64 * h, kvh * p.g, z);
-            bulk_store_drain();
-          }
-        } else if (r < rows) {  // the sequence's last tile: only its own rows
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                ((size_t)(q0 + r / p.g) * p.H + kvh * p.g + r % p.g) * DH);
-#pragma unroll
-          for (int u = 0; u < DH / 8; ++u) dst[u] = piece(u);
+          dst[u] = w;
         }
-      } else {
-        *abort = 1;
-        raise_status(p.status, PA_STATUS_TIMEOUT);
       }
+    }
+    if (!ok) {
+      *abort = 1;
+      raise_status(p.status, PA_STATUS_TIMEOUT);
     }
   }
 
@@ -565,20 +713,27 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 
 template <int DH>
 cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const CUtensorMap& qmap, const CUtensorMap& omap, int pairs, cudaStream_t stream) {
+                                 const CUtensorMap& qmap, int pairs, cudaStream_t stream) {
   constexpr size_t kBytes = PfCfg<DH>::kBytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  static int sms[64];
   static std::once_flag once[64];
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t init_err = cudaSuccess;
   std::call_once(once[dev], [&] {
     init_err = cudaFuncSetAttribute(prefill_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBytes);
+    if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
   });
   if (init_err != cudaSuccess) return init_err;
+  if (sms[dev] < 1) return cudaErrorInvalidConfiguration;
+  // Persistent CTAs, one per SM (the shared memory allows no more).
+  const long long items = (long long)a.S * a.Hkv * pairs;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int grid = (int)std::min<long long>(items, sms[dev]);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.Hkv, (unsigned)a.S, (unsigned)pairs);
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreadsT);
   cfg.dynamicSmemBytes = kBytes;
   cfg.stream = stream;
@@ -587,19 +742,18 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, omap, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, a, pairs, (int)items);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, const CUtensorMap& omap, cudaStream_t stream) {
+                              const CUtensorMap& qmap, cudaStream_t stream) {
   const int tiles = (a.max_query_len * a.g + kM - 1) / kM;
   const int pairs = (tiles + kTiles - 1) / kTiles;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
-  if (pairs > 65535 || a.S > 65535 || a.Hkv > 65535) return cudaErrorInvalidConfiguration;
-  if (a.D == 128) return launch_prefill_tc_dh<128>(a, kmap, vmap, qmap, omap, pairs, stream);
-  if (a.D == 64) return launch_prefill_tc_dh<64>(a, kmap, vmap, qmap, omap, pairs, stream);
+  if (a.D == 128) return launch_prefill_tc_dh<128>(a, kmap, vmap, qmap, pairs, stream);
+  if (a.D == 64) return launch_prefill_tc_dh<64>(a, kmap, vmap, qmap, pairs, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,64 +1,85 @@
-"""The synchronisation protocol of the tcgen05 prefill kernel
+"""The synchronisation protocol of the persistent tcgen05 prefill kernel
 (csrc/prefill_tc.cu), checked on the CPU by a randomised discrete-event
 model: no deadlock, every mbarrier wait sees exactly the phase it means
 (never one two phases later that passes the same parity test), and every
 buffer holds the right data whenever a copy, an MMA, the softmax or the
 epilogue touches it.
 
-The model follows the kernel's roles and its order of operations:
-  * a key producer: both query tiles, then the keys of chunk c into ring
-    stage c % 3 once the stage's previous chunk has been released;
-  * a value producer: the values of chunk c into stage c % 2 likewise;
-  * one MMA thread: S of both tiles for chunk 0, then per chunk c and tile t
-    (if the tile attends chunk c) P·V_t(c) once P_t(c) is in, then S_t(c+1);
-    a stage is released by a commit after the last MMA that reads it;
-  * per tile a softmax: wait for S_t(c), rescale O_t at once (the commit
-    that released S_t(c) covers P·V_t(c-1)), write P_t(c) over S_t, arrive;
-    after the last chunk wait for the tile's last P·V and read O_t;
-  * the tensor pipe runs the MMA thread's operations in issue order, a
-    commit arriving when everything issued before it has completed.
-TMA copies and MMAs take random times; planted mistakes (a stage of keys
-released after the first of its two readers, S issued before the P·V that
-reads the buffer it overwrites, an epilogue without its wait, a producer
-waiting on the wrong parity) show that the checks catch each kind of
-failure: stale data, a deadlock."""
+A CTA works through a list of items, each a pair of query tiles attending
+the same chunks of keys (nch = the longer tile's count; the shorter tile's
+extra keys are masked).  The model follows the kernel's roles and order:
+  * a key producer: per item, once the previous item's last S of both tiles
+    has completed (q_empty), both query tiles; then the keys of every chunk
+    into ring stage k % 2 (k counting chunks over the CTA's items) once both
+    tiles have released the stage's previous chunk;
+  * a value producer: the values of chunk k into stage k % 3 likewise;
+  * one MMA warp per tile (a single thread issues tcgen05.mma at a bounded
+    rate, so each tile gets its own): per item S_t(0), then per chunk c
+    P·V_t(c) once P_t(c) is in, releasing the values right away, then
+    S_t(c+1), releasing its keys; the query tiles after its last S.  Each
+    release is a commit, so it arrives when the warp's earlier MMAs are
+    done; a stage needs one from each tile.  The first P·V of an item
+    overwrites O_t without a barrier of its own: it waits for P_t(0), which
+    the warpgroup writes only after it has read the previous item's O_t
+    (the model checks that it has);
+  * per tile a softmax warpgroup: wait for S_t(c) and for its turn (the two
+    warpgroups take strict turns, tile 0's chunk k before tile 1's chunk k
+    before tile 0's chunk k + 1, so that one tile's softmax runs while the
+    other tile's products do), rescale O_t at once (the commit that
+    released S_t(c) covers P·V_t(c-1)), write P_t(c) over S_t, arrive, pass
+    the turn; after the item's last chunk wait for its last P·V, read O_t,
+    then store the rows;
+  * the tensor pipe runs the operations in issue order, a commit arriving
+    when everything issued before it has completed.
+TMA copies, MMAs and the softmax take random times.  Planted mistakes (a
+stage of keys released by one tile's commit alone, S issued before the P·V
+that reads the buffer it overwrites, an epilogue without its wait, a
+producer waiting on the wrong parity, query tiles reloaded without waiting
+for q_empty, values never released by one tile) show that the checks catch
+each kind of failure: stale data, a deadlock."""
 
 import pytest
 
 from tests._event_sim import Bar, EventSim
 
-K_STAGES, V_STAGES = 3, 2
+K_STAGES, V_STAGES = 2, 3
 
 
 class Sim(EventSim):
-    def __init__(self, nch, seed, mutate=None):
+    def __init__(self, items, seed, mutate=None):
         super().__init__(seed)
-        self.nch = nch  # chunks each tile attends (0: no such tile)
-        self.n = max(nch)
+        self.items = [tuple(x) for x in items]  # (nch0, nch1) per item, nch1 <= nch0 only if nch1 == 0
         self.mutate = mutate
+        # the stage and query-tile releases take one commit from each tile's MMA warp
         self.full_k = [Bar(f"full_k{i}", 1) for i in range(K_STAGES)]
-        self.empty_k = [Bar(f"empty_k{i}", 1) for i in range(K_STAGES)]
+        self.empty_k = [Bar(f"empty_k{i}", 1 if mutate == "k_count_one" else 2) for i in range(K_STAGES)]
         self.full_v = [Bar(f"full_v{i}", 1) for i in range(V_STAGES)]
-        self.empty_v = [Bar(f"empty_v{i}", 1) for i in range(V_STAGES)]
+        self.empty_v = [Bar(f"empty_v{i}", 2) for i in range(V_STAGES)]
         self.s_full = [Bar(f"s_full{t}", 1) for t in range(2)]
         self.p_full = [Bar(f"p_full{t}", 128) for t in range(2)]
         self.o_final = [Bar(f"o_final{t}", 1) for t in range(2)]
         self.q_full = [Bar(f"q_full{t}", 1) for t in range(2)]
-        # buffer contents
+        self.q_empty = Bar("q_empty", 2)
+        # softmax turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk k + 1, ...
+        self.turn = [Bar(f"turn{t}", 4) for t in range(2)]
+        # buffer contents, tagged (item, chunk)
         self.k_stage = [None] * K_STAGES
         self.v_stage = [None] * V_STAGES
-        self.q_tile = [False, False]
-        self.s_buf = [None, None]  # ("S", c) or ("P", c)
-        self.o_last = [-1, -1]  # last chunk accumulated into O_t
+        self.q_tile = [None, None]  # item whose query tile has landed
+        self.s_buf = [None, None]  # ("S", i, c) or ("P", i, c)
+        self.o_last = [None, None]  # (item, last chunk accumulated into O_t)
+        self.o_read = [None, None]  # item whose O_t the epilogue has read
         self.pipe_free = 0.0
 
     def run(self):
-        roles = [self.key_producer(), self.value_producer(), self.mma()]
-        roles += [self.softmax(t) for t in range(2) if self.nch[t] > 0]
-        return self.run_roles(roles, {"kp", "vp", "mma"} | {f"sm{t}" for t in range(2) if self.nch[t] > 0})
+        roles = [self.key_producer(), self.value_producer(), self.mma(0), self.mma(1), self.softmax(0),
+                 self.softmax(1)]
+        return self.run_roles(roles, {"kp", "vp", "mma0", "mma1", "sm0", "sm1"})
 
     # --- copies and the tensor pipe ---
     def pipe(self, duration, start, end):
+        # one tensor pipe, operations in issue order (that keeps each warp's
+        # own operations in order too)
         t0 = max(self.now, self.pipe_free)
         self.pipe_free = t0 + duration
         self.at(t0, start)
@@ -69,142 +90,183 @@ class Sim(EventSim):
 
     # --- roles ---
     def key_producer(self):
-        for t in range(2):
-            if self.nch[t]:
+        k, qi = 0, 0
+        for i, nch in enumerate(self.items):
+            if qi > 0 and self.mutate != "no_q_empty_wait":
+                yield ("wait", self.q_empty, (qi - 1) & 1, qi, f"key producer q_empty item {i}")
+            for t in range(2):
                 self.expect_tx(self.q_full[t], 2)
-                self.copy(self.q_full[t], 2, lambda t=t: self.q_tile.__setitem__(t, True))
-        for c in range(self.n):
-            st = c % K_STAGES
-            flip = 0 if self.mutate == "producer_parity" else 1
-            yield ("wait", self.empty_k[st], ((c // K_STAGES) & 1) ^ flip, c // K_STAGES, f"key producer c{c}")
-            self.expect_tx(self.full_k[st], 1)
-            self.copy(self.full_k[st], 1, lambda st=st, c=c: self.k_stage.__setitem__(st, c))
-            yield ("delay", self.rng.uniform(0.0, 0.5))
+                self.copy(self.q_full[t], 2, lambda t=t, i=i: self.q_tile.__setitem__(t, i))
+            qi += 1
+            for c in range(max(nch)):
+                st = k % K_STAGES
+                flip = 0 if self.mutate == "producer_parity" else 1
+                yield ("wait", self.empty_k[st], ((k // K_STAGES) & 1) ^ flip, k // K_STAGES, f"key producer {i}.{c}")
+                self.expect_tx(self.full_k[st], 1)
+                self.copy(self.full_k[st], 1, lambda st=st, tag=(i, c): self.k_stage.__setitem__(st, tag))
+                k += 1
+                yield ("delay", self.rng.uniform(0.0, 0.5))
         self.done.add("kp")
 
     def value_producer(self):
-        for c in range(self.n):
-            st = c % V_STAGES
-            yield ("wait", self.empty_v[st], ((c // V_STAGES) & 1) ^ 1, c // V_STAGES, f"value producer c{c}")
-            self.expect_tx(self.full_v[st], 1)
-            self.copy(self.full_v[st], 1, lambda st=st, c=c: self.v_stage.__setitem__(st, c))
-            yield ("delay", self.rng.uniform(0.0, 0.5))
+        k = 0
+        for i, nch in enumerate(self.items):
+            for c in range(max(nch)):
+                st = k % V_STAGES
+                yield ("wait", self.empty_v[st], ((k // V_STAGES) & 1) ^ 1, k // V_STAGES, f"value producer {i}.{c}")
+                self.expect_tx(self.full_v[st], 1)
+                self.copy(self.full_v[st], 1, lambda st=st, tag=(i, c): self.v_stage.__setitem__(st, tag))
+                k += 1
+                yield ("delay", self.rng.uniform(0.0, 0.5))
         self.done.add("vp")
 
-    def issue_s(self, t, c):
-        st = c % K_STAGES
-
+    def issue_s(self, i, t, c, kst):
         def start():
-            if not self.q_tile[t]:
-                self.fail(f"S{t}({c}) reads a query tile that has not landed")
-            if self.k_stage[st] != c:
-                self.fail(f"S{t}({c}) starts on keys of chunk {self.k_stage[st]}")
+            if self.q_tile[t] != i:
+                self.fail(f"S{t}({i}.{c}) reads the query tile of item {self.q_tile[t]}")
+            if self.k_stage[kst] != (i, c):
+                self.fail(f"S{t}({i}.{c}) starts on keys {self.k_stage[kst]}")
 
         def end():
-            if self.k_stage[st] != c:
-                self.fail(f"S{t}({c}): keys of stage {st} overwritten while it ran")
-            self.s_buf[t] = ("S", c)
+            if self.k_stage[kst] != (i, c):
+                self.fail(f"S{t}({i}.{c}): keys of stage {kst} overwritten while it ran")
+            if self.q_tile[t] != i:
+                self.fail(f"S{t}({i}.{c}): query tile overwritten while it ran")
+            self.s_buf[t] = ("S", i, c)
 
         self.pipe(self.rng.uniform(0.3, 2.0), start, end)
         self.commit(self.s_full[t])
 
-    def issue_pv(self, t, c):
-        st = c % V_STAGES
+    def issue_pv(self, i, t, c, vst):
+        nch_t = max(self.items[i])
 
         def start():
-            if self.s_buf[t] != ("P", c):
-                self.fail(f"PV{t}({c}) reads {self.s_buf[t]} instead of P({c})")
-            if self.v_stage[st] != c:
-                self.fail(f"PV{t}({c}) starts on values of chunk {self.v_stage[st]}")
-            if self.o_last[t] != c - 1:
-                self.fail(f"PV{t}({c}) accumulates onto O holding chunk {self.o_last[t]}")
+            if self.s_buf[t] != ("P", i, c):
+                self.fail(f"PV{t}({i}.{c}) reads {self.s_buf[t]} instead of P")
+            if self.v_stage[vst] != (i, c):
+                self.fail(f"PV{t}({i}.{c}) starts on values {self.v_stage[vst]}")
+            if c > 0 and self.o_last[t] != (i, c - 1):
+                self.fail(f"PV{t}({i}.{c}) accumulates onto O holding {self.o_last[t]}")
+            if c == 0 and self.o_last[t] is not None and self.o_read[t] != self.o_last[t][0]:
+                self.fail(f"PV{t}({i}.0) overwrites O of item {self.o_last[t][0]} before the epilogue read it")
 
         def end():
-            if self.v_stage[st] != c or self.s_buf[t] != ("P", c):
-                self.fail(f"PV{t}({c}): operands overwritten while it ran")
-            self.o_last[t] = c
+            if self.v_stage[vst] != (i, c) or self.s_buf[t] != ("P", i, c):
+                self.fail(f"PV{t}({i}.{c}): operands overwritten while it ran")
+            self.o_last[t] = (i, c)
 
         self.pipe(self.rng.uniform(0.3, 2.0), start, end)
-        if c + 1 == self.nch[t]:
+        if c + 1 == nch_t:
             self.commit(self.o_final[t])
 
-    def mma(self):
-        nch = self.nch
-        for t in range(2):
-            if nch[t]:
-                yield ("wait", self.q_full[t], 0, 1, f"mma q{t}")
-        yield ("wait", self.full_k[0], 0, 1, "mma k0")
-        for t in range(2):
-            if nch[t]:
-                self.issue_s(t, 0)
-        self.commit(self.empty_k[0])
-        for c in range(self.n):
-            yield ("wait", self.full_v[c % V_STAGES], (c // V_STAGES) & 1, c // V_STAGES + 1, f"mma v{c}")
-            k_next = False
-            tiles = [1, 0] if self.mutate == "release_k_after_first" else [0, 1]
-            for t in (0, 1):
-                if c >= nch[t]:
+    def mma(self, t):
+        """MMA warp of tile t: its S and P·V for every chunk of every item."""
+        kq, vq, sp, it = 0, 0, 0, 0
+        for i, nch in enumerate(self.items):
+            n = max(nch)
+            yield ("wait", self.q_full[t], it & 1, it + 1, f"mma{t} q item {i}")
+            yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1, f"mma{t} k {i}.0")
+            self.issue_s(i, t, 0, kq % K_STAGES)
+            self.commit(self.empty_k[kq % K_STAGES])
+            kq += 1
+            if n == 1:
+                self.commit(self.q_empty)
+            for c in range(n):
+                vst = vq % V_STAGES
+                yield ("wait", self.full_v[vst], (vq // V_STAGES) & 1, vq // V_STAGES + 1, f"mma{t} v {i}.{c}")
+                yield ("wait", self.p_full[t], sp & 1, sp + 1, f"mma{t} p {i}.{c}")
+                sp += 1
+                if self.mutate == "s_before_pv" and c + 1 < n:
+                    yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1,
+                           f"mma{t} k {i}.{c + 1}")
+                    self.issue_s(i, t, c + 1, kq % K_STAGES)
+                    self.issue_pv(i, t, c, vst)
+                    self.commit(self.empty_v[vst])
+                    self.commit(self.empty_k[kq % K_STAGES])
+                    kq += 1
+                    vq += 1
                     continue
-                yield ("wait", self.p_full[t], c & 1, c + 1, f"mma p{t}({c})")
-                if self.mutate == "s_before_pv" and c + 1 < nch[t]:
-                    if not k_next:
-                        yield ("wait", self.full_k[(c + 1) % K_STAGES], ((c + 1) // K_STAGES) & 1,
-                               (c + 1) // K_STAGES + 1, f"mma k{c + 1}")
-                        k_next = True
-                    self.issue_s(t, c + 1)
-                    self.issue_pv(t, c)
-                    if t == 1 or c + 1 >= nch[1]:
-                        self.commit(self.empty_k[(c + 1) % K_STAGES])
-                    continue
-                self.issue_pv(t, c)
-                if c + 1 < nch[t]:
-                    if not k_next:
-                        yield ("wait", self.full_k[(c + 1) % K_STAGES], ((c + 1) // K_STAGES) & 1,
-                               (c + 1) // K_STAGES + 1, f"mma k{c + 1}")
-                        k_next = True
-                    self.issue_s(t, c + 1)
-                    last = t == tiles[1] or c + 1 >= nch[1]
-                    if last:
-                        self.commit(self.empty_k[(c + 1) % K_STAGES])
-            self.commit(self.empty_v[c % V_STAGES])
-            yield ("delay", self.rng.uniform(0.0, 0.3))
-        self.done.add("mma")
+                self.issue_pv(i, t, c, vst)
+                if not (self.mutate == "v_release_one_tile" and t == 0):
+                    self.commit(self.empty_v[vst])
+                vq += 1
+                if c + 1 < n:
+                    yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1,
+                           f"mma{t} k {i}.{c + 1}")
+                    self.issue_s(i, t, c + 1, kq % K_STAGES)
+                    self.commit(self.empty_k[kq % K_STAGES])
+                    kq += 1
+                    if c + 1 == n - 1:
+                        self.commit(self.q_empty)
+                yield ("delay", self.rng.uniform(0.0, 0.3))
+            it += 1
+        self.done.add(f"mma{t}")
 
     def softmax(self, t):
-        for c in range(self.nch[t]):
-            yield ("wait", self.s_full[t], c & 1, c + 1, f"softmax{t} s({c})")
-            if self.s_buf[t] != ("S", c):
-                self.fail(f"softmax{t}({c}) reads {self.s_buf[t]} instead of S({c})")
-            if c > 0 and self.o_last[t] != c - 1:
-                self.fail(f"softmax{t}({c}) rescales O holding chunk {self.o_last[t]}, not {c - 1}")
-            yield ("delay", self.rng.uniform(0.5, 4.0))
-            if self.s_buf[t] != ("S", c):
-                self.fail(f"softmax{t}({c}): S overwritten while it was read")
-            self.s_buf[t] = ("P", c)
-            self.arrive(self.p_full[t], 128)
-        if self.mutate != "no_final_wait":
-            yield ("wait", self.o_final[t], 0, 1, f"softmax{t} epilogue")
-        if self.o_last[t] != self.nch[t] - 1:
-            self.fail(f"epilogue {t} reads O holding chunk {self.o_last[t]}, not {self.nch[t] - 1}")
+        sc, ot = 0, 0
+        for i, nch in enumerate(self.items):
+            n = max(nch)
+            for c in range(n):
+                yield ("wait", self.s_full[t], sc & 1, sc + 1, f"softmax{t} s {i}.{c}")
+                # strict alternation of the two warpgroups' softmax turns
+                if t == 0 and sc > 0:
+                    yield ("wait", self.turn[0], (sc - 1) & 1, sc, f"softmax0 turn {i}.{c}")
+                elif t == 1:
+                    yield ("wait", self.turn[1], sc & 1, sc + 1, f"softmax1 turn {i}.{c}")
+                sc += 1
+                if self.s_buf[t] != ("S", i, c):
+                    self.fail(f"softmax{t}({i}.{c}) reads {self.s_buf[t]}")
+                if c > 0 and self.o_last[t] != (i, c - 1):
+                    self.fail(f"softmax{t}({i}.{c}) rescales O holding {self.o_last[t]}")
+                yield ("delay", self.rng.uniform(0.5, 4.0))
+                if self.s_buf[t] != ("S", i, c):
+                    self.fail(f"softmax{t}({i}.{c}): S overwritten while it was read")
+                self.s_buf[t] = ("P", i, c)
+                self.arrive(self.p_full[t], 128)
+                self.arrive(self.turn[1 - t], 4)
+            if self.mutate != "no_final_wait":
+                yield ("wait", self.o_final[t], ot & 1, ot + 1, f"softmax{t} epilogue {i}")
+            if self.o_last[t] != (i, n - 1):
+                self.fail(f"epilogue {t} of item {i} reads O holding {self.o_last[t]}")
+            yield ("delay", self.rng.uniform(0.2, 1.5))  # tensor-memory loads of O
+            if self.o_last[t] != (i, n - 1):
+                self.fail(f"epilogue {t} of item {i}: O changed while it was read")
+            self.o_read[t] = i
+            ot += 1
+            yield ("delay", self.rng.uniform(0.5, 3.0))  # normalise and store the rows
         self.done.add(f"sm{t}")
 
 
-# (chunks of tile 0, chunks of tile 1): equal, the later tile one chunk
-# longer, a single valid tile, one chunk, longer than every ring
-SHAPES = [(1, 1), (1, 0), (1, 2), (2, 2), (3, 3), (3, 4), (4, 0), (5, 6), (7, 7), (8, 8), (6, 7)]
+# Item lists a CTA may get: (chunks of tile 0, chunks of tile 1).  The later
+# tile attends as many chunks or one more; a sequence's last pair may have
+# one tile.  Lists mix single-chunk items, items longer than every ring and
+# one-tile items.
+ITEM_LISTS = [
+    [(1, 1)],
+    [(1, 0)],
+    [(8, 8)],
+    [(1, 1), (1, 1), (1, 1)],
+    [(3, 4), (2, 0), (5, 5)],
+    [(8, 8), (7, 8), (1, 0), (4, 4), (1, 2)],
+    [(1, 0), (1, 0), (2, 2), (1, 0)],
+    [(6, 7), (3, 3), (3, 4), (2, 2), (1, 1), (1, 0)],
+    [(2, 3)] * 5,
+    [(5, 0), (5, 6)],
+]
 
 
-@pytest.mark.parametrize("nch", SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
-def test_prefill_protocol_is_race_free(nch):
-    for seed in range(60):
-        v = Sim(nch, seed).run()
+@pytest.mark.parametrize("items", ITEM_LISTS, ids=lambda s: "-".join(f"{a}x{b}" for a, b in s))
+def test_prefill_protocol_is_race_free(items):
+    for seed in range(40):
+        v = Sim(items, seed).run()
         assert not v, f"seed {seed}: {v[:3]}"
 
 
-@pytest.mark.parametrize("mutate", ["release_k_after_first", "s_before_pv", "no_final_wait", "producer_parity"])
+@pytest.mark.parametrize("mutate", ["k_count_one", "s_before_pv", "no_final_wait", "producer_parity",
+                                    "no_q_empty_wait", "v_release_one_tile"])
 def test_planted_protocol_mistakes_are_caught(mutate):
     caught = 0
-    for nch in [(3, 3), (5, 6), (8, 8)]:
-        for seed in range(40):
-            caught += bool(Sim(nch, seed, mutate).run())
+    for items in ([(3, 3), (5, 6)], [(8, 8), (2, 2), (4, 4)], [(1, 1)] * 4, [(2, 2), (1, 0), (3, 3)]):
+        for seed in range(30):
+            caught += bool(Sim(items, seed, mutate).run())
     assert caught > 0

@@ -399,7 +399,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   cudaError_t e;
   if (dtype == PA_BF16) {
     CUtensorMap kmap, vmap;
-    const bool inter = pa::decode_tc_interleaved(head_dim, block_size);
+    const bool inter = pa::decode_tc_interleaved(head_dim, block_size, pg.n > 0);
     rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
     if (rc) return rc;
     rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);

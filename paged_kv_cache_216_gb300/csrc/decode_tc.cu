@@ -40,6 +40,7 @@
 
 #include "device_common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pa {
 namespace {
@@ -66,20 +67,31 @@ struct TcCfg {
   static constexpr int kOStride = D + 4;  // floats per (warp, head) row; +4 spreads banks
   static constexpr int kOBuf = kConsumerWarps * kMaxGroup * kOStride * 4;
   static constexpr int kML = kConsumerWarps * kMaxGroup * 8;
-  // mbarriers: full[kStages], empty[kStages], qfull[2], qempty[2], epi_full, epi_done
-  static constexpr int kBars = (2 * kStages + 6) * 8;
+  // mbarriers: full[kStages], empty[kStages], qfull[2], qempty[2], epi_full, epi_done, and for
+  // shared-prefix items q_ready, s_ready, p_ready, o_done, drained
+  static constexpr int kBars = (2 * kStages + 6 + 5) * 8;
   // byte offsets from the 1024-aligned base
   static constexpr int kOffQ = kStages * kStage;
   static constexpr int kOffO = kOffQ + 2 * kQSlot;
   static constexpr int kOffML = kOffO + kOBuf;
   static constexpr int kOffDesc = kOffML + kML;  // int4 per Q slot: {s, part, kvh, ctx or -1}
   static constexpr int kOffBar = kOffDesc + 2 * 16;
-  static constexpr int kOffAbort = kOffBar + kBars;
+  static constexpr int kOffAbort = kOffBar + kBars;  // abort flag, then the tensor-memory address
   static constexpr size_t kBytes = 1024 + kOffAbort + 16;
+  // Tensor memory of a shared-prefix item (kGroupRows lanes): O (fp32, D
+  // columns), S of a chunk (fp32, kChunk columns; P as bf16 pairs over its
+  // first half), the query rows (bf16 pairs, D / 2 columns).
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColO = 0, kColS = 128, kColQ = 192;
+  static_assert(D <= 128 && kColS + kChunk <= kColQ && kColQ + D / 2 <= kTmemCols, "tensor-memory columns");
 };
 
 struct Bars {
   uint64_t *full, *empty, *qfull, *qempty, *epi_full, *epi_done;
+  // shared-prefix items: every warp's query rows are in tensor memory; S of
+  // a chunk is in; every warp's P of a chunk is in; the item's last P·V is
+  // done; every MMA issued is done
+  uint64_t *q_ready, *s_ready, *p_ready, *o_done, *drained;
 };
 
 template <int D>
@@ -92,6 +104,11 @@ __device__ __forceinline__ Bars bars_at(uint8_t* base) {
   b.qempty = b.qfull + 2;
   b.epi_full = b.qempty + 2;
   b.epi_done = b.epi_full + 1;
+  b.q_ready = b.epi_done + 1;
+  b.s_ready = b.q_ready + 1;
+  b.p_ready = b.s_ready + 1;
+  b.o_done = b.p_ready + 1;
+  b.drained = b.o_done + 1;
   return b;
 }
 
@@ -161,18 +178,20 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
     // ordinary items; a shared-prefix item covers a whole partition).
     const bool shared = kShared && ctx < 0;
     const int ts = prx & 0xffff, part = prx >> 16, kvh = idx % p.Hkv;
-    const int s0 = shared ? (ctx >> 4) & 0xffff : ts;
-    const int nm = shared ? ctx & 15 : 1;
+    const int s0 = shared ? (ctx >> 8) & 0xffff : ts;
+    const int nm = shared ? ctx & 0xff : 1;
     const int t0 = part * p.P, t1 = shared ? t0 + p.P : min(ctx, t0 + p.P);
     if (lane == 0) {
-      // a shared item's descriptor also carries its member count and a flag
-      const int dy = kShared ? part | (nm << 16) | (shared ? 1 << 20 : 0) : part;
-      desc[slot] = make_int4(s0, dy, kvh, shared ? t1 : ctx);
-      mbar_arrive_expect_tx(&bar.qfull[slot], (uint32_t)nm * qbytes);
-      for (int i = 0; i < nm; ++i) {
-        const __nv_bfloat16* src =
-            static_cast<const __nv_bfloat16*>(p.q) + ((size_t)(s0 + i) * p.H + (size_t)kvh * p.g) * D;
-        bulk_load(base + C::kOffQ + slot * C::kQSlot + i * qbytes, src, qbytes, &bar.qfull[slot]);
+      if (shared) {
+        // A shared item's descriptor carries its member count and a flag; the
+        // consumers load its query rows into tensor memory themselves.
+        desc[slot] = make_int4(s0, part | (nm << 16) | (1 << 24), kvh, t1);
+        mbar_arrive(&bar.qfull[slot]);
+      } else {
+        desc[slot] = make_int4(s0, part, kvh, ctx);
+        mbar_arrive_expect_tx(&bar.qfull[slot], qbytes);
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.q) + ((size_t)s0 * p.H + (size_t)kvh * p.g) * D;
+        bulk_load(base + C::kOffQ + slot * C::kQSlot, src, qbytes, &bar.qfull[slot]);
       }
     }
     ++nq;
@@ -239,8 +258,177 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
   }
 }
 
+// A shared-prefix item: one partition of a group's shared prefix, one KV
+// head, the query rows of up to kGroupRows / g members (row r = member
+// r / g, head r % g) -- a dense tile, so it runs on the 5th-generation tensor
+// cores with its accumulators in tensor memory, and every block of the
+// partition is read once for the whole tile.  All four consumer warps take
+// part: thread r owns row r (tensor-memory lane r) and thread 0 issues the
+// MMAs.  Per 32-token chunk of the ring: S = Q Kᵀ (M 128, N 32, K = D: A the
+// query rows in tensor memory, B the keys in the stage), the online softmax
+// of each row masked to its own sequence's length (a member may end inside
+// the shared part), P as bf16 over S, then O += P V (A = P in tensor memory,
+// B the values, an MN-major operand) and a commit that frees the stage.  O
+// is rescaled only when a row's max grows by more than 2^8 (the stale max
+// serves O and the sum alike).  The result of each row is its member's
+// split-K partial for this partition; the log-sum-exp merge combines it with
+// the member's other partitions.  Returns false after a time-out.
+template <int D>
+__device__ bool group_item(const DecodeArgs& p, uint8_t* base, const Bars& bar, uint32_t tmem, int s0, int nm,
+                           int part, int kvh, int t1, uint32_t& kseq, uint32_t& gi, uint32_t& gch,
+                           volatile int* abort) {
+  using C = TcCfg<D>;
+  constexpr float kRescaleLog2 = 8.f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = threadIdx.x;
+  const bool issuer = threadIdx.x == 0;
+  const int rows = nm * p.g;
+  const int t0 = part * p.P;
+  const int nch = (t1 - t0) / kChunk;  // a shared partition is whole, P a multiple of kChunk
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  int s = 0, qh = 0, lim = 0;  // the row's sequence, query head, and tokens it attends
+  if (r < rows) {
+    s = s0 + r / p.g;
+    qh = kvh * p.g + r % p.g;
+    lim = min(max(__ldg(p.context_lens + s), 0), p.max_ctx);
+  }
+  // The row's query into tensor memory (bf16 pairs; rows past the members: zeros).
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + ((size_t)s * p.H + qh) * D);
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x = r < rows ? __ldg(src + 4 * i + j) : make_uint4(0, 0, 0, 0);
+        w[4 * j] = x.x;
+        w[4 * j + 1] = x.y;
+        w[4 * j + 2] = x.z;
+        w[4 * j + 3] = x.w;
+      }
+      tmem_st16(lane_base + C::kColQ + 16 * i, w);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.q_ready);
+  }
+  const uint32_t id_s = instr_desc(kGroupRows, kChunk, false);
+  const uint32_t id_o = instr_desc(kGroupRows, D, true);
+  const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  for (int ch = 0; ch < nch; ++ch, ++kseq, ++gch) {
+    const int stage = kseq % C::kStages;
+    const uint32_t sk = smem_addr(base + stage * C::kStage);
+    if (issuer) {
+      // the keys of the chunk (and, first, every warp's query rows) are in
+      bool okm = mbar_spin(&bar.full[stage], (kseq / C::kStages) & 1, abort, p.wait_limit_ns);
+      if (okm && ch == 0) okm = mbar_spin(bar.q_ready, gi & 1, abort, p.wait_limit_ns);
+      if (okm) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8,
+                 smem_desc(sk + (kk >> 2) * kHalfBytes, 16, 1024) + (uint64_t)(((kk & 3) * 32) >> 4), id_s, kk > 0);
+        mma_commit(bar.s_ready);
+      } else {
+        give_up(p, abort);
+      }
+    }
+    if (!__all_sync(kFull, mbar_wait(bar.s_ready, gch & 1, abort, p.wait_limit_ns))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t raw[kChunk];
+    tmem_ld16_nowait(lane_base + C::kColS, raw);
+    tmem_ld16_nowait(lane_base + C::kColS + 16, raw + 16);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    // tokens of the chunk this row attends (none for a row past the members)
+    const int nvalid = min(kChunk, lim - (t0 + ch * kChunk));
+    float sc[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) sc[j] = j < nvalid ? __uint_as_float(raw[j]) : -INFINITY;
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < kChunk / 2; ++j) m4[j & 3] = fmax3(m4[j & 3], sc[2 * j], sc[2 * j + 1]);
+    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+    const bool grow = mx > m_run + kRescaleLog2 || (m_run == -INFINITY && mx != -INFINITY);
+    const float m_new = grow ? mx : m_run;
+    const float alpha = grow ? exp2f(m_run - m_new) : 1.f;  // m_run = -inf: alpha 0
+    if (ch > 0 && __any_sync(kFull, grow && m_run != -INFINITY)) {
+      // O holds P·V of the chunks before: the commit that released S covers them
+#pragma unroll 1
+      for (int i = 0; i < D / 16; ++i) {
+        float v[16];
+        tmem_ld16(lane_base + C::kColO + 16 * i, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q] = __float_as_uint(v[q] * alpha);
+        tmem_st16(lane_base + C::kColO + 16 * i, w);
+      }
+    }
+    l_run *= alpha;
+    m_run = m_new;
+    const float base_m = m_run == -INFINITY ? 0.f : m_run;
+    const float2 nb2 = make_float2(-base_m, -base_m);
+    float2 l2 = make_float2(0.f, 0.f);
+    uint32_t w[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float2 x = __ffma2_rn(make_float2(sc[2 * q], sc[2 * q + 1]), sl2, nb2);
+      const float2 e = make_float2(ex2_ftz(x.x), ex2_ftz(x.y));
+      l2 = __fadd2_rn(l2, e);
+      w[q] = pack_bf16x2(e.x, e.y);
+    }
+    l_run += l2.x + l2.y;
+    tmem_st16(lane_base + C::kColS, w);  // P over the first 16 columns of S
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.p_ready);
+    if (issuer) {
+      if (mbar_spin(bar.p_ready, gch & 1, abort, p.wait_limit_ns)) {
+        tc_fence_after();
+        const uint32_t sv = sk + C::kRegion;
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk)
+          mma_ts(tmem + C::kColO, tmem + C::kColS + kk * 8,
+                 smem_desc(sv, kHalfBytes, 1024) + (uint64_t)((kk * 16 * 128) >> 4), id_o, ch > 0 || kk > 0);
+        mma_commit(&bar.empty[stage]);  // the stage is free once this chunk's products are done
+        if (ch + 1 == nch) mma_commit(bar.o_done);
+      } else {
+        give_up(p, abort);
+      }
+    }
+  }
+  // the row's partial: un-normalised O, running max and sum
+  if (ok) ok = __all_sync(kFull, mbar_wait(bar.o_done, gi & 1, abort, p.wait_limit_ns));
+  if (ok) {
+    tc_fence_after();
+    uint32_t o[D];
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) tmem_ld16_nowait(lane_base + C::kColO + 16 * i, o + 16 * i);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    // a row whose sequence ends before this partition has no partial here
+    // (the merge does not read it)
+    if (r < rows && lim > t0) {
+      const size_t wi = ((size_t)s * p.max_parts + part) * p.H + qh;
+      float4* dst = reinterpret_cast<float4*>(p.ws_o + wi * D);
+#pragma unroll
+      for (int u = 0; u < D / 4; ++u)
+        dst[u] = make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]), __uint_as_float(o[4 * u + 2]),
+                             __uint_as_float(o[4 * u + 3]));
+      p.ws_ml[wi] = make_float2(m_run, l_run);
+    }
+  }
+  ++gi;
+  return ok;
+}
+
 template <int D, bool kInter, bool kShared>
-__device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort) {
+__device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort, uint32_t tmem) {
   using C = TcCfg<D>;
   constexpr int KS = D / 16;  // k-steps of the Q·Kᵀ product
   constexpr int MT = D / 16;  // m-tiles of the Oᵀ = Vᵀ Pᵀ product
@@ -254,6 +442,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
   float2* sML = reinterpret_cast<float2*>(base + C::kOffML);
   const uint32_t base_addr = smem_addr(base);
   uint32_t kseq = 0;
+  uint32_t gi = 0, gch = 0;  // shared-prefix items and their chunks so far
 
   for (uint32_t n = 0;; ++n) {
     const int slot = n & 1;
@@ -263,15 +452,35 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     }
     const int4 d = desc[slot];
     if (d.w < 0) return;  // no work left
+    if (kShared && ((d.y >> 24) & 1)) {
+      // a shared-prefix item: every warp works on it (the query slot is not used)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.qempty[slot]);
+      if (!group_item<D>(p, base, bar, tmem, d.x, (d.y >> 16) & 0xff, d.y & 0xffff, d.z, d.w, kseq, gi, gch, abort)) {
+        give_up(p, abort);
+        return;
+      }
+      // the item epilogue's handshake, which keeps its phases one per item
+      if (n > 0 && !mbar_wait(bar.epi_done, (n - 1) & 1, abort, p.wait_limit_ns)) {
+        give_up(p, abort);
+        return;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.epi_full);
+      if (!mbar_wait(bar.epi_full, n & 1, abort, p.wait_limit_ns)) {
+        give_up(p, abort);
+        return;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.epi_done);
+      continue;
+    }
     const int s0 = d.x, kvh = d.z, ctx = d.w;
-    const int part = kShared ? d.y & 0xffff : d.y, nm = kShared ? (d.y >> 16) & 15 : 1;
-    const bool shared = kShared && ((d.y >> 20) & 1);
+    const int part = d.y;
     const int t0 = part * p.P, t1 = min(ctx, t0 + p.P);
     const int nch = (t1 - t0 + kChunk - 1) / kChunk;
-    const int np = shared ? 2 : (ctx + p.P - 1) / p.P;  // a shared item always leaves a partial
-    const int nrow = nm * p.g;                           // rows of S: (sequence, query head) pairs
-    // Tokens row gq attends: its own sequence's length on a shared item.
-    const int lim = !shared ? ctx : gq < nrow ? min(max(__ldg(p.context_lens + s0 + gq / p.g), 0), p.max_ctx) : 0;
+    const int np = (ctx + p.P - 1) / p.P;
+    const int nrow = p.g;  // rows of S: the query heads of the KV head
     uint32_t qa[KS][2];
     {
       const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(base + C::kOffQ + slot * C::kQSlot);
@@ -333,7 +542,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
       }
       // Online softmax (log2 domain) for head row gq over this chunk.
       // tokens of the chunk row gq may attend
-      const int left = kShared ? min(nv, lim - (t0 + ch * kChunk)) : nv;
+      const int left = nv;
       float mx = -INFINITY;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
@@ -348,8 +557,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
       const float m_new = fmaxf(m_run, mx);
-      // A row with no token yet (shared items only) keeps weight 0.
-      const float m_use = (kShared && m_new == -INFINITY) ? 0.f : m_new;
+      const float m_use = m_new;
       const float alpha = exp2f(m_run - m_use);
       float ls = 0.f;
 #pragma unroll
@@ -430,7 +638,6 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         mw[w] = sML[w * kMaxGroup + h].x;
         M = fmaxf(M, mw[w]);
       }
-      if (kShared && M == -INFINITY) M = 0.f;  // a shared-item row without tokens here: all weights 0
       float L = 0.f, acc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = 0.f;
@@ -449,8 +656,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         acc[6] += wt * x1.z;
         acc[7] += wt * x1.w;
       }
-      const int s = kShared ? s0 + h / p.g : s0;
-      const int qh = kShared ? kvh * p.g + h % p.g : kvh * p.g + h;
+      const int s = s0;
+      const int qh = kvh * p.g + h;
       if (np <= 1) {  // one partition, or an empty context (zero row)
         uint4 pk = make_uint4(0, 0, 0, 0);
         if (np == 1) {
@@ -483,11 +690,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffAbort);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffAbort + 4);
+  const Bars b = bars_at<D>(base);
   if (threadIdx.x == 0) {
-    const Bars b = bars_at<D>(base);
     for (int k = 0; k < C::kStages; ++k) {
       mbar_init(&b.full[k], 1);   // producer arrival + TMA bytes
-      mbar_init(&b.empty[k], 1);  // the consuming warp
+      mbar_init(&b.empty[k], 1);  // the consuming warp (or the commit of a shared item's products)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&b.qfull[k], 1);                // producer arrival + Q bytes
@@ -495,10 +703,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mbar_init(b.epi_full, kConsumerWarps);  // every warp's state is in shared memory
     mbar_init(b.epi_done, kConsumerWarps);  // every warp has finished the combine
+    mbar_init(b.q_ready, kConsumerWarps);
+    mbar_init(b.s_ready, 1);
+    mbar_init(b.p_ready, kConsumerWarps);
+    mbar_init(b.o_done, 1);
+    mbar_init(b.drained, 1);
     *abort = 0;
     fence_barrier_init();
   }
+  // Shared-prefix items keep their tiles in tensor memory: 256 columns per
+  // CTA, two CTAs per SM.
+  if (kShared && (threadIdx.x >> 5) == 0) tmem_alloc(tslot, C::kTmemCols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = kShared ? *tslot : 0u;
   pdl_launch_dependents();
   if ((threadIdx.x >> 5) == kConsumerWarps) {
     if ((threadIdx.x & 31) == 0) {
@@ -507,7 +726,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     producer<D, kInter, kShared>(&kmap, &vmap, p, base, abort);
   } else {
-    consumer<D, kInter, kShared>(p, base, abort);
+    consumer<D, kInter, kShared>(p, base, abort, tmem);
+  }
+  if (kShared) {
+    // Every MMA issued has completed before tensor memory is released.
+    if (threadIdx.x == 0) {
+      mma_commit(b.drained);
+      const volatile int never = 0;
+      mbar_wait(b.drained, 0, &never, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+      tc_fence_after();
+      tmem_free(tmem, C::kTmemCols);
+    }
   }
 }
 
@@ -515,26 +748,29 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 size_t decode_tc_smem_bytes(int D) { return D == 128 ? TcCfg<128>::kBytes : TcCfg<64>::kBytes; }
 
-bool decode_tc_interleaved(int D, int B) { return D == 128 && B == 8; }
+bool decode_tc_interleaved(int D, int B, bool shared_items) { return D == 128 && B == 8 && !shared_items; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   const size_t smem = decode_tc_smem_bytes(a.D);
-  const bool inter = decode_tc_interleaved(a.D, a.B);
+  const bool inter = decode_tc_interleaved(a.D, a.B, a.shared_items != 0);
   using Kern = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
-  // [shared items][D == 128 ? (inter ? 2 : 1) : 0]
+  // [shared items][D == 128 ? (inter ? 2 : 1) : 0]; shared-prefix items read
+  // their stages as tensor-core operands, which the interleaved layout is not
   static const Kern kernels[2][3] = {
       {paged_decode_tc_kernel<64, false, false>, paged_decode_tc_kernel<128, false, false>,
        paged_decode_tc_kernel<128, true, false>},
       {paged_decode_tc_kernel<64, false, true>, paged_decode_tc_kernel<128, false, true>,
-       paged_decode_tc_kernel<128, true, true>}};
+       paged_decode_tc_kernel<128, false, true>}};
   const Kern kern = kernels[a.shared_items ? 1 : 0][a.D == 128 ? (inter ? 2 : 1) : 0];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   // Per-device launch shape, computed once (threads of one process share it).
+  // Per-device launch shape of each variant, computed once (threads of one
+  // process share it).
   struct Shape {
-    int sms = 0, per_sm128 = 0, per_sm64 = 0;
+    int sms = 0, per_sm[2][3] = {};
   };
   static Shape shapes[64];
   static std::once_flag once[64];
@@ -544,24 +780,24 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
     Shape sh;
     init_err = cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev);
     for (int v = 0; v < 2 && init_err == cudaSuccess; ++v)
-      for (int k = 0; k < 3 && init_err == cudaSuccess; ++k)
-        init_err = cudaFuncSetAttribute(kernels[v][k], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(k ? TcCfg<128>::kBytes : TcCfg<64>::kBytes));
-    // The variants share one launch shape; take the smallest occupancy.
-    sh.per_sm128 = sh.per_sm64 = 1 << 30;
-    for (int v = 0; v < 2 && init_err == cudaSuccess; ++v)
       for (int k = 0; k < 3 && init_err == cudaSuccess; ++k) {
-        int n = 0;
-        init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernels[v][k], kThreads,
-                                                                 k ? TcCfg<128>::kBytes : TcCfg<64>::kBytes);
-        int& per = k ? sh.per_sm128 : sh.per_sm64;
-        per = std::min(per, n);
+        const size_t bytes = k ? TcCfg<128>::kBytes : TcCfg<64>::kBytes;
+        init_err = cudaFuncSetAttribute(kernels[v][k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (init_err == cudaSuccess)
+          init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm[v][k], kernels[v][k], kThreads, bytes);
       }
     shapes[dev] = sh;
   });
   if (init_err != cudaSuccess) return init_err;
   const Shape& sh = shapes[dev];
-  const int per_sm = a.D == 128 ? sh.per_sm128 : sh.per_sm64;
+  int per_sm = sh.per_sm[a.shared_items ? 1 : 0][a.D == 128 ? (inter ? 2 : 1) : 0];
+  if (a.shared_items) {
+    // The occupancy query counts a kernel that allocates tensor memory as
+    // one CTA per SM.  This one holds 256 of the SM's 512 columns, so two
+    // fit, as registers and shared memory allow (the same as the plain
+    // variant's); a CTA that does not fit waits for one to finish.
+    per_sm = std::min(sh.per_sm[0][a.D == 128 ? 1 : 0], (int)(512 / TcCfg<128>::kTmemCols));
+  }
   if (per_sm < 1 || sh.sms < 1) return cudaErrorInvalidConfiguration;
   const long long total = (long long)a.max_parts * a.S * a.Hkv;  // upper bound of the work items
   const int grid = (int)std::min<long long>(total, (long long)sh.sms * per_sm);

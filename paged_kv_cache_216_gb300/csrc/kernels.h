@@ -48,16 +48,19 @@ struct DecodeArgs {
   int withhold_chunk;
 };
 
-constexpr int kMaxGroup = 8;
+constexpr int kMaxGroup = 8;   // query rows of an ordinary decode work item (heads of one KV head)
+constexpr int kGroupRows = 128;  // query rows of a shared-prefix work item (one tensor-core tile)
 
 // Groups of sequences whose contexts start with the same tokens in the same
 // cache blocks (prefix sharing, "Day 6/90 of Inference Engineering",
 // PagedAttention notes, paragraph 5).  Group i is sequences
 // first[i] .. first[i] + count[i] - 1; its first parts[i] partitions
 // (parts[i] * P tokens) are shared.  The work list attends each shared
-// partition with shared-prefix items, each covering the query rows of up to
-// kMaxGroup / g members at once, and leaves the members' own items for those
-// partitions out.
+// partition, per KV head, with shared-prefix items that each cover the
+// query rows of up to kGroupRows / g members -- one item per partition and
+// KV head for a group of up to 128 / g members, so each shared block is read
+// once per group -- and leaves the members' own items for those partitions
+// out.
 constexpr int kMaxPrefixGroups = 64;
 
 struct PrefixGroups {
@@ -68,15 +71,15 @@ struct PrefixGroups {
 };
 
 // Members per shared-prefix item: their g query rows each fill the
-// kMaxGroup rows a work item has.
-__host__ __device__ inline int prefix_members_per_item(int g) { return g >= kMaxGroup ? 1 : kMaxGroup / g; }
+// kGroupRows rows (tensor-memory lanes) of the item's tile.
+__host__ __device__ inline int prefix_members_per_item(int g) { return kGroupRows / g; }
 
 // Work-list entry of a shared-prefix item: the table of sequence `table_seq`
 // (the group's first), partition `part`, query rows of sequences s0 .. s0 +
-// nm - 1.  The second word is negative, which tells it from an ordinary
-// entry {s | part << 16, context length}.
+// nm - 1 (nm <= 128).  The second word is negative, which tells it from an
+// ordinary entry {s | part << 16, context length}.
 __host__ __device__ inline int2 prefix_entry(int table_seq, int part, int s0, int nm) {
-  return make_int2(table_seq | (part << 16), (int)(0x80000000u | ((unsigned)s0 << 4) | (unsigned)nm));
+  return make_int2(table_seq | (part << 16), (int)(0x80000000u | ((unsigned)s0 << 8) | (unsigned)nm));
 }
 
 // Shared partitions of sequence s (0 if it is in no group).
@@ -101,8 +104,9 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
 size_t decode_tc_smem_bytes(int D);
 // Whether the tensor-core kernel loads whole [B x D] slabs as one TMA box
 // of 2B lines of 128 bytes (true) or one box per 64-dim half (false); the
-// cache tensor maps must be made to match.
-bool decode_tc_interleaved(int D, int B);
+// cache tensor maps must be made to match.  Calls with shared-prefix items
+// use the per-half boxes.
+bool decode_tc_interleaved(int D, int B, bool shared_items);
 
 // FP8 (E4M3) caches, head_dim 128, bf16 q/out; same work list, workspace and
 // merge as the bf16 kernel.  scale_log2 must include the K scale.

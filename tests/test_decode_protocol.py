@@ -15,6 +15,14 @@ The model follows the kernel's roles:
     with k % 4 == w and releases each stage; then the item epilogue: wait
     until every warp has finished combining the previous item, store its
     state, wait until all four have, combine, and arrive.
+  * shared-prefix items (a tile of query rows on the tensor cores): the
+    warps release the query slot, store their query rows and arrive
+    (q_ready); warp 0 waits for each chunk's stage, issues S and commits
+    s_ready; every warp runs its softmax rows and arrives (p_ready); warp 0
+    issues P·V and commits the stage's release, and after the last chunk
+    o_done, which every warp waits for; then the item epilogue's handshake.
+    The tensor pipe runs warp 0's operations in order; a commit arrives when
+    everything before it is done.
 With S a multiple of four every stage always belongs to the same warp, so
 a warp never tests a stage whose earlier phase is still pending for
 another warp.  With S = 5 or 6 a warp running ahead passes the parity test
@@ -30,9 +38,12 @@ END = "end"
 
 
 class DecodeSim(EventSim):
-    def __init__(self, items, stages, seed):
+    def __init__(self, items, stages, seed, mutate=None):
         super().__init__(seed)
-        self.items = items  # chunks of each work item (0 for an empty context)
+        self.mutate = mutate
+        # chunks of each work item (0 for an empty context); ("g", n) is a
+        # shared-prefix item of n chunks
+        self.items = items
         self.S = stages
         self.full = [Bar(f"full{i}", 1) for i in range(stages)]
         self.empty = [Bar(f"empty{i}", 1) for i in range(stages)]
@@ -45,6 +56,27 @@ class DecodeSim(EventSim):
         self.q = [None, None]  # item whose query rows each slot holds
         self.state = [None] * WARPS  # item whose partial state each warp has stored
         self.combined = {}  # item -> warps that finished its combine
+        self.q_ready = Bar("q_ready", WARPS)
+        self.s_ready = Bar("s_ready", 1)
+        self.p_ready = Bar("p_ready", WARPS)
+        self.o_done = Bar("o_done", 1)
+        self.pipe_free = 0.0
+        self.gi = [0] * WARPS  # shared-prefix items each warp has finished
+        self.gch = [0] * WARPS  # their chunks
+        self.s_done = -1  # last chunk whose S has completed
+
+    @staticmethod
+    def chunks(item):
+        return item[1] if isinstance(item, tuple) else item
+
+    def pipe(self, duration, start, end):
+        t0 = max(self.now, self.pipe_free)
+        self.pipe_free = t0 + duration
+        self.at(t0, start)
+        self.at(t0 + duration, end)
+
+    def commit(self, bar):
+        self.pipe(0.0, lambda: None, lambda: self.arrive(bar))
 
     def run(self):
         roles = [self.producer()] + [self.consumer(w) for w in range(WARPS)]
@@ -60,9 +92,12 @@ class DecodeSim(EventSim):
                 self.arrive(self.qfull[slot])
                 break
             self.desc[slot] = n
-            self.expect_tx(self.qfull[slot], 1)
-            self.copy(self.qfull[slot], 1, lambda slot=slot, n=n: self.q.__setitem__(slot, n))
-            for _ in range(self.items[n]):
+            if isinstance(self.items[n], tuple):  # a shared-prefix item: no query copy
+                self.arrive(self.qfull[slot])
+            else:
+                self.expect_tx(self.qfull[slot], 1)
+                self.copy(self.qfull[slot], 1, lambda slot=slot, n=n: self.q.__setitem__(slot, n))
+            for _ in range(self.chunks(self.items[n])):
                 st = k % self.S
                 yield ("wait", self.empty[st], ((k // self.S) & 1) ^ 1, k // self.S, f"producer chunk {k}")
                 self.expect_tx(self.full[st], 1)
@@ -80,6 +115,14 @@ class DecodeSim(EventSim):
             if self.desc[slot] == END:
                 self.done.add(f"w{w}")
                 return
+            if isinstance(self.items[n], tuple):
+                if self.desc[slot] != n:
+                    self.fail(f"warp {w} item {n}: slot holds descriptor {self.desc[slot]}")
+                self.arrive(self.qempty[slot])
+                k = yield from self.group(w, n, k)
+                yield from self.epilogue(w, n)
+                n += 1
+                continue
             if self.desc[slot] != n or self.q[slot] != n:
                 self.fail(f"warp {w} item {n}: slot holds descriptor {self.desc[slot]}, query {self.q[slot]}")
             yield ("delay", self.rng.uniform(0.0, 0.5))
@@ -97,7 +140,61 @@ class DecodeSim(EventSim):
                         self.fail(f"warp {w}: stage {st} overwritten while chunk {k} was read")
                     self.arrive(self.empty[st])
                 k += 1
-            # item epilogue
+            yield from self.epilogue(w, n)
+            n += 1
+
+    def group(self, w, n, k):
+        """A shared-prefix item; returns the chunk count after it."""
+        gi = self.gi[w]
+        yield ("delay", self.rng.uniform(0.1, 1.0))  # query rows into tensor memory
+        self.arrive(self.q_ready)
+        for _ in range(self.items[n][1]):
+            st = k % self.S
+            gch = self.gch[w]
+            if w == 0:
+                yield ("wait", self.full[st], (k // self.S) & 1, k // self.S + 1, f"issuer chunk {k}")
+                if self.gch[0] == self.gch_start(n):
+                    yield ("wait", self.q_ready, gi & 1, gi + 1, f"issuer q_ready item {n}")
+
+                def s_start(st=st, k=k):
+                    if self.stage[st] != k:
+                        self.fail(f"S of chunk {k} reads chunk {self.stage[st]}")
+
+                def s_end(k=k):
+                    self.s_done = k
+                self.pipe(self.rng.uniform(0.2, 1.5), s_start, s_end)
+                self.commit(self.s_ready)
+            if self.mutate != "no_s_wait":
+                yield ("wait", self.s_ready, gch & 1, gch + 1, f"warp {w} s_ready chunk {k}")
+            if self.s_done != k:
+                self.fail(f"warp {w} reads S of chunk {k} before it is done (S done up to {self.s_done})")
+            yield ("delay", self.rng.uniform(0.2, 2.0))  # softmax of the warp's rows
+            self.arrive(self.p_ready)
+            if w == 0:
+                yield ("wait", self.p_ready, gch & 1, gch + 1, f"issuer p_ready chunk {k}")
+
+                def pv_end(st=st, k=k):
+                    if self.stage[st] != k:
+                        self.fail(f"P·V of chunk {k} read a stage overwritten with {self.stage[st]}")
+                if self.mutate == "release_before_pv":
+                    self.commit(self.empty[st])
+                    self.pipe(self.rng.uniform(0.2, 1.5), lambda: None, pv_end)
+                else:
+                    self.pipe(self.rng.uniform(0.2, 1.5), lambda: None, pv_end)
+                    self.commit(self.empty[st])
+                if _ + 1 == self.items[n][1]:
+                    self.commit(self.o_done)
+            self.gch[w] += 1
+            k += 1
+        yield ("wait", self.o_done, gi & 1, gi + 1, f"warp {w} o_done item {n}")
+        self.gi[w] += 1
+        return k
+
+    def gch_start(self, n):
+        return sum(self.items[i][1] for i in range(n) if isinstance(self.items[i], tuple))
+
+    def epilogue(self, w, n):
+        if True:
             if n > 0:
                 yield ("wait", self.epi_done, (n - 1) & 1, n, f"warp {w} epilogue {n} (previous combine)")
                 if len(self.combined.get(n - 1, ())) != WARPS:
@@ -112,11 +209,14 @@ class DecodeSim(EventSim):
                 self.fail(f"warp {w}: a state was overwritten during the combine of item {n}")
             self.combined.setdefault(n, set()).add(w)
             self.arrive(self.epi_done)
-            n += 1
 
 
-def _items(rng):
-    return [rng.choice([0, 1, 2, 3, 5, 8, 13]) for _ in range(rng.randint(1, 9))]
+def _items(rng, group=False):
+    items = [rng.choice([0, 1, 2, 3, 5, 8, 13]) for _ in range(rng.randint(1, 9))]
+    if group:  # shared-prefix items at the head of the list, as the planner puts them, and one more anywhere
+        items = [("g", rng.choice([1, 2, 4, 16])) for _ in range(rng.randint(1, 3))] + items
+        items.insert(rng.randint(0, len(items)), ("g", rng.choice([1, 3, 8])))
+    return items
 
 
 @pytest.mark.parametrize("stages", [4, 8, 12])
@@ -134,4 +234,23 @@ def test_stage_counts_not_a_multiple_of_the_warps_are_caught(stages):
     import random
 
     caught = sum(bool(DecodeSim(_items(random.Random(1000 + seed)), stages, seed).run()) for seed in range(150))
+    assert caught > 0
+
+
+@pytest.mark.parametrize("stages", [4, 8])
+def test_decode_protocol_with_shared_prefix_items_is_race_free(stages):
+    import random
+
+    for seed in range(150):
+        items = _items(random.Random(2000 + seed), group=True)
+        v = DecodeSim(items, stages, seed).run()
+        assert not v, f"seed {seed}, items {items}: {v[:3]}"
+
+
+@pytest.mark.parametrize("mutate", ["release_before_pv", "no_s_wait"])
+def test_planted_shared_item_mistakes_are_caught(mutate):
+    import random
+
+    caught = sum(bool(DecodeSim(_items(random.Random(3000 + seed), group=True), 4, seed, mutate).run())
+                 for seed in range(100))
     assert caught > 0

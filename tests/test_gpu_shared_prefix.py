@@ -75,8 +75,12 @@ CASES = {
     "g4_d128_b16": (31, 7, 16, 4, 128, 16, 64, [(0, 5, 256)], (256, 700)),
     # MHA g = 1, head_dim 64, two groups with sequences outside both
     "g1_d64_b32": (32, 8, 4, 4, 64, 32, 64, [(1, 3, 128), (4, 2, 320)], (320, 900)),
-    # g = 8 with 12 members: 96 rows, two row tiles (the second half empty)
-    "g8_d128_b8_two_tiles": (33, 13, 16, 2, 128, 8, 32, [(0, 12, 96)], (96, 400)),
+    # g = 8 with 12 members: 96 of the 128 rows of a tile, block size 8
+    "g8_d128_b8": (33, 13, 16, 2, 128, 8, 32, [(0, 12, 96)], (96, 400)),
+    # g = 8 with 20 members: 160 rows, two tiles per shared partition
+    "g8_two_tiles": (37, 23, 16, 2, 128, 16, 64, [(1, 20, 128)], (128, 420)),
+    # g = 4 with 40 members: 160 rows, two tiles (the second one partly empty)
+    "g4_40_members": (38, 44, 8, 2, 128, 16, 64, [(2, 40, 192)], (192, 480)),
     # a one-member group and a prefix that is not a whole number of partitions
     "g2_ragged_groups": (34, 9, 8, 4, 128, 16, 128, [(0, 1, 256), (2, 4, 384), (6, 3, 200)], (384, 1100)),
     # the GQA prefix workload's shape at a smaller batch: 1024-token prefix, P = 512

@@ -78,7 +78,7 @@ def _parse_shared(buf):
     nsh = int(sh.sum())
     assert sh[:nsh].all() and not sh[nsh:].any()  # shared items head the list
     x, y = ent[:nsh, 0], ent[:nsh, 1]
-    shared = [(int(a & 0xFFFF), int(a >> 16), int((b >> 4) & 0xFFFF), int(b & 15)) for a, b in zip(x, y)]
+    shared = [(int(a & 0xFFFF), int(a >> 16), int((b >> 8) & 0xFFFF), int(b & 0xFF)) for a, b in zip(x, y)]
     o = ent[nsh:]
     return int(hdr[0]), o[:, 0] & 0xFFFF, o[:, 0] >> 16, o[:, 1], shared
 
@@ -86,8 +86,9 @@ def _parse_shared(buf):
 @pytest.mark.parametrize("P,g", [(32, 4), (64, 1), (64, 8)])
 def test_plan_shares_prefix_partitions(ops, P, g):
     """With prefix groups the list starts with one shared item per (group,
-    shared partition, run of 8/g consecutive members), then holds every
-    other (sequence, partition) pair exactly once, longest first."""
+    shared partition, run of 128/g consecutive members: one tensor-core tile
+    of query rows), then holds every other (sequence, partition) pair
+    exactly once, longest first."""
     rng = np.random.default_rng(100 + P + g)
     ctx = rng.integers(150, 900, size=23).astype(np.int32)
     ctx[1] = 3 * P  # ends exactly at its group's shared part
@@ -100,7 +101,7 @@ def test_plan_shares_prefix_partitions(ops, P, g):
     counter, s, part, c, shared = _parse_shared(buf)
     assert counter == 0
     skip = _skip_of(groups, len(ctx), P, mx)
-    nm = 8 // g
+    nm = 128 // g
     want_shared = set()
     for first, count, prefix in groups:
         for p in range(prefix // P):

@@ -293,8 +293,10 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
  * Shared-prefix decode [Day6 paragraph 5: sequences forked from one prompt
  * share its cache blocks].  The same result as pa_decode (and, with a plan,
  * pa_decode_planned), but each block a group of sequences shares is read
- * once per kMaxGroup / g members (8 query rows; 8 members for g = 1, 2 for
- * g = 4) instead of once per member.
+ * once per 128 / g members -- once per group for groups of up to 128 / g
+ * sequences -- instead of once per member: a shared partition is attended,
+ * per KV head, as one tile of 128 query rows (member x head) on the
+ * 5th-generation tensor cores.
  *   groups      host, [num_groups][3] int32: first sequence, number of
  *               sequences, shared prefix length in tokens.  Group i is
  *               sequences first .. first + count - 1 of the batch; the
@@ -312,6 +314,8 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
  * its own length.  Groups whose prefix is shorter than one partition, and
  * calls where no context spans two partitions, fall back to plain decode
  * for those sequences.  bf16 only; the workspace is sized as for pa_decode.
+ * A call with prefix groups reads 8-token blocks as two boxes per block
+ * rather than one (the tiles' operand layout).
  */
 #define PA_MAX_PREFIX_GROUPS 64
 int pa_decode_shared_prefix(const void* q, const void* k_cache,

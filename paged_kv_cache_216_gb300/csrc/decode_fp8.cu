@@ -11,7 +11,7 @@
 // through an atomic counter; warp 4 loads each item's g query rows and
 // streams its blocks by TMA into a 4-stage shared-memory ring (one box of
 // [B tokens x 128 bytes] per block for keys and one for values, 128-byte
-// swizzle), 64 tokens per stage; warps 0-3 take the stages in turn and
+// swizzle), 64 tokens per stage; warps 0-3 take the chunks in turn and
 // merge their (max, sum, O) states at the end of the item.  Head dim 128.
 //
 // The consumer never widens a whole stage: it reads codes with ldmatrix and
@@ -49,15 +49,17 @@ constexpr int kD = 128;                      // head_dim
 constexpr int kChunk = 64;                   // tokens per pipeline stage
 constexpr int kRegion = kChunk * kD;         // 8 KB: the keys (or values) of a stage
 constexpr int kStage = 2 * kRegion;
-constexpr int kStages = 4;
+// Five stages (80 KB) fit two CTAs per SM; with the stage count not a
+// multiple of the consumer warps, a stage passes from warp to warp, so a
+// warp waits for the release of its stage's previous chunk before testing
+// the stage's full barrier (which could otherwise be two phases behind and
+// pass the parity test on the wrong phase).
+constexpr int kStages = 5;
 constexpr int NTILES = kChunk / 8;           // 8-token tiles of S per stage
 constexpr int KSTEPS = kChunk / 16;          // 16-token steps of P·V per stage
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr unsigned kFull = 0xffffffffu;
-// chunk k goes to consumer warp k % 4 and stage k % kStages: a multiple, so
-// every stage always belongs to one warp
-static_assert(kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
 constexpr int kQSlot = kMaxGroup * kD * 2;   // bf16 query rows of one item
 constexpr int kOStride = kD + 4;
 constexpr int kOBuf = kConsumerWarps * kMaxGroup * kOStride * 4;
@@ -283,6 +285,10 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     for (int ch = 0; ch < nch; ++ch, ++kseq) {
       if ((int)(kseq & (kConsumerWarps - 1)) != warp) continue;
       const int stage = kseq % kStages;
+      if (kseq >= (uint32_t)kStages && !mbar_wait(&bar.empty[stage], ((kseq - kStages) / kStages) & 1, abort)) {
+        give_up(p, abort);
+        return;
+      }
       if (!mbar_wait(&bar.full[stage], (kseq / kStages) & 1, abort)) {
         give_up(p, abort);
         return;

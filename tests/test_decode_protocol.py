@@ -26,8 +26,10 @@ The model follows the kernel's roles:
 With S a multiple of four every stage always belongs to the same warp, so
 a warp never tests a stage whose earlier phase is still pending for
 another warp.  With S = 5 or 6 a warp running ahead passes the parity test
-on a phase two behind, which is why the kernel asserts the multiple (and
-why these checks are shown to fire for 5 and 6)."""
+on a phase two behind, which is why the bf16 kernel asserts the multiple
+(and why these checks are shown to fire for 5 and 6).  A ring of any size
+is safe when a warp first waits for the release of its stage's previous
+chunk (the FP8 kernel's five-stage ring does this)."""
 
 import pytest
 
@@ -38,9 +40,10 @@ END = "end"
 
 
 class DecodeSim(EventSim):
-    def __init__(self, items, stages, seed, mutate=None):
+    def __init__(self, items, stages, seed, mutate=None, release_wait=False):
         super().__init__(seed)
         self.mutate = mutate
+        self.release_wait = release_wait
         # chunks of each work item (0 for an empty context); ("g", n) is a
         # shared-prefix item of n chunks
         self.items = items
@@ -132,6 +135,10 @@ class DecodeSim(EventSim):
             for _ in range(self.items[n]):
                 if k % WARPS == w:
                     st = k % self.S
+                    if self.release_wait and k >= self.S:
+                        # the stage's previous chunk (another warp's) has been released
+                        yield ("wait", self.empty[st], ((k - self.S) // self.S) & 1, (k - self.S) // self.S + 1,
+                               f"warp {w} release of chunk {k - self.S}")
                     yield ("wait", self.full[st], (k // self.S) & 1, k // self.S + 1, f"warp {w} chunk {k}")
                     if self.stage[st] != k:
                         self.fail(f"warp {w} reads chunk {self.stage[st]} from stage {st}, wanted {k}")
@@ -254,3 +261,17 @@ def test_planted_shared_item_mistakes_are_caught(mutate):
     caught = sum(bool(DecodeSim(_items(random.Random(3000 + seed), group=True), 4, seed, mutate).run())
                  for seed in range(100))
     assert caught > 0
+
+
+@pytest.mark.parametrize("stages", [5, 6, 7])
+def test_any_stage_count_is_race_free_when_a_warp_waits_for_the_previous_release(stages):
+    """With S not a multiple of four a stage passes between warps; a warp
+    that first waits for the release of the stage's previous chunk can
+    never test a full barrier two phases behind (the FP8 kernel's ring)."""
+    import random
+
+    for seed in range(150):
+        for group in (False, True):
+            items = _items(random.Random(4000 + seed), group=group)
+            v = DecodeSim(items, stages, seed, release_wait=True).run()
+            assert not v, f"seed {seed}, items {items}: {v[:3]}"

@@ -17,18 +17,23 @@
 // The consumer never widens a whole stage: it reads codes with ldmatrix and
 // converts them in registers (cvt e4m3x2 -> f16x2, exact), so each code
 // crosses shared memory once.
-//  * S = Q Kᵀ (mma.m16n8k16 f16, query heads as rows of A): a 16-bit
-//    ldmatrix of a K row gives a thread four consecutive dims of one token,
-//    so the k order of each 16-dim step is permuted -- k 2t, 2t+1 are dims
-//    4t, 4t+1 and k 2t+8, 2t+9 are dims 4t+2, 4t+3 -- and Q's fragments are
-//    built in the same order (a dot product does not depend on it).
+//  * Sᵀ = K Qᵀ (mma.m16n8k16 f16): 16 tokens of a step as the rows of A,
+//    the query heads as the 8 columns of B (g of them real), so one MMA
+//    covers twice the tokens that Q Kᵀ with the heads as rows would.  A
+//    16-bit ldmatrix of key rows gives a lane four consecutive dims of one
+//    token, so each 16-dim step uses a permuted k order -- k 2t, 2t+1 are
+//    dims 4t, 4t+1 and k 2t+8, 2t+9 are dims 4t+2, 4t+3 -- and Q's fragments
+//    are built in the same order (a dot product does not depend on it).
 //  * Oᵀ = Vᵀ Pᵀ: the 8-bit transposing ldmatrix (m16n16) of a 16-token x
-//    16-dim V tile gives a thread one dim of four consecutive tokens, so the
+//    16-dim V tile gives a lane one dim of four consecutive tokens, so the
 //    token order of each 16-token step is permuted the same way (k 2t, 2t+1
-//    are tokens 4t, 4t+1 and k 2t+8, 2t+9 tokens 4t+2, 4t+3).  To let P
-//    come straight from the S accumulators, the 8 tokens of S tile 2j are
-//    tokens {0,1,4,5,8,9,12,13} of step j and those of tile 2j+1 tokens
-//    {2,3,6,7,10,11,14,15} (the K ldmatrix gathers its rows in that order).
+//    are tokens 4t, 4t+1 and k 2t+8, 2t+9 tokens 4t+2, 4t+3).  The rows of
+//    each step's Sᵀ are gathered in the matching order -- tokens
+//    {0,1,4,5,8,9,12,13} then {2,3,6,7,10,11,14,15} -- so that a transposing
+//    movmatrix of each 8 x 8 half of P gives exactly the B operand.
+//  * The online softmax keeps, per lane, heads 2t and 2t+1; their maxima
+//    are reduced over the eight lanes holding the other tokens, and O (held
+//    as Oᵀ, heads as columns) is rescaled without shuffles.
 // Every wait is bounded (device_common.cuh); a time-out raises
 // PA_STATUS_TIMEOUT and the CTA winds down.
 
@@ -55,7 +60,6 @@ constexpr int kStage = 2 * kRegion;
 // the stage's full barrier (which could otherwise be two phases behind and
 // pass the parity test on the wrong phase).
 constexpr int kStages = 5;
-constexpr int NTILES = kChunk / 8;           // 8-token tiles of S per stage
 constexpr int KSTEPS = kChunk / 16;          // 16-token steps of P·V per stage
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -116,6 +120,14 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Transpose of an 8 x 8 matrix of 16-bit values held one row pair per lane
+// (lane 4r + c holds row r, columns 2c, 2c + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 // Two bf16 (one 32-bit word) -> two f16; exact for |x| in [2^-14, 65504].
@@ -246,9 +258,11 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
   float* sO = reinterpret_cast<float*>(base + kOffO);
   float2* sML = reinterpret_cast<float2*>(base + kOffML);
   const uint32_t base_addr = smem_addr(base);
-  // Row of this lane's K ldmatrix address within a 16-token step: S tile
-  // 2j + h holds tokens 4(r / 2) + 2h + (r % 2), r = 0..7.
-  const int krow = 4 * ((lane & 7) >> 1) + (lane & 1);
+  // Key row of this lane's ldmatrix address within a 16-token step: rows
+  // 0-7 of the step's Sᵀ tile are tokens {0,1,4,5,8,9,12,13}, rows 8-15
+  // tokens {2,3,6,7,10,11,14,15} (lane L addresses row L % 8 of matrix L / 8;
+  // odd matrices hold rows 8-15).
+  const int krow = 4 * ((lane & 7) >> 1) + (lane & 1) + 2 * ((lane >> 3) & 1);
   uint32_t kseq = 0;
 
   for (uint32_t n = 0;; ++n) {
@@ -277,7 +291,8 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar.qempty[slot]);
 
-    float m_run = -INFINITY, l_run = 0.f;
+    // running max and (this lane's share of the) sum of heads 2tq, 2tq + 1
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float o[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -305,63 +320,79 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         fence_proxy_async_smem();
         __syncwarp();
       }
-      // S = Q Kᵀ : tiles of 8 tokens (rows = heads; only c0, c1 are real).
-      float sc[NTILES][4];
+      // Sᵀ = K Qᵀ per 16-token step j: rows = the step's tokens in the
+      // order above, columns = query heads (g of the 8 are real), k = dims in
+      // the permuted order of each 16-dim step.  A = keys from a 16-bit
+      // ldmatrix of the codes (a lane gets four consecutive dims of a token,
+      // converted to two f16 pairs), B = the query rows.
+      float st[KSTEPS][4];
 #pragma unroll
-      for (int nt = 0; nt < NTILES; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      for (int jj = 0; jj < KSTEPS; ++jj) {
+        st[jj][0] = st[jj][1] = st[jj][2] = st[jj][3] = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < NTILES; ++nt) {
-        const int r = 16 * (nt >> 1) + 2 * (nt & 1) + krow;
-#pragma unroll
-        for (int kb = 0; kb < KS / 4; ++kb) {
+        for (int kb = 0; kb < KS / 2; ++kb) {
           uint32_t w[4];
-          ldmatrix_x4(sk + swz(r, 4 * kb + (lane >> 3)), w[0], w[1], w[2], w[3]);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int ks = 4 * kb + m;
-            mma_f16_16816(sc[nt], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(w[m]), e4m3x2_to_f16x2(w[m] >> 16));
-          }
+          ldmatrix_x4(sk + swz(16 * jj + krow, 2 * kb + (lane >> 4)), w[0], w[1], w[2], w[3]);
+          mma_f16_16816(st[jj], e4m3x2_to_f16x2(w[0]), e4m3x2_to_f16x2(w[1]), e4m3x2_to_f16x2(w[0] >> 16),
+                        e4m3x2_to_f16x2(w[1] >> 16), qa[2 * kb][0], qa[2 * kb][1]);
+          mma_f16_16816(st[jj], e4m3x2_to_f16x2(w[2]), e4m3x2_to_f16x2(w[3]), e4m3x2_to_f16x2(w[2] >> 16),
+                        e4m3x2_to_f16x2(w[3] >> 16), qa[2 * kb + 1][0], qa[2 * kb + 1][1]);
         }
       }
-      // Online softmax (log2 domain) for head row gq over this chunk.
-      float mx = -INFINITY;
+      // Online softmax (log2 domain) of heads 2tq, 2tq + 1 over this chunk:
+      // this lane holds tokens 4(gq / 2) + (gq % 2) and that + 2 of each step;
+      // the other seven of each head are on the lanes with the same tq.
+      const int tok_lo = 4 * (gq >> 1) + (gq & 1);
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int nt = 0; nt < NTILES; ++nt) {
+      for (int jj = 0; jj < KSTEPS; ++jj) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tok = 16 * (nt >> 1) + 4 * tq + 2 * (nt & 1) + e;
-          const float v = tok < nv ? sc[nt][e] * p.scale_log2 : -INFINITY;
-          sc[nt][e] = v;
-          mx = fmaxf(mx, v);
+        for (int c = 0; c < 4; ++c) {
+          const int tok = 16 * jj + tok_lo + 2 * (c >> 1);
+          const float v = tok < nv ? st[jj][c] * p.scale_log2 : -INFINITY;
+          st[jj][c] = v;
+          mx[c & 1] = fmaxf(mx[c & 1], v);
         }
       }
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = exp2f(m_run - m_new);
-      float ls = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < NTILES; ++nt) {
-        sc[nt][0] = exp2f(sc[nt][0] - m_new);
-        sc[nt][1] = exp2f(sc[nt][1] - m_new);
-        ls += sc[nt][0] + sc[nt][1];
+      for (int off = 4; off < 32; off <<= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(kFull, mx[0], off));
+        mx[1] = fmaxf(mx[1], __shfl_xor_sync(kFull, mx[1], off));
       }
-      l_run = l_run * alpha + ls;
-      m_run = m_new;
-      const float a_lo = __shfl_sync(kFull, alpha, 8 * tq);
-      const float a_hi = __shfl_sync(kFull, alpha, 8 * tq + 4);
+      float alpha[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float m_new = fmaxf(m_run[e], mx[e]);
+        alpha[e] = exp2f(m_run[e] - m_new);
+        m_run[e] = m_new;
+        l_run[e] *= alpha[e];
+      }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        o[mt][0] *= a_lo;
-        o[mt][1] *= a_hi;
-        o[mt][2] *= a_lo;
-        o[mt][3] *= a_hi;
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
+      }
+      // P in f16; a transposing movmatrix of each 8 x 8 half of a step turns
+      // (token row, head pair) into (head gq, tokens 4tq, 4tq + 1) and
+      // (head gq, tokens 4tq + 2, 4tq + 3): the B operand of Oᵀ = Vᵀ Pᵀ in the
+      // token order of the values' transposing ldmatrix.
+      uint32_t pb[KSTEPS][2];
+#pragma unroll
+      for (int jj = 0; jj < KSTEPS; ++jj) {
+        const float e0 = exp2f(st[jj][0] - m_run[0]), e1 = exp2f(st[jj][1] - m_run[1]);
+        const float e2 = exp2f(st[jj][2] - m_run[0]), e3 = exp2f(st[jj][3] - m_run[1]);
+        l_run[0] += e0 + e2;
+        l_run[1] += e1 + e3;
+        pb[jj][0] = movmatrix_trans(pack_f16x2(e0, e1));
+        pb[jj][1] = movmatrix_trans(pack_f16x2(e2, e3));
       }
       // Oᵀ += Vᵀ Pᵀ : 16 tokens per step, 16 dims per tile.
 #pragma unroll
       for (int kt = 0; kt < KSTEPS; ++kt) {
-        const uint32_t pb0 = pack_f16x2(sc[2 * kt][0], sc[2 * kt][1]);          // tokens 4t, 4t+1
-        const uint32_t pb1 = pack_f16x2(sc[2 * kt + 1][0], sc[2 * kt + 1][1]);  // tokens 4t+2, 4t+3
+        const uint32_t pb0 = pb[kt][0];  // tokens 4tq, 4tq+1 of the step, head gq
+        const uint32_t pb1 = pb[kt][1];  // tokens 4tq+2, 4tq+3
         const int r = 16 * kt + (lane & 15);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -380,10 +411,16 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
       give_up(p, abort);
       return;
     }
-    float l = l_run;
-    l += __shfl_xor_sync(kFull, l, 1);
-    l += __shfl_xor_sync(kFull, l, 2);
-    if (tq == 0 && gq < p.g) sML[warp * kMaxGroup + gq] = make_float2(m_run, l);
+    float l0 = l_run[0], l1 = l_run[1];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    if (gq == 0) {
+      if (2 * tq < p.g) sML[warp * kMaxGroup + 2 * tq] = make_float2(m_run[0], l0);
+      if (2 * tq + 1 < p.g) sML[warp * kMaxGroup + 2 * tq + 1] = make_float2(m_run[1], l1);
+    }
     float* ob = sO + warp * kMaxGroup * kOStride;
     const int h0 = 2 * tq, h1 = 2 * tq + 1;
 #pragma unroll

@@ -25,40 +25,49 @@
 //    after griddepcontrol.wait; lane b issues block b of a chunk from
 //    block-table entries fetched 32 at a time.  Warp 8 first loads the
 //    item's query tiles, one 3D box per 64-dim half, once the previous
-//    item's last S has completed, and prefetches the next item's into L2;
-//  * warps 10 and 11 (MMA, one per tile): one thread issues the tile's
+//    item's last S has completed, and prefetches the next item's into L2.
+//    Value rows past a sequence's end (in its last block) are cleared by
+//    warp 9 once their copy has landed, and the value ring starts as zeros,
+//    so every value row a P·V reads is finite (masked keys get exact zero
+//    weights, and 0 x NaN would still be NaN);
+//  * warps 10 and 11 (MMA, one per tile): lane 0 alone issues the tile's
 //    S = Q Kᵀ (M 128, N 128, K = head_dim: head_dim / 16 tcgen05.mma
 //    kind::f16 from shared-memory descriptors) and O += P V (M 128,
 //    N = head_dim, K 128: eight MMAs, P read from tensor memory, V an
 //    MN-major operand in shared memory), per chunk c P·V(c) then S(c + 1),
-//    spinning on one barrier at a time.  A thread issues about one MMA per
-//    64 cycles, about what one takes, so one thread for both tiles would
-//    leave the tensor cores idle half the time; with one each, one tile's
-//    products run while the other tile's softmax does (ping-pong).
-//    tcgen05.commit signals the mbarriers and releases each stage right
-//    after the tile's last MMA that reads it (a stage is free once both
-//    tiles have released it), and the query tiles after the item's last S;
+//    spinning on one barrier at a time; the other lanes idle, since a
+//    warp-wide synchronisation after a group of MMAs waits for the tensor
+//    cores to take the group.  A thread issues about one MMA per 64 cycles,
+//    about what one takes, so one thread for both tiles would leave the
+//    tensor cores idle half the time; with one each, one tile's products
+//    run while the other tile's softmax does (ping-pong).  A commit signals
+//    each S (and, after the item's last P·V, the end of O);
 //  * warps 0-3 and 4-7 (softmax, one warpgroup per tile): thread t of a
-//    warpgroup owns query row t of its tile (tensor-memory lane t): it
-//    reads its 128 scores (tcgen05.ld), masks keys past its position, keeps
-//    the running max and sum, writes P as bf16 back to tensor memory
-//    (tcgen05.st) and rescales its row of O only when its max grows by more
-//    than 2^8 (otherwise the stale max stays: exp2 values up to 256 are
-//    exact enough and O and the sum use the same max); at the end of the
-//    item it reads its row of O, divides by the sum and stores it.  The
-//    exponentials are one packed FMA per two scores (scale and max) and one
-//    ex2 each; the max is taken three operands at a time.  The two
-//    warpgroups take strict turns, chunk by chunk, so that one tile's
-//    softmax runs while the other tile's products do;
-// Both tiles attend all of the item's chunks (the earlier tile's keys past
-// its rows' positions are masked), which keeps the two MMA warps' releases
-// symmetric.  Tensor memory (512 columns allocated once per CTA): O of tile
-// t at columns DH·t .. DH·t + DH - 1 and its S at 2·DH + 128t (DH =
-// head_dim); P is written over the first half of its S.  Value rows past the
-// pair's keys are zeroed in shared memory before the first P·V of that stage
-// so stale cache rows cannot turn 0 x NaN into NaN.  Every wait is bounded;
-// on a time-out the kernel raises PA_STATUS_TIMEOUT, stops issuing work,
-// lets its copies and products in flight finish, and exits.
+//    warpgroup owns query row t of its tile (tensor-memory lane t).  Once S
+//    of a chunk is done it releases the chunk's keys, the previous chunk's
+//    values (the commit that signalled S also covers the P·V issued before
+//    it) and, after the item's last S, the query tiles: one arrival per
+//    tile, so the MMA thread spends no commits on releases.  It reads its
+//    128 scores (tcgen05.ld), masks keys past its position, keeps the
+//    running max and sum, writes P as bf16 back to tensor memory
+//    (tcgen05.st; one arrival per warp) and rescales its row of O only when
+//    its max grows by more than 2^8 (otherwise the stale max stays: exp2
+//    values up to 256 are exact enough and O and the sum use the same max);
+//    at the end of the item it reads its row of O, divides by the sum and
+//    stores it.  The exponentials are one packed FMA per two scores (scale
+//    and max) and one ex2 each; the max is taken three operands at a time.
+//    The two warpgroups take strict turns, chunk by chunk, so that one
+//    tile's softmax runs while the other tile's products do.
+// The softmax warpgroups run with 224 registers a thread and the producer
+// and MMA warps with 56 (setmaxnreg), so that the 128 scores of a row stay
+// in registers.  Both tiles attend all of the item's chunks (the earlier
+// tile's keys past its rows' positions are masked), which keeps the two
+// tiles' releases symmetric.  Tensor memory (512 columns allocated once
+// per CTA): O of tile t at columns DH·t .. DH·t + DH - 1 and its S at
+// 2·DH + 128t (DH = head_dim); P is written over the first half of its S.
+// Every wait is bounded; on a time-out the kernel raises PA_STATUS_TIMEOUT,
+// stops issuing work, lets its copies and products in flight finish, and
+// exits.
 
 #include <cuda_bf16.h>
 
@@ -82,6 +91,17 @@ constexpr int kSoftWarps = 4;           // per tile
 constexpr int kProducerWarp = kTiles * kSoftWarps;  // keys; the next warp streams values
 constexpr int kMmaWarp = kProducerWarp + 2;         // tile 0's MMAs; the next warp issues tile 1's
 constexpr int kThreadsT = (kTiles * kSoftWarps + 2 + kTiles) * 32;
+// Registers per thread: the launch gets kRegsLaunch (what 384 threads at one
+// CTA per SM compile to); then the softmax warpgroups raise theirs to
+// kRegsSoft and the warpgroup of producers and MMA warps lowers its own to
+// kRegsAux.  The split must fit in what the launch reserved, or the raise
+// would wait forever; the host checks the compiled count before launching.
+constexpr int kRegsLaunch = 168, kRegsSoft = 224, kRegsAux = 56;
+static_assert(kTiles * kSoftWarps * 32 * kRegsSoft + (kThreadsT - kTiles * kSoftWarps * 32) * kRegsAux <=
+                  kThreadsT * kRegsLaunch,
+              "register split exceeds the launch's registers");
+static_assert(kProducerWarp % 4 == 0 && kThreadsT - kProducerWarp * 32 == 128,
+              "producers and MMA warps form one warpgroup");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of a query tile
 constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage of K (or V)
@@ -100,8 +120,8 @@ struct PfCfg {
   static constexpr int kOffK = kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
-  // barriers: the rings, kTileBars per tile, q_empty, drained per MMA warp, softmax turn per tile
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 1 + 2 * kTiles) * 8;  // tensor-memory address, abort flag
+  // barriers: the rings, kTileBars per tile, q_empty, drained per MMA warp, softmax turn per tile, v_land
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 1 + 2 * kTiles + 1) * 8;  // tensor-memory address, abort flag
   static constexpr size_t kBytes = 1024 + kOffMisc + 16;
   static constexpr uint32_t kColO = 0, kColS = 2 * DH;
   static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
@@ -116,7 +136,7 @@ constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grow
 // derives the same chunk counts from them, so they need no messages beyond
 // the pipeline's barriers.
 struct PfItem {
-  int s, kvh, pair, q0, rows, first_pos, row00;
+  int s, kvh, pair, q0, rows, first_pos, row00, ctx;
   int nch, t_end;              // chunks of keys the pair attends, and its keys
   int state;                   // 0: work; 1: no rows of the sequence in this pair; 2: inconsistent lengths
 };
@@ -135,6 +155,7 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs
     return it;
   }
   it.q0 = q0;
+  it.ctx = ctx;
   it.rows = n_new * p.g;
   it.first_pos = ctx - n_new;
   it.row00 = it.pair * kTiles * kM;
@@ -181,13 +202,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // the item's last S of both tiles is done: the query tiles are free
   uint64_t* drained = q_empty + 1;                     // per MMA warp: every MMA it issued is done
   uint64_t* turn = drained + kTiles;                   // per tile: the other warpgroup has passed it the turn
+  uint64_t* v_land = turn + kTiles;                    // the values of a chunk that holds rows past its sequence have landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
 
   if (tid == 0) {
-    // a stage (and the query tiles) is free once both tiles' MMA warps
-    // have released it
+    // a stage (and the query tiles) is free once both tiles' softmax
+    // warpgroups have released it
     for (int k = 0; k < kStagesK; ++k) {
       mbar_init(&full_k[k], 1);
       mbar_init(&empty_k[k], kTiles);
@@ -198,7 +220,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), kSoftWarps * 32);
+      mbar_init(p_full(t), kSoftWarps);  // one arrival per warp
       mbar_init(o_final(t), 1);
       mbar_init(q_full(t), 1);
     }
@@ -207,9 +229,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       mbar_init(drained + t, 1);
       mbar_init(turn + t, kSoftWarps);
     }
+    mbar_init(v_land, 1);
     *abort = 0;
     fence_barrier_init();
   }
+  // Value rows that no copy writes must still be finite (their weights are
+  // exact zeros, and 0 x NaN is NaN): the value ring starts as zeros, and
+  // rows past a sequence's end are cleared after their copy lands.
+  for (int u = tid; u < kStagesV * kKVStage / 16; u += kThreadsT)
+    reinterpret_cast<uint4*>(base + kOffV)[u] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();  // before any copy into the ring
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tslot)),
                  "r"(kTmemCols));
@@ -220,240 +249,242 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == kProducerWarp || warp == kProducerWarp + 1) {
-    // One warp streams the keys, the next the values, each into its own
-    // ring, so neither waits behind the other's release.  Lane b loads
-    // block b of a chunk; block-table entries are fetched 32 at a time, one
-    // per lane, a window ahead, so no TMA issue waits on a dependent load.
-    // The key warp also loads each item's query tiles, once the previous
-    // item's last S has completed.
-    const int kv = warp - kProducerWarp;  // 0 keys, 1 values
-    const int bpc = kN / p.B;             // blocks per chunk (block sizes 8, 16, 32: 16, 8 or 4, dividing 32)
-    // The other pairs of the same sequence and KV head read the same keys
-    // and values: keep them in L2.
-    const uint64_t policy = policy_evict_last();
-    const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
-    uint64_t* fulls = kv == 0 ? full_k : full_v;
-    uint64_t* empties = kv == 0 ? empty_k : empty_v;
-    const int stages = kv == 0 ? kStagesK : kStagesV;
-    uint32_t k = 0;                // chunks issued into this ring over the CTA's items
-    uint32_t qi = 0, qn[kTiles] = {0, 0};  // items whose query tiles were issued; loads per tile
-    bool waited = false, ok = true;
-    for (int r = 0; ok; ++r) {
-      const int j = pf_item_index(r, b, G);
-      if (j >= num_items) break;
-      const PfItem it = pf_item(p, j, pairs);
-      if (it.state) continue;
-      if (kv == 0) {
-        // The query tiles (an input the append does not write), one box per
-        // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past
-        // the sequence read the next sequence's queries (or zeros past the
-        // last token); their scores are all masked and their rows never stored.
-        int okq = 1;
-        if (lane == 0) {
-          if (qi > 0) okq = mbar_wait(q_empty, (qi - 1) & 1, abort);
-          if (okq) {
-            const uint64_t qpol = policy_evict_first();
-#pragma unroll 1
-            for (int t = 0; t < kTiles; ++t) {
-              const int z = it.q0 + (it.row00 + t * kM) / p.g;
-              mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
-#pragma unroll
-              for (int h = 0; h < C::kHalves; ++h)
-                tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, it.kvh * p.g, z, qpol);
-              ++qn[t];
-            }
-            // The next item's query tiles into L2, so that their load at the
-            // item boundary does not wait on HBM.
-            const int jn = pf_item_index(r + 1, b, G);
-            if (jn < num_items) {
-              const PfItem nx = pf_item(p, jn, pairs);
-              if (!nx.state)
-                for (int t = 0; t < kTiles; ++t) {
-                  const int z = nx.q0 + (nx.row00 + t * kM) / p.g;
-                  for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(&qmap, 64 * h, nx.kvh * p.g, z);
-                }
-            }
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, okq, 0)) {
-          ok = false;
-          break;
-        }
-        ++qi;
-      }
-      if (!waited) {
-        pdl_wait_primary();  // the prompts' keys and values are in the cache from here on
-        waited = true;
-      }
-      const int32_t* row = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
-      const int nblk = (it.t_end + p.B - 1) / p.B;
-      int cur = load_block_id(row, lane, nblk);
-      int nxt = load_block_id(row, 32 + lane, nblk);
-      int wbase = 0;
-      for (int c = 0; c < it.nch; ++c, ++k) {
-        const int jb = c * bpc;
-        if (jb >= wbase + 32) {
-          cur = nxt;
-          wbase += 32;
-          nxt = load_block_id(row, wbase + 32 + lane, nblk);
-        }
-        int id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
-        const int nb = (min(kN, it.t_end - c * kN) + p.B - 1) / p.B;
-        if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
-          raise_status(p.status, PA_STATUS_BAD_BLOCK);
-          id = 0;
-        }
-        const int st = (int)(k % (uint32_t)stages);
-        int okc = 1;
-        if (lane == 0) {
-          okc = mbar_wait(&empties[st], ((k / stages) & 1) ^ 1, abort);
-          if (okc) mbar_arrive_expect_tx(&fulls[st], (uint32_t)(nb * p.B * 128 * C::kHalves));
-        }
-        if (!__shfl_sync(0xffffffffu, okc, 0)) {
-          ok = false;
-          break;
-        }
-        __syncwarp();  // the expected byte count is set before any copy can land
-        if (lane < nb) {
-          const int y = (id * p.Hkv + it.kvh) * p.B;
-          uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) tma_load_2d(d + h * kKVHalf, map, &fulls[st], 64 * h, y, policy);
-        }
-      }
-    }
-    if (!ok) {
-      if (lane == 0) {
-        *abort = 1;
-        raise_status(p.status, PA_STATUS_TIMEOUT);
-        // Let copies already issued land before the CTA's shared memory goes away.
-        const volatile int never = 0;
-        for (uint32_t c = (k > (uint32_t)stages ? k - stages : 0); c < k; ++c)
-          mbar_wait(&fulls[c % stages], (c / stages) & 1, &never);
-        for (int t = 0; t < kTiles; ++t)
-          if (qn[t] > 0) mbar_wait(q_full(t), (qn[t] - 1) & 1, &never);
-      }
-      __syncwarp();
-    }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    // MMA warp of tile t: one thread issues the tile's MMAs in a fixed
-    // order, waiting for one barrier at a time: per item S(0), then per
-    // chunk c P·V(c) as soon as P(c) is in and right behind it S(c + 1).
-    // One thread issues at most about one tcgen05.mma every 64 cycles, about
-    // the time an M 128 N 128 K 16 MMA takes, so each tile has its own
-    // issuing warp and the tensor cores interleave the two tiles' work: one
-    // tile's products run while the other tile's softmax does.  The tile's
-    // MMAs run in issue order: S(c + 1) overwrites P(c) only after P·V(c)
-    // has read it, and the commit that releases S(c + 1) to the softmax also
-    // covers P·V(c), so the softmax may rescale O at once.  The first P·V of
-    // an item overwrites O without a barrier of its own: it waits for P(0),
-    // which the warpgroup writes only after it has read the previous item's
-    // O.  Both tiles attend every chunk of the item (keys past a row's
-    // position are masked), so the stage releases are symmetric: a commit
-    // from each tile's warp after its last MMA that reads the stage (values
-    // right after P·V, keys after S), and one after its item's last S for
-    // the query tiles.
-    const int t = warp - kMmaWarp;
-    const uint32_t id_s = instr_desc(kM, kN, false);
-    const uint32_t id_o = instr_desc(kM, DH, true);
-    bool ok = true;
-    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
-      int r = 1;
-      if (lane == 0) r = mbar_spin(bar, parity, abort);
-      ok = ok && __shfl_sync(0xffffffffu, r, 0);
-      return ok;
-    };
-    // Descriptors are built once per group; a k-step adds its byte offset
-    // / 16 to the address field (every shared address is below 256 KB, so
-    // the 14-bit field never carries).
-    const uint64_t a_q = smem_desc(sbase + t * kQTile, 16, 1024);
-    const uint32_t s_cols = tmem + kColS + (uint32_t)t * 128;
-    const uint32_t o_cols = tmem + kColO + (uint32_t)t * DH;
-    auto issue_s = [&](int kst) {  // lane 0; the keys in stage kst have landed
-      tc_fence_after();
-      const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < DH / 16; ++kk) {
-        const int hlf = kk >> 2, w = kk & 3;
-        mma_ss(s_cols, a_q + (uint64_t)((hlf * kQHalf + w * 32) >> 4), b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4),
-               id_s, kk > 0);
-      }
-      mma_commit(s_full(t));
-    };
-    auto issue_pv = [&](int vst, bool acc) {  // lane 0; P and the values in stage vst are in
-      tc_fence_after();
-      const uint64_t b0 = smem_desc(sbase + kOffV + vst * kKVStage, kKVHalf, 1024);
-#pragma unroll
-      for (int kk = 0; kk < kN / 16; ++kk)
-        mma_ts(o_cols, s_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, acc || kk > 0);
-    };
-    uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
-    for (int r = 0; ok; ++r) {
-      const int j = pf_item_index(r, b, G);
-      if (j >= num_items) break;
-      const PfItem it = pf_item(p, j, pairs);
-      if (it.state) continue;
-      if (!wait_bar(q_full(t), nit & 1)) break;
-      if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
-      if (lane == 0) {
-        issue_s((int)(kq % kStagesK));
-        mma_commit(&empty_k[kq % kStagesK]);
-        if (it.nch == 1) mma_commit(q_empty);
-      }
-      __syncwarp();
-      ++kq;
-      for (int c = 0; c < it.nch; ++c) {
-        const int vst = (int)(vq % kStagesV);
-        if (!wait_bar(&full_v[vst], (vq / kStagesV) & 1)) break;
-        const int nv = min(kN, it.t_end - c * kN);
-        if (nv < kN) {
-          // Value rows past the pair's keys: zeros (their keys are masked).
-          // Both tiles' warps write the same zeros; each orders its own
-          // writes before its own P·V.
-          uint8_t* vs = base + kOffV + vst * kKVStage;
-          for (int u = lane; u < (kN - nv) * 8 * C::kHalves; u += 32) {
-            const int hlf = u / ((kN - nv) * 8), rem = u % ((kN - nv) * 8);
-            *reinterpret_cast<uint4*>(vs + hlf * kKVHalf + (nv + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (!wait_bar(p_full(t), sp & 1)) break;
-        ++sp;
-        if (lane == 0) {
-          issue_pv(vst, c > 0);
-          if (c + 1 == it.nch) mma_commit(o_final(t));
-          mma_commit(&empty_v[vst]);
-        }
-        __syncwarp();
-        ++vq;
-        if (c + 1 < it.nch) {
-          if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
+  if (warp >= kProducerWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsAux));
+    if (warp < kMmaWarp) {
+      // One warp streams the keys, the next the values, each into its own
+      // ring, so neither waits behind the other's release.  Lane b loads
+      // block b of a chunk; block-table entries are fetched 32 at a time, one
+      // per lane, a window ahead, so no TMA issue waits on a dependent load.
+      // The key warp also loads each item's query tiles, once the previous
+      // item's last S has completed.
+      const int kv = warp - kProducerWarp;  // 0 keys, 1 values
+      const int bpc = kN / p.B;             // blocks per chunk (block sizes 8, 16, 32: 16, 8 or 4, dividing 32)
+      // The other pairs of the same sequence and KV head read the same keys
+      // and values: keep them in L2.
+      const uint64_t policy = policy_evict_last();
+      const CUtensorMap* map = kv == 0 ? &kmap : &vmap;
+      uint64_t* fulls = kv == 0 ? full_k : full_v;
+      uint64_t* empties = kv == 0 ? empty_k : empty_v;
+      const int stages = kv == 0 ? kStagesK : kStagesV;
+      uint32_t k = 0;                // chunks issued into this ring over the CTA's items
+      uint32_t qi = 0, qn[kTiles] = {0, 0};  // items whose query tiles were issued; loads per tile
+      uint32_t vl = 0;               // chunks of values cleared past their sequence's end
+      bool waited = false, ok = true, landing = false;
+      for (int r = 0; ok; ++r) {
+        const int j = pf_item_index(r, b, G);
+        if (j >= num_items) break;
+        const PfItem it = pf_item(p, j, pairs);
+        if (it.state) continue;
+        if (kv == 0) {
+          // The query tiles (an input the append does not write), one box per
+          // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past
+          // the sequence read the next sequence's queries (or zeros past the
+          // last token); their scores are all masked and their rows never stored.
+          int okq = 1;
           if (lane == 0) {
-            issue_s((int)(kq % kStagesK));
-            mma_commit(&empty_k[kq % kStagesK]);
-            if (c + 2 == it.nch) mma_commit(q_empty);
+            if (qi > 0) okq = mbar_wait(q_empty, (qi - 1) & 1, abort);
+            if (okq) {
+              const uint64_t qpol = policy_evict_first();
+#pragma unroll 1
+              for (int t = 0; t < kTiles; ++t) {
+                const int z = it.q0 + (it.row00 + t * kM) / p.g;
+                mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
+#pragma unroll
+                for (int h = 0; h < C::kHalves; ++h)
+                  tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, it.kvh * p.g, z, qpol);
+                ++qn[t];
+              }
+              // The next item's query tiles into L2, so that their load at the
+              // item boundary does not wait on HBM.
+              const int jn = pf_item_index(r + 1, b, G);
+              if (jn < num_items) {
+                const PfItem nx = pf_item(p, jn, pairs);
+                if (!nx.state)
+                  for (int t = 0; t < kTiles; ++t) {
+                    const int z = nx.q0 + (nx.row00 + t * kM) / p.g;
+                    for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(&qmap, 64 * h, nx.kvh * p.g, z);
+                  }
+              }
+            }
           }
-          __syncwarp();
-          ++kq;
+          if (!__shfl_sync(0xffffffffu, okq, 0)) {
+            ok = false;
+            break;
+          }
+          ++qi;
+        }
+        if (!waited) {
+          pdl_wait_primary();  // the prompts' keys and values are in the cache from here on
+          waited = true;
+        }
+        const int32_t* row = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+        const int nblk = (it.t_end + p.B - 1) / p.B;
+        int cur = load_block_id(row, lane, nblk);
+        int nxt = load_block_id(row, 32 + lane, nblk);
+        int wbase = 0;
+        for (int c = 0; c < it.nch; ++c, ++k) {
+          const int jb = c * bpc;
+          if (jb >= wbase + 32) {
+            cur = nxt;
+            wbase += 32;
+            nxt = load_block_id(row, wbase + 32 + lane, nblk);
+          }
+          int id = __shfl_sync(0xffffffffu, cur, (jb - wbase + lane) & 31);
+          const int nb = (min(kN, it.t_end - c * kN) + p.B - 1) / p.B;
+          if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
+            raise_status(p.status, PA_STATUS_BAD_BLOCK);
+            id = 0;
+          }
+          const int st = (int)(k % (uint32_t)stages);
+          // A chunk of values whose last block runs past the sequence's end
+          // (stage rows z0 .. z1 - 1): its copies signal v_land instead, the
+          // rows past the end are cleared once they have landed, and a plain
+          // arrival then releases the chunk to the MMA warps.
+          const int z0 = it.ctx - c * kN, z1 = nb * p.B;
+          const bool clear = kv == 1 && z0 < z1;
+          uint64_t* land = clear ? v_land : &fulls[st];
+          int okc = 1;
+          if (lane == 0) {
+            okc = mbar_wait(&empties[st], ((k / stages) & 1) ^ 1, abort);
+            if (okc) mbar_arrive_expect_tx(land, (uint32_t)(nb * p.B * 128 * C::kHalves));
+          }
+          if (!__shfl_sync(0xffffffffu, okc, 0)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();  // the expected byte count is set before any copy can land
+          if (lane < nb) {
+            const int y = (id * p.Hkv + it.kvh) * p.B;
+            uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) tma_load_2d(d + h * kKVHalf, map, land, 64 * h, y, policy);
+          }
+          if (clear) {
+            int okl = 1;
+            if (lane == 0) okl = mbar_wait(v_land, vl & 1, abort);
+            ++vl;
+            if (!__shfl_sync(0xffffffffu, okl, 0)) {
+              ok = false;
+              landing = true;
+              break;
+            }
+            uint8_t* vs = base + kOffV + st * kKVStage;
+            const int units = (z1 - z0) * 8;  // 16-byte units past the end, per 64-dim half
+            for (int u = lane; u < units * C::kHalves; u += 32) {
+              const int h = u / units, rem = u % units;
+              *reinterpret_cast<uint4*>(vs + h * kKVHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();  // the zeros before the tensor cores' reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&fulls[st]);
+          }
         }
       }
-      ++nit;
+      if (!ok) {
+        if (lane == 0) {
+          *abort = 1;
+          raise_status(p.status, PA_STATUS_TIMEOUT);
+          // Let copies already issued land before the CTA's shared memory goes away.
+          const volatile int never = 0;
+          for (uint32_t c = (k > (uint32_t)stages ? k - stages : 0); c < k; ++c)
+            mbar_wait(&fulls[c % stages], (c / stages) & 1, &never);
+          if (landing) mbar_wait(v_land, (vl - 1) & 1, &never);
+          for (int t = 0; t < kTiles; ++t)
+            if (qn[t] > 0) mbar_wait(q_full(t), (qn[t] - 1) & 1, &never);
+        }
+        __syncwarp();
+      }
+    } else {
+      // MMA warp of tile t: its lane 0 alone issues the tile's MMAs in a
+      // fixed order, waiting for one barrier at a time: per item S(0), then
+      // per chunk c P·V(c) as soon as P(c) is in and right behind it S(c + 1).
+      // The other lanes have nothing to do: a warp-wide synchronisation right
+      // after a group of MMAs waited for the group to be taken by the tensor
+      // cores, several hundred cycles on the tile's critical path.  One thread
+      // issues at most about one tcgen05.mma every 64 cycles, about the time
+      // an M 128 N 128 K 16 MMA takes, so each tile has its own issuing warp
+      // and the tensor cores interleave the two tiles' work: one tile's
+      // products run while the other tile's softmax does.  The tile's MMAs
+      // run in issue order: S(c + 1) overwrites P(c) only after P·V(c) has
+      // read it, and the commit that releases S(c + 1) to the softmax also
+      // covers P·V(c), so the softmax may rescale O at once (and releases the
+      // stages).  The first P·V of an item overwrites O without a barrier of
+      // its own: it waits for P(0), which the warpgroup writes only after it
+      // has read the previous item's O.  Value rows past the pair's keys need
+      // no clearing here: their weights are exact zeros and the rows hold
+      // finite values (see the value producer).
+      if (lane == 0) {
+        const int t = warp - kMmaWarp;
+        const uint32_t id_s = instr_desc(kM, kN, false);
+        const uint32_t id_o = instr_desc(kM, DH, true);
+        bool ok = true;
+        auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+          ok = ok && mbar_spin(bar, parity, abort);
+          return ok;
+        };
+        // Descriptors are built once per group; a k-step adds its byte offset
+        // / 16 to the address field (every shared address is below 256 KB, so
+        // the 14-bit field never carries).
+        const uint64_t a_q = smem_desc(sbase + t * kQTile, 16, 1024);
+        const uint32_t s_cols = tmem + kColS + (uint32_t)t * 128;
+        const uint32_t o_cols = tmem + kColO + (uint32_t)t * DH;
+        auto issue_s = [&](int kst) {  // the keys in stage kst have landed
+          tc_fence_after();
+          const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const int hlf = kk >> 2, w = kk & 3;
+            mma_ss(s_cols, a_q + (uint64_t)((hlf * kQHalf + w * 32) >> 4),
+                   b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4), id_s, kk > 0);
+          }
+          mma_commit(s_full(t));
+        };
+        auto issue_pv = [&](int vst, bool acc) {  // P and the values in stage vst are in
+          tc_fence_after();
+          const uint64_t b0 = smem_desc(sbase + kOffV + vst * kKVStage, kKVHalf, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kN / 16; ++kk)
+            mma_ts(o_cols, s_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, acc || kk > 0);
+        };
+        uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
+        for (int r = 0; ok; ++r) {
+          const int j = pf_item_index(r, b, G);
+          if (j >= num_items) break;
+          const PfItem it = pf_item(p, j, pairs);
+          if (it.state) continue;
+          if (!wait_bar(q_full(t), nit & 1)) break;
+          if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
+          issue_s((int)(kq % kStagesK));
+          ++kq;
+          for (int c = 0; c < it.nch; ++c) {
+            const int vst = (int)(vq % kStagesV);
+            if (!wait_bar(&full_v[vst], (vq / kStagesV) & 1)) break;
+            if (!wait_bar(p_full(t), sp & 1)) break;
+            ++sp;
+            issue_pv(vst, c > 0);
+            if (c + 1 == it.nch) mma_commit(o_final(t));
+            ++vq;
+            if (c + 1 < it.nch) {
+              if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
+              issue_s((int)(kq % kStagesK));
+              ++kq;
+            }
+          }
+          ++nit;
+        }
+        if (!ok) {
+          *abort = 1;
+          raise_status(p.status, PA_STATUS_TIMEOUT);
+        }
+        // Every MMA this thread issued has completed before tensor memory is released.
+        mma_commit(drained + t);
+        const volatile int never = 0;
+        mbar_wait(drained + t, 0, &never);
+      }
     }
-    if (!ok) {
-      *abort = 1;
-      raise_status(p.status, PA_STATUS_TIMEOUT);
-    }
-    // Every MMA this warp issued has completed before tensor memory is released.
-    if (lane == 0) {
-      mma_commit(drained + t);
-      const volatile int never = 0;
-      mbar_wait(drained + t, 0, &never);
-    }
-    __syncwarp();
-  } else if (warp < kProducerWarp) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
     // softmax warpgroup t: thread lt owns row lt of its tile (tensor-memory lane lt)
     const int t = warp / kSoftWarps, lt = tid - t * kM;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
@@ -481,6 +512,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(s_full(t), sc_n & 1, abort))) {
           ok = false;
           break;
+        }
+        // S(c) is done, so this tile is done with the stage of keys it
+        // read, and with the values of chunk c - 1: the commit that
+        // signalled S(c) also covers the P·V(c - 1) issued before it.  After
+        // the item's last S the query tiles are free too.
+        if (lt == 0) {
+          mbar_arrive(&empty_k[sc_n % kStagesK]);
+          if (c > 0) mbar_arrive(&empty_v[(sc_n - 1) % kStagesV]);
+          if (c + 1 == nch_t) mbar_arrive(q_empty);
         }
         // Strict turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk
         // k + 1, ...: one warpgroup's softmax runs while the other tile's
@@ -552,11 +592,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           tmem_st16(s_cols + 16 * i, w);  // P over the first 64 columns of its S
         }
         l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+        // tcgen05.st and its wait are warp-wide: once the wait returns, the
+        // warp's P is in tensor memory, and one arrival speaks for the warp.
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
-        mbar_arrive(p_full(t));
         __syncwarp();
-        if (lane == 0) mbar_arrive(turn + (1 - t));  // the other tile's turn
+        if (lane == 0) {
+          mbar_arrive(p_full(t));
+          mbar_arrive(turn + (1 - t));  // the other tile's turn
+        }
       }
       if (!ok) break;
       if (!__all_sync(0xffffffffu, mbar_wait(o_final(t), ot & 1, abort))) {
@@ -564,6 +608,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         break;
       }
       ++ot;
+      if (lt == 0) mbar_arrive(&empty_v[(sc_n - 1) % kStagesV]);  // the item's last P·V is done
       // Read the row of O (all loads in flight at once).  The next item's
       // first P·V overwrites it only after this warpgroup's next P(0),
       // which comes after these loads have completed.
@@ -616,6 +661,11 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
   std::call_once(once[dev], [&] {
     init_err = cudaFuncSetAttribute(prefill_tc_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBytes);
     if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    // The kernel's register split assumes kRegsLaunch registers a thread at
+    // launch: with fewer, its setmaxnreg.inc could never be granted.
+    cudaFuncAttributes fa{};
+    if (init_err == cudaSuccess) init_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<DH>);
+    if (init_err == cudaSuccess && fa.numRegs != kRegsLaunch) init_err = cudaErrorInvalidConfiguration;
   });
   if (init_err != cudaSuccess) return init_err;
   if (sms[dev] < 1) return cudaErrorInvalidConfiguration;

@@ -112,6 +112,31 @@ int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, 
   return PA_OK;
 }
 
+// The cache [N_blk][Hkv][B][D] bf16 for the tcgen05 prefill, as 4D
+// (64 dims, 8 rows, 64-dim half, group of 8 rows): a box of (64, 8, D / 64,
+// B / 8) brings one block of one head in one copy and lands as groups of 8
+// rows, each group holding its halves 1 KB apart ([group][half][8 rows]
+// [128 B], 128-byte swizzle), so 8-row groups are a uniform D / 64 KB apart:
+// the layout of a K-major operand of the tensor cores (keys) and of an
+// MN-major one (values).  Two 2D boxes per block (one per half) were half as
+// large, and a chunk of 128 keys and values was 32 boxes: more than the
+// TMA unit issues in the time the tensor cores take for the chunk.
+int make_block_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D) {
+  auto fn = encode_fn();
+  if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t groups = (cuuint64_t)num_blocks * Hkv * B / 8;
+  const cuuint32_t halves = (cuuint32_t)(D / 64);
+  cuuint64_t dims[4] = {64u, 8u, halves, groups};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2u, 128u, (cuuint64_t)D * 16u};
+  cuuint32_t box[4] = {64u, 8u, halves, (cuuint32_t)(B / 8)};
+  cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                  elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (block map)");
+  return PA_OK;
+}
+
 // Query rows of one KV head for the tcgen05 prefill: q [T][H][D] bf16 as a
 // 3D tensor (dims, head, token); a box of 64 dims x g heads x 128 / g tokens
 // lands as 128 rows of 128 bytes, row = token * g + head, 128-byte swizzle.
@@ -529,9 +554,9 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
   // 5th-generation tensor cores (tcgen05) for head_dim 64 and 128
   CUtensorMap kmap, vmap, qmap;
-  rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
+  rc = make_block_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
   if (rc) return rc;
-  rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, false);
+  rc = make_block_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
   if (rc) return rc;
   rc = make_query_map(&qmap, q, num_tokens, num_heads, g, head_dim);
   if (rc) return rc;

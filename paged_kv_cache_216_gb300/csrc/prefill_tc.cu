@@ -20,9 +20,11 @@
 //    of each item, 128 tokens per stage, into rings of their own (2 stages
 //    of keys, 3 of values: values are needed a softmax later than keys)
 //    that run on across items, with an L2 policy that keeps them for the
-//    other pairs of the same sequence and head, as 2D TMA boxes of
-//    [B tokens x 64 dims] with 128-byte swizzle (the K-major UMMA layout),
-//    after griddepcontrol.wait; lane b issues block b of a chunk from
+//    other pairs of the same sequence and head, one TMA box per block
+//    (a 4D view of the cache: groups of 8 rows with both 64-dim halves,
+//    128-byte swizzle, which is the layout of a K-major operand of the
+//    tensor cores for keys and of an MN-major one for values), after
+//    griddepcontrol.wait; lane b issues block b of a chunk from
 //    block-table entries fetched 32 at a time.  Warp 8 first loads the
 //    item's query tiles, one 3D box per 64-dim half, once the previous
 //    item's last S has completed, and prefetches the next item's into L2.
@@ -105,6 +107,9 @@ static_assert(kProducerWarp % 4 == 0 && kThreadsT - kProducerWarp * 32 == 128,
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQHalf = kM * 128;         // bytes of one 64-dim half of a query tile
 constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage of K (or V)
+// A stage holds its keys (or values) in groups of 8 rows, each group both
+// 64-dim halves, 1 KB apart ([group][half][8 rows][128 B]), so that one TMA
+// box brings a whole block (see kv_row_offset).
 // full_k[], empty_k[], full_v[], empty_v[]; per tile s_full, p_full,
 // o_final, q_full
 constexpr int kTileBars = 4;
@@ -120,8 +125,8 @@ struct PfCfg {
   static constexpr int kOffK = kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
-  // barriers: the rings, kTileBars per tile, q_empty, drained per MMA warp, softmax turn per tile, v_land
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 1 + 2 * kTiles + 1) * 8;  // tensor-memory address, abort flag
+  // barriers: the rings, kTileBars per tile, q_empty, drained and softmax turn per tile, v_land
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 3 * kTiles + 1) * 8;  // tensor-memory address, abort flag
   static constexpr size_t kBytes = 1024 + kOffMisc + 16;
   static constexpr uint32_t kColO = 0, kColS = 2 * DH;
   static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
@@ -129,6 +134,24 @@ struct PfCfg {
   static_assert(kColS + kTiles * 128 <= kTmemCols, "tensor-memory columns");
 };
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
+
+// 4D tiled TMA load of one box (a block of the cache, see the block map of
+// the host side); x is the innermost (element) coordinate.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Byte offset in a stage of keys or values of key row t (within the chunk)
+// and 64-dim half h: 8-row groups kHalves KB apart, halves 1 KB apart.
+template <int kHalves>
+__device__ __forceinline__ int kv_row_offset(int t, int h) {
+  return (t >> 3) * (kHalves * 1024) + h * 1024 + (t & 7) * 128;
+}
 
 // Work item j of S * Hkv * pairs: pair of query tiles pairs - 1 - j / (S * Hkv)
 // (the pairs with the most keys first), sequence (j / Hkv) % S, KV head
@@ -199,8 +222,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   auto p_full = [&](int t) { return tile_bars + t * kTileBars + 1; };
   auto o_final = [&](int t) { return tile_bars + t * kTileBars + 2; };
   auto q_full = [&](int t) { return tile_bars + t * kTileBars + 3; };
-  uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // the item's last S of both tiles is done: the query tiles are free
-  uint64_t* drained = q_empty + 1;                     // per MMA warp: every MMA it issued is done
+  uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // per tile: the item's last S is done, the query tile is free
+  uint64_t* drained = q_empty + kTiles;                // per MMA warp: every MMA it issued is done
   uint64_t* turn = drained + kTiles;                   // per tile: the other warpgroup has passed it the turn
   uint64_t* v_land = turn + kTiles;                    // the values of a chunk that holds rows past its sequence have landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
@@ -224,8 +247,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       mbar_init(o_final(t), 1);
       mbar_init(q_full(t), 1);
     }
-    mbar_init(q_empty, kTiles);
     for (int t = 0; t < kTiles; ++t) {
+      mbar_init(q_empty + t, 1);
       mbar_init(drained + t, 1);
       mbar_init(turn + t, kSoftWarps);
     }
@@ -268,7 +291,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint64_t* empties = kv == 0 ? empty_k : empty_v;
       const int stages = kv == 0 ? kStagesK : kStagesV;
       uint32_t k = 0;                // chunks issued into this ring over the CTA's items
-      uint32_t qi = 0, qn[kTiles] = {0, 0};  // items whose query tiles were issued; loads per tile
+      uint32_t qn[kTiles] = {0, 0};  // query-tile loads per tile
       uint32_t vl = 0;               // chunks of values cleared past their sequence's end
       bool waited = false, ok = true, landing = false;
       for (int r = 0; ok; ++r) {
@@ -276,43 +299,45 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (j >= num_items) break;
         const PfItem it = pf_item(p, j, pairs);
         if (it.state) continue;
-        if (kv == 0) {
-          // The query tiles (an input the append does not write), one box per
-          // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past
-          // the sequence read the next sequence's queries (or zeros past the
-          // last token); their scores are all masked and their rows never stored.
+        // The query tiles (an input the append does not write), one box per
+        // 64-dim half: 128 / g tokens x g heads of this KV head.  Rows past
+        // the sequence read the next sequence's queries (or zeros past the
+        // last token); their scores are all masked and their rows never
+        // stored.  Tile t's is loaded once the tile's last S of the previous
+        // item has completed: tile 0's first, then the item's first keys,
+        // then tile 1's (which runs about half a chunk behind tile 0).
+        auto load_q = [&](int t) {
           int okq = 1;
           if (lane == 0) {
-            if (qi > 0) okq = mbar_wait(q_empty, (qi - 1) & 1, abort);
+            if (qn[t] > 0) okq = mbar_wait(q_empty + t, (qn[t] - 1) & 1, abort);
             if (okq) {
-              const uint64_t qpol = policy_evict_first();
-#pragma unroll 1
-              for (int t = 0; t < kTiles; ++t) {
-                const int z = it.q0 + (it.row00 + t * kM) / p.g;
-                mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
+              const int z = it.q0 + (it.row00 + t * kM) / p.g;
+              mbar_arrive_expect_tx(q_full(t), (uint32_t)kQTile);
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h)
-                  tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, it.kvh * p.g, z, qpol);
-                ++qn[t];
-              }
-              // The next item's query tiles into L2, so that their load at the
-              // item boundary does not wait on HBM.
-              const int jn = pf_item_index(r + 1, b, G);
-              if (jn < num_items) {
-                const PfItem nx = pf_item(p, jn, pairs);
-                if (!nx.state)
-                  for (int t = 0; t < kTiles; ++t) {
-                    const int z = nx.q0 + (nx.row00 + t * kM) / p.g;
-                    for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(&qmap, 64 * h, nx.kvh * p.g, z);
-                  }
-              }
+              for (int h = 0; h < C::kHalves; ++h)
+                tma_load_3d(base + t * kQTile + h * kQHalf, &qmap, q_full(t), 64 * h, it.kvh * p.g, z,
+                            policy_evict_first());
+              ++qn[t];
             }
           }
-          if (!__shfl_sync(0xffffffffu, okq, 0)) {
+          return __shfl_sync(0xffffffffu, okq, 0) != 0;
+        };
+        if (kv == 0) {
+          if (!load_q(0)) {
             ok = false;
             break;
           }
-          ++qi;
+          // The next item's query tiles into L2, so that their loads at the
+          // item boundary do not wait on HBM.
+          const int jn = pf_item_index(r + 1, b, G);
+          if (lane == 0 && jn < num_items) {
+            const PfItem nx = pf_item(p, jn, pairs);
+            if (!nx.state)
+              for (int t = 0; t < kTiles; ++t) {
+                const int z = nx.q0 + (nx.row00 + t * kM) / p.g;
+                for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(&qmap, 64 * h, nx.kvh * p.g, z);
+              }
+          }
         }
         if (!waited) {
           pdl_wait_primary();  // the prompts' keys and values are in the cache from here on
@@ -354,11 +379,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             break;
           }
           __syncwarp();  // the expected byte count is set before any copy can land
-          if (lane < nb) {
-            const int y = (id * p.Hkv + it.kvh) * p.B;
-            uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128;
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h) tma_load_2d(d + h * kKVHalf, map, land, 64 * h, y, policy);
+          if (lane < nb) {  // block `lane` of the chunk: one box of B rows, both halves
+            const int grp = (id * p.Hkv + it.kvh) * (p.B / 8);
+            uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128 * C::kHalves;
+            tma_load_4d(d, map, land, 0, 0, 0, grp, policy);
+          }
+          if (kv == 0 && c == 0 && !load_q(1)) {
+            ok = false;
+            ++k;  // chunk 0's keys were issued
+            break;
           }
           if (clear) {
             int okl = 1;
@@ -373,7 +402,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             const int units = (z1 - z0) * 8;  // 16-byte units past the end, per 64-dim half
             for (int u = lane; u < units * C::kHalves; u += 32) {
               const int h = u / units, rem = u % units;
-              *reinterpret_cast<uint4*>(vs + h * kKVHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vs + kv_row_offset<C::kHalves>(z0 + rem / 8, h) + (rem % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();  // the zeros before the tensor cores' reads
             __syncwarp();
@@ -431,21 +461,24 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         const uint32_t o_cols = tmem + kColO + (uint32_t)t * DH;
         auto issue_s = [&](int kst) {  // the keys in stage kst have landed
           tc_fence_after();
-          const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage, 16, 1024);
+          // keys: K-major, 8-row groups kHalves KB apart, halves 1 KB apart
+          const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage, 16, C::kHalves * 1024);
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
             const int hlf = kk >> 2, w = kk & 3;
             mma_ss(s_cols, a_q + (uint64_t)((hlf * kQHalf + w * 32) >> 4),
-                   b0 + (uint64_t)((hlf * kKVHalf + w * 32) >> 4), id_s, kk > 0);
+                   b0 + (uint64_t)((hlf * 1024 + w * 32) >> 4), id_s, kk > 0);
           }
           mma_commit(s_full(t));
         };
         auto issue_pv = [&](int vst, bool acc) {  // P and the values in stage vst are in
           tc_fence_after();
-          const uint64_t b0 = smem_desc(sbase + kOffV + vst * kKVStage, kKVHalf, 1024);
+          // values: MN-major, the dims' halves 1 KB apart, 8-key groups
+          // kHalves KB apart; a K-step of 16 keys is two groups
+          const uint64_t b0 = smem_desc(sbase + kOffV + vst * kKVStage, 1024, C::kHalves * 1024);
 #pragma unroll
           for (int kk = 0; kk < kN / 16; ++kk)
-            mma_ts(o_cols, s_cols + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), id_o, acc || kk > 0);
+            mma_ts(o_cols, s_cols + kk * 8, b0 + (uint64_t)((kk * 2 * C::kHalves * 1024) >> 4), id_o, acc || kk > 0);
         };
         uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
         for (int r = 0; ok; ++r) {
@@ -462,11 +495,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             if (!wait_bar(&full_v[vst], (vq / kStagesV) & 1)) break;
             if (!wait_bar(p_full(t), sp & 1)) break;
             ++sp;
+            // The next chunk's keys are awaited before any MMA, so that P·V(c)
+            // and S(c + 1) go out back to back: a barrier test right after a
+            // group of MMAs waits for the group to be taken.
+            const bool more = c + 1 < it.nch;
+            if (more && !wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
             issue_pv(vst, c > 0);
-            if (c + 1 == it.nch) mma_commit(o_final(t));
+            if (!more) mma_commit(o_final(t));
             ++vq;
-            if (c + 1 < it.nch) {
-              if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
+            if (more) {
               issue_s((int)(kq % kStagesK));
               ++kq;
             }
@@ -520,7 +557,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (lt == 0) {
           mbar_arrive(&empty_k[sc_n % kStagesK]);
           if (c > 0) mbar_arrive(&empty_v[(sc_n - 1) % kStagesV]);
-          if (c + 1 == nch_t) mbar_arrive(q_empty);
+          if (c + 1 == nch_t) mbar_arrive(q_empty + t);
         }
         // Strict turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk
         // k + 1, ...: one warpgroup's softmax runs while the other tile's

@@ -93,6 +93,31 @@ def test_prefill_matches_oracle(pa, name):
     assert pa.get_status() == 0
 
 
+def _poison_past_context(b, B):
+    """Rows of each sequence's last block past its context hold NaN (keys)
+    and +Inf (values), as rows never written may: masked keys must not let
+    them into any output."""
+    for s, ctx in enumerate(b["ctx"]):
+        if ctx % B:
+            blk = b["tables"][s, (int(ctx) - 1) // B]
+            b["kc"][blk, :, ctx % B:, :] = 0x7FC0  # bf16 NaN
+            b["vc"][blk, :, ctx % B:, :] = 0x7F80  # bf16 +Inf
+
+
+@pytest.mark.parametrize("name", ["g4_d128_b16", "g8_d128_b8", "g1_d64_b32", "g4_d64_b8", "g2_long_prompt"])
+def test_prefill_ignores_non_finite_rows_past_the_context(pa, name):
+    prev, new, H, Hkv, D, B = CASES[name]
+    b = _batch(sum(new) + 3 * len(prev), prev, new, H, Hkv, D, B)
+    _poison_past_context(b, B)
+    out, kc, vc = _run(pa, b)
+    kc_o, vc_o, ref = oracle_prefill(b["q"], b["k"], b["v"], b["slots"], b["qs"], b["ctx"], b["tables"], b["kc"],
+                                     b["vc"], b["scale"], "bf16")
+    assert np.array_equal(to_bits(kc), kc_o) and np.array_equal(to_bits(vc), vc_o)
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    assert_close(out, ref, "bf16", name + " with non-finite rows past the context")
+    assert pa.get_status() == 0
+
+
 def test_prefill_of_one_token_per_sequence_is_decode(pa):
     """n_s = 1 everywhere: the rows equal paged decode over the appended
     cache (both within tolerance of the same oracle values)."""

@@ -8,24 +8,25 @@ epilogue touches it.
 A CTA works through a list of items, each a pair of query tiles attending
 the same chunks of keys (nch = the longer tile's count; the shorter tile's
 extra keys are masked).  The model follows the kernel's roles and order:
-  * a key producer: per item, once the previous item's last S of both tiles
-    has completed (q_empty), both query tiles; then the keys of every chunk
-    into ring stage k % 2 (k counting chunks over the CTA's items) once both
-    tiles have released the stage's previous chunk;
+  * a key producer: per item, query tile 0 once tile 0's last S of the
+    previous item has completed (q_empty_0), the keys of the first chunk,
+    query tile 1 likewise (q_empty_1), then the keys of the other chunks;
+    keys of chunk k (counting over the CTA's items) go into ring stage k % 2
+    once both tiles have released the stage's previous chunk;
   * a value producer: the values of chunk k into stage k % 3 likewise; for
     a chunk that holds rows past its sequence's end, the copy signals
     v_land, the producer waits for it, clears those rows and then arrives
     on the stage's full barrier itself;
-  * one MMA thread per tile: per item S_t(0), then per chunk c P·V_t(c) once
-    P_t(c) is in, then S_t(c+1); a commit signals S_t(c) (it arrives when
+  * one MMA thread per tile: per item S_t(0), then per chunk c, once P_t(c)
+    and the keys of chunk c + 1 are in, P·V_t(c) and S_t(c+1); a commit signals S_t(c) (it arrives when
     every MMA the thread issued before it is done, so it also covers
     P·V_t(c-1)) and, after the item's last P·V, o_final.  The first P·V of an
     item overwrites O_t without a barrier of its own: it waits for P_t(0),
     which the warpgroup writes only after it has read the previous item's
     O_t (the model checks that it has);
   * per tile a softmax warpgroup: wait for S_t(c); release the keys of chunk
-    c, the values of chunk c - 1 and, after the item's last S, the query
-    tiles (one arrival per tile); wait for its turn (the two warpgroups take
+    c, the values of chunk c - 1 and, after the item's last S, its query
+    tile (one arrival per tile); wait for its turn (the two warpgroups take
     strict turns, tile 0's chunk k before tile 1's chunk k before tile 0's
     chunk k + 1); rescale O_t (the commit that signalled S_t(c) covers
     P·V_t(c-1)), write P_t(c) over S_t, arrive (one arrival per warp), pass
@@ -65,7 +66,7 @@ class Sim(EventSim):
         self.p_full = [Bar(f"p_full{t}", 4) for t in range(2)]
         self.o_final = [Bar(f"o_final{t}", 1) for t in range(2)]
         self.q_full = [Bar(f"q_full{t}", 1) for t in range(2)]
-        self.q_empty = Bar("q_empty", 2)
+        self.q_empty = [Bar(f"q_empty{t}", 1) for t in range(2)]
         # softmax turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk k + 1, ...
         self.turn = [Bar(f"turn{t}", 4) for t in range(2)]
         # buffer contents, tagged (item, chunk)
@@ -97,16 +98,19 @@ class Sim(EventSim):
         self.pipe(0.0, lambda: None, lambda: self.arrive(bar))
 
     # --- roles ---
+    def load_q(self, i, t):
+        if i > 0 and self.mutate != "no_q_empty_wait":
+            yield ("wait", self.q_empty[t], (i - 1) & 1, i, f"key producer q_empty{t} item {i}")
+        self.expect_tx(self.q_full[t], 2)
+        self.copy(self.q_full[t], 2, lambda t=t, i=i: self.q_tile.__setitem__(t, i))
+
     def key_producer(self):
-        k, qi = 0, 0
+        k = 0
         for i, nch in enumerate(self.items):
-            if qi > 0 and self.mutate != "no_q_empty_wait":
-                yield ("wait", self.q_empty, (qi - 1) & 1, qi, f"key producer q_empty item {i}")
-            for t in range(2):
-                self.expect_tx(self.q_full[t], 2)
-                self.copy(self.q_full[t], 2, lambda t=t, i=i: self.q_tile.__setitem__(t, i))
-            qi += 1
+            yield from self.load_q(i, 0)
             for c in range(max(nch)):
+                if c == 1:
+                    yield from self.load_q(i, 1)
                 st = k % K_STAGES
                 flip = 0 if self.mutate == "producer_parity" else 1
                 yield ("wait", self.empty_k[st], ((k // K_STAGES) & 1) ^ flip, k // K_STAGES, f"key producer {i}.{c}")
@@ -116,6 +120,8 @@ class Sim(EventSim):
                 self.copy(self.full_k[st], 1, lambda st=st, tag=(i, c): self.k_stage.__setitem__(st, tag))
                 k += 1
                 yield ("delay", self.rng.uniform(0.0, 0.5))
+            if max(nch) == 1:
+                yield from self.load_q(i, 1)
         self.done.add("kp")
 
     def value_producer(self):
@@ -204,9 +210,10 @@ class Sim(EventSim):
                 yield ("wait", self.full_v[vst], (vq // V_STAGES) & 1, vq // V_STAGES + 1, f"mma{t} v {i}.{c}")
                 yield ("wait", self.p_full[t], sp & 1, sp + 1, f"mma{t} p {i}.{c}")
                 sp += 1
-                if self.mutate == "s_before_pv" and c + 1 < n:
+                if c + 1 < n:
                     yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1,
                            f"mma{t} k {i}.{c + 1}")
+                if self.mutate == "s_before_pv" and c + 1 < n:
                     self.issue_s(i, t, c + 1, kq % K_STAGES)
                     self.issue_pv(i, t, c, vst)
                     kq += 1
@@ -215,8 +222,6 @@ class Sim(EventSim):
                 self.issue_pv(i, t, c, vst)
                 vq += 1
                 if c + 1 < n:
-                    yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1,
-                           f"mma{t} k {i}.{c + 1}")
                     self.issue_s(i, t, c + 1, kq % K_STAGES)
                     kq += 1
                 yield ("delay", self.rng.uniform(0.0, 0.3))
@@ -240,7 +245,7 @@ class Sim(EventSim):
                 if c > 0 and not (self.mutate == "v_release_one_tile" and t == 0):
                     self.arrive(self.empty_v[(sc - 1) % V_STAGES])
                 if c + 1 == n:
-                    self.arrive(self.q_empty)
+                    self.arrive(self.q_empty[t])
                 # strict alternation of the two warpgroups' softmax turns
                 if t == 0 and sc > 0:
                     yield ("wait", self.turn[0], (sc - 1) & 1, sc, f"softmax0 turn {i}.{c}")

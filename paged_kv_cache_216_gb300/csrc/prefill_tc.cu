@@ -493,13 +493,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           for (int c = 0; c < it.nch; ++c) {
             const int vst = (int)(vq % kStagesV);
             if (!wait_bar(&full_v[vst], (vq / kStagesV) & 1)) break;
-            if (!wait_bar(p_full(t), sp & 1)) break;
-            ++sp;
-            // The next chunk's keys are awaited before any MMA, so that P·V(c)
-            // and S(c + 1) go out back to back: a barrier test right after a
-            // group of MMAs waits for the group to be taken.
+            // The next chunk's keys are awaited before P(c) and before any
+            // MMA: P·V(c) and S(c + 1) then go out back to back (a barrier
+            // test right after a group of MMAs waits for the group to be
+            // taken), and the test (slow while the tensor cores read shared
+            // memory) overlaps the softmax instead of following it.
             const bool more = c + 1 < it.nch;
             if (more && !wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
+            if (!wait_bar(p_full(t), sp & 1)) break;
+            ++sp;
             issue_pv(vst, c > 0);
             if (!more) mma_commit(o_final(t));
             ++vq;

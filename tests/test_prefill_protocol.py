@@ -17,8 +17,8 @@ extra keys are masked).  The model follows the kernel's roles and order:
     a chunk that holds rows past its sequence's end, the copy signals
     v_land, the producer waits for it, clears those rows and then arrives
     on the stage's full barrier itself;
-  * one MMA thread per tile: per item S_t(0), then per chunk c, once P_t(c)
-    and the keys of chunk c + 1 are in, P·V_t(c) and S_t(c+1); a commit signals S_t(c) (it arrives when
+  * one MMA thread per tile: per item S_t(0), then per chunk c, once the
+    keys of chunk c + 1 and P_t(c) are in, P·V_t(c) and S_t(c+1); a commit signals S_t(c) (it arrives when
     every MMA the thread issued before it is done, so it also covers
     P·V_t(c-1)) and, after the item's last P·V, o_final.  The first P·V of an
     item overwrites O_t without a barrier of its own: it waits for P_t(0),
@@ -208,11 +208,11 @@ class Sim(EventSim):
             for c in range(n):
                 vst = vq % V_STAGES
                 yield ("wait", self.full_v[vst], (vq // V_STAGES) & 1, vq // V_STAGES + 1, f"mma{t} v {i}.{c}")
-                yield ("wait", self.p_full[t], sp & 1, sp + 1, f"mma{t} p {i}.{c}")
-                sp += 1
                 if c + 1 < n:
                     yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1,
                            f"mma{t} k {i}.{c + 1}")
+                yield ("wait", self.p_full[t], sp & 1, sp + 1, f"mma{t} p {i}.{c}")
+                sp += 1
                 if self.mutate == "s_before_pv" and c + 1 < n:
                     self.issue_s(i, t, c + 1, kq % K_STAGES)
                     self.issue_pv(i, t, c, vst)

@@ -63,15 +63,31 @@ DECODE_FP8_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_fp8.cu", "paged_kv_c
                       "paged_kv_cache_216_gb300/csrc/kernels.h")
 
 
-def decode_kernel_hash(sources=DECODE_SOURCES) -> str:
-    """Hash of the decode kernel's sources: DRAM counters taken on another
-    version of the kernel are not reported."""
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string literals
+    are kept whole), so that a comment edit does not count as a kernel
+    change."""
+    import re
+
+    pat = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
+    out = pat.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
+    return "\n".join(line.rstrip() for line in out.splitlines() if line.strip())
+
+
+def decode_kernel_hash(sources=DECODE_SOURCES, read=None) -> str:
+    """Hash of the decode kernel's sources, comments left out: DRAM counters
+    taken on another version of the kernel are not reported.  `read(rel)`
+    may supply a file's text (default: the working tree)."""
     import hashlib
 
     h = hashlib.sha256()
     for rel in sources:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        if read is None:
+            with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(rel)
+        h.update(strip_comments(text).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -163,9 +163,9 @@ struct PrefillArgs {
   int num_blocks, max_blocks_per_seq, max_ctx, max_query_len;
   float scale_log2;
 };
-// Prefill on tcgen05, head_dim 64 or 128: persistent CTAs, one per SM; kmap/vmap: the bf16 cache maps
-// with boxes of [B rows x 64 dims] (not the interleaved form); qmap: q as (dims, head, token) with
-// boxes of [64 dims x g heads x 128 / g tokens].
+// Prefill on tcgen05, head_dim 64 or 128: persistent CTAs, one per SM; kmap/vmap: the bf16 caches as
+// 4D (64 dims, 8 rows, 64-dim half, 8-row group) with boxes of one block (64, 8, D / 64, B / 8); qmap:
+// q as (dims, head, token) with boxes of [64 dims x g heads x 128 / g tokens].
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                               const CUtensorMap& qmap, cudaStream_t stream);
 

@@ -83,3 +83,17 @@ def test_dram_counters_only_for_the_captured_kernel(monkeypatch):
         # another version of the sources: the stored counters are not reported
         monkeypatch.setattr(bench, "DECODE_SOURCES", ("bench.py",))
         assert bench.decode_traffic("mha_bf16") is None
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The hash that gates the committed DRAM counters changes with the code
+    and not with its comments (string literals are code)."""
+    import bench
+
+    a = 'int f() {  // sum\n  /* two\n lines */ return g("a // b");\n}\n'
+    b = 'int f() {\n\n  return g("a // b");  // other words\n}\n'
+    c = 'int f() {\n  return g("a // c");\n}\n'
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    src = {"x": a}
+    assert bench.decode_kernel_hash(("x",), src.get) == bench.decode_kernel_hash(("x",), {"x": b}.get)

@@ -64,14 +64,14 @@ DECODE_FP8_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_fp8.cu", "paged_kv_c
 
 
 def strip_comments(src: str) -> str:
-    """C/C++ source without its comments and blank lines (string literals
-    are kept whole), so that a comment edit does not count as a kernel
-    change."""
+    """C/C++ source without its comments, blank lines and runs of spaces
+    (string literals are kept), so that a comment edit does not count as a
+    kernel change."""
     import re
 
     pat = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
     out = pat.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
-    return "\n".join(line.rstrip() for line in out.splitlines() if line.strip())
+    return "\n".join(" ".join(line.split()) for line in out.splitlines() if line.strip())
 
 
 def decode_kernel_hash(sources=DECODE_SOURCES, read=None) -> str:

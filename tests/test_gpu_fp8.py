@@ -93,6 +93,10 @@ SMALL = {
                                                           ctx_hi=600, steps=0),
     "g2_b32": Workload(name="g2", dtype="bf16", num_seqs=5, num_heads=4, num_kv_heads=2, head_dim=128,
                        block_size=32, seed=61, ctx_lo=1, ctx_hi=800),
+    # 8-token blocks with an odd number of KV heads: one head per work item
+    # (with an even number the kernel takes two heads per item)
+    "odd_hkv_b8": Workload(name="odd", dtype="bf16", num_seqs=5, num_heads=6, num_kv_heads=3, head_dim=128,
+                           block_size=8, seed=62, ctx_lo=1, ctx_hi=700),
 }
 
 
@@ -139,10 +143,10 @@ def test_fp8_context_edges(pa, b, g):
     assert pa.get_status() == 0
 
 
-def test_fp8_nan_codes_past_the_context_are_ignored(pa):
-    w = SMALL["serving_g4_b8"].replace(block_size=16)
+@pytest.mark.parametrize("b", [8, 16])
+def test_fp8_nan_codes_past_the_context_are_ignored(pa, b):
+    w = SMALL["serving_g4_b8"].replace(block_size=b)
     case, kc, vc, k_codes, v_codes = _fp8_case(pa, w)
-    b = w.block_size
     kb, vb = kc.view(torch.uint8), vc.view(torch.uint8)
     for s in range(w.num_seqs):  # NaN codes in the unused rows of every last block
         n = int(case.ctx[s])

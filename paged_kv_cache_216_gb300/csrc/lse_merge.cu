@@ -10,10 +10,11 @@
 //
 // Each (sequence, query head) gets `wpr` warps (8 for contexts of 32 or more
 // partitions, else 1) and a CTA of eight warps serves 8 / wpr of
-// them; warp w of a group folds partitions w, w + wpr, ... into a running
-// (max, sum, O) with online rescaling, lanes holding D/32 consecutive dims
-// so each partial row is one coalesced 4*D-byte line, and the group's warps
-// are combined through shared memory.  Sequences that fit one partition were written by the decode
+// them; warp w of a group takes partitions w, w + wpr, ...: it finds their
+// max and weight sum first (the lanes taking partitions), then sums the
+// weighted partial rows, lanes holding D/32 consecutive dims so each row is
+// one coalesced 4*D-byte line and no row's load waits for another's; the
+// group's warps are combined through shared memory.  Sequences that fit one partition were written by the decode
 // kernel and are skipped, unless they belong to a prefix group: there even a
 // single partition is a partial written by the shared-prefix kernel.  Launched with programmatic dependent launch: the
 // CTAs may start while the decode kernel drains and wait for its results
@@ -55,10 +56,23 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   if (np >= first) {
     const size_t base = (size_t)s * p.max_parts * p.H + h;  // row of partition 0
-#pragma unroll 4
-    for (int pp = wg; pp < np; pp += wpr) {
-      const size_t wi = base + (size_t)pp * p.H;
-      const float2 ml = p.ws_ml[wi];
+    const int cnt = np > wg ? (np - wg + wpr - 1) / wpr : 0;  // this warp's partitions wg, wg + wpr, ...
+    // Their max and weight sum first, the lanes taking partitions: then the
+    // weight of every partial row is known and the rows' loads below do not
+    // wait on one another (a running max would chain them).
+    for (int i = lane; i < cnt; i += 32) m = fmaxf(m, p.ws_ml[base + (size_t)(wg + i * wpr) * p.H].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    for (int i = lane; i < cnt; i += 32) {
+      const float2 ml = p.ws_ml[base + (size_t)(wg + i * wpr) * p.H];
+      l += exp2f(ml.x - m) * ml.y;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll 8
+    for (int i = 0; i < cnt; ++i) {
+      const size_t wi = base + (size_t)(wg + i * wpr) * p.H;
+      const float b = exp2f(p.ws_ml[wi].x - m);
       float x[E];
       if constexpr (E == 4) {
         const float4 v = *reinterpret_cast<const float4*>(p.ws_o + wi * D + lane * E);
@@ -67,12 +81,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
         const float2 v = *reinterpret_cast<const float2*>(p.ws_o + wi * D + lane * E);
         x[0] = v.x, x[1] = v.y;
       }
-      const float mn = fmaxf(m, ml.x);
-      const float a = exp2f(m - mn), b = exp2f(ml.x - mn);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + x[e] * b;
-      l = l * a + ml.y * b;
-      m = mn;
+      for (int e = 0; e < E; ++e) acc[e] += x[e] * b;
     }
   }
   if (wpr > 1) {  // combine the group's warps through shared memory

@@ -306,7 +306,8 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
  * The caller guarantees that the first `prefix` tokens of every member are
  * stored in the same physical blocks, listed in the table of the group's
  * first sequence, and that prefix <= max_context_len.  The whole partitions
- * of the prefix (floor(prefix / P) * P tokens, P the partition size) become
+ * of the prefix (floor(prefix / P) * P tokens, P the partition size, which
+ * for partition_size 0 is pa_decode_partition_size_shared_prefix's) become
  * shared work items of the decode kernel, each attending one partition for
  * several members at once and storing their split-K partials; the members'
  * other partitions are decoded as usual and the log-sum-exp merge combines
@@ -328,6 +329,21 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache,
                             int partition_size, const int32_t* groups,
                             int num_groups, void* workspace,
                             size_t workspace_bytes, int dtype, void* stream);
+
+/*
+ * Partition size that pa_decode_shared_prefix and
+ * pa_decode_planned_shared_prefix use for these sizes and groups: the given
+ * `partition_size` if > 0, else pa_decode_partition_size's choice doubled,
+ * up to 1024 tokens, while every group's prefix still holds a whole
+ * partition (fewer shared items and partials per group).  groups as for
+ * pa_decode_shared_prefix (only the prefix lengths are read here).  Returns
+ * the size, or a negative PA_ERR_* code.
+ */
+int pa_decode_partition_size_shared_prefix(int num_seqs, int num_kv_heads,
+                                           int max_context_len,
+                                           int partition_size,
+                                           const int32_t* groups,
+                                           int num_groups);
 
 /* Host work list for pa_decode_planned_shared_prefix: the list of
  * pa_decode_plan_host with the groups' shared partitions as shared items

@@ -41,6 +41,7 @@ SIGNATURES = {
     "pa_cache_append": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_decode_partition_size": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
+    "pa_decode_partition_size_shared_prefix": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_int]),
     "pa_decode_workspace_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _vp]),

@@ -175,6 +175,9 @@ constexpr int kMinPartition = 64;
 // 173-176 us; narrower batches keep the split for balance.
 constexpr long long kWideBatch = 1024;
 constexpr int kWholeContext = 4096;
+// Calls with prefix groups lengthen the partitions up to this many tokens
+// while each group's prefix still holds a whole partition.
+constexpr int kMaxSharedPartition = 1024;
 
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -326,6 +329,20 @@ int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len
   return P;
 }
 
+int pa_decode_partition_size_shared_prefix(int num_seqs, int num_kv_heads, int max_context_len, int partition_size,
+                                           const int32_t* groups, int num_groups) {
+  int P = pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size);
+  if (P < 0 || partition_size > 0 || num_groups <= 0) return P;
+  if (!groups) return pa_fail(PA_ERR_INVALID, "pa_decode_partition_size_shared_prefix: null groups");
+  // Longer partitions while every group's prefix still holds a whole one:
+  // fewer shared items and partials per group (on a 64-sequence GQA batch
+  // with a 1024-token prefix, 1024 gave 115.6 us against 118.4 us at 512).
+  int shortest = max_context_len;
+  for (int i = 0; i < num_groups; ++i) shortest = std::min(shortest, std::max(groups[3 * i + 2], 0));
+  while (P < kMaxSharedPartition && 2 * P <= shortest) P *= 2;
+  return P;
+}
+
 size_t pa_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                  int partition_size) {
   WsLayout l;
@@ -369,7 +386,9 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return pa_fail(PA_ERR_INVALID, "pa_decode: misaligned pointer");
-  const int P = pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size);
+  const int P = num_groups ? pa_decode_partition_size_shared_prefix(num_seqs, num_kv_heads, max_context_len,
+                                                                     partition_size, groups, num_groups)
+                           : pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size);
   if (P < 0) return P;
   const long long parts = cdiv(max_context_len, P);
   if (parts * num_seqs * num_kv_heads >= (1LL << 31)) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: too many work items");

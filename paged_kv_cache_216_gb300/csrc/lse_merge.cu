@@ -9,16 +9,19 @@
 // 大模型推理优化的显存管理革新" section 3.1 gives, up to rounding.
 //
 // Each (sequence, query head) gets `wpr` warps (8 for contexts of 32 or more
-// partitions, else 1) and a CTA of eight warps serves 8 / wpr of
-// them; warp w of a group takes partitions w, w + wpr, ...: it finds their
-// max and weight sum first (the lanes taking partitions), then sums the
-// weighted partial rows, lanes holding D/32 consecutive dims so each row is
-// one coalesced 4*D-byte line and no row's load waits for another's; the
-// group's warps are combined through shared memory.  Sequences that fit one partition were written by the decode
-// kernel and are skipped, unless they belong to a prefix group: there even a
-// single partition is a partial written by the shared-prefix kernel.  Launched with programmatic dependent launch: the
-// CTAs may start while the decode kernel drains and wait for its results
-// with griddepcontrol.wait.
+// partitions, else 1) and a CTA of eight warps serves 8 / wpr of them; warp
+// w of a group takes partitions w, w + wpr, ...  Up to 32 of them, lane i
+// reads partition i's (max, sum) once; the warp reduces the max and the
+// weighted sum with shuffles and hands each partition's weight to the other
+// lanes, which then sum the weighted partial rows, lane L holding D/32
+// consecutive dims (each row one coalesced 4*D-byte line, no row's load
+// waiting for another's, 16 rows in flight).  The group's warps are combined
+// through shared memory.  Sequences that fit one partition were written by
+// the decode kernel and are skipped, unless they belong to a prefix group:
+// there even a single partition is a partial written by the shared-prefix
+// items.  Launched with programmatic dependent launch: the CTAs start while
+// the decode kernel drains, read the context lengths (inputs) and only then
+// wait for the decode kernel's results with griddepcontrol.wait.
 
 #include <cuda_bf16.h>
 
@@ -39,10 +42,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
   constexpr int E = D / 32;
   __shared__ float s_m[kMaxWarps], s_l[kMaxWarps];
   __shared__ __align__(16) float s_o[kMaxWarps][D];
-  pdl_wait_primary();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long sh = (long long)blockIdx.x * (kMaxWarps / wpr) + warp / wpr;
   const int wg = warp % wpr;  // warp within its (sequence, head) group
+  // The row's partition count comes from the inputs, not from the decode
+  // kernel's results: it is known before the wait for them.
   int s = 0, h = 0, np = 0, first = 2;  // merge when np >= first
   if (sh < (long long)p.S * p.H) {
     s = (int)(sh / p.H);
@@ -51,6 +55,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
     np = (ctx + p.P - 1) / p.P;
     if (pg.n > 0 && prefix_parts_of(pg, s) > 0) first = 1;
   }
+  pdl_wait_primary();
   float m = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
@@ -60,29 +65,58 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
     // Their max and weight sum first, the lanes taking partitions: then the
     // weight of every partial row is known and the rows' loads below do not
     // wait on one another (a running max would chain them).
-    for (int i = lane; i < cnt; i += 32) m = fmaxf(m, p.ws_ml[base + (size_t)(wg + i * wpr) * p.H].x);
+    if (cnt <= 32) {
+      // one partition per lane: its (max, sum) is read once and its weight
+      // handed to the other lanes
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (lane < cnt) ml = p.ws_ml[base + (size_t)(wg + lane * wpr) * p.H];
+      m = ml.x;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    for (int i = lane; i < cnt; i += 32) {
-      const float2 ml = p.ws_ml[base + (size_t)(wg + i * wpr) * p.H];
-      l += exp2f(ml.x - m) * ml.y;
-    }
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const float w = lane < cnt ? exp2f(ml.x - m) : 0.f;
+      l = w * ml.y;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-#pragma unroll 8
-    for (int i = 0; i < cnt; ++i) {
-      const size_t wi = base + (size_t)(wg + i * wpr) * p.H;
-      const float b = exp2f(p.ws_ml[wi].x - m);
-      float x[E];
-      if constexpr (E == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(p.ws_o + wi * D + lane * E);
-        x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(p.ws_o + wi * D + lane * E);
-        x[0] = v.x, x[1] = v.y;
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll 16
+      for (int i = 0; i < cnt; ++i) {
+        const float b = __shfl_sync(0xffffffffu, w, i);
+        const float* src = p.ws_o + (base + (size_t)(wg + i * wpr) * p.H) * D + lane * E;
+        float x[E];
+        if constexpr (E == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          x[0] = v.x, x[1] = v.y;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += x[e] * b;
+      }
+    } else {
+      for (int i = lane; i < cnt; i += 32) m = fmaxf(m, p.ws_ml[base + (size_t)(wg + i * wpr) * p.H].x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      for (int i = lane; i < cnt; i += 32) {
+        const float2 ml = p.ws_ml[base + (size_t)(wg + i * wpr) * p.H];
+        l += exp2f(ml.x - m) * ml.y;
       }
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += x[e] * b;
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll 8
+      for (int i = 0; i < cnt; ++i) {
+        const size_t wi = base + (size_t)(wg + i * wpr) * p.H;
+        const float b = exp2f(p.ws_ml[wi].x - m);
+        float x[E];
+        if constexpr (E == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(p.ws_o + wi * D + lane * E);
+          x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(p.ws_o + wi * D + lane * E);
+          x[0] = v.x, x[1] = v.y;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += x[e] * b;
+      }
     }
   }
   if (wpr > 1) {  // combine the group's warps through shared memory

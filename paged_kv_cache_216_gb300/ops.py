@@ -92,8 +92,16 @@ def copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
                                _dtype_code(k_cache), _stream(stream)))
 
 
-def decode_partition_size(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_size: int = 0) -> int:
-    return check(lib().pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size))
+def decode_partition_size(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_size: int = 0,
+                          prefix_groups=None) -> int:
+    """The partition size a decode call uses (the library's choice for 0);
+    with prefix groups, the one the shared-prefix calls use."""
+    g = prefix_groups_array(prefix_groups)
+    if g is None:
+        return check(lib().pa_decode_partition_size(num_seqs, num_kv_heads, max_context_len, partition_size))
+    return check(lib().pa_decode_partition_size_shared_prefix(num_seqs, num_kv_heads, max_context_len,
+                                                              partition_size, ctypes.c_void_p(g.ctypes.data),
+                                                              g.shape[0]))
 
 
 def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
@@ -234,7 +242,8 @@ def paged_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens, 
     _cuda_contig(out)
     _need(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
     if workspace is None:
-        workspace = decode_workspace(s, h, hkv, d, max_context_len, partition_size, q.device)
+        p = decode_partition_size(s, hkv, max_context_len, partition_size, prefix_groups)
+        workspace = decode_workspace(s, h, hkv, d, max_context_len, p, q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     gp, gn, _keep = _groups_args(prefix_groups)
     check(lib().pa_decode_shared_prefix(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),

@@ -80,7 +80,9 @@ class ServingEngine:
         s = self.seq_ids.shape[0]
         self.num_seqs = s
         self.width = -(-self.max_context_len // b)
-        self.partition_size = ops.decode_partition_size(s, hkv, self.max_context_len, partition_size)
+        self.partition_size = ops.decode_partition_size(
+            s, hkv, self.max_context_len, partition_size,
+            prefix_groups if k_cache.dtype == torch.bfloat16 else None)
         self.bf16 = k_cache.dtype == torch.bfloat16
         # E4M3 caches: new tokens arrive in bf16 and are stored as codes of
         # x / scale; kv_scales = (k_scale, v_scale).

@@ -7,12 +7,14 @@ should a host-side check ever stop refusing one of them, the call fails with
 a CUDA "no device" error there instead of launching a kernel on the bogus
 address on whatever GPU this suite runs on."""
 
+import ctypes
 import json
 import os
 import re
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 from tests._lib_fixture import ensure_built
@@ -174,6 +176,20 @@ def test_partition_and_workspace_sizing(L):
     p = L.pa_decode_partition_size(1, 1, 5000, 0)
     assert p % 32 == 0 and 64 <= p < 512
     assert L.pa_decode_partition_size(1, 1, 100, 33) == -1
+    # with prefix groups: doubled up to 1024 while every prefix holds a
+    # whole partition; explicit sizes and wide batches unchanged
+    def shared(S, hkv, mx, P, groups):
+        g = np.ascontiguousarray(np.asarray(groups, dtype=np.int32).reshape(-1, 3))
+        return L.pa_decode_partition_size_shared_prefix(S, hkv, mx, P, ctypes.c_void_p(g.ctypes.data), g.shape[0])
+    assert shared(64, 8, 8200, 0, [(0, 32, 1024)]) == 1024
+    assert shared(64, 8, 8200, 0, [(0, 32, 1024), (40, 4, 600)]) == 512
+    assert shared(64, 8, 8200, 0, [(0, 32, 5000)]) == 1024
+    assert shared(64, 8, 8200, 256, [(0, 32, 1024)]) == 256
+    assert shared(9, 8, 2600, 0, [(0, 6, 1024)]) == 1024  # from 128
+    assert shared(9, 8, 2600, 0, [(0, 6, 100)]) == L.pa_decode_partition_size(9, 8, 2600, 0)
+    assert shared(256, 8, 4116, 0, [(0, 32, 1024)]) == 4096
+    assert L.pa_decode_partition_size_shared_prefix(64, 8, 8200, 0, None, 0) == 512
+    assert L.pa_decode_partition_size_shared_prefix(64, 8, 8200, 0, None, 1) < 0
     # one partition: header + work list only
     assert L.pa_decode_workspace_bytes(4, 8, 128, 512, 512) == 256 + 256
     # header, work list (8 B per sequence x partition, 256-aligned), then

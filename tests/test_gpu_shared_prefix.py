@@ -87,6 +87,9 @@ CASES = {
     "g4_p512": (35, 9, 32, 8, 128, 16, 512, [(0, 6, 1024)], (1025, 2600)),
     # 20 members of g = 4: 80 rows in two tiles
     "g4_80_rows": (36, 22, 8, 2, 128, 32, 64, [(0, 20, 192)], (192, 500)),
+    # the library's partition choice (P 0): 128 for plain decode of this
+    # batch, lengthened to 1024 (the whole prefix) with the group
+    "g4_auto_partition": (39, 9, 32, 8, 128, 16, 0, [(0, 6, 1024)], (1025, 2600)),
 }
 
 

@@ -11,11 +11,11 @@
 // rows), the rows being (new token, query head) pairs, token-major; the
 // pairs with the most keys come first.  Both tiles of an item read every
 // stage of keys and values, so each TMA box feeds 256 rows.  The kernel is
-// persistent: one CTA per SM (384 threads) walks a fixed list of items --
-// rounds of one item per CTA, alternately in and against CTA order -- so the
-// set-up (barriers, tensor memory) is paid once per SM, there is no tail of
-// whole waves, and the next item's loads overlap the current item's last
-// products and epilogue.  Roles:
+// persistent: one CTA per SM (384 threads) walks a fixed list of items
+// (pf_item_index: the CTAs that take one item fewer take the costliest
+// ones), so the set-up (barriers, tensor memory) is paid once per SM, there
+// is no tail of whole waves, and the next item's loads overlap the current
+// item's last products and epilogue.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
 //    of each item, 128 tokens per stage, into rings of their own (2 stages
 //    of keys, 3 of values: values are needed a softmax later than keys)
@@ -194,10 +194,21 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs
   return it;
 }
 
-// The r-th item of CTA b of G: rounds of G items, alternately in and against
-// CTA order, so that a CTA given one of the costliest items of a round gets
-// one of the cheapest of the next.
-__device__ __forceinline__ int pf_item_index(int r, int b, int G) { return r * G + ((r & 1) ? G - 1 - b : b); }
+// The r-th item of CTA b of G over n items (negative: CTA b has no r-th
+// item).  With n = q·G + e, the first G - e CTAs take q items each and the
+// last e take q + 1: the costliest q·(G - e) items (the list runs from the
+// most keys to the fewest) go to the CTAs with fewer items and the rest to
+// the others, each group in rounds of one item per CTA, alternately in and
+// against CTA order, so that a CTA given one of the costliest items of a
+// round gets one of the cheapest of the next.  On 512 items of 5-8 chunks
+// on 152 CTAs the busiest CTA gets 22 chunks, the least possible (a
+// single snake over all CTAs gave it 25).
+__device__ __forceinline__ int pf_item_index(int r, int b, int G, int n) {
+  const int q = n / G, e = n - q * G, ga = G - e;
+  if (b < ga) return r < q ? r * ga + ((r & 1) ? ga - 1 - b : b) : -1;
+  const int bb = b - ga;
+  return r <= q ? q * ga + r * e + ((r & 1) ? e - 1 - bb : bb) : -1;
+}
 
 template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
@@ -295,8 +306,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint32_t vl = 0;               // chunks of values cleared past their sequence's end
       bool waited = false, ok = true, landing = false;
       for (int r = 0; ok; ++r) {
-        const int j = pf_item_index(r, b, G);
-        if (j >= num_items) break;
+        const int j = pf_item_index(r, b, G, num_items);
+        if (j < 0) break;
         const PfItem it = pf_item(p, j, pairs);
         if (it.state) continue;
         // The query tiles (an input the append does not write), one box per
@@ -329,8 +340,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           }
           // The next item's query tiles into L2, so that their loads at the
           // item boundary do not wait on HBM.
-          const int jn = pf_item_index(r + 1, b, G);
-          if (lane == 0 && jn < num_items) {
+          const int jn = pf_item_index(r + 1, b, G, num_items);
+          if (lane == 0 && jn >= 0) {
             const PfItem nx = pf_item(p, jn, pairs);
             if (!nx.state)
               for (int t = 0; t < kTiles; ++t) {
@@ -482,8 +493,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         };
         uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
         for (int r = 0; ok; ++r) {
-          const int j = pf_item_index(r, b, G);
-          if (j >= num_items) break;
+          const int j = pf_item_index(r, b, G, num_items);
+          if (j < 0) break;
           const PfItem it = pf_item(p, j, pairs);
           if (it.state) continue;
           if (!wait_bar(q_full(t), nit & 1)) break;
@@ -533,8 +544,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     uint32_t sc_n = 0, ot = 0;  // S phases consumed, items finished by this tile
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int j = pf_item_index(r, b, G);
-      if (j >= num_items) break;
+      const int j = pf_item_index(r, b, G, num_items);
+      if (j < 0) break;
       const PfItem it = pf_item(p, j, pairs);
       if (it.state == 2) {
         if (t == 0 && lt == 0 && it.pair == 0 && it.kvh == 0) raise_status(p.status, PA_STATUS_BAD_CONTEXT);

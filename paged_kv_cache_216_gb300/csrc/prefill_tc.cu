@@ -12,8 +12,8 @@
 // pairs with the most keys come first.  Both tiles of an item read every
 // stage of keys and values, so each TMA box feeds 256 rows.  The kernel is
 // persistent: one CTA per SM (384 threads) walks a fixed list of items
-// (pf_item_index: the CTAs that take one item fewer take the costliest
-// ones), so the set-up (barriers, tensor memory) is paid once per SM, there
+// (PfOrder: one snake over the CTAs, or the costliest items to the CTAs
+// that take one item fewer, whichever is better balanced), so the set-up (barriers, tensor memory) is paid once per SM, there
 // is no tail of whole waves, and the next item's loads overlap the current
 // item's last products and epilogue.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
@@ -126,8 +126,9 @@ struct PfCfg {
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
   // barriers: the rings, kTileBars per tile, q_empty, drained and softmax turn per tile, v_land
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 3 * kTiles + 1) * 8;  // tensor-memory address, abort flag
-  static constexpr size_t kBytes = 1024 + kOffMisc + 16;
+  // tensor-memory address, abort flag, the busiest CTA's load in both orders, the CTA's PfOrder
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 3 * kTiles + 1) * 8;
+  static constexpr size_t kBytes = 1024 + kOffMisc + 32;
   static constexpr uint32_t kColO = 0, kColS = 2 * DH;
   static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
   static_assert(kBytes <= 227 * 1024, "shared memory of one CTA");
@@ -194,21 +195,45 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs
   return it;
 }
 
-// The r-th item of CTA b of G over n items (negative: CTA b has no r-th
-// item).  With n = q·G + e, the first G - e CTAs take q items each and the
-// last e take q + 1: the costliest q·(G - e) items (the list runs from the
-// most keys to the fewest) go to the CTAs with fewer items and the rest to
-// the others, each group in rounds of one item per CTA, alternately in and
+// The items of one CTA: item r (r < count) is
+//     base + r * stride + (r even ? slot : stride - 1 - slot),
+// i.e. rounds of `stride` items over `stride` CTAs, alternately in and
 // against CTA order, so that a CTA given one of the costliest items of a
-// round gets one of the cheapest of the next.  On 512 items of 5-8 chunks
-// on 152 CTAs the busiest CTA gets 22 chunks, the least possible (a
-// single snake over all CTAs gave it 25).
-__device__ __forceinline__ int pf_item_index(int r, int b, int G, int n) {
+// round gets one of the cheapest of the next.  Two orders of n items on G
+// CTAs (n = q·G + e):
+//  * plain: one snake over all G CTAs;
+//  * count-aware: the first G - e CTAs take q items each and the last e take
+//    q + 1; the costliest q·(G - e) items (the list runs from the most keys
+//    to the fewest) go to the CTAs with fewer items and the rest to the
+//    others, each group a snake of its own.
+// On 512 items of 5-8 chunks (128 of each) on 152 CTAs the count-aware order
+// gives the busiest CTA 22 chunks, the least possible, against 25 in the
+// plain one; on ragged batches it can do worse, so the kernel takes
+// whichever leaves the busiest CTA less work.
+struct PfOrder {
+  int base, stride, slot, count;
+};
+
+__device__ __forceinline__ PfOrder pf_order(int b, int G, int n, bool aware) {
   const int q = n / G, e = n - q * G, ga = G - e;
-  if (b < ga) return r < q ? r * ga + ((r & 1) ? ga - 1 - b : b) : -1;
-  const int bb = b - ga;
-  return r <= q ? q * ga + r * e + ((r & 1) ? e - 1 - bb : bb) : -1;
+  if (!aware) return PfOrder{0, G, b, q + ((q & 1) ? (b >= ga ? 1 : 0) : (b < e ? 1 : 0))};
+  if (b < ga) return PfOrder{0, ga, b, q};
+  return PfOrder{q * ga, e, b - ga, q + 1};
 }
+
+__device__ __forceinline__ int pf_item_at(const PfOrder& o, int r) {
+  return r < o.count ? o.base + r * o.stride + ((r & 1) ? o.stride - 1 - o.slot : o.slot) : -1;
+}
+
+// Cost of an item for the choice of order: its chunks of keys plus one for
+// its start and end (0 for a pair without rows).
+__device__ __forceinline__ int pf_item_cost(const PrefillArgs& p, int j, int pairs) {
+  const PfItem it = pf_item(p, j, pairs);
+  return it.state ? 0 : it.nch + 1;
+}
+
+// The choice is made when every CTA has at most this many items.
+constexpr int kMaxCheckedItemsPerCta = 16;
 
 template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
@@ -267,6 +292,38 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     *abort = 0;
     fence_barrier_init();
   }
+  // The order of the item lists (PfOrder): every CTA finds the same one
+  // from the same inputs.  The costs of the (pair, sequence) items, the same
+  // for every KV head, go to the value ring before it is cleared; thread c
+  // sums CTA c's list in both orders.  The lengths are inputs the append
+  // kernel does not write: no wait for it is needed.
+  int* cost = reinterpret_cast<int*>(base + kOffV);
+  int* busiest = reinterpret_cast<int*>(base + C::kOffMisc + 8);  // plain, count-aware
+  PfOrder* order = reinterpret_cast<PfOrder*>(base + C::kOffMisc + 16);
+  const int ncost = pairs * p.S;
+  const bool check = num_items <= kMaxCheckedItemsPerCta * G && ncost <= kStagesV * kKVStage / 4;
+  if (check)
+    for (int i = tid; i < ncost; i += kThreadsT) cost[i] = pf_item_cost(p, i * p.Hkv, pairs);
+  if (tid == 0) busiest[0] = busiest[1] = 0;
+  __syncthreads();
+  if (check)
+    for (int c0 = 0; c0 < G; c0 += kThreadsT) {
+      const int c = c0 + tid;
+      int load[2] = {0, 0};
+      if (c < G)
+        for (int a = 0; a < 2; ++a) {
+          const PfOrder o = pf_order(c, G, num_items, a == 1);
+          for (int r = 0; r < o.count; ++r) load[a] += cost[pf_item_at(o, r) / p.Hkv];
+        }
+      load[0] = __reduce_max_sync(0xffffffffu, load[0]);
+      load[1] = __reduce_max_sync(0xffffffffu, load[1]);
+      if (lane == 0) {
+        atomicMax(&busiest[0], load[0]);
+        atomicMax(&busiest[1], load[1]);
+      }
+    }
+  __syncthreads();
+  if (tid == 0) *order = pf_order(b, G, num_items, check && busiest[1] < busiest[0]);
   // Value rows that no copy writes must still be finite (their weights are
   // exact zeros, and 0 x NaN is NaN): the value ring starts as zeros, and
   // rows past a sequence's end are cleared after their copy lands.
@@ -306,7 +363,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint32_t vl = 0;               // chunks of values cleared past their sequence's end
       bool waited = false, ok = true, landing = false;
       for (int r = 0; ok; ++r) {
-        const int j = pf_item_index(r, b, G, num_items);
+        const int j = pf_item_at(*order, r);
         if (j < 0) break;
         const PfItem it = pf_item(p, j, pairs);
         if (it.state) continue;
@@ -340,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           }
           // The next item's query tiles into L2, so that their loads at the
           // item boundary do not wait on HBM.
-          const int jn = pf_item_index(r + 1, b, G, num_items);
+          const int jn = pf_item_at(*order, r + 1);
           if (lane == 0 && jn >= 0) {
             const PfItem nx = pf_item(p, jn, pairs);
             if (!nx.state)
@@ -493,7 +550,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         };
         uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
         for (int r = 0; ok; ++r) {
-          const int j = pf_item_index(r, b, G, num_items);
+          const int j = pf_item_at(*order, r);
           if (j < 0) break;
           const PfItem it = pf_item(p, j, pairs);
           if (it.state) continue;
@@ -544,7 +601,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     uint32_t sc_n = 0, ot = 0;  // S phases consumed, items finished by this tile
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int j = pf_item_index(r, b, G, num_items);
+      const int j = pf_item_at(*order, r);
       if (j < 0) break;
       const PfItem it = pf_item(p, j, pairs);
       if (it.state == 2) {

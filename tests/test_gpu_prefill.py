@@ -153,6 +153,23 @@ def test_prefill_larger_max_query_len_and_bad_lengths(pa):
     assert_close(out2[rows], ref[rows], "bf16", "other sequences")
 
 
+def _check_sampled_tokens(b, out, kc, prev, tokens, H, Hkv):
+    """Tokens tokens[s] (indices among sequence s's new tokens) of every
+    sequence against the oracle's per-token definition, every KV head."""
+    kc_o, vc_o = cache_append(b["kc"], b["vc"], b["k"], b["v"], b["slots"])
+    assert np.array_equal(to_bits(kc), kc_o)
+    g = H // Hkv
+    for s, idx in enumerate(tokens):
+        for i in idx:
+            row = int(b["qs"][s]) + i
+            p = prev[s] + i
+            for kv in range(Hkv):
+                kr = to_f64(gather_sequence(kc_o, b["tables"][s], p + 1, kv), "bf16")
+                vr = to_f64(gather_sequence(vc_o, b["tables"][s], p + 1, kv), "bf16")
+                ref = decode_one(to_f64(b["q"][row, kv * g:(kv + 1) * g], "bf16"), kr, vr, b["scale"])
+                assert_close(out[row, kv * g:(kv + 1) * g], ref, "bf16", f"s{s} i{i} kv{kv}")
+
+
 def test_prefill_bench_shape_sampled(pa):
     """The benchmark's prefill batch (8 sequences, 512 cached + 512 new
     tokens, 32/8 heads): sampled tokens (first, last, random) of every
@@ -160,17 +177,39 @@ def test_prefill_bench_shape_sampled(pa):
     S, prev_n, new_n, H, Hkv, D, B = 8, 512, 512, 32, 8, 128, 16
     b = _batch(5, [prev_n] * S, [new_n] * S, H, Hkv, D, B)
     out, kc, vc = _run(pa, b)
-    kc_o, vc_o = cache_append(b["kc"], b["vc"], b["k"], b["v"], b["slots"])
-    assert np.array_equal(to_bits(kc), kc_o)
     rng = np.random.default_rng(6)
-    g = H // Hkv
-    for s in range(S):
-        for i in sorted({0, new_n - 1, int(rng.integers(new_n))}):
-            row = int(b["qs"][s]) + i
-            p = prev_n + i
-            for kv in range(Hkv):
-                kr = to_f64(gather_sequence(kc_o, b["tables"][s], p + 1, kv), "bf16")
-                vr = to_f64(gather_sequence(vc_o, b["tables"][s], p + 1, kv), "bf16")
-                ref = decode_one(to_f64(b["q"][row, kv * g:(kv + 1) * g], "bf16"), kr, vr, b["scale"])
-                assert_close(out[row, kv * g:(kv + 1) * g], ref, "bf16", f"s{s} i{i} kv{kv}")
+    tokens = [sorted({0, new_n - 1, int(rng.integers(new_n))}) for _ in range(S)]
+    _check_sampled_tokens(b, out, kc, [prev_n] * S, tokens, H, Hkv)
+    assert pa.get_status() == 0
+
+
+# Ragged batches of more work items (sequence, KV head, pair of 128-row
+# tiles) than CTAs, not a multiple of them: with these lengths the kernel
+# takes one snake over all CTAs for the first (its busiest CTA would get 32
+# chunk units against 52 in the count-aware order) and the count-aware
+# order for the second (44 against 52).
+RAGGED = {
+    "plain_order": ([1688, 112, 1352, 2027, 333], [113, 74, 10, 613, 31]),
+    "count_aware_order": ([0, 300, 1200, 50, 2000, 700], [900, 64, 513, 1024, 200, 777]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RAGGED))
+def test_prefill_ragged_many_items_sampled(pa, name):
+    """One token of every pair of tiles of every sequence (its first and a
+    random one), plus each sequence's last, so that every work item is
+    checked against the oracle."""
+    prev, new = RAGGED[name]
+    H, Hkv, D, B = 32, 8, 128, 16
+    b = _batch(7, prev, new, H, Hkv, D, B)
+    out, kc, vc = _run(pa, b)
+    rng = np.random.default_rng(8)
+    per_pair = 256 // (H // Hkv)  # new tokens per pair of tiles
+    tokens = []
+    for n in new:
+        idx = {n - 1}
+        for t0 in range(0, n, per_pair):
+            idx |= {t0, int(rng.integers(t0, min(n, t0 + per_pair)))}
+        tokens.append(sorted(idx))
+    _check_sampled_tokens(b, out, kc, prev, tokens, H, Hkv)
     assert pa.get_status() == 0

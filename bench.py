@@ -559,24 +559,53 @@ def run_reference(args, rank, world):
 PREFILL_SHAPE = dict(num_seqs=8, cached=512, new=512, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16)
 
 
+def _ragged_prefill_shape():
+    """8 prompts of U[64, 2048] new tokens after U[0, 4096] cached ones
+    (seeded), heads and blocks as PREFILL_SHAPE."""
+    rng = np.random.default_rng(3)
+    cached = [int(x) for x in rng.integers(0, 4097, size=8)]
+    new = [int(x) for x in rng.integers(64, 2049, size=8)]
+    return dict(PREFILL_SHAPE, cached=cached, new=new)
+
+
+PREFILL_RAGGED_SHAPE = _ragged_prefill_shape()
+
+
+def _prefill_shape(args):
+    return PREFILL_RAGGED_SHAPE if getattr(args, "prefill_ragged", False) else PREFILL_SHAPE
+
+
+def _per_seq(sh):
+    S = sh["num_seqs"]
+    as_list = lambda x: [int(v) for v in x] if isinstance(x, (list, tuple)) else [int(x)] * S
+    return as_list(sh["cached"]), as_list(sh["new"])
+
+
 def prefill_batch(seed: int = 11, **shape):
-    """Seeded synthetic prefill batch: every sequence has `cached` tokens in
-    the pool and `new` prompt tokens to append and attend; shuffled tables."""
+    """Seeded synthetic prefill batch: sequence s has `cached` tokens in the
+    pool and `new` prompt tokens to append and attend (one value for every
+    sequence, or one per sequence); shuffled tables."""
     sh = dict(PREFILL_SHAPE, **shape)
-    S, c, n, H, Hkv, D, B = (sh[k] for k in ("num_seqs", "cached", "new", "num_heads", "num_kv_heads", "head_dim",
-                                            "block_size"))
+    S, H, Hkv, D, B = (sh[k] for k in ("num_seqs", "num_heads", "num_kv_heads", "head_dim", "block_size"))
+    cached, new = _per_seq(sh)
     rng = np.random.default_rng(seed)
-    nb_seq = -(-(c + n) // B)
-    N = S * nb_seq + 8
+    nb = [-(-(c + n) // B) for c, n in zip(cached, new)]
+    N = sum(nb) + 8
     perm = rng.permutation(N).astype(np.int32)
-    tables = perm[:S * nb_seq].reshape(S, nb_seq)
-    pos = c + np.arange(n)
-    slots = (tables[:, pos // B] * B + pos % B).reshape(-1).astype(np.int64)
-    T = S * n
+    tables = np.zeros((S, max(nb)), dtype=np.int32)
+    slots = []
+    at = 0
+    for s in range(S):
+        tables[s, :nb[s]] = perm[at:at + nb[s]]
+        at += nb[s]
+        pos = cached[s] + np.arange(new[s])
+        slots.append(tables[s, pos // B] * B + pos % B)
+    T = sum(new)
     return dict(q=normal((T, H, D), 1.0, "bf16", seed, 31), k=normal((T, Hkv, D), 1.0, "bf16", seed, 32),
                 v=normal((T, Hkv, D), 1.0, "bf16", seed, 33), kc=normal((N, Hkv, B, D), 1.0, "bf16", seed, 34),
-                vc=normal((N, Hkv, B, D), 1.0, "bf16", seed, 35), slots=slots, tables=tables,
-                qs=(np.arange(S + 1) * n).astype(np.int32), ctx=np.full(S, c + n, dtype=np.int32), shape=sh,
+                vc=normal((N, Hkv, B, D), 1.0, "bf16", seed, 35), slots=np.concatenate(slots).astype(np.int64),
+                tables=tables, qs=np.r_[0, np.cumsum(new)].astype(np.int32),
+                ctx=np.array([c + n for c, n in zip(cached, new)], dtype=np.int32), shape=sh,
                 scale=1.0 / np.sqrt(D))
 
 
@@ -584,8 +613,9 @@ def prefill_flops(b) -> float:
     """Attention FLOPs of a prefill call: each new token's query head does
     2·D flops per key for Q·Kᵀ and 2·D for P·V over its keys 0..p."""
     sh = b["shape"]
-    keys = sum(sh["cached"] + i + 1 for i in range(sh["new"]))
-    return float(keys) * sh["num_seqs"] * sh["num_heads"] * sh["head_dim"] * 4
+    cached, new = _per_seq(sh)
+    keys = sum(n * c + n * (n + 1) // 2 for c, n in zip(cached, new))
+    return float(keys) * sh["num_heads"] * sh["head_dim"] * 4
 
 
 def run_prefill(args, rank, world, local):
@@ -599,8 +629,9 @@ def run_prefill(args, rank, world, local):
     build.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    b = prefill_batch(seed=11 + rank)
+    b = prefill_batch(seed=11 + rank, **_prefill_shape(args))
     sh = b["shape"]
+    cached, new = _per_seq(sh)
 
     def to_dev(a):
         if a.dtype == np.uint16:
@@ -610,7 +641,7 @@ def run_prefill(args, rank, world, local):
     q, k, v, kc, vc = (to_dev(b[x]) for x in ("q", "k", "v", "kc", "vc"))
     slots, qs, ctx, tables = (to_dev(b[x]) for x in ("slots", "qs", "ctx", "tables"))
     out = torch.empty_like(q)
-    mql, mctx = sh["new"], sh["cached"] + sh["new"]
+    mql, mctx = max(new), int(b["ctx"].max())
 
     def call(qq=q, kk=k, vv=v, oo=out):
         pa.prefill(qq, kk, vv, slots, qs, ctx, tables, mql, mctx, b["scale"], kc, vc, out=oo)
@@ -670,9 +701,10 @@ def run_prefill(args, rank, world, local):
         "metric": "prefill attention TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(t_dev / K * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill_bf16", **sh, "tokens_per_step": sh["num_seqs"] * sh["new"],
+        "config": {"workload": "prefill_ragged_bf16" if args.prefill_ragged else "prefill_bf16", **sh,
+                   "tokens_per_step": sum(new),
                    "flops_per_step": flops, "l2": "flushed before every step", "parallelism": f"replicas x{world}"},
-        "prefill_tokens_per_s": round(allreduce_sum(float(sh["num_seqs"] * sh["new"] * K), world) / t_dev, 1),
+        "prefill_tokens_per_s": round(allreduce_sum(float(sum(new) * K), world) / t_dev, 1),
         "e2e": {"value": round(allreduce_sum(flops * K, world) / t_e2e / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size())},
         "gpu_launches": 2 * K,
@@ -684,23 +716,27 @@ def run_prefill(args, rank, world, local):
     return res
 
 
-def prefill_oracle_sample(budget_s: float):
+def prefill_oracle_sample(budget_s: float, shape=None):
     """Oracle prefill on whole sequences of the bench batch for a bounded
     time: TFLOP/s of the sample."""
     from oracle.prefill import prefill as oracle_prefill
 
-    b = prefill_batch()
+    b = prefill_batch(**(shape or PREFILL_SHAPE))
     sh = b["shape"]
-    n = sh["new"]
+    cached, new = _per_seq(sh)
     t0 = time.perf_counter()
     done = 0
+    keys = 0
     while time.perf_counter() - t0 < budget_s and done < sh["num_seqs"]:
-        rows = slice(done * n, (done + 1) * n)
-        oracle_prefill(b["q"][rows], b["k"][rows], b["v"][rows], b["slots"][rows], np.array([0, n], np.int32),
+        q0, q1 = int(b["qs"][done]), int(b["qs"][done + 1])
+        rows = slice(q0, q1)
+        oracle_prefill(b["q"][rows], b["k"][rows], b["v"][rows], b["slots"][rows], np.array([0, q1 - q0], np.int32),
                        b["ctx"][done:done + 1], b["tables"][done:done + 1], b["kc"], b["vc"], b["scale"], "bf16")
+        c, n = cached[done], new[done]
+        keys += n * c + n * (n + 1) // 2
         done += 1
     t = time.perf_counter() - t0
-    flops = prefill_flops(b) / sh["num_seqs"] * done
+    flops = float(keys) * sh["num_heads"] * sh["head_dim"] * 4
     return flops / t / 1e12, f"oracle prefill of {done} of the {sh['num_seqs']} sequences in {t:.1f} s"
 
 
@@ -710,15 +746,15 @@ def run_reference_prefill(args, world):
     metric, unit and workload."""
     vals, desc = [], ""
     for _ in range(args.steps):
-        v, desc = prefill_oracle_sample(max(0.5, args.ref_budget / max(1, args.steps)))
+        v, desc = prefill_oracle_sample(max(0.5, args.ref_budget / max(1, args.steps)), _prefill_shape(args))
         vals.append(v)
     value = statistics.median(vals)
-    sh = dict(PREFILL_SHAPE)
+    sh = _prefill_shape(args)
     return {
         "metric": "prefill attention TFLOP/s", "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": "prefill_bf16", **sh},
+        "config": {"workload": "prefill_ragged_bf16" if args.prefill_ragged else "prefill_bf16", **sh},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -741,9 +777,12 @@ def main():
                     help="split-K partition size in tokens (default: the workload's, 0 = library choice)")
     ap.add_argument("--prefill", action="store_true",
                     help="time prefill (append + causal attention of 8 x 512 new tokens after 512 cached)")
+    ap.add_argument("--prefill-ragged", action="store_true",
+                    help="time prefill on 8 ragged prompts (U[64, 2048] new tokens after U[0, 4096] cached)")
     ap.add_argument("--no-prefix-groups", action="store_true",
                     help="decode prefix-sharing sequences one by one (no shared-prefix kernel)")
     args = ap.parse_args()
+    args.prefill = args.prefill or args.prefill_ragged
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
@@ -755,7 +794,7 @@ def main():
     if args.prefill:
         res = run_prefill(args, rank, world, local)
         if rank == 0:
-            val, desc = prefill_oracle_sample(min(args.cpu_budget, 15.0))
+            val, desc = prefill_oracle_sample(min(args.cpu_budget, 15.0), _prefill_shape(args))
             res["cpu_baseline"] = {"value": round(val, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                                    "sample": desc}
             print(json.dumps(res), flush=True)

@@ -11,11 +11,13 @@
 // rows), the rows being (new token, query head) pairs, token-major; the
 // pairs with the most keys come first.  Both tiles of an item read every
 // stage of keys and values, so each TMA box feeds 256 rows.  The kernel is
-// persistent: one CTA per SM (384 threads) walks a fixed list of items
-// (PfOrder: one snake over the CTAs, or the costliest items to the CTAs
-// that take one item fewer, whichever is better balanced), so the set-up (barriers, tensor memory) is paid once per SM, there
-// is no tail of whole waves, and the next item's loads overlap the current
-// item's last products and epilogue.  Roles:
+// persistent: one CTA per SM (384 threads) walks a fixed list of items that
+// it computes in its prologue (the items sorted by cost when the prompts are
+// ragged; a snake over the CTAs, or the costliest items to the CTAs that
+// take one item fewer, whichever leaves the busiest CTA less work), so the
+// set-up (barriers, tensor memory) is paid once per SM, there is no tail of
+// whole waves, and the next item's loads overlap the current item's last
+// products and epilogue.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
 //    of each item, 128 tokens per stage, into rings of their own (2 stages
 //    of keys, 3 of values: values are needed a softmax later than keys)
@@ -113,6 +115,9 @@ constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage 
 // full_k[], empty_k[], full_v[], empty_v[]; per tile s_full, p_full,
 // o_final, q_full
 constexpr int kTileBars = 4;
+// Items a CTA can list in shared memory; launches hold at most kListCap
+// items per CTA (the host splits larger batches over several launches).
+constexpr int kListCap = 440;
 
 // Layout for head_dim DH (64 or 128): tiles and stages hold DH / 64 halves
 // of 64 dims; O of tile t at columns DH·t .. DH·t + DH - 1, S of tile t at
@@ -126,9 +131,11 @@ struct PfCfg {
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
   // barriers: the rings, kTileBars per tile, q_empty, drained and softmax turn per tile, v_land
-  // tensor-memory address, abort flag, the busiest CTA's load in both orders, the CTA's PfOrder
   static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 3 * kTiles + 1) * 8;
-  static constexpr size_t kBytes = 1024 + kOffMisc + 32;
+  // misc: tensor-memory address, abort flag, the busiest CTA's load of each
+  // candidate list (4), the CTA's item count; then its items
+  static constexpr int kOffList = kOffMisc + 32;
+  static constexpr size_t kBytes = 1024 + kOffList + 4 * kListCap;
   static constexpr uint32_t kColO = 0, kColS = 2 * DH;
   static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
   static_assert(kBytes <= 227 * 1024, "shared memory of one CTA");
@@ -195,21 +202,18 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs
   return it;
 }
 
-// The items of one CTA: item r (r < count) is
-//     base + r * stride + (r even ? slot : stride - 1 - slot),
-// i.e. rounds of `stride` items over `stride` CTAs, alternately in and
-// against CTA order, so that a CTA given one of the costliest items of a
-// round gets one of the cheapest of the next.  Two orders of n items on G
-// CTAs (n = q·G + e):
+// The items of one CTA in a list of n items: item r (r < count) is list
+// position base + r * stride + (r even ? slot : stride - 1 - slot), i.e.
+// rounds of `stride` items over `stride` CTAs, alternately in and against
+// CTA order, so that a CTA given one of the costliest items of a round gets
+// one of the cheapest of the next.  Two orders on G CTAs (n = q·G + e):
 //  * plain: one snake over all G CTAs;
 //  * count-aware: the first G - e CTAs take q items each and the last e take
-//    q + 1; the costliest q·(G - e) items (the list runs from the most keys
-//    to the fewest) go to the CTAs with fewer items and the rest to the
-//    others, each group a snake of its own.
+//    q + 1; the costliest q·(G - e) items go to the CTAs with fewer items and
+//    the rest to the others, each group a snake of its own.
 // On 512 items of 5-8 chunks (128 of each) on 152 CTAs the count-aware order
 // gives the busiest CTA 22 chunks, the least possible, against 25 in the
-// plain one; on ragged batches it can do worse, so the kernel takes
-// whichever leaves the busiest CTA less work.
+// plain one; on ragged batches it can do worse.
 struct PfOrder {
   int base, stride, slot, count;
 };
@@ -221,24 +225,128 @@ __device__ __forceinline__ PfOrder pf_order(int b, int G, int n, bool aware) {
   return PfOrder{q * ga, e, b - ga, q + 1};
 }
 
-__device__ __forceinline__ int pf_item_at(const PfOrder& o, int r) {
-  return r < o.count ? o.base + r * o.stride + ((r & 1) ? o.stride - 1 - o.slot : o.slot) : -1;
+__device__ __forceinline__ int pf_list_pos(const PfOrder& o, int r) {
+  return o.base + r * o.stride + ((r & 1) ? o.stride - 1 - o.slot : o.slot);
 }
 
-// Cost of an item for the choice of order: its chunks of keys plus one for
-// its start and end (0 for a pair without rows).
+// Cost of an item for balancing: its chunks of keys plus one for its start
+// and end (0 for a pair without rows).
 __device__ __forceinline__ int pf_item_cost(const PrefillArgs& p, int j, int pairs) {
   const PfItem it = pf_item(p, j, pairs);
   return it.state ? 0 : it.nch + 1;
 }
 
-// The choice is made when every CTA has at most this many items.
+// The candidate lists are compared when every CTA has at most this many
+// items, and the items sorted when the batch has at most this many (pair,
+// sequence) entries and cost levels.
 constexpr int kMaxCheckedItemsPerCta = 16;
+constexpr int kMaxSortedEntries = 2048;
+constexpr int kMaxCostLevels = 1024;
+
+// The CTA's list of items.  Every CTA computes the same assignment from
+// the same inputs (the lengths, which the append kernel does not write:
+// no wait for it is needed), in the value ring before it is cleared.
+// Items are (pair, sequence, KV head), the KV heads of an entry (pair,
+// sequence) consecutive; entries are listed pair-major, the pairs with the
+// most keys first, or -- when that is not already from the costliest to
+// the cheapest, as it is not for ragged prompts -- sorted by cost, most
+// first, stably (a counting sort; warp 0 places the entries in order).
+// Of the lists {pair-major, sorted} x orders {plain, count-aware}, the one
+// whose busiest CTA has the least cost is taken.  A launch of a batch
+// split over several launches (first_item > 0, or more items than fit the
+// comparison) takes the pair-major list in the plain order.
+// Called by every thread of the CTA, before the value ring is cleared:
+// `cost` is the ring (ring_ints ints of scratch), `busiest` 4 ints, the
+// CTA's item count and items go to *my_count and my_items.
+__device__ __noinline__ void pf_build_list(const PrefillArgs& p, int pairs, int first_item, int num_items,
+                                           int* cost, int ring_ints, int* busiest, int* my_count, int* my_items) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = (int)gridDim.x, b = (int)blockIdx.x;
+  const int E = pairs * p.S;
+  const int levels = (p.max_ctx + kN - 1) / kN + 2;  // costs are below this
+  const bool check = first_item == 0 && num_items == E * p.Hkv && num_items <= kMaxCheckedItemsPerCta * G &&
+                     E <= ring_ints / 2;
+  bool sorting = check && E <= kMaxSortedEntries && levels <= kMaxCostLevels && 2 * E + levels <= ring_ints;
+  int* sorted = cost + E;            // [E] entries by cost, most first
+  int* next = sorted + E;            // [levels] per cost level: the next free position
+  if (check)
+    for (int i = tid; i < E; i += kThreadsT) cost[i] = pf_item_cost(p, i * p.Hkv, pairs);
+  if (tid < 4) busiest[tid] = 0;
+  if (sorting)
+    for (int i = tid; i < levels; i += kThreadsT) next[i] = 0;
+  __syncthreads();
+  if (sorting) {
+    bool in_order = true;
+    for (int i = tid; i + 1 < E; i += kThreadsT) in_order = in_order && cost[i] >= cost[i + 1];
+    sorting = !__syncthreads_and(in_order);
+  }
+  if (sorting) {
+    for (int i = tid; i < E; i += kThreadsT) atomicAdd(&next[cost[i]], 1);
+    __syncthreads();
+    if (tid == 0) {  // positions of the levels, costliest first
+      int at = 0;
+      for (int c = levels - 1; c >= 0; --c) {
+        const int k = next[c];
+        next[c] = at;
+        at += k;
+      }
+    }
+    __syncthreads();
+    if (warp == 0)
+      for (int i0 = 0; i0 < E; i0 += 32) {
+        const int i = i0 + lane;
+        const int c = i < E ? cost[i] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, c);
+        const int before = __popc(peers & ((1u << lane) - 1u));
+        const int pos = c >= 0 ? next[c] + before : 0;
+        __syncwarp();
+        if (c >= 0) {
+          sorted[pos] = i;
+          if (before == 0) next[c] += __popc(peers);
+        }
+        __syncwarp();
+      }
+    __syncthreads();
+  }
+  if (check)
+    for (int c0 = 0; c0 < G; c0 += kThreadsT) {
+      const int c = c0 + tid;
+      int load[4] = {0, 0, 0, 0};
+      if (c < G)
+        for (int k = 0; k < (sorting ? 4 : 2); ++k) {
+          const PfOrder o = pf_order(c, G, num_items, k & 1);
+          for (int r = 0; r < o.count; ++r) {
+            const int e = pf_list_pos(o, r) / p.Hkv;
+            load[k] += cost[k >= 2 ? sorted[e] : e];
+          }
+        }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) load[k] = __reduce_max_sync(0xffffffffu, load[k]);
+      if (lane == 0)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) atomicMax(&busiest[k], load[k]);
+    }
+  __syncthreads();
+  {
+    int pick = 0;  // pair-major, plain
+    if (check)
+      for (int k = 1; k < (sorting ? 4 : 2); ++k)
+        if (busiest[k] < busiest[pick]) pick = k;
+    const PfOrder o = pf_order(b, G, num_items, pick & 1);
+    if (warp == 0)
+      for (int r = lane; r < o.count; r += 32) {
+        const int j = pf_list_pos(o, r);
+        my_items[r] = first_item + (pick >= 2 ? sorted[j / p.Hkv] * p.Hkv + j % p.Hkv : j);
+      }
+    if (tid == 0) *my_count = o.count;
+  }
+}
 
 template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap qmap, const PrefillArgs p, int pairs, int num_items) {
+                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ PrefillArgs p, int pairs, int first_item,
+                      int num_items) {
   using C = PfCfg<DH>;
   constexpr int kQTile = C::kQTile, kKVStage = C::kKVStage, kOffK = C::kOffK, kOffV = C::kOffV;
   constexpr uint32_t kColO = C::kColO, kColS = C::kColS;
@@ -292,44 +400,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     *abort = 0;
     fence_barrier_init();
   }
-  // The order of the item lists (PfOrder): every CTA finds the same one
-  // from the same inputs.  The costs of the (pair, sequence) items, the same
-  // for every KV head, go to the value ring before it is cleared; thread c
-  // sums CTA c's list in both orders.  The lengths are inputs the append
-  // kernel does not write: no wait for it is needed.
-  int* cost = reinterpret_cast<int*>(base + kOffV);
-  int* busiest = reinterpret_cast<int*>(base + C::kOffMisc + 8);  // plain, count-aware
-  PfOrder* order = reinterpret_cast<PfOrder*>(base + C::kOffMisc + 16);
-  const int ncost = pairs * p.S;
-  const bool check = num_items <= kMaxCheckedItemsPerCta * G && ncost <= kStagesV * kKVStage / 4;
-  if (check)
-    for (int i = tid; i < ncost; i += kThreadsT) cost[i] = pf_item_cost(p, i * p.Hkv, pairs);
-  if (tid == 0) busiest[0] = busiest[1] = 0;
-  __syncthreads();
-  if (check)
-    for (int c0 = 0; c0 < G; c0 += kThreadsT) {
-      const int c = c0 + tid;
-      int load[2] = {0, 0};
-      if (c < G)
-        for (int a = 0; a < 2; ++a) {
-          const PfOrder o = pf_order(c, G, num_items, a == 1);
-          for (int r = 0; r < o.count; ++r) load[a] += cost[pf_item_at(o, r) / p.Hkv];
-        }
-      load[0] = __reduce_max_sync(0xffffffffu, load[0]);
-      load[1] = __reduce_max_sync(0xffffffffu, load[1]);
-      if (lane == 0) {
-        atomicMax(&busiest[0], load[0]);
-        atomicMax(&busiest[1], load[1]);
-      }
-    }
-  __syncthreads();
-  if (tid == 0) *order = pf_order(b, G, num_items, check && busiest[1] < busiest[0]);
-  // Value rows that no copy writes must still be finite (their weights are
-  // exact zeros, and 0 x NaN is NaN): the value ring starts as zeros, and
-  // rows past a sequence's end are cleared after their copy lands.
-  for (int u = tid; u < kStagesV * kKVStage / 16; u += kThreadsT)
-    reinterpret_cast<uint4*>(base + kOffV)[u] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();  // before any copy into the ring
+  int* my_count = reinterpret_cast<int*>(base + C::kOffMisc + 24);
+  int* my_items = reinterpret_cast<int*>(base + C::kOffList);
+  pf_build_list(p, pairs, first_item, num_items, reinterpret_cast<int*>(base + kOffV), kStagesV * kKVStage / 4,
+                reinterpret_cast<int*>(base + C::kOffMisc + 8), my_count, my_items);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tslot)),
                  "r"(kTmemCols));
@@ -358,12 +432,22 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint64_t* fulls = kv == 0 ? full_k : full_v;
       uint64_t* empties = kv == 0 ? empty_k : empty_v;
       const int stages = kv == 0 ? kStagesK : kStagesV;
+      if (kv == 1) {
+        // Value rows that no copy writes must still be finite (their weights
+        // are exact zeros, and 0 x NaN is NaN): the value ring starts as
+        // zeros (it held the item lists' scratch until the set-up's barrier),
+        // and rows past a sequence's end are cleared after their copy lands.
+        for (int u = lane; u < kStagesV * kKVStage / 16; u += 32)
+          reinterpret_cast<uint4*>(base + kOffV)[u] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();  // before any copy into the ring
+        __syncwarp();
+      }
       uint32_t k = 0;                // chunks issued into this ring over the CTA's items
       uint32_t qn[kTiles] = {0, 0};  // query-tile loads per tile
       uint32_t vl = 0;               // chunks of values cleared past their sequence's end
       bool waited = false, ok = true, landing = false;
       for (int r = 0; ok; ++r) {
-        const int j = pf_item_at(*order, r);
+        const int j = (r < *my_count ? my_items[r] : -1);
         if (j < 0) break;
         const PfItem it = pf_item(p, j, pairs);
         if (it.state) continue;
@@ -397,7 +481,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           }
           // The next item's query tiles into L2, so that their loads at the
           // item boundary do not wait on HBM.
-          const int jn = pf_item_at(*order, r + 1);
+          const int jn = (r + 1 < *my_count ? my_items[r + 1] : -1);
           if (lane == 0 && jn >= 0) {
             const PfItem nx = pf_item(p, jn, pairs);
             if (!nx.state)
@@ -550,7 +634,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         };
         uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
         for (int r = 0; ok; ++r) {
-          const int j = pf_item_at(*order, r);
+          const int j = (r < *my_count ? my_items[r] : -1);
           if (j < 0) break;
           const PfItem it = pf_item(p, j, pairs);
           if (it.state) continue;
@@ -601,7 +685,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     uint32_t sc_n = 0, ot = 0;  // S phases consumed, items finished by this tile
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int j = pf_item_at(*order, r);
+      const int j = (r < *my_count ? my_items[r] : -1);
       if (j < 0) break;
       const PfItem it = pf_item(p, j, pairs);
       if (it.state == 2) {
@@ -776,21 +860,29 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
   });
   if (init_err != cudaSuccess) return init_err;
   if (sms[dev] < 1) return cudaErrorInvalidConfiguration;
-  // Persistent CTAs, one per SM (the shared memory allows no more).
+  // Persistent CTAs, one per SM (the shared memory allows no more), each
+  // listing at most kListCap items: a larger batch takes several launches,
+  // each over a contiguous range of the items.
   const long long items = (long long)a.S * a.Hkv * pairs;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int grid = (int)std::min<long long>(items, sms[dev]);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreadsT);
-  cfg.dynamicSmemBytes = kBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, a, pairs, (int)items);
+  const long long per_launch = (long long)kListCap * sms[dev];
+  for (long long first = 0; first < items; first += per_launch) {
+    const long long n = std::min(per_launch, items - first);
+    const int grid = (int)std::min<long long>(n, sms[dev]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreadsT);
+    cfg.dynamicSmemBytes = kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, a, pairs, (int)first, (int)n);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace

@@ -76,6 +76,28 @@ def test_prefill_flops_brute_force():
             assert b["slots"][s * sh["new"] + i] == b["tables"][s, p // B] * B + p % B
 
 
+def test_ragged_prefill_batch_and_flops():
+    sh = dict(num_seqs=3, cached=[0, 9, 30], new=[4, 17, 1], num_heads=4, num_kv_heads=2, head_dim=64, block_size=8)
+    b = bench.prefill_batch(seed=4, **sh)
+    keys = sum(c + i + 1 for c, n in zip(sh["cached"], sh["new"]) for i in range(n))
+    assert bench.prefill_flops(b) == keys * sh["num_heads"] * sh["head_dim"] * 4
+    assert list(b["qs"]) == [0, 4, 21, 22] and list(b["ctx"]) == [4, 26, 31]
+    assert b["q"].shape == (22, 4, 64) and b["k"].shape == (22, 2, 64)
+    B = sh["block_size"]
+    used = set()
+    for s, (c, n) in enumerate(zip(sh["cached"], sh["new"])):
+        nb = -(-(c + n) // B)
+        used |= set(b["tables"][s, :nb].tolist())
+        for i in range(n):
+            p = c + i
+            assert b["slots"][b["qs"][s] + i] == b["tables"][s, p // B] * B + p % B
+    assert len(used) == sum(-(-(c + n) // B) for c, n in zip(sh["cached"], sh["new"]))  # no block shared
+    # the bench's ragged batch: 8 prompts, lengths in their stated ranges
+    r = bench.PREFILL_RAGGED_SHAPE
+    assert len(r["cached"]) == len(r["new"]) == r["num_seqs"] == 8
+    assert all(0 <= c <= 4096 for c in r["cached"]) and all(64 <= n <= 2048 for n in r["new"])
+
+
 def test_dram_counters_only_for_the_captured_kernel(monkeypatch):
     v = bench.decode_traffic("mha_bf16")
     assert v is None or v > 0

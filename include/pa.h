@@ -272,6 +272,17 @@ int pa_prefill(const void* q, const void* k, const void* v,
                int num_blocks, int dtype, void* stream);
 
 /*
+ * Test hook for pa_prefill's split of a large batch; not for production
+ * use.  A prefill kernel launch lists at most 440 work items per CTA, and a
+ * batch with more is attended by several launches, each over a contiguous
+ * range of the items.  This sets a smaller bound on the items of one launch
+ * (items_per_launch >= 1), so that a small batch takes the several-launch
+ * path; 0 restores the default.  It applies to the calls that follow, from
+ * every thread.  Returns PA_OK, or PA_ERR_INVALID for a negative value.
+ */
+int pa_prefill_test_items_per_launch(int items_per_launch);
+
+/*
  * Paged decode over FP8 caches written by pa_cache_append_fp8: the result of
  * pa_decode with K = e4m3(code) * k_scale and V = e4m3(code) * v_scale.  q
  * and out are bf16; head_dim 128; products in FP16 on tensor cores, sums in

@@ -76,11 +76,14 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
 #include "device_common.cuh"
 #include "kernels.h"
+#include "pa.h"
+#include "pa_internal.h"
 #include "tcgen05.cuh"
 
 namespace pa {
@@ -838,6 +841,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
 }
 
+// Test hook (pa_prefill_test_items_per_launch): a smaller bound on the
+// items of one launch; 0 for none.
+std::atomic<int> g_items_per_launch{0};
+
 template <int DH>
 cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const CUtensorMap& qmap, int pairs, cudaStream_t stream) {
@@ -865,7 +872,9 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
   // each over a contiguous range of the items.
   const long long items = (long long)a.S * a.Hkv * pairs;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const long long per_launch = (long long)kListCap * sms[dev];
+  long long per_launch = (long long)kListCap * sms[dev];
+  const int cap = g_items_per_launch.load(std::memory_order_relaxed);
+  if (cap > 0) per_launch = std::min<long long>(per_launch, cap);
   for (long long first = 0; first < items; first += per_launch) {
     const long long n = std::min(per_launch, items - first);
     const int grid = (int)std::min<long long>(n, sms[dev]);
@@ -898,3 +907,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
 }
 
 }  // namespace pa
+
+extern "C" int pa_prefill_test_items_per_launch(int items_per_launch) {
+  if (items_per_launch < 0) return pa_fail(PA_ERR_INVALID, "pa_prefill_test_items_per_launch: negative");
+  pa::g_items_per_launch.store(items_per_launch, std::memory_order_relaxed);
+  return PA_OK;
+}

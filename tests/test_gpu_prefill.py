@@ -213,3 +213,26 @@ def test_prefill_ragged_many_items_sampled(pa, name):
         tokens.append(sorted(idx))
     _check_sampled_tokens(b, out, kc, prev, tokens, H, Hkv)
     assert pa.get_status() == 0
+
+
+@pytest.mark.parametrize("cap", [7, 50])
+def test_prefill_over_several_launches(pa, cap):
+    """A batch attended by several kernel launches, each over a contiguous
+    range of the work items (the path of batches with more items than one
+    launch lists), here forced with a small bound on the items of a launch:
+    the same result as one launch, and the oracle's."""
+    prev, new, H, Hkv, D, B = CASES["g4_d128_b16"]  # 48 work items
+    b = _batch(21, prev, new, H, Hkv, D, B)
+    one, _, _ = _run(pa, b)
+    assert pa.lib().pa_prefill_test_items_per_launch(cap) == 0
+    try:
+        out, kc, vc = _run(pa, b)
+    finally:
+        assert pa.lib().pa_prefill_test_items_per_launch(0) == 0
+    kc_o, vc_o, ref = oracle_prefill(b["q"], b["k"], b["v"], b["slots"], b["qs"], b["ctx"], b["tables"], b["kc"],
+                                     b["vc"], b["scale"], "bf16")
+    assert np.array_equal(to_bits(kc), kc_o) and np.array_equal(to_bits(vc), vc_o)
+    assert_close(out, ref, "bf16", f"{cap} items per launch")
+    assert torch.equal(out, one)
+    assert pa.get_status() == 0
+    assert pa.lib().pa_prefill_test_items_per_launch(-1) == -1

@@ -25,12 +25,14 @@
 //    dims 4t, 4t+1 and k 2t+8, 2t+9 are dims 4t+2, 4t+3 -- and Q's fragments
 //    are built in the same order (a dot product does not depend on it).
 //  * Oᵀ = Vᵀ Pᵀ: the 8-bit transposing ldmatrix (m16n16) of a 16-token x
-//    16-dim V tile gives a lane one dim of four consecutive tokens, so the
+//    16-dim V tile gives a lane one dim of four consecutive tile rows, so the
 //    token order of each 16-token step is permuted the same way (k 2t, 2t+1
-//    are tokens 4t, 4t+1 and k 2t+8, 2t+9 tokens 4t+2, 4t+3).  The rows of
-//    each step's Sᵀ are gathered in the matching order -- tokens
-//    {0,1,4,5,8,9,12,13} then {2,3,6,7,10,11,14,15} -- so that a transposing
-//    movmatrix of each 8 x 8 half of P gives exactly the B operand.
+//    are tile rows 4t, 4t+1 and k 2t+8, 2t+9 tile rows 4t+2, 4t+3; tile row
+//    i is token pf8_row(i)).  The rows of each step's Sᵀ are gathered in the
+//    matching order -- tokens {0,1,4,5,10,11,14,15} then {2,3,6,7,8,9,12,13}
+//    -- so that a transposing movmatrix of each 8 x 8 half of P gives exactly
+//    the B operand, and the eight key rows of each 8 x 8 matrix lie in eight
+//    different bank groups.
 //  * The online softmax keeps, per lane, heads 2t and 2t+1; their maxima
 //    are reduced over the eight lanes holding the other tokens, and O (held
 //    as Oᵀ, heads as columns) is rescaled without shuffles.
@@ -99,6 +101,14 @@ __device__ __forceinline__ Bars bars_at(uint8_t* base) {
 __device__ __forceinline__ void ldmatrix_b8_trans(uint32_t addr, uint32_t& d0, uint32_t& d1) {
   asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];" : "=r"(d0), "=r"(d1) : "r"(addr));
 }
+
+// Token of tile row i (0-15) of a 16-token step of values: rows 0-7 are
+// tokens 0-7, rows 8-15 tokens 10, 11, 8, 9, 14, 15, 12, 13.  Any order
+// serves (the key rows follow it); this one makes the rows that one 8 x 8
+// matrix of the keys' ldmatrix reads fall in eight different 16-byte bank
+// groups of the 128-byte swizzle (the plain order put tokens t and t + 8
+// in the same one).
+__device__ __forceinline__ int pf8_row(int i) { return i ^ ((i & 8) >> 2); }
 
 // Two E4M3 codes (low byte first) -> two f16 (low half first); exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
@@ -259,10 +269,12 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
   float2* sML = reinterpret_cast<float2*>(base + kOffML);
   const uint32_t base_addr = smem_addr(base);
   // Key row of this lane's ldmatrix address within a 16-token step: rows
-  // 0-7 of the step's Sᵀ tile are tokens {0,1,4,5,8,9,12,13}, rows 8-15
-  // tokens {2,3,6,7,10,11,14,15} (lane L addresses row L % 8 of matrix L / 8;
-  // odd matrices hold rows 8-15).
-  const int krow = 4 * ((lane & 7) >> 1) + (lane & 1) + 2 * ((lane >> 3) & 1);
+  // 0-7 of the step's Sᵀ tile are tokens {0,1,4,5,10,11,14,15}, rows 8-15
+  // tokens {2,3,6,7,8,9,12,13} (lane L addresses row L % 8 of matrix L / 8;
+  // odd matrices hold rows 8-15): the order of the values' tile rows
+  // (pf8_row), each half eight different rows modulo 8, i.e. eight different
+  // 16-byte bank groups of the swizzled stage.
+  const int krow = pf8_row(4 * ((lane & 7) >> 1) + (lane & 1) + 2 * ((lane >> 3) & 1));
   uint32_t kseq = 0;
 
   for (uint32_t n = 0;; ++n) {
@@ -340,15 +352,16 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         }
       }
       // Online softmax (log2 domain) of heads 2tq, 2tq + 1 over this chunk:
-      // this lane holds tokens 4(gq / 2) + (gq % 2) and that + 2 of each step;
-      // the other seven of each head are on the lanes with the same tq.
+      // this lane holds tokens pf8_row(4(gq / 2) + (gq % 2)) and
+      // pf8_row(that + 2) of each step; the other seven of each head are on
+      // the lanes with the same tq.
       const int tok_lo = 4 * (gq >> 1) + (gq & 1);
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int jj = 0; jj < KSTEPS; ++jj) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int tok = 16 * jj + tok_lo + 2 * (c >> 1);
+          const int tok = 16 * jj + pf8_row(tok_lo + 2 * (c >> 1));
           const float v = tok < nv ? st[jj][c] * p.scale_log2 : -INFINITY;
           st[jj][c] = v;
           mx[c & 1] = fmaxf(mx[c & 1], v);
@@ -388,12 +401,13 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         pb[jj][0] = movmatrix_trans(pack_f16x2(e0, e1));
         pb[jj][1] = movmatrix_trans(pack_f16x2(e2, e3));
       }
-      // Oᵀ += Vᵀ Pᵀ : 16 tokens per step, 16 dims per tile.
+      // Oᵀ += Vᵀ Pᵀ : 16 tokens per step, 16 dims per tile; lane i < 16
+      // addresses tile row i, token pf8_row(i) of the step.
 #pragma unroll
       for (int kt = 0; kt < KSTEPS; ++kt) {
-        const uint32_t pb0 = pb[kt][0];  // tokens 4tq, 4tq+1 of the step, head gq
-        const uint32_t pb1 = pb[kt][1];  // tokens 4tq+2, 4tq+3
-        const int r = 16 * kt + (lane & 15);
+        const uint32_t pb0 = pb[kt][0];  // tile rows 4tq, 4tq+1 of the step, head gq
+        const uint32_t pb1 = pb[kt][1];  // tile rows 4tq+2, 4tq+3
+        const int r = 16 * kt + pf8_row(lane & 15);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t d0, d1;

@@ -58,7 +58,7 @@ def kv_bytes(ctx: np.ndarray, w, groups=None, partition_size: int = 0, elem_byte
 
 
 DECODE_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_tc.cu", "paged_kv_cache_216_gb300/csrc/device_common.cuh",
-                  "paged_kv_cache_216_gb300/csrc/kernels.h")
+                  "paged_kv_cache_216_gb300/csrc/kernels.h", "paged_kv_cache_216_gb300/csrc/block_layout.cuh")
 DECODE_FP8_SOURCES = ("paged_kv_cache_216_gb300/csrc/decode_fp8.cu", "paged_kv_cache_216_gb300/csrc/device_common.cuh",
                       "paged_kv_cache_216_gb300/csrc/kernels.h")
 

@@ -97,30 +97,17 @@ int make_cache_map_fp8(CUtensorMap* map, const void* base, int num_blocks, int H
   return PA_OK;
 }
 
-int make_cache_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D, bool inter) {
-  auto fn = encode_fn();
-  if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t rows = (cuuint64_t)num_blocks * Hkv * B;
-  cuuint64_t dims[2] = {inter ? 64u : (cuuint64_t)D, inter ? rows * (D / 64) : rows};
-  cuuint64_t strides[1] = {inter ? 128u : (cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, inter ? (cuuint32_t)(B * (D / 64)) : (cuuint32_t)B};
-  cuuint32_t elem_strides[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  return PA_OK;
-}
-
-// The cache [N_blk][Hkv][B][D] bf16 for the tcgen05 prefill, as 4D
-// (64 dims, 8 rows, 64-dim half, group of 8 rows): a box of (64, 8, D / 64,
-// B / 8) brings one block of one head in one copy and lands as groups of 8
-// rows, each group holding its halves 1 KB apart ([group][half][8 rows]
-// [128 B], 128-byte swizzle), so 8-row groups are a uniform D / 64 KB apart:
-// the layout of a K-major operand of the tensor cores (keys) and of an
-// MN-major one (values).  Two 2D boxes per block (one per half) were half as
-// large, and a chunk of 128 keys and values was 32 boxes: more than the
-// TMA unit issues in the time the tensor cores take for the chunk.
+// The cache [N_blk][Hkv][B][D] bf16 for the tensor-core kernels (decode and
+// prefill), as 4D (64 dims, 8 rows, 64-dim half, group of 8 rows): a box of
+// (64, 8, D / 64, B / 8) brings one block of one head in one copy and lands
+// as groups of 8 rows, each group holding its halves 1 KB apart ([group]
+// [half][8 rows][128 B], 128-byte swizzle), so 8-row groups are a uniform
+// D / 64 KB apart: the layout of a K-major operand of the tensor cores
+// (keys) and of an MN-major one (values), and for ldmatrix eight rows of a
+// half in eight different bank groups.  Two 2D boxes per block (one per
+// half) were half as large: for the prefill a chunk of 128 keys and values
+// was 32 boxes, more than the TMA unit issues in the time the tensor cores
+// take for the chunk.
 int make_block_map(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B, int D) {
   auto fn = encode_fn();
   if (!fn) return pa_fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
@@ -443,10 +430,9 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   cudaError_t e;
   if (dtype == PA_BF16) {
     CUtensorMap kmap, vmap;
-    const bool inter = pa::decode_tc_interleaved(head_dim, block_size, pg.n > 0);
-    rc = make_cache_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
+    rc = make_block_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
     if (rc) return rc;
-    rc = make_cache_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim, inter);
+    rc = make_block_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
     if (rc) return rc;
     if (!plan) {
       e = pa::launch_decode_plan(a, pg, st);

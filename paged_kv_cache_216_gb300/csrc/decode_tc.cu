@@ -38,6 +38,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "block_layout.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -117,18 +118,7 @@ __device__ __forceinline__ void give_up(const DecodeArgs& p, volatile int* abort
   raise_status(p.status, PA_STATUS_TIMEOUT);
 }
 
-// kInter: each 256-byte token row is two 128-byte lines of the stage
-// (line 2t + half) and one TMA box brings a whole [B x D] slab; otherwise
-// the two 64-dim halves of a chunk are separate 32-line regions (line
-// half*32 + t) filled by one box per half.  The first halves the number of
-// TMA requests (used for 8-token blocks, whose per-half boxes are only
-// 1 KB); the second keeps ldmatrix free of bank conflicts.
-template <int D, bool kInter>
-__device__ __forceinline__ int stage_line(int t, int half) {
-  return kInter ? 2 * t + half : half * kChunk + t;
-}
-
-template <int D, bool kInter, bool kShared>
+template <int D, bool kShared>
 __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const DecodeArgs& p, uint8_t* base,
                          volatile int* abort) {
   using C = TcCfg<D>;
@@ -226,20 +216,11 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
       if (issue && lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * chunk_block_bytes);
       __syncwarp();
       if (issue && lane < nb) {
-        const int y = (id * p.Hkv + kvh) * p.B;
-        if constexpr (kInter) {
-          uint8_t* sk = base + stage * C::kStage + lane * p.B * 256;
-          tma_load_2d(sk, kmap, &bar.full[stage], 0, 2 * y, policy);
-          tma_load_2d(sk + C::kRegion, vmap, &bar.full[stage], 0, 2 * y, policy);
-        } else {
-          uint8_t* sk = base + stage * C::kStage + lane * p.B * 128;
-          uint8_t* sv = sk + C::kRegion;
-#pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf) {
-            tma_load_2d(sk + hf * kHalfBytes, kmap, &bar.full[stage], hf * 64, y, policy);
-            tma_load_2d(sv + hf * kHalfBytes, vmap, &bar.full[stage], hf * 64, y, policy);
-          }
-        }
+        // one box per block: both halves of its B rows, 8-row groups
+        uint8_t* sk = base + stage * C::kStage + lane * p.B * D * 2;
+        const int grp = (id * p.Hkv + kvh) * (p.B >> 3);
+        tma_load_4d(sk, kmap, &bar.full[stage], 0, 0, 0, grp, policy);
+        tma_load_4d(sk + C::kRegion, vmap, &bar.full[stage], 0, 0, 0, grp, policy);
       }
       if (ch == 0 && lane == 0 && nxt_idx < total) nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
     }
@@ -329,7 +310,8 @@ __device__ bool group_item(const DecodeArgs& p, uint8_t* base, const Bars& bar, 
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8,
-                 smem_desc(sk + (kk >> 2) * kHalfBytes, 16, 1024) + (uint64_t)(((kk & 3) * 32) >> 4), id_s, kk > 0);
+                 smem_desc(sk, 16, C::kHalves * 1024) + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4), id_s,
+                 kk > 0);
         mma_commit(bar.s_ready);
       } else {
         give_up(p, abort);
@@ -394,7 +376,8 @@ __device__ bool group_item(const DecodeArgs& p, uint8_t* base, const Bars& bar, 
 #pragma unroll
         for (int kk = 0; kk < kChunk / 16; ++kk)
           mma_ts(tmem + C::kColO, tmem + C::kColS + kk * 8,
-                 smem_desc(sv, kHalfBytes, 1024) + (uint64_t)((kk * 16 * 128) >> 4), id_o, ch > 0 || kk > 0);
+                 smem_desc(sv, 1024, C::kHalves * 1024) + (uint64_t)((kk * 2 * C::kHalves * 1024) >> 4), id_o,
+                 ch > 0 || kk > 0);
         mma_commit(&bar.empty[stage]);  // the stage is free once this chunk's products are done
         if (ch + 1 == nch) mma_commit(bar.o_done);
       } else {
@@ -427,7 +410,7 @@ __device__ bool group_item(const DecodeArgs& p, uint8_t* base, const Bars& bar, 
   return ok;
 }
 
-template <int D, bool kInter, bool kShared>
+template <int D, bool kShared>
 __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort, uint32_t tmem) {
   using C = TcCfg<D>;
   constexpr int KS = D / 16;  // k-steps of the Q·Kᵀ product
@@ -516,7 +499,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         for (int u = lane; u < units; u += 32) {
           const int r = nv + u / (C::kHalves * 8);
           const int rem = u % (C::kHalves * 8);
-          *reinterpret_cast<uint4*>(vrow + stage_line<D, kInter>(r, rem >> 3) * 128 + (rem & 7) * 16) =
+          *reinterpret_cast<uint4*>(vrow + kv_row_offset<C::kHalves>(r, rem >> 3) + (rem & 7) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -532,8 +515,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
         for (int nt = 0; nt < 4; ++nt) {
           const int t = nt * 8 + (lane & 7);
           const int cidx = 4 * kk + (lane >> 3);
-          const int line = stage_line<D, kInter>(t, cidx >> 3);
-          const uint32_t addr = sk + line * 128 + (((cidx & 7) ^ (line & 7)) << 4);
+          const uint32_t addr = sk + kv_row_offset<C::kHalves>(t, cidx >> 3) + (((cidx & 7) ^ (t & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(addr, b0, b1, b2, b3);
           mma_bf16_16816(sc[nt], qa[2 * kk][0], 0u, qa[2 * kk][1], 0u, b0, b1);
@@ -586,8 +568,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int cidx = 2 * mt + ((lane >> 3) & 1);
-          const int line = stage_line<D, kInter>(t, cidx >> 3);
-          const uint32_t addr = sv + line * 128 + (((cidx & 7) ^ (line & 7)) << 4);
+          const uint32_t addr = sv + kv_row_offset<C::kHalves>(t, cidx >> 3) + (((cidx & 7) ^ (t & 7)) << 4);
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4_trans(addr, a0, a1, a2, a3);
           mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
@@ -682,7 +663,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
   }
 }
 
-template <int D, bool kInter, bool kShared>
+template <int D, bool kShared>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const DecodeArgs p) {
@@ -724,9 +705,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    producer<D, kInter, kShared>(&kmap, &vmap, p, base, abort);
+    producer<D, kShared>(&kmap, &vmap, p, base, abort);
   } else {
-    consumer<D, kInter, kShared>(p, base, abort, tmem);
+    consumer<D, kShared>(p, base, abort, tmem);
   }
   if (kShared) {
     // Every MMA issued has completed before tensor memory is released.
@@ -748,29 +729,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 size_t decode_tc_smem_bytes(int D) { return D == 128 ? TcCfg<128>::kBytes : TcCfg<64>::kBytes; }
 
-bool decode_tc_interleaved(int D, int B, bool shared_items) { return D == 128 && B == 8 && !shared_items; }
-
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream) {
   const size_t smem = decode_tc_smem_bytes(a.D);
-  const bool inter = decode_tc_interleaved(a.D, a.B, a.shared_items != 0);
   using Kern = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
-  // [shared items][D == 128 ? (inter ? 2 : 1) : 0]; shared-prefix items read
-  // their stages as tensor-core operands, which the interleaved layout is not
-  static const Kern kernels[2][3] = {
-      {paged_decode_tc_kernel<64, false, false>, paged_decode_tc_kernel<128, false, false>,
-       paged_decode_tc_kernel<128, true, false>},
-      {paged_decode_tc_kernel<64, false, true>, paged_decode_tc_kernel<128, false, true>,
-       paged_decode_tc_kernel<128, false, true>}};
-  const Kern kern = kernels[a.shared_items ? 1 : 0][a.D == 128 ? (inter ? 2 : 1) : 0];
+  // [shared items][D == 128]
+  static const Kern kernels[2][2] = {
+      {paged_decode_tc_kernel<64, false>, paged_decode_tc_kernel<128, false>},
+      {paged_decode_tc_kernel<64, true>, paged_decode_tc_kernel<128, true>}};
+  const int v = a.shared_items ? 1 : 0, k = a.D == 128 ? 1 : 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  // Per-device launch shape, computed once (threads of one process share it).
   // Per-device launch shape of each variant, computed once (threads of one
   // process share it).
   struct Shape {
-    int sms = 0, per_sm[2][3] = {};
+    int sms = 0, per_sm[2][2] = {};
   };
   static Shape shapes[64];
   static std::once_flag once[64];
@@ -779,24 +753,26 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const
   std::call_once(once[dev], [&] {
     Shape sh;
     init_err = cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev);
-    for (int v = 0; v < 2 && init_err == cudaSuccess; ++v)
-      for (int k = 0; k < 3 && init_err == cudaSuccess; ++k) {
-        const size_t bytes = k ? TcCfg<128>::kBytes : TcCfg<64>::kBytes;
-        init_err = cudaFuncSetAttribute(kernels[v][k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    for (int vi = 0; vi < 2 && init_err == cudaSuccess; ++vi)
+      for (int ki = 0; ki < 2 && init_err == cudaSuccess; ++ki) {
+        const size_t bytes = ki ? TcCfg<128>::kBytes : TcCfg<64>::kBytes;
+        init_err = cudaFuncSetAttribute(kernels[vi][ki], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (init_err == cudaSuccess)
-          init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm[v][k], kernels[v][k], kThreads, bytes);
+          init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm[vi][ki], kernels[vi][ki], kThreads,
+                                                                   bytes);
       }
     shapes[dev] = sh;
   });
   if (init_err != cudaSuccess) return init_err;
   const Shape& sh = shapes[dev];
-  int per_sm = sh.per_sm[a.shared_items ? 1 : 0][a.D == 128 ? (inter ? 2 : 1) : 0];
+  const Kern kern = kernels[v][k];
+  int per_sm = sh.per_sm[v][k];
   if (a.shared_items) {
     // The occupancy query counts a kernel that allocates tensor memory as
     // one CTA per SM.  This one holds 256 of the SM's 512 columns, so two
     // fit, as registers and shared memory allow (the same as the plain
     // variant's); a CTA that does not fit waits for one to finish.
-    per_sm = std::min(sh.per_sm[0][a.D == 128 ? 1 : 0], (int)(512 / TcCfg<128>::kTmemCols));
+    per_sm = std::min(sh.per_sm[0][k], (int)(512 / TcCfg<128>::kTmemCols));
   }
   if (per_sm < 1 || sh.sms < 1) return cudaErrorInvalidConfiguration;
   const long long total = (long long)a.max_parts * a.S * a.Hkv;  // upper bound of the work items

@@ -97,16 +97,12 @@ __host__ __device__ inline int prefix_parts_of(const PrefixGroups& pg, int s) {
   return (at >= 0 && s < pg.first[at] + pg.count[at]) ? pg.parts[at] : 0;
 }
 
-// bf16, tensor cores; grid = persistent CTAs.
+// bf16, tensor cores; grid = persistent CTAs.  kmap/vmap: the bf16 caches
+// as 4D block maps (one box per block of one KV head, block_layout.cuh).
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream);
 // Dynamic shared memory of the tensor-core kernel for this head_dim.
 size_t decode_tc_smem_bytes(int D);
-// Whether the tensor-core kernel loads whole [B x D] slabs as one TMA box
-// of 2B lines of 128 bytes (true) or one box per 64-dim half (false); the
-// cache tensor maps must be made to match.  Calls with shared-prefix items
-// use the per-half boxes.
-bool decode_tc_interleaved(int D, int B, bool shared_items);
 
 // FP8 (E4M3) caches, head_dim 128, bf16 q/out; same work list, workspace and
 // merge as the bf16 kernel.  scale_log2 must include the K scale.

@@ -80,6 +80,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "block_layout.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 #include "pa.h"
@@ -145,24 +146,6 @@ struct PfCfg {
   static_assert(kColS + kTiles * 128 <= kTmemCols, "tensor-memory columns");
 };
 constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grows by more than 2^8
-
-// 4D tiled TMA load of one box (a block of the cache, see the block map of
-// the host side); x is the innermost (element) coordinate.
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
-                                            int w, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
-// Byte offset in a stage of keys or values of key row t (within the chunk)
-// and 64-dim half h: 8-row groups kHalves KB apart, halves 1 KB apart.
-template <int kHalves>
-__device__ __forceinline__ int kv_row_offset(int t, int h) {
-  return (t >> 3) * (kHalves * 1024) + h * 1024 + (t & 7) * 128;
-}
 
 // Work item j of S * Hkv * pairs: pair of query tiles pairs - 1 - j / (S * Hkv)
 // (the pairs with the most keys first), sequence (j / Hkv) % S, KV head

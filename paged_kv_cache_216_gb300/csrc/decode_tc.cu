@@ -14,12 +14,13 @@
 //    through an atomic counter, the dynamic work queue of the same page's
 //    section 3.2; the producer claims the next item as it starts one.
 //  * Warp 4 is the producer.  For each item it writes the item's descriptor
-//    and bulk-copies its g query rows into a 2-slot Q ring, then streams the item's keys and values
-//    32 tokens at a time into a ring of shared-memory stages: per cache block
-//    of the chunk, one 2D TMA box of [B rows x 64 dims] per 64-dim half, for
-//    K and for V, with 128-byte swizzle.  Block ids are read 32 at a time
-//    (one per lane) one window ahead.  This is the prefetch of the same
-//    page's section 2.2, done by the copy engine.
+//    and bulk-copies its g query rows into a 2-slot Q ring, then streams
+//    the item's keys and values 32 tokens at a time into a ring of
+//    shared-memory stages: one TMA box per cache block of the chunk for K
+//    and one for V (the 4D block view of block_layout.cuh: 8-row groups
+//    holding both 64-dim halves, 128-byte swizzle).  Block ids are read 32
+//    at a time (one per lane) one window ahead.  This is the prefetch of the
+//    same page's section 2.2, done by the copy engine.
 //  * Warps 0-3 are consumers; warp w takes the item's chunks w, w+4, ...
 //    For a chunk, S = Q Kᵀ uses mma.m16n8k16 with the g query heads as the
 //    16 rows of A (rows >= g are zero) and 8 tokens per B tile (ldmatrix
@@ -49,7 +50,7 @@ namespace {
 constexpr int kChunk = 32;  // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kHalfBytes = kChunk * 128;  // one 64-dim half of 32 rows
+constexpr int kHalfBytes = kChunk * 128;  // one 64-dim half of a chunk's 32 rows
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>

@@ -15,7 +15,9 @@
 // weighted sum with shuffles and hands each partition's weight to the other
 // lanes, which then sum the weighted partial rows, lane L holding D/32
 // consecutive dims (each row one coalesced 4*D-byte line, no row's load
-// waiting for another's, 16 rows in flight).  The group's warps are combined
+// waiting for another's, 16 rows in flight).  When no context has more than
+// 16 partitions, a variant issues a warp's (max, sum) and row loads all
+// together, one round trip to L2 instead of two.  The group's warps are combined
 // through shared memory.  Sequences that fit one partition were written by
 // the decode kernel and are skipped, unless they belong to a prefix group:
 // there even a single partition is a partial written by the shared-prefix
@@ -35,8 +37,11 @@ namespace pa {
 namespace {
 
 constexpr int kMaxWarps = 8;
+// Calls whose contexts have at most this many partitions run a variant in
+// which each warp (one per row) issues all its loads at once.
+constexpr int kBatch = 16;
 
-template <typename T, int D>
+template <typename T, int D, bool kAllAtOnce>
 __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeArgs p, int wpr,
                                                                     const __grid_constant__ PrefixGroups pg) {
   constexpr int E = D / 32;
@@ -65,7 +70,41 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
     // Their max and weight sum first, the lanes taking partitions: then the
     // weight of every partial row is known and the rows' loads below do not
     // wait on one another (a running max would chain them).
-    if (cnt <= 32) {
+    if (kAllAtOnce) {
+      // every load at once (cnt <= kBatch): lane i < cnt reads partition i's (max, sum),
+      // and each lane its dims of all cnt partial rows; the weights follow
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (lane < cnt) ml = p.ws_ml[base + (size_t)(wg + lane * wpr) * p.H];
+      float x[kBatch][E];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (i < cnt) {
+          const float* src = p.ws_o + (base + (size_t)(wg + i * wpr) * p.H) * D + lane * E;
+          if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            x[i][0] = v.x, x[i][1] = v.y, x[i][2] = v.z, x[i][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            x[i][0] = v.x, x[i][1] = v.y;
+          }
+        }
+      }
+      m = ml.x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const float w = lane < cnt ? exp2f(ml.x - m) : 0.f;
+      l = w * ml.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const float b = __shfl_sync(0xffffffffu, w, i);
+        if (i < cnt) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] += x[i][e] * b;
+        }
+      }
+    } else if (cnt <= 32) {
       // one partition per lane: its (max, sum) is read once and its weight
       // handed to the other lanes
       float2 ml = make_float2(-INFINITY, 0.f);
@@ -155,8 +194,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32) lse_merge_kernel(const DecodeA
 
 template <typename T, int D>
 cudaError_t launch_typed(const DecodeArgs& a, const PrefixGroups& pg, cudaStream_t stream) {
-  // Warps per (sequence, head): enough to keep several partial rows in
-  // flight for the longest context without idling warps on short ones.
+  // Warps per (sequence, head): one while every context has at most kBatch
+  // partitions (all loads at once), else enough to keep several partial rows
+  // in flight for the longest context without idling warps on short ones.
+  const bool all_at_once = a.max_parts <= kBatch;
   const int wpr = a.max_parts >= 32 ? 8 : 1;
   const long long pairs = (long long)a.S * a.H;
   const int per_cta = kMaxWarps / wpr;
@@ -170,7 +211,8 @@ cudaError_t launch_typed(const DecodeArgs& a, const PrefixGroups& pg, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D>, a, wpr, pg);
+  if (all_at_once) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D, true>, a, wpr, pg);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<T, D, false>, a, wpr, pg);
 }
 
 }  // namespace

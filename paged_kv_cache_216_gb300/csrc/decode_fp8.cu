@@ -60,10 +60,14 @@ constexpr int kStage = 2 * kRegion;
 // multiple of the consumer warps, a stage passes from warp to warp, so a
 // warp waits for the release of its stage's previous chunk before testing
 // the stage's full barrier (which could otherwise be two phases behind and
-// pass the parity test on the wrong phase).
+// pass the parity test on the wrong phase).  That wait is itself exact
+// only while there are no more consumer warps than stages: a warp at chunk
+// k knows that chunk k - W - S was released (its previous chunk, k - W, was
+// filled after it), and its parity tests need chunk k - 2S released.
 constexpr int kStages = 5;
 constexpr int KSTEPS = kChunk / 16;          // 16-token steps of P·V per stage
 constexpr int kConsumerWarps = 4;
+static_assert(kConsumerWarps <= kStages, "the stage hand-off between warps needs W <= S");
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kQSlot = kMaxGroup * kD * 2;   // bf16 query rows of one item

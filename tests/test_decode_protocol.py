@@ -40,8 +40,9 @@ END = "end"
 
 
 class DecodeSim(EventSim):
-    def __init__(self, items, stages, seed, mutate=None, release_wait=False):
+    def __init__(self, items, stages, seed, mutate=None, release_wait=False, warps=WARPS):
         super().__init__(seed)
+        self.W = warps
         self.mutate = mutate
         self.release_wait = release_wait
         # chunks of each work item (0 for an empty context); ("g", n) is a
@@ -51,21 +52,21 @@ class DecodeSim(EventSim):
         self.full = [Bar(f"full{i}", 1) for i in range(stages)]
         self.empty = [Bar(f"empty{i}", 1) for i in range(stages)]
         self.qfull = [Bar(f"qfull{i}", 1) for i in range(2)]
-        self.qempty = [Bar(f"qempty{i}", WARPS) for i in range(2)]
-        self.epi_full = Bar("epi_full", WARPS)
-        self.epi_done = Bar("epi_done", WARPS)
+        self.qempty = [Bar(f"qempty{i}", self.W) for i in range(2)]
+        self.epi_full = Bar("epi_full", self.W)
+        self.epi_done = Bar("epi_done", self.W)
         self.stage = [None] * stages  # chunk held by each stage
         self.desc = [None, None]  # item described by each slot
         self.q = [None, None]  # item whose query rows each slot holds
-        self.state = [None] * WARPS  # item whose partial state each warp has stored
+        self.state = [None] * self.W  # item whose partial state each warp has stored
         self.combined = {}  # item -> warps that finished its combine
-        self.q_ready = Bar("q_ready", WARPS)
+        self.q_ready = Bar("q_ready", self.W)
         self.s_ready = Bar("s_ready", 1)
-        self.p_ready = Bar("p_ready", WARPS)
+        self.p_ready = Bar("p_ready", self.W)
         self.o_done = Bar("o_done", 1)
         self.pipe_free = 0.0
-        self.gi = [0] * WARPS  # shared-prefix items each warp has finished
-        self.gch = [0] * WARPS  # their chunks
+        self.gi = [0] * self.W  # shared-prefix items each warp has finished
+        self.gch = [0] * self.W  # their chunks
         self.s_done = -1  # last chunk whose S has completed
 
     @staticmethod
@@ -82,8 +83,8 @@ class DecodeSim(EventSim):
         self.pipe(0.0, lambda: None, lambda: self.arrive(bar))
 
     def run(self):
-        roles = [self.producer()] + [self.consumer(w) for w in range(WARPS)]
-        return self.run_roles(roles, {"producer"} | {f"w{w}" for w in range(WARPS)})
+        roles = [self.producer()] + [self.consumer(w) for w in range(self.W)]
+        return self.run_roles(roles, {"producer"} | {f"w{w}" for w in range(self.W)})
 
     def producer(self):
         k = 0
@@ -133,7 +134,7 @@ class DecodeSim(EventSim):
                 self.fail(f"warp {w} item {n}: query overwritten while read")
             self.arrive(self.qempty[slot])
             for _ in range(self.items[n]):
-                if k % WARPS == w:
+                if k % self.W == w:
                     st = k % self.S
                     if self.release_wait and k >= self.S:
                         # the stage's previous chunk (another warp's) has been released
@@ -204,7 +205,7 @@ class DecodeSim(EventSim):
         if True:
             if n > 0:
                 yield ("wait", self.epi_done, (n - 1) & 1, n, f"warp {w} epilogue {n} (previous combine)")
-                if len(self.combined.get(n - 1, ())) != WARPS:
+                if len(self.combined.get(n - 1, ())) != self.W:
                     self.fail(f"warp {w} stores item {n} before item {n - 1} is combined")
             self.state[w] = n
             self.arrive(self.epi_full)
@@ -275,3 +276,24 @@ def test_any_stage_count_is_race_free_when_a_warp_waits_for_the_previous_release
             items = _items(random.Random(4000 + seed), group=group)
             v = DecodeSim(items, stages, seed, release_wait=True).run()
             assert not v, f"seed {seed}, items {items}: {v[:3]}"
+
+
+@pytest.mark.parametrize("warps,stages,race_free", [(6, 5, False), (6, 6, True), (6, 7, True), (4, 5, True)])
+def test_stage_passing_needs_no_more_warps_than_stages(warps, stages, race_free):
+    """A warp that waits for its stage's previous release (the FP8 kernel's
+    protocol) can still pass that wait, and the full one after it, two
+    phases early when the consumer warps outnumber the stages: a warp at
+    chunk k knows only that chunks up to k - W - S were released (its own
+    previous chunk k - W was filled), while its parity waits are exact only
+    if chunk k - 2S was.  With W <= S that always holds."""
+    import random
+
+    caught = 0
+    for seed in range(150):
+        items = _items(random.Random(3000 + seed))
+        caught += bool(DecodeSim(items, stages, seed, release_wait=True, warps=warps).run())
+    if race_free:
+        assert caught == 0
+    else:
+        assert caught > 0
+

@@ -35,13 +35,24 @@ def _check_common(d):
 
 
 def test_decode_reference_line():
+    """The line for a given workload (the tiny batch: the default long-context
+    batch takes minutes to synthesise on a slow host; the arm is the same)."""
     sys.path.insert(0, ROOT)
     import bench
 
-    d = _run()
+    d = _run("--workload", "tiny_f32")
     _check_common(d)
     assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
-    assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD
+    assert d["config"]["workload"] == "tiny_f32"
+
+
+def test_reference_arm_defaults_to_our_workload():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.DEFAULT_WORKLOAD == "long_bf16"
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert 'ap.add_argument("--workload", default=DEFAULT_WORKLOAD' in src
 
 
 def test_prefill_reference_line():

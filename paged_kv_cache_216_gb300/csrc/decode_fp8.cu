@@ -6,13 +6,15 @@
 // ("Core Ideas" 1).  Stored code c of a cache with scale s reads as
 // e4m3(c) * s.
 //
-// Same schedule as the bf16 kernel (decode_tc.cu): persistent CTAs take
-// (sequence, partition, KV head) items from the longest-first work list
-// through an atomic counter; warp 4 loads each item's g query rows and
-// streams its blocks by TMA into a 4-stage shared-memory ring (one box of
+// The schedule of the bf16 kernel (decode_tc.cu): persistent CTAs, two per
+// SM, take (sequence, partition, KV head) items from the longest-first work
+// list through an atomic counter; warp 5 loads each item's g query rows and
+// streams its blocks by TMA into a 5-stage shared-memory ring (one box of
 // [B tokens x 128 bytes] per block for keys and one for values, 128-byte
-// swizzle), 64 tokens per stage; warps 0-3 take the chunks in turn and
-// merge their (max, sum, O) states at the end of the item.  Head dim 128.
+// swizzle), 64 tokens per stage; warps 0-4 take the chunks in turn (one
+// more consumer warp than the bf16 kernel: this consumer does about three
+// times the work per byte) and merge their (max, sum, O) states at the end
+// of the item.  Head dim 128.
 //
 // The consumer never widens a whole stage: it reads codes with ldmatrix and
 // converts them in registers (cvt e4m3x2 -> f16x2, exact), so each code
@@ -56,17 +58,19 @@ constexpr int kD = 128;                      // head_dim
 constexpr int kChunk = 64;                   // tokens per pipeline stage
 constexpr int kRegion = kChunk * kD;         // 8 KB: the keys (or values) of a stage
 constexpr int kStage = 2 * kRegion;
-// Five stages (80 KB) fit two CTAs per SM; with the stage count not a
-// multiple of the consumer warps, a stage passes from warp to warp, so a
-// warp waits for the release of its stage's previous chunk before testing
-// the stage's full barrier (which could otherwise be two phases behind and
-// pass the parity test on the wrong phase).  That wait is itself exact
-// only while there are no more consumer warps than stages: a warp at chunk
-// k knows that chunk k - W - S was released (its previous chunk, k - W, was
-// filled after it), and its parity tests need chunk k - 2S released.
+// Five stages (80 KB) fit two CTAs per SM.  Chunk k goes to stage k mod S
+// and consumer warp k mod W; when S is not a multiple of W a stage passes
+// from warp to warp, so a warp waits for the release of its stage's
+// previous chunk before testing the stage's full barrier (which could
+// otherwise be two phases behind and pass the parity test on the wrong
+// phase).  That wait is itself exact only while there are no more consumer
+// warps than stages: a warp at chunk k knows that chunk k - W - S was
+// released (its previous chunk, k - W, was filled after it), and its parity
+// tests need chunk k - 2S released.  (With W = S = 5 each stage belongs to
+// one warp; the wait stays for other counts.)
 constexpr int kStages = 5;
 constexpr int KSTEPS = kChunk / 16;          // 16-token steps of P·V per stage
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 5;
 static_assert(kConsumerWarps <= kStages, "the stage hand-off between warps needs W <= S");
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr unsigned kFull = 0xffffffffu;
@@ -314,7 +318,7 @@ __device__ void consumer(const DecodeArgs& p, uint8_t* base, volatile int* abort
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     for (int ch = 0; ch < nch; ++ch, ++kseq) {
-      if ((int)(kseq & (kConsumerWarps - 1)) != warp) continue;
+      if ((int)(kseq % kConsumerWarps) != warp) continue;
       const int stage = kseq % kStages;
       if (kseq >= (uint32_t)kStages && !mbar_wait(&bar.empty[stage], ((kseq - kStages) / kStages) & 1, abort)) {
         give_up(p, abort);

@@ -326,8 +326,6 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
  * its own length.  Groups whose prefix is shorter than one partition, and
  * calls where no context spans two partitions, fall back to plain decode
  * for those sequences.  bf16 only; the workspace is sized as for pa_decode.
- * A call with prefix groups reads 8-token blocks as two boxes per block
- * rather than one (the tiles' operand layout).
  */
 #define PA_MAX_PREFIX_GROUPS 64
 int pa_decode_shared_prefix(const void* q, const void* k_cache,

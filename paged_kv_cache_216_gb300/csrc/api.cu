@@ -77,10 +77,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tensor map over a bf16 cache for the tensor-core kernel.  Either a 2D
-// array [N*Hkv*B rows][D] read in boxes of B rows x 64 dims, or (interleaved)
-// [N*Hkv*B*2 lines][64] read in boxes of 2B lines, one (block, head) slab per
-// box; 128-byte swizzle in both.
 // Tensor map over an E4M3 cache (head_dim 128): [N*Hkv*B rows][128 bytes],
 // one box of B rows per (block, head) slab, 128-byte swizzle.
 int make_cache_map_fp8(CUtensorMap* map, const void* base, int num_blocks, int Hkv, int B) {

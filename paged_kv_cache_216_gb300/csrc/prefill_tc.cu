@@ -17,61 +17,63 @@
 // take one item fewer, whichever leaves the busiest CTA less work), so the
 // set-up (barriers, tensor memory) is paid once per SM, there is no tail of
 // whole waves, and the next item's loads overlap the current item's last
-// products and epilogue.  Roles:
+// products and epilogue.  The keys are taken in steps of 64: per tile two
+// S buffers in tensor memory, so that S of the next step is ready when the
+// softmax finishes a step.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
-//    of each item, 128 tokens per stage, into rings of their own (2 stages
-//    of keys, 3 of values: values are needed a softmax later than keys)
-//    that run on across items, with an L2 policy that keeps them for the
-//    other pairs of the same sequence and head, one TMA box per block
-//    (a 4D view of the cache: groups of 8 rows with both 64-dim halves,
-//    128-byte swizzle, which is the layout of a K-major operand of the
-//    tensor cores for keys and of an MN-major one for values), after
+//    of each item, 128 tokens (two steps) per stage, into rings of their
+//    own (2 stages of keys, 3 of values: values are needed a softmax later
+//    than keys) that run on across items, with an L2 policy that keeps them
+//    for the other pairs of the same sequence and head, one TMA box per
+//    block (a 4D view of the cache: groups of 8 rows with both 64-dim
+//    halves, 128-byte swizzle, which is the layout of a K-major operand of
+//    the tensor cores for keys and of an MN-major one for values), after
 //    griddepcontrol.wait; lane b issues block b of a chunk from
 //    block-table entries fetched 32 at a time.  Warp 8 first loads the
 //    item's query tiles, one 3D box per 64-dim half, once the previous
-//    item's last S has completed, and prefetches the next item's into L2.
-//    Value rows past a sequence's end (in its last block) are cleared by
-//    warp 9 once their copy has landed, and the value ring starts as zeros,
-//    so every value row a P·V reads is finite (masked keys get exact zero
-//    weights, and 0 x NaN would still be NaN);
+//    item's last S has completed.  Value rows past a sequence's end (in its
+//    last block) are cleared by warp 9 once their copy has landed, and the
+//    value ring starts as zeros, so every value row a P·V reads is finite
+//    (masked keys get exact zero weights, and 0 x NaN would still be NaN);
 //  * warps 10 and 11 (MMA, one per tile): lane 0 alone issues the tile's
-//    S = Q Kᵀ (M 128, N 128, K = head_dim: head_dim / 16 tcgen05.mma
+//    S = Q Kᵀ (M 128, N 64, K = head_dim: head_dim / 16 tcgen05.mma
 //    kind::f16 from shared-memory descriptors) and O += P V (M 128,
-//    N = head_dim, K 128: eight MMAs, P read from tensor memory, V an
-//    MN-major operand in shared memory), per chunk c P·V(c) then S(c + 1),
-//    spinning on one barrier at a time; the other lanes idle, since a
-//    warp-wide synchronisation after a group of MMAs waits for the tensor
-//    cores to take the group.  A thread issues about one MMA per 64 cycles,
-//    about what one takes, so one thread for both tiles would leave the
-//    tensor cores idle half the time; with one each, one tile's products
-//    run while the other tile's softmax does (ping-pong).  A commit signals
-//    each S (and, after the item's last P·V, the end of O);
-//  * warps 0-3 and 4-7 (softmax, one warpgroup per tile): thread t of a
-//    warpgroup owns query row t of its tile (tensor-memory lane t).  Once S
-//    of a chunk is done it releases the chunk's keys, the previous chunk's
-//    values (the commit that signalled S also covers the P·V issued before
-//    it) and, after the item's last S, the query tiles: one arrival per
-//    tile, so the MMA thread spends no commits on releases.  It reads its
-//    128 scores (tcgen05.ld), masks keys past its position, keeps the
-//    running max and sum, writes P as bf16 back to tensor memory
-//    (tcgen05.st; one arrival per warp) and rescales its row of O only when
-//    its max grows by more than 2^8 (otherwise the stale max stays: exp2
-//    values up to 256 are exact enough and O and the sum use the same max);
-//    at the end of the item it reads its row of O, divides by the sum and
-//    stores it.  The exponentials are one packed FMA per two scores (scale
-//    and max) and one ex2 each; the max is taken three operands at a time.
-//    The two warpgroups take strict turns, chunk by chunk, so that one
-//    tile's softmax runs while the other tile's products do.
+//    N = head_dim, K 64: four MMAs, P read from tensor memory, V an
+//    MN-major operand in shared memory): per item S(0) and S(1) into the
+//    two buffers, then per step u, once P(u) is in, P·V(u) and S(u + 2)
+//    into the buffer P·V(u) has just read, and one commit into that
+//    buffer's barrier; the other lanes idle, since a warp-wide
+//    synchronisation after a group of MMAs waits for the tensor cores to
+//    take the group.  With one issuing thread per tile the tensor cores
+//    interleave the two tiles' products;
+//  * warps 0-3 and 4-7 (softmax, one warpgroup per tile, both running at
+//    once): thread t of a warpgroup owns query row t of its tile
+//    (tensor-memory lane t).  Per step it takes the commit that follows
+//    S(u) (it also covers P·V(u - 2)) and releases, as far as its tile is
+//    concerned, the keys after the second step of a chunk, the values
+//    after the second P·V of a chunk, and the query tile after the item's
+//    last S: one arrival per tile, so the MMA thread spends no commits on
+//    releases.  It reads its 64 scores (tcgen05.ld), masks keys past its
+//    position, keeps the running max and sum, writes P as bf16 over S
+//    (tcgen05.st; one arrival per warp on the buffer's P barrier) and
+//    rescales its row of O only when its max grows by more than 2^8
+//    (otherwise the stale max stays: exp2 values up to 256 are exact
+//    enough and O and the sum use the same max), after taking the next
+//    commit, which covers P·V(u - 1).  The exponentials are one packed FMA
+//    per two scores (scale and max) and one ex2 each; the max is taken
+//    three operands at a time.  At the end of the item it takes the
+//    commits that cover the last P·V, reads its row of O, divides by the
+//    sum, and the four lanes of each quad trade 32-byte pieces so that
+//    every store writes whole 128-byte lines.
 // The softmax warpgroups run with 224 registers a thread and the producer
-// and MMA warps with 56 (setmaxnreg), so that the 128 scores of a row stay
-// in registers.  Both tiles attend all of the item's chunks (the earlier
-// tile's keys past its rows' positions are masked), which keeps the two
-// tiles' releases symmetric.  Tensor memory (512 columns allocated once
-// per CTA): O of tile t at columns DH·t .. DH·t + DH - 1 and its S at
-// 2·DH + 128t (DH = head_dim); P is written over the first half of its S.
-// Every wait is bounded; on a time-out the kernel raises PA_STATUS_TIMEOUT,
-// stops issuing work, lets its copies and products in flight finish, and
-// exits.
+// and MMA warps with 56 (setmaxnreg).  Both tiles attend all of the item's
+// steps (the earlier tile's keys past its rows' positions are masked),
+// which keeps the two tiles' releases symmetric.  Tensor memory (512
+// columns allocated once per CTA): O of tile t at columns DH·t .. DH·t +
+// DH - 1 and its S buffers at 2·DH + 128t and 2·DH + 128t + 64 (DH =
+// head_dim); P is written over the first half of its buffer.  Every wait
+// is bounded; on a time-out the kernel raises PA_STATUS_TIMEOUT, stops
+// issuing work, lets its copies and products in flight finish, and exits.
 
 #include <cuda_bf16.h>
 
@@ -92,7 +94,8 @@ namespace {
 
 constexpr int kM = 128;                 // query rows per tile (one tensor-memory lane each)
 constexpr int kTiles = 2;               // query tiles per CTA, sharing every stage
-constexpr int kN = 128;                 // keys per stage (the N of S = Q Kᵀ)
+constexpr int kN = 128;                 // keys per stage of the rings
+constexpr int kSub = 64;                // keys per softmax step (the N of S = Q Kᵀ)
 constexpr int kStagesK = 2;             // stages in the key ring
 constexpr int kStagesV = 3;             // stages in the value ring (values are needed later than keys)
 constexpr int kSoftWarps = 4;           // per tile
@@ -116,16 +119,17 @@ constexpr int kKVHalf = kN * 128;        // bytes of one 64-dim half of a stage 
 // A stage holds its keys (or values) in groups of 8 rows, each group both
 // 64-dim halves, 1 KB apart ([group][half][8 rows][128 B]), so that one TMA
 // box brings a whole block (see kv_row_offset).
-// full_k[], empty_k[], full_v[], empty_v[]; per tile s_full, p_full,
-// o_final, q_full
-constexpr int kTileBars = 4;
+// full_k[], empty_k[], full_v[], empty_v[]; per tile s_full and p_full of
+// each S buffer, q_full
+constexpr int kTileBars = 5;
 // Items a CTA can list in shared memory; launches hold at most kListCap
 // items per CTA (the host splits larger batches over several launches).
 constexpr int kListCap = 440;
 
 // Layout for head_dim DH (64 or 128): tiles and stages hold DH / 64 halves
-// of 64 dims; O of tile t at columns DH·t .. DH·t + DH - 1, S of tile t at
-// 2·DH + 128t (128 columns), P (bf16 pairs) over the first 64 columns of S.
+// of 64 dims; O of tile t at columns DH·t .. DH·t + DH - 1, its two S
+// buffers (64 columns each) at 2·DH + 128t and 2·DH + 128t + 64, the P
+// (bf16 pairs) of a buffer over its first 32 columns.
 template <int DH>
 struct PfCfg {
   static constexpr int kHalves = DH / 64;
@@ -134,8 +138,8 @@ struct PfCfg {
   static constexpr int kOffK = kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
-  // barriers: the rings, kTileBars per tile, q_empty, drained and softmax turn per tile, v_land
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 3 * kTiles + 1) * 8;
+  // barriers: the rings, kTileBars per tile, q_empty and drained per tile, v_land
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 2 * kTiles + 1) * 8;
   // misc: tensor-memory address, abort flag, the busiest CTA's load of each
   // candidate list (4), the CTA's item count; then its items
   static constexpr int kOffList = kOffMisc + 32;
@@ -154,7 +158,7 @@ constexpr float kRescaleLog2 = 8.f;      // rescale O only when a row's max grow
 // the pipeline's barriers.
 struct PfItem {
   int s, kvh, pair, q0, rows, first_pos, row00, ctx;
-  int nch, t_end;              // chunks of keys the pair attends, and its keys
+  int nch, nsub, t_end;        // stages (128 keys) and steps (64 keys) the pair attends, and its keys
   int state;                   // 0: work; 1: no rows of the sequence in this pair; 2: inconsistent lengths
 };
 
@@ -185,6 +189,7 @@ __device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs
   // the keys past their positions.
   it.t_end = it.first_pos + (min(it.rows, it.row00 + kTiles * kM) - 1) / p.g + 1;
   it.nch = (it.t_end + kN - 1) / kN;
+  it.nsub = (it.t_end + kSub - 1) / kSub;
   return it;
 }
 
@@ -339,23 +344,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = (int)gridDim.x, b = (int)blockIdx.x;
 
   uint64_t* full_k = reinterpret_cast<uint64_t*>(base + C::kOffBars);
   uint64_t* empty_k = full_k + kStagesK;
   uint64_t* full_v = empty_k + kStagesK;
   uint64_t* empty_v = full_v + kStagesV;
   uint64_t* tile_bars = empty_v + kStagesV;  // kTileBars per tile
-  // per tile: [0] S of a chunk is in, [1] P of a chunk is in, [2] the item's
-  // last P·V is done, [3] the item's query tile is in
-  auto s_full = [&](int t) { return tile_bars + t * kTileBars; };
-  auto p_full = [&](int t) { return tile_bars + t * kTileBars + 1; };
-  auto o_final = [&](int t) { return tile_bars + t * kTileBars + 2; };
-  auto q_full = [&](int t) { return tile_bars + t * kTileBars + 3; };
+  // per tile: [0], [1] the MMAs issued before a commit into buffer 0 or 1
+  // are done, [2], [3] P of a step is in buffer 0 or 1, [4] the item's
+  // query tile is in
+  auto s_full = [&](int t, int buf) { return tile_bars + t * kTileBars + buf; };
+  auto p_full = [&](int t, int buf) { return tile_bars + t * kTileBars + 2 + buf; };
+  auto q_full = [&](int t) { return tile_bars + t * kTileBars + 4; };
   uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // per tile: the item's last S is done, the query tile is free
   uint64_t* drained = q_empty + kTiles;                // per MMA warp: every MMA it issued is done
-  uint64_t* turn = drained + kTiles;                   // per tile: the other warpgroup has passed it the turn
-  uint64_t* v_land = turn + kTiles;                    // the values of a chunk that holds rows past its sequence have landed
+  uint64_t* v_land = drained + kTiles;                 // the values of a chunk that holds rows past its sequence have landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
@@ -372,15 +375,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       mbar_init(&empty_v[k], kTiles);
     }
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), kSoftWarps);  // one arrival per warp
-      mbar_init(o_final(t), 1);
+      mbar_init(s_full(t, 0), 1);
+      mbar_init(s_full(t, 1), 1);
+      mbar_init(p_full(t, 0), kSoftWarps);  // one arrival per warp
+      mbar_init(p_full(t, 1), kSoftWarps);
       mbar_init(q_full(t), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(q_empty + t, 1);
       mbar_init(drained + t, 1);
-      mbar_init(turn + t, kSoftWarps);
     }
     mbar_init(v_land, 1);
     *abort = 0;
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         // last token); their scores are all masked and their rows never
         // stored.  Tile t's is loaded once the tile's last S of the previous
         // item has completed: tile 0's first, then the item's first keys,
-        // then tile 1's (which runs about half a chunk behind tile 0).
+        // then tile 1's.
         auto load_q = [&](int t) {
           int okq = 1;
           if (lane == 0) {
@@ -464,17 +467,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           if (!load_q(0)) {
             ok = false;
             break;
-          }
-          // The next item's query tiles into L2, so that their loads at the
-          // item boundary do not wait on HBM.
-          const int jn = (r + 1 < *my_count ? my_items[r + 1] : -1);
-          if (lane == 0 && jn >= 0) {
-            const PfItem nx = pf_item(p, jn, pairs);
-            if (!nx.state)
-              for (int t = 0; t < kTiles; ++t) {
-                const int z = nx.q0 + (nx.row00 + t * kM) / p.g;
-                for (int h = 0; h < C::kHalves; ++h) tma_prefetch_3d(&qmap, 64 * h, nx.kvh * p.g, z);
-              }
           }
         }
         if (!waited) {
@@ -565,26 +557,28 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       }
     } else {
       // MMA warp of tile t: its lane 0 alone issues the tile's MMAs in a
-      // fixed order, waiting for one barrier at a time: per item S(0), then
-      // per chunk c P·V(c) as soon as P(c) is in and right behind it S(c + 1).
-      // The other lanes have nothing to do: a warp-wide synchronisation right
-      // after a group of MMAs waited for the group to be taken by the tensor
-      // cores, several hundred cycles on the tile's critical path.  One thread
-      // issues at most about one tcgen05.mma every 64 cycles, about the time
-      // an M 128 N 128 K 16 MMA takes, so each tile has its own issuing warp
-      // and the tensor cores interleave the two tiles' work: one tile's
-      // products run while the other tile's softmax does.  The tile's MMAs
-      // run in issue order: S(c + 1) overwrites P(c) only after P·V(c) has
-      // read it, and the commit that releases S(c + 1) to the softmax also
-      // covers P·V(c), so the softmax may rescale O at once (and releases the
-      // stages).  The first P·V of an item overwrites O without a barrier of
-      // its own: it waits for P(0), which the warpgroup writes only after it
-      // has read the previous item's O.  Value rows past the pair's keys need
-      // no clearing here: their weights are exact zeros and the rows hold
-      // finite values (see the value producer).
+      // fixed order, waiting for one barrier at a time: per item S(0) and
+      // S(1) into the two buffers, then per step u P·V(u) as soon as P(u)
+      // is in and right behind it S(u + 2) into the same buffer.  The other
+      // lanes have nothing to do: a warp-wide synchronisation right after a
+      // group of MMAs waited for the group to be taken by the tensor cores,
+      // several hundred cycles on the tile's critical path.  Each tile has
+      // its own issuing thread and the tensor cores interleave the two
+      // tiles' work.  The tile's MMAs run in issue order: S(u + 2)
+      // overwrites P(u) only after P·V(u) has read it.  The commit after
+      // P·V(u) and S(u + 2) goes to the buffer's barrier: the softmax takes
+      // it before step u + 2 (or, to rescale O, at step u + 1).  Each buffer
+      // has its own P barrier: P(u + 2) can only arrive after this commit,
+      // which the thread issues after it has taken P(u), so no barrier runs
+      // two phases ahead of its waiter.  The first P·V of an item
+      // overwrites O without a barrier of its own: it waits for P(0), which
+      // the warpgroup writes only after it has read the previous item's O.
+      // Value rows past the pair's keys need no clearing here: their
+      // weights are exact zeros and the rows hold finite values (see the
+      // value producer).
       if (lane == 0) {
         const int t = warp - kMmaWarp;
-        const uint32_t id_s = instr_desc(kM, kN, false);
+        const uint32_t id_s = instr_desc(kM, kSub, false);
         const uint32_t id_o = instr_desc(kM, DH, true);
         bool ok = true;
         auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
@@ -595,59 +589,65 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         // / 16 to the address field (every shared address is below 256 KB, so
         // the 14-bit field never carries).
         const uint64_t a_q = smem_desc(sbase + t * kQTile, 16, 1024);
-        const uint32_t s_cols = tmem + kColS + (uint32_t)t * 128;
+        const uint32_t s_base = tmem + kColS + (uint32_t)t * 128;  // S buffer b at s_base + kSub·b
         const uint32_t o_cols = tmem + kColO + (uint32_t)t * DH;
-        auto issue_s = [&](int kst) {  // the keys in stage kst have landed
+        // S of keys kSub·h .. kSub·h + kSub - 1 of the stage kst into buffer b
+        auto issue_s = [&](int kst, int h, int b) {
           tc_fence_after();
           // keys: K-major, 8-row groups kHalves KB apart, halves 1 KB apart
-          const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage, 16, C::kHalves * 1024);
+          const uint64_t b0 = smem_desc(sbase + kOffK + kst * kKVStage + h * (kSub / 8) * C::kHalves * 1024, 16,
+                                        C::kHalves * 1024);
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
             const int hlf = kk >> 2, w = kk & 3;
-            mma_ss(s_cols, a_q + (uint64_t)((hlf * kQHalf + w * 32) >> 4),
+            mma_ss(s_base + kSub * b, a_q + (uint64_t)((hlf * kQHalf + w * 32) >> 4),
                    b0 + (uint64_t)((hlf * 1024 + w * 32) >> 4), id_s, kk > 0);
           }
-          mma_commit(s_full(t));
         };
-        auto issue_pv = [&](int vst, bool acc) {  // P and the values in stage vst are in
+        // O += P(buffer b) · (values kSub·h .. of the stage vst)
+        auto issue_pv = [&](int vst, int h, int b, bool acc) {
           tc_fence_after();
           // values: MN-major, the dims' halves 1 KB apart, 8-key groups
           // kHalves KB apart; a K-step of 16 keys is two groups
           const uint64_t b0 = smem_desc(sbase + kOffV + vst * kKVStage, 1024, C::kHalves * 1024);
 #pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk)
-            mma_ts(o_cols, s_cols + kk * 8, b0 + (uint64_t)((kk * 2 * C::kHalves * 1024) >> 4), id_o, acc || kk > 0);
+          for (int kk = 0; kk < kSub / 16; ++kk)
+            mma_ts(o_cols, s_base + kSub * b + kk * 8,
+                   b0 + (uint64_t)((((kSub / 16) * h + kk) * 2 * C::kHalves * 1024) >> 4), id_o, acc || kk > 0);
         };
-        uint32_t kq = 0, vq = 0, sp = 0, nit = 0;  // chunks of keys / values, P phases, items
+        uint32_t kq = 0, spc[2] = {0, 0}, nit = 0;  // chunks of keys (and values) before the item, P phases per buffer, items
         for (int r = 0; ok; ++r) {
           const int j = (r < *my_count ? my_items[r] : -1);
           if (j < 0) break;
           const PfItem it = pf_item(p, j, pairs);
           if (it.state) continue;
+          const int ns = it.nsub;
           if (!wait_bar(q_full(t), nit & 1)) break;
           if (!wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
-          issue_s((int)(kq % kStagesK));
-          ++kq;
-          for (int c = 0; c < it.nch; ++c) {
-            const int vst = (int)(vq % kStagesV);
-            if (!wait_bar(&full_v[vst], (vq / kStagesV) & 1)) break;
-            // The next chunk's keys are awaited before P(c) and before any
-            // MMA: P·V(c) and S(c + 1) then go out back to back (a barrier
-            // test right after a group of MMAs waits for the group to be
-            // taken), and the test (slow while the tensor cores read shared
-            // memory) overlaps the softmax instead of following it.
-            const bool more = c + 1 < it.nch;
-            if (more && !wait_bar(&full_k[kq % kStagesK], (kq / kStagesK) & 1)) break;
-            if (!wait_bar(p_full(t), sp & 1)) break;
-            ++sp;
-            issue_pv(vst, c > 0);
-            if (!more) mma_commit(o_final(t));
-            ++vq;
-            if (more) {
-              issue_s((int)(kq % kStagesK));
-              ++kq;
-            }
+          issue_s((int)(kq % kStagesK), 0, 0);
+          mma_commit(s_full(t, 0));
+          if (ns > 1) {
+            issue_s((int)(kq % kStagesK), 1, 1);
+            mma_commit(s_full(t, 1));
           }
+          for (int u = 0; u < ns; ++u) {
+            const int b = u & 1;
+            const uint32_t vc = kq + (u >> 1);        // chunk of values of step u
+            const uint32_t kc = kq + ((u + 2) >> 1);  // chunk of keys of step u + 2
+            const bool more = u + 2 < ns;
+            if (b == 0 && !wait_bar(&full_v[vc % kStagesV], (vc / kStagesV) & 1)) break;
+            // The keys S(u + 2) reads are awaited before P(u) and before any
+            // MMA: P·V(u) and S(u + 2) then go out back to back (a barrier
+            // test right after a group of MMAs waits for the group to be
+            // taken).
+            if (more && b == 0 && !wait_bar(&full_k[kc % kStagesK], (kc / kStagesK) & 1)) break;
+            if (!wait_bar(p_full(t, b), spc[b] & 1)) break;
+            ++spc[b];
+            issue_pv((int)(vc % kStagesV), b, b, u > 0);
+            if (more) issue_s((int)(kc % kStagesK), b, b);  // into the buffer P·V(u) has just read
+            mma_commit(s_full(t, b));  // P·V(u) and S(u + 2) are done
+          }
+          kq += (uint32_t)it.nch;
           ++nit;
         }
         if (!ok) {
@@ -666,10 +666,25 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const int t = warp / kSoftWarps, lt = tid - t * kM;
     const uint32_t lane_base = tmem + ((uint32_t)((warp % kSoftWarps) * 32) << 16);
     const uint32_t o_cols = lane_base + kColO + (uint32_t)t * DH;
-    const uint32_t s_cols = lane_base + kColS + (uint32_t)t * 128;
+    const uint32_t s_base = lane_base + kColS + (uint32_t)t * 128;  // S buffer b at s_base + kSub·b
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-    uint32_t sc_n = 0, ot = 0;  // S phases consumed, items finished by this tile
+    // Phases consumed per S buffer, chunks of keys (and values) before the item.
+    uint32_t sfc[2] = {0, 0}, ch = 0;
     bool ok = true;
+    // Commit C(v) of an item of ns steps is the MMA thread's commit into
+    // buffer v % 2 that follows S(v) (v = 0, 1) or P·V(v - 2) and, for
+    // v < ns, S(v); once it is taken, every MMA issued before it is done.
+    // The warp waits together (warp-wide tensor-memory accesses follow).
+    // After P·V of the second step of a chunk (or the item's last) the
+    // chunk's values are free as far as this tile is concerned.
+    auto take = [&](int v, int ns) {
+      const bool w = __all_sync(0xffffffffu, mbar_wait(s_full(t, v & 1), sfc[v & 1] & 1, abort));
+      ++sfc[v & 1];
+      tc_fence_after();
+      const int pw = v - 2;
+      if (lt == 0 && pw >= 0 && ((pw & 1) || pw == ns - 1)) mbar_arrive(&empty_v[(ch + (pw >> 1)) % kStagesV]);
+      return w;
+    };
     for (int r = 0; ok; ++r) {
       const int j = (r < *my_count ? my_items[r] : -1);
       if (j < 0) break;
@@ -679,68 +694,84 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         continue;
       }
       if (it.state) continue;
-      const int nch_t = it.nch;  // both tiles attend every chunk of the item
+      const int ns = it.nsub;  // both tiles attend every step of the item
       const int row0 = it.row00 + t * kM;
       const int rr = row0 + lt;
       const int pos = rr < it.rows ? it.first_pos + rr / p.g : -1;  // keys 0 .. pos
       float m_run = -INFINITY, l_run = 0.f;
-      for (int c = 0; c < nch_t; ++c) {
-        // the warp leaves together (warp-wide tensor-memory accesses follow)
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full(t), sc_n & 1, abort))) {
+      bool ahead = false;  // the previous step has taken this step's commit
+      for (int u = 0; u < ns; ++u) {
+        const int b = u & 1;
+        if (!ahead && !take(u, ns)) {  // S(u) is in
           ok = false;
           break;
         }
-        // S(c) is done, so this tile is done with the stage of keys it
-        // read, and with the values of chunk c - 1: the commit that
-        // signalled S(c) also covers the P·V(c - 1) issued before it.  After
-        // the item's last S the query tiles are free too.
+        ahead = false;
+        // S(u) is done: after the second step of a chunk (or the item's
+        // last) its keys are free as far as this tile is concerned, and
+        // after the item's last S its query tile.
         if (lt == 0) {
-          mbar_arrive(&empty_k[sc_n % kStagesK]);
-          if (c > 0) mbar_arrive(&empty_v[(sc_n - 1) % kStagesV]);
-          if (c + 1 == nch_t) mbar_arrive(q_empty + t);
+          if (b == 1 || u + 1 == ns) mbar_arrive(&empty_k[(ch + (u >> 1)) % kStagesK]);
+          if (u + 1 == ns) mbar_arrive(q_empty + t);
         }
-        // Strict turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk
-        // k + 1, ...: one warpgroup's softmax runs while the other tile's
-        // products do, and the two never contend for the exp2 unit.  Each
-        // warpgroup is one turn behind the other at most, so a barrier is
-        // never two phases ahead of its waiter.
-        const bool my_turn = t == 0 ? (sc_n == 0 || mbar_wait(turn, (sc_n - 1) & 1, abort))
-                                    : mbar_wait(turn + 1, sc_n & 1, abort);
-        if (!__all_sync(0xffffffffu, my_turn)) {
-          ok = false;
-          break;
-        }
-        ++sc_n;
-        tc_fence_after();
-        uint32_t raw[kN];
+        const uint32_t s_cols = s_base + kSub * b;
+        uint32_t raw[kSub];
 #pragma unroll
-        for (int i = 0; i < kN / 16; ++i) tmem_ld16_nowait(s_cols + 16 * i, raw + 16 * i);
+        for (int i = 0; i < kSub / 16; ++i) tmem_ld16_nowait(s_cols + 16 * i, raw + 16 * i);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        float sc[kN];
+        float sc[kSub];
 #pragma unroll
-        for (int q = 0; q < kN; ++q) sc[q] = __uint_as_float(raw[q]);
-        // Keys t0 .. t0 + nvalid - 1 of this chunk are at or before the row's
-        // position; masking is needed only in chunks that cross it.
-        const int t0 = c * kN;
-        const int nvalid = min(kN, pos - t0 + 1);
-        if (nvalid < kN) {
+        for (int q = 0; q < kSub; ++q) sc[q] = __uint_as_float(raw[q]);
+        // Keys t0 .. t0 + nvalid - 1 of this step are at or before the row's
+        // position; masking is needed only in steps that cross it.
+        const int t0 = u * kSub;
+        const int nvalid = min(kSub, pos - t0 + 1);
+        if (nvalid < kSub) {
 #pragma unroll
-          for (int q = 0; q < kN; ++q) sc[q] = q < nvalid ? sc[q] : -INFINITY;
+          for (int q = 0; q < kSub; ++q) sc[q] = q < nvalid ? sc[q] : -INFINITY;
         }
         // max of the raw (unscaled) scores: three-input max, four chains
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q = 0; q < kN / 2; ++q) m4[q & 3] = fmax3(m4[q & 3], sc[2 * q], sc[2 * q + 1]);
+        for (int q = 0; q < kSub / 2; ++q) m4[q & 3] = fmax3(m4[q & 3], sc[2 * q], sc[2 * q + 1]);
         const float mxr = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         const float mx = mxr * p.scale_log2;  // scale > 0: the max of the scaled scores
         // Raise the running max (and rescale O) only when it grows past the
         // threshold; the decision is made per warp because tensor-memory
         // loads and stores are warp-wide.
         const bool grow = mx > m_run + kRescaleLog2 || (m_run == -INFINITY && mx != -INFINITY);
+        const bool rescale = grow && m_run != -INFINITY;  // O holds products to scale
         const float m_new = grow ? mx : m_run;
         const float alpha = grow ? exp2f(m_run - m_new) : 1.f;  // m_run = -inf: alpha 0
-        if (c > 0 && __any_sync(0xffffffffu, grow && m_run != -INFINITY)) {
-          // O holds P·V(c - 1): the commit that released S(c) covers it
+        const float base_m = m_new == -INFINITY ? 0.f : m_new;
+        const float2 nb2 = make_float2(-base_m, -base_m);
+        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < kSub / 32; ++i) {  // exp2(s * scale - max): one packed FMA per two scores
+          uint32_t w[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float2 x = __ffma2_rn(make_float2(sc[32 * i + 2 * q], sc[32 * i + 2 * q + 1]), sl2, nb2);
+            const float2 e = make_float2(ex2_ftz(x.x), ex2_ftz(x.y));
+            l2[q & 1] = __fadd2_rn(l2[q & 1], e);
+            w[q] = pack_bf16x2(e.x, e.y);
+          }
+          tmem_st16(s_cols + 16 * i, w);  // P over the first kSub / 2 columns of its buffer
+        }
+        l_run = l_run * alpha + ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y));
+        m_run = m_new;
+        // tcgen05.st and its wait are warp-wide: once the wait returns, the
+        // warp's P is in tensor memory.
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        if (u > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O must hold every product before this step's before it is
+          // rescaled: P·V(u - 1) is covered by C(u + 1), which the next step
+          // would wait for anyway.  The next P·V waits for this step's P.
+          if (!take(u + 1, ns)) {
+            ok = false;
+            break;
+          }
+          ahead = true;
 #pragma unroll 1
           for (int i = 0; i < DH / 16; ++i) {
             float v[16];
@@ -750,64 +781,76 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             for (int q = 0; q < 16; ++q) w[q] = __float_as_uint(v[q] * alpha);
             tmem_st16(o_cols + 16 * i, w);
           }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        l_run *= alpha;
-        m_run = m_new;
-        const float base_m = m_run == -INFINITY ? 0.f : m_run;
-        const float2 nb2 = make_float2(-base_m, -base_m);
-        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int i = 0; i < kN / 32; ++i) {  // exp2(s * scale - max): one packed FMA per two scores
-          uint32_t w[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float2 x = __ffma2_rn(make_float2(sc[32 * i + 2 * q], sc[32 * i + 2 * q + 1]), sl2, nb2);
-            const float2 e = make_float2(ex2_ftz(x.x), ex2_ftz(x.y));
-            l2[q & 1] = __fadd2_rn(l2[q & 1], e);
-            w[q] = pack_bf16x2(e.x, e.y);
-          }
-          tmem_st16(s_cols + 16 * i, w);  // P over the first 64 columns of its S
-        }
-        l_run += (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
-        // tcgen05.st and its wait are warp-wide: once the wait returns, the
-        // warp's P is in tensor memory, and one arrival speaks for the warp.
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(p_full(t));
-          mbar_arrive(turn + (1 - t));  // the other tile's turn
+          mbar_arrive(p_full(t, b));  // one arrival speaks for the warp
         }
       }
       if (!ok) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(o_final(t), ot & 1, abort))) {
+      // The item's last P·V is covered by C(ns + 1), which follows C(ns)
+      // (there is none for a single step).
+      if ((ns > 1 && !ahead && !take(ns, ns)) || !take(ns + 1, ns)) {
         ok = false;
         break;
       }
-      ++ot;
-      if (lt == 0) mbar_arrive(&empty_v[(sc_n - 1) % kStagesV]);  // the item's last P·V is done
+      ch += (uint32_t)it.nch;
       // Read the row of O (all loads in flight at once).  The next item's
       // first P·V overwrites it only after this warpgroup's next P(0),
       // which comes after these loads have completed.
-      tc_fence_after();
       uint32_t o[DH];
 #pragma unroll
       for (int i = 0; i < DH / 16; ++i) tmem_ld16_nowait(o_cols + 16 * i, o + 16 * i);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       tc_fence_before();
-      if (rr < it.rows) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                              ((size_t)(it.q0 + rr / p.g) * p.H + it.kvh * p.g + rr % p.g) * DH);
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint32_t w[DH / 2];  // the row normalized, as bf16 pairs; piece k (32 bytes) is w[8k .. 8k + 7]
 #pragma unroll
-        for (int u = 0; u < DH / 8; ++u) {  // dims 8u .. 8u + 7 of the row, normalized, as bf16
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * u]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
-          dst[u] = w;
+      for (int q = 0; q < DH / 2; ++q)
+        w[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv, __uint_as_float(o[2 * q + 1]) * inv);
+      auto row_out = [&](int row) {  // the output row of query row `row` of the pair
+        return static_cast<__nv_bfloat16*>(p.out) +
+               ((size_t)(it.q0 + row / p.g) * p.H + it.kvh * p.g + row % p.g) * DH;
+      };
+      if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
+        // The four lanes of a quad trade pieces (a 4 x 4 transpose of
+        // 32-byte pieces per 128 bytes of row, two rounds of xor shuffles):
+        // lane j then holds piece 4h + j of each of the quad's four rows,
+        // so that each store of the warp writes eight whole 128-byte lines
+        // instead of 32 pieces of 32 lines.
+        const int jq = lane & 3;
+#pragma unroll
+        for (int h = 0; h < DH / 64; ++h) {
+          uint32_t* x = w + 32 * h;
+#pragma unroll
+          for (int m = 1; m <= 2; m <<= 1) {
+            const bool hi = (jq & m) != 0;
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+              if (sl & m) continue;  // the pair of pieces (sl, sl + m)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const uint32_t got = __shfl_xor_sync(0xffffffffu, hi ? x[8 * sl + e] : x[8 * (sl + m) + e], m);
+                if (hi)
+                  x[8 * sl + e] = got;
+                else
+                  x[8 * (sl + m) + e] = got;
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rq = rr - jq + i;  // row i of the quad
+            if (rq < it.rows) st_global_v8(row_out(rq) + 16 * (4 * h + jq), x + 8 * i);
+          }
         }
+      } else if (rr < it.rows) {  // 16-byte stores of the thread's own row
+        __nv_bfloat16* dst = row_out(rr);
+#pragma unroll
+        for (int u = 0; u < DH / 8; ++u)
+          reinterpret_cast<uint4*>(dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       }
     }
     if (!ok) {

@@ -6,8 +6,9 @@ buffer holds the right data whenever a copy, an MMA, the softmax or the
 epilogue touches it.
 
 A CTA works through a list of items, each a pair of query tiles attending
-the same chunks of keys (nch = the longer tile's count; the shorter tile's
-extra keys are masked).  The model follows the kernel's roles and order:
+the same keys in steps of 64 (ns steps = the longer tile's count; the
+shorter tile's extra keys are masked), the rings holding chunks of 128
+keys (two steps).  The model follows the kernel's roles and order:
   * a key producer: per item, query tile 0 once tile 0's last S of the
     previous item has completed (q_empty_0), the keys of the first chunk,
     query tile 1 likewise (q_empty_1), then the keys of the other chunks;
@@ -17,30 +18,40 @@ extra keys are masked).  The model follows the kernel's roles and order:
     a chunk that holds rows past its sequence's end, the copy signals
     v_land, the producer waits for it, clears those rows and then arrives
     on the stage's full barrier itself;
-  * one MMA thread per tile: per item S_t(0), then per chunk c, once the
-    keys of chunk c + 1 and P_t(c) are in, P·V_t(c) and S_t(c+1); a commit signals S_t(c) (it arrives when
-    every MMA the thread issued before it is done, so it also covers
-    P·V_t(c-1)) and, after the item's last P·V, o_final.  The first P·V of an
-    item overwrites O_t without a barrier of its own: it waits for P_t(0),
-    which the warpgroup writes only after it has read the previous item's
-    O_t (the model checks that it has);
-  * per tile a softmax warpgroup: wait for S_t(c); release the keys of chunk
-    c, the values of chunk c - 1 and, after the item's last S, its query
-    tile (one arrival per tile); wait for its turn (the two warpgroups take
-    strict turns, tile 0's chunk k before tile 1's chunk k before tile 0's
-    chunk k + 1); rescale O_t (the commit that signalled S_t(c) covers
-    P·V_t(c-1)), write P_t(c) over S_t, arrive (one arrival per warp), pass
-    the turn; after the item's last chunk wait for its last P·V, release its
-    values, read O_t, then store the rows;
+  * one MMA thread per tile with two S buffers: per item S_t(0) into
+    buffer 0 and S_t(1) into buffer 1, each followed by a commit into its
+    buffer's barrier (C(0), C(1)); then per step u, once the values of u,
+    the keys of u + 2 and P_t(u) are in (one P barrier per buffer, so that
+    P_t(u + 2) cannot arrive before the thread has taken P_t(u): it needs
+    C(u + 2)), P·V_t(u), S_t(u + 2) into the
+    buffer P·V_t(u) has just read (while u + 2 < ns) and a commit into
+    that buffer's barrier, C(u + 2).  A commit arrives when every MMA the
+    thread issued before it is done.  The first P·V of an item overwrites
+    O_t without a barrier of its own: it waits for P_t(0), which the
+    warpgroup writes only after it has read the previous item's O_t (the
+    model checks that it has);
+  * per tile a softmax warpgroup takes every commit once, in order: per
+    step u it takes C(u) (S_t(u) is in; unless the previous step took it);
+    taking C(v) for v >= 2 means P·V_t(v - 2) is done, and after the
+    second step of a chunk (or the item's last) the chunk's values are
+    free; it releases the keys of a chunk after its second step (or the
+    item's last) and, after the item's last S, the query tile (one arrival
+    per tile); reads S_t(u), writes P_t(u) over it; if the row's max grew
+    it takes C(u + 1) early (P·V_t(u - 1) is done) and rescales O_t;
+    arrives (one arrival per warp); after the item's last step it takes
+    C(ns) and C(ns + 1) (the last P·V), reads O_t, then stores the rows.
+    The two warpgroups run independently of each other;
   * the tensor pipe runs the operations in issue order, a commit arriving
     when everything issued before it has completed.
 TMA copies, MMAs and the softmax take random times.  Planted mistakes (a
-stage of keys released by one tile alone, keys released before their S has
-run, S issued before the P·V that reads the buffer it overwrites, an
-epilogue without its wait, a producer waiting on the wrong parity, query
-tiles reloaded without waiting for q_empty, values never released by one
-tile, rows cleared before their copy has landed) show that the checks
-catch each kind of failure: stale data, a deadlock."""
+stage of keys released by one tile alone, keys released after a chunk's
+first step, values released after a chunk's first P·V, S issued before the
+P·V that reads the buffer it overwrites, O rescaled without waiting for
+the previous P·V, both buffers' P on one barrier, an epilogue without its
+wait, a producer waiting on the wrong parity, query tiles reloaded without
+waiting for q_empty, values never released by one tile, rows cleared before
+their copy has landed) show that the checks catch each kind of failure:
+stale data, a deadlock."""
 
 import pytest
 
@@ -52,7 +63,7 @@ K_STAGES, V_STAGES = 2, 3
 class Sim(EventSim):
     def __init__(self, items, seed, mutate=None):
         super().__init__(seed)
-        self.items = [tuple(x) for x in items]  # (nch0, nch1) per item, nch1 <= nch0 only if nch1 == 0
+        self.items = [tuple(x) for x in items]  # (steps of tile 0, steps of tile 1); both tiles run the longer
         # the last chunk of every other item holds rows past its sequence's end
         self.clears = [i % 2 == 1 for i in range(len(self.items))]
         self.mutate = mutate
@@ -62,23 +73,28 @@ class Sim(EventSim):
         self.full_v = [Bar(f"full_v{i}", 1) for i in range(V_STAGES)]
         self.empty_v = [Bar(f"empty_v{i}", 2) for i in range(V_STAGES)]
         self.v_land = Bar("v_land", 1)
-        self.s_full = [Bar(f"s_full{t}", 1) for t in range(2)]
-        self.p_full = [Bar(f"p_full{t}", 4) for t in range(2)]
-        self.o_final = [Bar(f"o_final{t}", 1) for t in range(2)]
+        self.s_full = [[Bar(f"s_full{t}.{b}", 1) for b in range(2)] for t in range(2)]
+        self.p_full = [[Bar(f"p_full{t}.{b}", 4) for b in range(2)] for t in range(2)]
+        if mutate == "one_p_barrier":  # both buffers' P on one barrier
+            self.p_full = [[self.p_full[t][0]] * 2 for t in range(2)]
         self.q_full = [Bar(f"q_full{t}", 1) for t in range(2)]
         self.q_empty = [Bar(f"q_empty{t}", 1) for t in range(2)]
-        # softmax turns: tile 0's chunk k, tile 1's chunk k, tile 0's chunk k + 1, ...
-        self.turn = [Bar(f"turn{t}", 4) for t in range(2)]
-        # buffer contents, tagged (item, chunk)
+        # buffer contents, tagged (item, chunk) for the rings, (item, step) for S / P
         self.k_stage = [None] * K_STAGES
         self.v_stage = [None] * V_STAGES
         self.v_clean = [True] * V_STAGES  # rows past the sequence's end hold no stale copy
         self.k_busy = [0] * K_STAGES  # S operations reading the stage right now
+        self.v_busy = [0] * V_STAGES  # P·V operations reading the stage right now
         self.q_tile = [None, None]  # item whose query tile has landed
-        self.s_buf = [None, None]  # ("S", i, c) or ("P", i, c)
-        self.o_last = [None, None]  # (item, last chunk accumulated into O_t)
+        self.s_buf = [[None, None], [None, None]]  # per tile and buffer: ("S", i, u) or ("P", i, u)
+        self.o_last = [None, None]  # (item, last step accumulated into O_t)
+        self.o_busy = [False, False]  # a P·V of the tile is running
         self.o_read = [None, None]  # item whose O_t the epilogue has read
         self.pipe_free = 0.0
+
+    @staticmethod
+    def steps(item):
+        return max(item)
 
     def run(self):
         roles = [self.key_producer(), self.value_producer(), self.mma(0), self.mma(1), self.softmax(0),
@@ -106,9 +122,10 @@ class Sim(EventSim):
 
     def key_producer(self):
         k = 0
-        for i, nch in enumerate(self.items):
+        for i, item in enumerate(self.items):
+            nch = (self.steps(item) + 1) // 2
             yield from self.load_q(i, 0)
-            for c in range(max(nch)):
+            for c in range(nch):
                 if c == 1:
                     yield from self.load_q(i, 1)
                 st = k % K_STAGES
@@ -120,17 +137,19 @@ class Sim(EventSim):
                 self.copy(self.full_k[st], 1, lambda st=st, tag=(i, c): self.k_stage.__setitem__(st, tag))
                 k += 1
                 yield ("delay", self.rng.uniform(0.0, 0.5))
-            if max(nch) == 1:
+            if nch == 1:
                 yield from self.load_q(i, 1)
         self.done.add("kp")
 
     def value_producer(self):
         k, vl = 0, 0
-        for i, nch in enumerate(self.items):
-            n = max(nch)
+        for i, item in enumerate(self.items):
+            n = (self.steps(item) + 1) // 2
             for c in range(n):
                 st = k % V_STAGES
                 yield ("wait", self.empty_v[st], ((k // V_STAGES) & 1) ^ 1, k // V_STAGES, f"value producer {i}.{c}")
+                if self.v_busy[st]:
+                    self.fail(f"values {i}.{c} copied into stage {st} while a P·V reads it")
                 clear = self.clears[i] and c == n - 1
 
                 def land(st=st, tag=(i, c), clear=clear):
@@ -153,160 +172,181 @@ class Sim(EventSim):
                 yield ("delay", self.rng.uniform(0.0, 0.5))
         self.done.add("vp")
 
-    def issue_s(self, i, t, c, kst):
+    def issue_s(self, i, t, u, kst, b):
         def start():
             if self.q_tile[t] != i:
-                self.fail(f"S{t}({i}.{c}) reads the query tile of item {self.q_tile[t]}")
-            if self.k_stage[kst] != (i, c):
-                self.fail(f"S{t}({i}.{c}) starts on keys {self.k_stage[kst]}")
+                self.fail(f"S{t}({i}.{u}) reads the query tile of item {self.q_tile[t]}")
+            if self.k_stage[kst] != (i, u // 2):
+                self.fail(f"S{t}({i}.{u}) starts on keys {self.k_stage[kst]}")
             self.k_busy[kst] += 1
 
         def end():
             self.k_busy[kst] -= 1
-            if self.k_stage[kst] != (i, c):
-                self.fail(f"S{t}({i}.{c}): keys of stage {kst} overwritten while it ran")
+            if self.k_stage[kst] != (i, u // 2):
+                self.fail(f"S{t}({i}.{u}): keys of stage {kst} overwritten while it ran")
             if self.q_tile[t] != i:
-                self.fail(f"S{t}({i}.{c}): query tile overwritten while it ran")
-            self.s_buf[t] = ("S", i, c)
+                self.fail(f"S{t}({i}.{u}): query tile overwritten while it ran")
+            self.s_buf[t][b] = ("S", i, u)
 
-        self.pipe(self.rng.uniform(0.3, 2.0), start, end)
-        self.commit(self.s_full[t])
+        self.pipe(self.rng.uniform(0.2, 1.0), start, end)
 
-    def issue_pv(self, i, t, c, vst):
-        nch_t = max(self.items[i])
-
+    def issue_pv(self, i, t, u, vst, b):
         def start():
-            if self.s_buf[t] != ("P", i, c):
-                self.fail(f"PV{t}({i}.{c}) reads {self.s_buf[t]} instead of P")
-            if self.v_stage[vst] != (i, c):
-                self.fail(f"PV{t}({i}.{c}) starts on values {self.v_stage[vst]}")
+            if self.s_buf[t][b] != ("P", i, u):
+                self.fail(f"PV{t}({i}.{u}) reads {self.s_buf[t][b]} instead of P")
+            if self.v_stage[vst] != (i, u // 2):
+                self.fail(f"PV{t}({i}.{u}) starts on values {self.v_stage[vst]}")
             if not self.v_clean[vst]:
-                self.fail(f"PV{t}({i}.{c}) reads rows past the sequence's end before they were cleared")
-            if c > 0 and self.o_last[t] != (i, c - 1):
-                self.fail(f"PV{t}({i}.{c}) accumulates onto O holding {self.o_last[t]}")
-            if c == 0 and self.o_last[t] is not None and self.o_read[t] != self.o_last[t][0]:
+                self.fail(f"PV{t}({i}.{u}) reads rows past the sequence's end before they were cleared")
+            if u > 0 and self.o_last[t] != (i, u - 1):
+                self.fail(f"PV{t}({i}.{u}) accumulates onto O holding {self.o_last[t]}")
+            if u == 0 and self.o_last[t] is not None and self.o_read[t] != self.o_last[t][0]:
                 self.fail(f"PV{t}({i}.0) overwrites O of item {self.o_last[t][0]} before the epilogue read it")
+            self.o_busy[t] = True
+            self.v_busy[vst] += 1
 
         def end():
-            if self.v_stage[vst] != (i, c) or self.s_buf[t] != ("P", i, c):
-                self.fail(f"PV{t}({i}.{c}): operands overwritten while it ran")
-            self.o_last[t] = (i, c)
+            self.v_busy[vst] -= 1
+            if self.v_stage[vst] != (i, u // 2) or self.s_buf[t][b] != ("P", i, u):
+                self.fail(f"PV{t}({i}.{u}): operands overwritten while it ran")
+            self.o_last[t] = (i, u)
+            self.o_busy[t] = False
 
-        self.pipe(self.rng.uniform(0.3, 2.0), start, end)
-        if c + 1 == nch_t:
-            self.commit(self.o_final[t])
+        self.pipe(self.rng.uniform(0.2, 1.0), start, end)
 
     def mma(self, t):
-        """MMA thread of tile t: its S and P·V for every chunk of every item."""
-        kq, vq, sp, it = 0, 0, 0, 0
-        for i, nch in enumerate(self.items):
-            n = max(nch)
+        """MMA thread of tile t: its S and P·V for every step of every item."""
+        kq, spc, it = 0, [0, 0], 0
+        for i, item in enumerate(self.items):
+            ns = self.steps(item)
             yield ("wait", self.q_full[t], it & 1, it + 1, f"mma{t} q item {i}")
             yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1, f"mma{t} k {i}.0")
-            self.issue_s(i, t, 0, kq % K_STAGES)
-            kq += 1
-            for c in range(n):
-                vst = vq % V_STAGES
-                yield ("wait", self.full_v[vst], (vq // V_STAGES) & 1, vq // V_STAGES + 1, f"mma{t} v {i}.{c}")
-                if c + 1 < n:
-                    yield ("wait", self.full_k[kq % K_STAGES], (kq // K_STAGES) & 1, kq // K_STAGES + 1,
-                           f"mma{t} k {i}.{c + 1}")
-                yield ("wait", self.p_full[t], sp & 1, sp + 1, f"mma{t} p {i}.{c}")
-                sp += 1
-                if self.mutate == "s_before_pv" and c + 1 < n:
-                    self.issue_s(i, t, c + 1, kq % K_STAGES)
-                    self.issue_pv(i, t, c, vst)
-                    kq += 1
-                    vq += 1
-                    continue
-                self.issue_pv(i, t, c, vst)
-                vq += 1
-                if c + 1 < n:
-                    self.issue_s(i, t, c + 1, kq % K_STAGES)
-                    kq += 1
+            self.issue_s(i, t, 0, kq % K_STAGES, 0)
+            self.commit(self.s_full[t][0])
+            if ns > 1:
+                self.issue_s(i, t, 1, kq % K_STAGES, 1)
+                self.commit(self.s_full[t][1])
+            for u in range(ns):
+                b = u & 1
+                vc, kc = kq + u // 2, kq + (u + 2) // 2
+                more = u + 2 < ns
+                if b == 0:
+                    yield ("wait", self.full_v[vc % V_STAGES], (vc // V_STAGES) & 1, vc // V_STAGES + 1,
+                           f"mma{t} v {i}.{u}")
+                if more and b == 0:
+                    yield ("wait", self.full_k[kc % K_STAGES], (kc // K_STAGES) & 1, kc // K_STAGES + 1,
+                           f"mma{t} k {i}.{u + 2}")
+                yield ("wait", self.p_full[t][b], spc[b] & 1, spc[b] + 1, f"mma{t} p {i}.{u}")
+                spc[b] += 1
+                if self.mutate == "s_before_pv" and more:
+                    self.issue_s(i, t, u + 2, kc % K_STAGES, b)
+                    self.issue_pv(i, t, u, vc % V_STAGES, b)
+                else:
+                    self.issue_pv(i, t, u, vc % V_STAGES, b)
+                    if more:
+                        self.issue_s(i, t, u + 2, kc % K_STAGES, b)
+                self.commit(self.s_full[t][b])
                 yield ("delay", self.rng.uniform(0.0, 0.3))
+            kq += (ns + 1) // 2
             it += 1
         self.done.add(f"mma{t}")
 
+    def rescale(self, i, t, u):
+        if self.o_busy[t] or self.o_last[t] != (i, u - 1):
+            self.fail(f"softmax{t}({i}.{u}) rescales O holding {self.o_last[t]} (P·V running: {self.o_busy[t]})")
+        yield ("delay", self.rng.uniform(0.2, 0.8))
+        if self.o_busy[t] or self.o_last[t] != (i, u - 1):
+            self.fail(f"softmax{t}({i}.{u}): O changed while it was rescaled")
+
     def softmax(self, t):
-        sc, ot = 0, 0
-        early_k = self.mutate == "k_release_early" and t == 0
-        for i, nch in enumerate(self.items):
-            n = max(nch)
-            for c in range(n):
-                if early_k:  # releases the keys before S has run on them
-                    self.arrive(self.empty_k[sc % K_STAGES])
-                yield ("wait", self.s_full[t], sc & 1, sc + 1, f"softmax{t} s {i}.{c}")
-                # S(c) is done: the keys of chunk c, the values of chunk c - 1
-                # (the commit covers P·V(c - 1)) and, after the last S, the
-                # query tiles are free as far as this tile is concerned
-                if not early_k:
-                    self.arrive(self.empty_k[sc % K_STAGES])
-                if c > 0 and not (self.mutate == "v_release_one_tile" and t == 0):
-                    self.arrive(self.empty_v[(sc - 1) % V_STAGES])
-                if c + 1 == n:
+        sfc, ch = [0, 0], 0
+        one_tile_v = self.mutate == "v_release_one_tile" and t == 0
+
+        def take(i, v, ns):
+            """Commit C(v): everything the MMA thread issued before it is done."""
+            yield ("wait", self.s_full[t][v & 1], sfc[v & 1] & 1, sfc[v & 1] + 1, f"softmax{t} C({i}.{v})")
+            sfc[v & 1] += 1
+            pw = v - 2  # P·V(pw) is done
+            early = self.mutate == "v_release_early"
+            if pw >= 0 and not one_tile_v and ((pw % 2 == 0 and pw != ns - 1) if early else (pw & 1 or pw == ns - 1)):
+                self.arrive(self.empty_v[(ch + pw // 2) % V_STAGES])
+
+        for i, item in enumerate(self.items):
+            ns = self.steps(item)
+            ahead = False
+            for u in range(ns):
+                b = u & 1
+                if not ahead:
+                    yield from take(i, u, ns)
+                ahead = False
+                # S(u) is done: the keys of a chunk are free after its second
+                # step (or the item's last), the query tile after the last S
+                release_k = b == 0 if self.mutate == "k_release_early" else (b == 1 or u + 1 == ns)
+                if release_k:
+                    self.arrive(self.empty_k[(ch + u // 2) % K_STAGES])
+                if u + 1 == ns:
                     self.arrive(self.q_empty[t])
-                # strict alternation of the two warpgroups' softmax turns
-                if t == 0 and sc > 0:
-                    yield ("wait", self.turn[0], (sc - 1) & 1, sc, f"softmax0 turn {i}.{c}")
-                elif t == 1:
-                    yield ("wait", self.turn[1], sc & 1, sc + 1, f"softmax1 turn {i}.{c}")
-                sc += 1
-                if self.s_buf[t] != ("S", i, c):
-                    self.fail(f"softmax{t}({i}.{c}) reads {self.s_buf[t]}")
-                if c > 0 and self.o_last[t] != (i, c - 1):
-                    self.fail(f"softmax{t}({i}.{c}) rescales O holding {self.o_last[t]}")
-                yield ("delay", self.rng.uniform(0.5, 4.0))
-                if self.s_buf[t] != ("S", i, c):
-                    self.fail(f"softmax{t}({i}.{c}): S overwritten while it was read")
-                self.s_buf[t] = ("P", i, c)
-                self.arrive(self.p_full[t], 4)
-                self.arrive(self.turn[1 - t], 4)
+                if self.s_buf[t][b] != ("S", i, u):
+                    self.fail(f"softmax{t}({i}.{u}) reads {self.s_buf[t][b]}")
+                yield ("delay", self.rng.uniform(0.1, 0.6))  # tensor-memory loads of S
+                if self.s_buf[t][b] != ("S", i, u):
+                    self.fail(f"softmax{t}({i}.{u}): S overwritten while it was read")
+                yield ("delay", self.rng.uniform(0.3, 2.5))  # the exponentials
+                self.s_buf[t][b] = ("P", i, u)
+                if u > 0 and self.rng.random() < 0.4:  # the row's max grew: rescale O
+                    if self.mutate != "no_early_take":
+                        yield from take(i, u + 1, ns)
+                        ahead = True
+                    yield from self.rescale(i, t, u)
+                self.arrive(self.p_full[t][b], 4)
             if self.mutate != "no_final_wait":
-                yield ("wait", self.o_final[t], ot & 1, ot + 1, f"softmax{t} epilogue {i}")
-            if not (self.mutate == "v_release_one_tile" and t == 0):
-                self.arrive(self.empty_v[(sc - 1) % V_STAGES])
-            if self.o_last[t] != (i, n - 1):
+                if ns > 1 and not ahead:
+                    yield from take(i, ns, ns)
+                yield from take(i, ns + 1, ns)
+            if self.o_last[t] != (i, ns - 1):
                 self.fail(f"epilogue {t} of item {i} reads O holding {self.o_last[t]}")
             yield ("delay", self.rng.uniform(0.2, 1.5))  # tensor-memory loads of O
-            if self.o_last[t] != (i, n - 1):
+            if self.o_last[t] != (i, ns - 1):
                 self.fail(f"epilogue {t} of item {i}: O changed while it was read")
             self.o_read[t] = i
-            ot += 1
+            ch += (ns + 1) // 2
             yield ("delay", self.rng.uniform(0.5, 3.0))  # normalise and store the rows
         self.done.add(f"sm{t}")
 
 
-# Item lists a CTA may get: (chunks of tile 0, chunks of tile 1).  The later
-# tile attends as many chunks or one more; a sequence's last pair may have
-# one tile.  Lists mix single-chunk items, items longer than every ring and
-# one-tile items.
+# Item lists a CTA may get: (steps of tile 0, steps of tile 1), 64 keys a
+# step.  The later tile attends as many steps or more; a sequence's last
+# pair may have one tile.  Lists mix single-step items, items with an odd
+# number of steps (a chunk of keys with one step), items longer than every
+# ring and one-tile items.
 ITEM_LISTS = [
     [(1, 1)],
     [(1, 0)],
-    [(8, 8)],
+    [(2, 2)],
+    [(16, 16)],
     [(1, 1), (1, 1), (1, 1)],
-    [(3, 4), (2, 0), (5, 5)],
-    [(8, 8), (7, 8), (1, 0), (4, 4), (1, 2)],
-    [(1, 0), (1, 0), (2, 2), (1, 0)],
-    [(6, 7), (3, 3), (3, 4), (2, 2), (1, 1), (1, 0)],
-    [(2, 3)] * 5,
-    [(5, 0), (5, 6)],
+    [(5, 6), (3, 0), (9, 9)],
+    [(15, 16), (13, 15), (1, 0), (7, 8), (1, 3)],
+    [(1, 0), (2, 0), (3, 4), (1, 0)],
+    [(11, 13), (5, 6), (6, 7), (3, 4), (2, 2), (1, 0)],
+    [(3, 5)] * 5,
+    [(9, 0), (10, 11)],
 ]
 
 
 @pytest.mark.parametrize("items", ITEM_LISTS, ids=lambda s: "-".join(f"{a}x{b}" for a, b in s))
 def test_prefill_protocol_is_race_free(items):
-    for seed in range(40):
+    for seed in range(80):
         v = Sim(items, seed).run()
         assert not v, f"seed {seed}: {v[:3]}"
 
 
-@pytest.mark.parametrize("mutate", ["k_count_one", "k_release_early", "s_before_pv", "no_final_wait",
-                                    "producer_parity", "no_q_empty_wait", "v_release_one_tile", "no_land_wait"])
+@pytest.mark.parametrize("mutate", ["k_count_one", "k_release_early", "v_release_early", "s_before_pv",
+                                    "no_early_take", "one_p_barrier", "no_final_wait", "producer_parity",
+                                    "no_q_empty_wait", "v_release_one_tile", "no_land_wait"])
 def test_planted_protocol_mistakes_are_caught(mutate):
     caught = 0
-    for items in ([(3, 3), (5, 6)], [(8, 8), (2, 2), (4, 4)], [(1, 1)] * 4, [(2, 2), (1, 0), (3, 3)]):
+    for items in ([(5, 6), (9, 11)], [(16, 16), (3, 3), (7, 8)], [(1, 1)] * 4, [(4, 4), (1, 0), (5, 6)]):
         for seed in range(30):
             caught += bool(Sim(items, seed, mutate).run())
     assert caught > 0

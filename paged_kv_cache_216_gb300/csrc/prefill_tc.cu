@@ -27,8 +27,10 @@
 //    for the other pairs of the same sequence and head, one TMA box per
 //    block (a 4D view of the cache: groups of 8 rows with both 64-dim
 //    halves, 128-byte swizzle, which is the layout of a K-major operand of
-//    the tensor cores for keys and of an MN-major one for values), after
-//    griddepcontrol.wait; lane b issues block b of a chunk from
+//    the tensor cores for keys and of an MN-major one for values); chunks
+//    of cached tokens go out while the append kernel still runs, the first
+//    chunk that holds a new token after griddepcontrol.wait (the append
+//    writes only the new tokens' slots); lane b issues block b of a chunk from
 //    block-table entries fetched 32 at a time.  Warp 8 first loads the
 //    item's query tiles, one 3D box per 64-dim half, once the previous
 //    item's last S has completed.  Value rows past a sequence's end (in its
@@ -469,10 +471,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             break;
           }
         }
-        if (!waited) {
-          pdl_wait_primary();  // the prompts' keys and values are in the cache from here on
-          waited = true;
-        }
         const int32_t* row = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
         const int nblk = (it.t_end + p.B - 1) / p.B;
         int cur = load_block_id(row, lane, nblk);
@@ -490,6 +488,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           if (lane < nb && (unsigned)id >= (unsigned)p.num_blocks) {
             raise_status(p.status, PA_STATUS_BAD_BLOCK);
             id = 0;
+          }
+          // The append kernel writes only the slots of the new tokens
+          // (positions first_pos and later): chunks of older tokens are
+          // read before waiting for it, the first chunk that holds a new
+          // token after (griddepcontrol.wait).
+          if (!waited && (c + 1) * kN > it.first_pos) {
+            pdl_wait_primary();
+            waited = true;
           }
           const int st = (int)(k % (uint32_t)stages);
           // A chunk of values whose last block runs past the sequence's end
@@ -555,6 +561,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         }
         __syncwarp();
       }
+      // Every CTA waits for the append before it completes, even one whose
+      // items held no new token: a batch split over several launches makes
+      // each launch the next one's primary, and that launch's
+      // griddepcontrol.wait stands for the append only if this one's
+      // completion implies the append's.
+      if (!waited) pdl_wait_primary();
     } else {
       // MMA warp of tile t: its lane 0 alone issues the tile's MMAs in a
       // fixed order, waiting for one barrier at a time: per item S(0) and

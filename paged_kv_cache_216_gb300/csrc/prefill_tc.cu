@@ -164,7 +164,17 @@ struct PfItem {
   int state;                   // 0: work; 1: no rows of the sequence in this pair; 2: inconsistent lengths
 };
 
-__device__ __forceinline__ PfItem pf_item(const PrefillArgs& p, int j, int pairs) {
+// The lengths' fields the items are derived from, by value: the item-list
+// builder (a function of its own) reads them from registers rather than
+// through a reference to the kernel's arguments.
+struct PfLens {
+  const int32_t* query_start;
+  const int32_t* context_lens;
+  int S, T, Hkv, g, max_ctx, max_query_len;
+};
+
+template <class A>
+__device__ __forceinline__ PfItem pf_item(const A& p, int j, int pairs) {
   PfItem it{};
   const int per = p.S * p.Hkv;
   it.pair = pairs - 1 - j / per;
@@ -211,8 +221,8 @@ struct PfOrder {
   int base, stride, slot, count;
 };
 
-__device__ __forceinline__ PfOrder pf_order(int b, int G, int n, bool aware) {
-  const int q = n / G, e = n - q * G, ga = G - e;
+__device__ __forceinline__ PfOrder pf_order(int b, int G, int n, int q, bool aware) {  // q = n / G
+  const int e = n - q * G, ga = G - e;
   if (!aware) return PfOrder{0, G, b, q + ((q & 1) ? (b >= ga ? 1 : 0) : (b < e ? 1 : 0))};
   if (b < ga) return PfOrder{0, ga, b, q};
   return PfOrder{q * ga, e, b - ga, q + 1};
@@ -224,7 +234,8 @@ __device__ __forceinline__ int pf_list_pos(const PfOrder& o, int r) {
 
 // Cost of an item for balancing: its chunks of keys plus one for its start
 // and end (0 for a pair without rows).
-__device__ __forceinline__ int pf_item_cost(const PrefillArgs& p, int j, int pairs) {
+template <class A>
+__device__ __forceinline__ int pf_item_cost(const A& p, int j, int pairs) {
   const PfItem it = pf_item(p, j, pairs);
   return it.state ? 0 : it.nch + 1;
 }
@@ -251,7 +262,7 @@ constexpr int kMaxCostLevels = 1024;
 // Called by every thread of the CTA, before the value ring is cleared:
 // `cost` is the ring (ring_ints ints of scratch), `busiest` 4 ints, the
 // CTA's item count and items go to *my_count and my_items.
-__device__ __noinline__ void pf_build_list(const PrefillArgs& p, int pairs, int first_item, int num_items,
+__device__ __noinline__ void pf_build_list(const PfLens p, int pairs, int first_item, int num_items,
                                            int* cost, int ring_ints, int* busiest, int* my_count, int* my_items) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = (int)gridDim.x, b = (int)blockIdx.x;
@@ -260,6 +271,16 @@ __device__ __noinline__ void pf_build_list(const PrefillArgs& p, int pairs, int 
   const bool check = first_item == 0 && num_items == E * p.Hkv && num_items <= kMaxCheckedItemsPerCta * G &&
                      E <= ring_ints / 2;
   bool sorting = check && E <= kMaxSortedEntries && levels <= kMaxCostLevels && 2 * E + levels <= ring_ints;
+  const int q_all = num_items / G;
+  // j / Hkv without a division chain per item: a float estimate (j < 2^24)
+  // corrected by one either way
+  const float inv_hkv = 1.f / (float)p.Hkv;
+  auto div_hkv = [&](int j) {
+    int e = (int)((float)j * inv_hkv);
+    e -= e * p.Hkv > j ? 1 : 0;
+    e += (e + 1) * p.Hkv <= j ? 1 : 0;
+    return e;
+  };
   int* sorted = cost + E;            // [E] entries by cost, most first
   int* next = sorted + E;            // [levels] per cost level: the next free position
   if (check)
@@ -307,9 +328,9 @@ __device__ __noinline__ void pf_build_list(const PrefillArgs& p, int pairs, int 
       int load[4] = {0, 0, 0, 0};
       if (c < G)
         for (int k = 0; k < (sorting ? 4 : 2); ++k) {
-          const PfOrder o = pf_order(c, G, num_items, k & 1);
+          const PfOrder o = pf_order(c, G, num_items, q_all, k & 1);
           for (int r = 0; r < o.count; ++r) {
-            const int e = pf_list_pos(o, r) / p.Hkv;
+            const int e = div_hkv(pf_list_pos(o, r));
             load[k] += cost[k >= 2 ? sorted[e] : e];
           }
         }
@@ -325,7 +346,7 @@ __device__ __noinline__ void pf_build_list(const PrefillArgs& p, int pairs, int 
     if (check)
       for (int k = 1; k < (sorting ? 4 : 2); ++k)
         if (busiest[k] < busiest[pick]) pick = k;
-    const PfOrder o = pf_order(b, G, num_items, pick & 1);
+    const PfOrder o = pf_order(b, G, num_items, q_all, pick & 1);
     if (warp == 0)
       for (int r = lane; r < o.count; r += 32) {
         const int j = pf_list_pos(o, r);
@@ -393,7 +414,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
   int* my_count = reinterpret_cast<int*>(base + C::kOffMisc + 24);
   int* my_items = reinterpret_cast<int*>(base + C::kOffList);
-  pf_build_list(p, pairs, first_item, num_items, reinterpret_cast<int*>(base + kOffV), kStagesV * kKVStage / 4,
+  const PfLens lens{p.query_start, p.context_lens, p.S, p.T, p.Hkv, p.g, p.max_ctx, p.max_query_len};
+  pf_build_list(lens, pairs, first_item, num_items, reinterpret_cast<int*>(base + kOffV), kStagesV * kKVStage / 4,
                 reinterpret_cast<int*>(base + C::kOffMisc + 8), my_count, my_items);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tslot)),

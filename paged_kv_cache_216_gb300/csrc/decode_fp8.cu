@@ -11,7 +11,9 @@
 // list through an atomic counter; warp 5 loads each item's g query rows and
 // streams its blocks by TMA into a 5-stage shared-memory ring (one box of
 // [B tokens x 128 bytes] per block for keys and one for values, 128-byte
-// swizzle), 64 tokens per stage; warps 0-4 take the chunks in turn (one
+// swizzle; blocks of 8 tokens, 1 KB, by 16-byte cp.async into the same
+// layout instead, one TMA box per KB being beyond the TMA unit's rate of
+// boxes), 64 tokens per stage; warps 0-4 take the chunks in turn (one
 // more consumer warp than the bf16 kernel: this consumer does about three
 // times the work per byte) and merge their (max, sum, O) states at the end
 // of the item.  Head dim 128.
@@ -235,13 +237,42 @@ __device__ void producer(const CUtensorMap* kmap, const CUtensorMap* vmap, const
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * block_bytes);
-      __syncwarp();
-      if (lane < nb) {
-        const int y = (id * p.Hkv + kvh) * p.B;
-        uint8_t* sk = base + stage * kStage + lane * p.B * kD;
-        tma_load_2d(sk, kmap, &bar.full[stage], 0, y, policy);
-        tma_load_2d(sk + kRegion, vmap, &bar.full[stage], 0, y, policy);
+      if (p.B == 8) {
+        // Blocks of 8 tokens are 1 KB: one TMA box each would cap the
+        // stream at the TMA unit's rate of boxes.  The warp copies them in
+        // 16-byte pieces instead (lane: piece u of rows rp and rp + 4 of
+        // each block, 512 contiguous bytes per instruction), into the
+        // layout the boxes would have left (128-byte swizzle: piece u of
+        // stage row r at r * 128 + ((u ^ (r & 7)) << 4)); the stage's
+        // barrier completes once lane 0 has arrived and every lane's copies
+        // have landed.
+        const int u = lane & 7, rp = lane >> 3;
+        uint8_t* sk = base + stage * kStage;
+        const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
+        const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
+        for (int b = 0; b < nb; ++b) {
+          const size_t row0 = ((size_t)__shfl_sync(kFull, id, b) * p.Hkv + kvh) * 8;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int i = rp + 4 * h;  // row of the block
+            const uint32_t off = (uint32_t)((8 * b + i) * kD + ((u ^ i) << 4));
+            const size_t src = (row0 + i) * kD + u * 16;
+            cp_async16(sk + off, kc + src, policy);
+            cp_async16(sk + kRegion + off, vc + src, policy);
+          }
+        }
+        cp_async_mbar_arrive(&bar.full[stage]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.full[stage]);
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(&bar.full[stage], (uint32_t)nb * block_bytes);
+        __syncwarp();
+        if (lane < nb) {
+          const int y = (id * p.Hkv + kvh) * p.B;
+          uint8_t* sk = base + stage * kStage + lane * p.B * kD;
+          tma_load_2d(sk, kmap, &bar.full[stage], 0, y, policy);
+          tma_load_2d(sk + kRegion, vmap, &bar.full[stage], 0, y, policy);
+        }
       }
       if (ch == 0 && lane == 0 && nxt_idx < total) nxt_pr = __ldcg(p.plan + nxt_idx / p.Hkv);
     }

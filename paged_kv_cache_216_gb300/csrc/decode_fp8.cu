@@ -56,6 +56,20 @@
 namespace pa {
 namespace {
 
+// 16 bytes global -> shared by the load/store unit (not the TMA unit),
+// cached in L2 only, with an L2 eviction policy.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "l"(policy)
+               : "memory");
+}
+
+// The barrier's current phase also waits for every cp.async this thread has
+// issued so far (its pending count is raised now and lowered when they land).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 constexpr int kD = 128;                      // head_dim
 constexpr int kChunk = 64;                   // tokens per pipeline stage
 constexpr int kRegion = kChunk * kD;         // 8 KB: the keys (or values) of a stage

@@ -94,6 +94,13 @@
 namespace pa {
 namespace {
 
+// One 32-byte store of eight 32-bit words (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 constexpr int kM = 128;                 // query rows per tile (one tensor-memory lane each)
 constexpr int kTiles = 2;               // query tiles per CTA, sharing every stage
 constexpr int kN = 128;                 // keys per stage of the rings

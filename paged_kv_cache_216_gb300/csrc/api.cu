@@ -554,14 +554,16 @@ int pa_prefill(const void* q, const void* k, const void* v, const int64_t* slot_
   a.max_query_len = max_query_len;
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
   // 5th-generation tensor cores (tcgen05) for head_dim 64 and 128
-  CUtensorMap kmap, vmap, qmap;
+  CUtensorMap kmap, vmap, qmap, omap;
   rc = make_block_map(&kmap, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
   if (rc) return rc;
   rc = make_block_map(&vmap, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
   if (rc) return rc;
   rc = make_query_map(&qmap, q, num_tokens, num_heads, g, head_dim);
   if (rc) return rc;
-  e = pa::launch_prefill_tc(a, kmap, vmap, qmap, st);
+  rc = make_query_map(&omap, out, num_tokens, num_heads, g, head_dim);  // full tiles of output rows are stored by TMA
+  if (rc) return rc;
+  e = pa::launch_prefill_tc(a, kmap, vmap, qmap, omap, st);
   if (e != cudaSuccess) return cuda_fail(e, "pa_prefill launch");
   return PA_OK;
 }

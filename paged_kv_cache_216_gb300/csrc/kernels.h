@@ -161,9 +161,9 @@ struct PrefillArgs {
 };
 // Prefill on tcgen05, head_dim 64 or 128: persistent CTAs, one per SM; kmap/vmap: the bf16 caches as
 // 4D (64 dims, 8 rows, 64-dim half, 8-row group) with boxes of one block (64, 8, D / 64, B / 8); qmap:
-// q as (dims, head, token) with boxes of [64 dims x g heads x 128 / g tokens].
+// q as (dims, head, token) with boxes of [64 dims x g heads x 128 / g tokens]; omap: out, the same.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, cudaStream_t stream);
+                              const CUtensorMap& qmap, const CUtensorMap& omap, cudaStream_t stream);
 
 cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots, int T, void* k_cache,
                                 void* v_cache, int num_blocks, int Hkv, int D, int B, int elem_bytes,

@@ -22,8 +22,7 @@
 // softmax finishes a step.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
 //    of each item, 128 tokens (two steps) per stage, into rings of their
-//    own (2 stages of keys, 3 of values: values are needed a softmax later
-//    than keys) that run on across items, with an L2 policy that keeps them
+//    own (2 stages each) that run on across items, with an L2 policy that keeps them
 //    for the other pairs of the same sequence and head, one TMA box per
 //    block (a 4D view of the cache: groups of 8 rows with both 64-dim
 //    halves, 128-byte swizzle, which is the layout of a K-major operand of
@@ -64,9 +63,11 @@
 //    commit, which covers P·V(u - 1).  The exponentials are one packed FMA
 //    per two scores (scale and max) and one ex2 each; the max is taken
 //    three operands at a time.  At the end of the item it takes the
-//    commits that cover the last P·V, reads its row of O, divides by the
-//    sum, and the four lanes of each quad trade 32-byte pieces so that
-//    every store writes whole 128-byte lines.
+//    commits that cover the last P·V, reads its row of O and divides by
+//    the sum; a tile of 128 query rows is staged in shared memory (one
+//    buffer, the two tiles' in turns) and stored by TMA, the rows of a
+//    sequence's last tile directly, the four lanes of each quad trading
+//    32-byte pieces so that every store writes whole 128-byte lines.
 // The softmax warpgroups run with 224 registers a thread and the producer
 // and MMA warps with 56 (setmaxnreg).  Both tiles attend all of the item's
 // steps (the earlier tile's keys past its rows' positions are masked),
@@ -106,7 +107,7 @@ constexpr int kTiles = 2;               // query tiles per CTA, sharing every st
 constexpr int kN = 128;                 // keys per stage of the rings
 constexpr int kSub = 64;                // keys per softmax step (the N of S = Q Kᵀ)
 constexpr int kStagesK = 2;             // stages in the key ring
-constexpr int kStagesV = 3;             // stages in the value ring (values are needed later than keys)
+constexpr int kStagesV = 2;             // stages in the value ring
 constexpr int kSoftWarps = 4;           // per tile
 constexpr int kProducerWarp = kTiles * kSoftWarps;  // keys; the next warp streams values
 constexpr int kMmaWarp = kProducerWarp + 2;         // tile 0's MMAs; the next warp issues tile 1's
@@ -146,9 +147,10 @@ struct PfCfg {
   static constexpr int kKVStage = kHalves * kKVHalf;
   static constexpr int kOffK = kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
-  static constexpr int kOffBars = kOffV + kStagesV * kKVStage;
-  // barriers: the rings, kTileBars per tile, q_empty and drained per tile, v_land
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 2 * kTiles + 1) * 8;
+  static constexpr int kOffOut = kOffV + kStagesV * kKVStage;  // one tile's output rows, staged for a TMA store
+  static constexpr int kOffBars = kOffOut + kQTile;
+  // barriers: the rings, kTileBars per tile, q_empty and drained per tile, v_land, out_free
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 2 * kTiles + 2) * 8;
   // misc: tensor-memory address, abort flag, the busiest CTA's load of each
   // candidate list (4), the CTA's item count; then its items
   static constexpr int kOffList = kOffMisc + 32;
@@ -366,8 +368,8 @@ __device__ __noinline__ void pf_build_list(const PfLens p, int pairs, int first_
 template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ PrefillArgs p, int pairs, int first_item,
-                      int num_items) {
+                      const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                      const __grid_constant__ PrefillArgs p, int pairs, int first_item, int num_items) {
   using C = PfCfg<DH>;
   constexpr int kQTile = C::kQTile, kKVStage = C::kKVStage, kOffK = C::kOffK, kOffV = C::kOffV;
   constexpr uint32_t kColO = C::kColO, kColS = C::kColS;
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // per tile: the item's last S is done, the query tile is free
   uint64_t* drained = q_empty + kTiles;                // per MMA warp: every MMA it issued is done
   uint64_t* v_land = drained + kTiles;                 // the values of a chunk that holds rows past its sequence have landed
+  uint64_t* out_free = v_land + 1;                     // a tile's turn on the output staging buffer has ended
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
   const uint32_t sbase = smem_addr(base);
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       mbar_init(drained + t, 1);
     }
     mbar_init(v_land, 1);
+    mbar_init(out_free, 1);
     *abort = 0;
     fence_barrier_init();
   }
@@ -709,8 +713,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t o_cols = lane_base + kColO + (uint32_t)t * DH;
     const uint32_t s_base = lane_base + kColS + (uint32_t)t * 128;  // S buffer b at s_base + kSub·b
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-    // Phases consumed per S buffer, chunks of keys (and values) before the item.
-    uint32_t sfc[2] = {0, 0}, ch = 0;
+    // Phases consumed per S buffer, chunks of keys (and values) before the
+    // item, items finished.
+    uint32_t sfc[2] = {0, 0}, ch = 0, done = 0;
     bool ok = true;
     // Commit C(v) of an item of ns steps is the MMA thread's commit into
     // buffer v % 2 that follows S(v) (v = 0, 1) or P·V(v - 2) and, for
@@ -855,45 +860,82 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         return static_cast<__nv_bfloat16*>(p.out) +
                ((size_t)(it.q0 + row / p.g) * p.H + it.kvh * p.g + row % p.g) * DH;
       };
-      if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
-        // The four lanes of a quad trade pieces (a 4 x 4 transpose of
-        // 32-byte pieces per 128 bytes of row, two rounds of xor shuffles):
-        // lane j then holds piece 4h + j of each of the quad's four rows,
-        // so that each store of the warp writes eight whole 128-byte lines
-        // instead of 32 pieces of 32 lines.
-        const int jq = lane & 3;
+      // A tile whose 128 rows are all query rows is staged in shared memory
+      // (the layout its query tile had) and written by two TMA stores, one
+      // per 64-dim half, so that the warpgroup is free within a few hundred
+      // cycles; the two tiles have one staging buffer and take turns
+      // (tile 0 of an item, tile 1, tile 0 of the next item, ...), turn k
+      // waiting for the end of turn k - 1.  Other tiles (a sequence's last)
+      // store their rows directly.
+      const uint32_t turn = 2 * done + (uint32_t)t;
+      bool turn_ok = true;
+      if (lt == 0 && turn > 0) turn_ok = mbar_wait(out_free, (turn - 1) & 1, abort);
+      if (!named_barrier_and(1 + t, kM, turn_ok)) {
+        ok = false;
+        break;
+      }
+      ++done;
+      if (row0 + kM <= it.rows) {
+        uint8_t* stage = base + C::kOffOut;
 #pragma unroll
-        for (int h = 0; h < DH / 64; ++h) {
-          uint32_t* x = w + 32 * h;
+        for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
-          for (int m = 1; m <= 2; m <<= 1) {
-            const bool hi = (jq & m) != 0;
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(stage + h * kQHalf + lt * 128 + ((u ^ (lt & 7)) << 4)) =
+                make_uint4(w[32 * h + 4 * u], w[32 * h + 4 * u + 1], w[32 * h + 4 * u + 2], w[32 * h + 4 * u + 3]);
+        fence_proxy_async_smem();  // the rows before the TMA unit reads them
+        named_barrier_sync(1 + t, kM);
+        if (lt == 0) {
 #pragma unroll
-            for (int sl = 0; sl < 4; ++sl) {
-              if (sl & m) continue;  // the pair of pieces (sl, sl + m)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_store_3d(&omap, stage + h * kQHalf, 64 * h, it.kvh * p.g, it.q0 + row0 / p.g);
+          bulk_store_drain();  // the buffer has been read
+          mbar_arrive(out_free);
+        }
+      } else {
+        if (lt == 0) mbar_arrive(out_free);  // the turn passes at once
+        if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
+          // The four lanes of a quad trade pieces (a 4 x 4 transpose of
+          // 32-byte pieces per 128 bytes of row, two rounds of xor shuffles):
+          // lane j then holds piece 4h + j of each of the quad's four rows,
+          // so that each store of the warp writes eight whole 128-byte lines
+          // instead of 32 pieces of 32 lines.
+          const int jq = lane & 3;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const uint32_t got = __shfl_xor_sync(0xffffffffu, hi ? x[8 * sl + e] : x[8 * (sl + m) + e], m);
-                if (hi)
-                  x[8 * sl + e] = got;
-                else
-                  x[8 * (sl + m) + e] = got;
+          for (int h = 0; h < DH / 64; ++h) {
+            uint32_t* x = w + 32 * h;
+#pragma unroll
+            for (int m = 1; m <= 2; m <<= 1) {
+              const bool hi = (jq & m) != 0;
+#pragma unroll
+              for (int sl = 0; sl < 4; ++sl) {
+                if (sl & m) continue;  // the pair of pieces (sl, sl + m)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const uint32_t got = __shfl_xor_sync(0xffffffffu, hi ? x[8 * sl + e] : x[8 * (sl + m) + e], m);
+                  if (hi)
+                    x[8 * sl + e] = got;
+                  else
+                    x[8 * (sl + m) + e] = got;
+                }
               }
             }
-          }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rq = rr - jq + i;  // row i of the quad
-            if (rq < it.rows) st_global_v8(row_out(rq) + 16 * (4 * h + jq), x + 8 * i);
+            for (int i = 0; i < 4; ++i) {
+              const int rq = rr - jq + i;  // row i of the quad
+              if (rq < it.rows) st_global_v8(row_out(rq) + 16 * (4 * h + jq), x + 8 * i);
+            }
           }
+        } else if (rr < it.rows) {  // 16-byte stores of the thread's own row
+          __nv_bfloat16* dst = row_out(rr);
+#pragma unroll
+          for (int u = 0; u < DH / 8; ++u)
+            reinterpret_cast<uint4*>(dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
-      } else if (rr < it.rows) {  // 16-byte stores of the thread's own row
-        __nv_bfloat16* dst = row_out(rr);
-#pragma unroll
-        for (int u = 0; u < DH / 8; ++u)
-          reinterpret_cast<uint4*>(dst)[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       }
     }
+    // The stores issued by TMA are complete before the kernel ends.
+    if (lt == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     if (!ok) {
       *abort = 1;
       raise_status(p.status, PA_STATUS_TIMEOUT);
@@ -914,7 +956,7 @@ std::atomic<int> g_items_per_launch{0};
 
 template <int DH>
 cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const CUtensorMap& qmap, int pairs, cudaStream_t stream) {
+                                 const CUtensorMap& qmap, const CUtensorMap& omap, int pairs, cudaStream_t stream) {
   constexpr size_t kBytes = PfCfg<DH>::kBytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -955,7 +997,7 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, a, pairs, (int)first, (int)n);
+    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, omap, a, pairs, (int)first, (int)n);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -964,12 +1006,12 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                              const CUtensorMap& qmap, cudaStream_t stream) {
+                              const CUtensorMap& qmap, const CUtensorMap& omap, cudaStream_t stream) {
   const int tiles = (a.max_query_len * a.g + kM - 1) / kM;
   const int pairs = (tiles + kTiles - 1) / kTiles;
   if (tiles <= 0 || a.S <= 0) return cudaSuccess;
-  if (a.D == 128) return launch_prefill_tc_dh<128>(a, kmap, vmap, qmap, pairs, stream);
-  if (a.D == 64) return launch_prefill_tc_dh<64>(a, kmap, vmap, qmap, pairs, stream);
+  if (a.D == 128) return launch_prefill_tc_dh<128>(a, kmap, vmap, qmap, omap, pairs, stream);
+  if (a.D == 64) return launch_prefill_tc_dh<64>(a, kmap, vmap, qmap, omap, pairs, stream);
   return cudaErrorInvalidValue;
 }
 

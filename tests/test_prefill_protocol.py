@@ -14,7 +14,7 @@ keys (two steps).  The model follows the kernel's roles and order:
     query tile 1 likewise (q_empty_1), then the keys of the other chunks;
     keys of chunk k (counting over the CTA's items) go into ring stage k % 2
     once both tiles have released the stage's previous chunk;
-  * a value producer: the values of chunk k into stage k % 3 likewise; for
+  * a value producer: the values of chunk k into stage k % 2 likewise; for
     a chunk that holds rows past its sequence's end, the copy signals
     v_land, the producer waits for it, clears those rows and then arrives
     on the stage's full barrier itself;
@@ -39,7 +39,10 @@ keys (two steps).  The model follows the kernel's roles and order:
     per tile); reads S_t(u), writes P_t(u) over it; if the row's max grew
     it takes C(u + 1) early (P·V_t(u - 1) is done) and rescales O_t;
     arrives (one arrival per warp); after the item's last step it takes
-    C(ns) and C(ns + 1) (the last P·V), reads O_t, then stores the rows.
+    C(ns) and C(ns + 1) (the last P·V), reads O_t, then stages its rows in
+    the output buffer the two tiles share in turns (tile 0 of an item, tile
+    1, tile 0 of the next, ..., each turn waiting for the previous one's
+    end on out_free) for a TMA store.
     The two warpgroups run independently of each other;
   * the tensor pipe runs the operations in issue order, a commit arriving
     when everything issued before it has completed.
@@ -47,8 +50,8 @@ TMA copies, MMAs and the softmax take random times.  Planted mistakes (a
 stage of keys released by one tile alone, keys released after a chunk's
 first step, values released after a chunk's first P·V, S issued before the
 P·V that reads the buffer it overwrites, O rescaled without waiting for
-the previous P·V, both buffers' P on one barrier, an epilogue without its
-wait, a producer waiting on the wrong parity, query tiles reloaded without
+the previous P·V, both buffers' P on one barrier, a tile staging its rows
+without waiting for its turn, an epilogue without its wait, a producer waiting on the wrong parity, query tiles reloaded without
 waiting for q_empty, values never released by one tile, rows cleared before
 their copy has landed) show that the checks catch each kind of failure:
 stale data, a deadlock."""
@@ -57,7 +60,7 @@ import pytest
 
 from tests._event_sim import Bar, EventSim
 
-K_STAGES, V_STAGES = 2, 3
+K_STAGES, V_STAGES = 2, 2
 
 
 class Sim(EventSim):
@@ -73,6 +76,8 @@ class Sim(EventSim):
         self.full_v = [Bar(f"full_v{i}", 1) for i in range(V_STAGES)]
         self.empty_v = [Bar(f"empty_v{i}", 2) for i in range(V_STAGES)]
         self.v_land = Bar("v_land", 1)
+        self.out_free = Bar("out_free", 1)  # turns on the output staging buffer: tile 0, tile 1, tile 0, ...
+        self.out_owner = None
         self.s_full = [[Bar(f"s_full{t}.{b}", 1) for b in range(2)] for t in range(2)]
         self.p_full = [[Bar(f"p_full{t}.{b}", 4) for b in range(2)] for t in range(2)]
         if mutate == "one_p_barrier":  # both buffers' P on one barrier
@@ -259,7 +264,7 @@ class Sim(EventSim):
             self.fail(f"softmax{t}({i}.{u}): O changed while it was rescaled")
 
     def softmax(self, t):
-        sfc, ch = [0, 0], 0
+        sfc, ch, done = [0, 0], 0, 0
         one_tile_v = self.mutate == "v_release_one_tile" and t == 0
 
         def take(i, v, ns):
@@ -310,7 +315,17 @@ class Sim(EventSim):
                 self.fail(f"epilogue {t} of item {i}: O changed while it was read")
             self.o_read[t] = i
             ch += (ns + 1) // 2
-            yield ("delay", self.rng.uniform(0.5, 3.0))  # normalise and store the rows
+            # the output staging buffer, the two tiles' in turn
+            turn = 2 * done + t
+            done += 1
+            if turn > 0 and self.mutate != "no_turn_wait":
+                yield ("wait", self.out_free, (turn - 1) & 1, turn, f"softmax{t} staging turn {i}")
+            if self.out_owner is not None:
+                self.fail(f"epilogue {t} of item {i} stages its rows while tile {self.out_owner} uses the buffer")
+            self.out_owner = t
+            yield ("delay", self.rng.uniform(0.5, 3.0))  # stage the rows, the TMA store reads them
+            self.out_owner = None
+            self.arrive(self.out_free)
         self.done.add(f"sm{t}")
 
 
@@ -342,7 +357,7 @@ def test_prefill_protocol_is_race_free(items):
 
 
 @pytest.mark.parametrize("mutate", ["k_count_one", "k_release_early", "v_release_early", "s_before_pv",
-                                    "no_early_take", "one_p_barrier", "no_final_wait", "producer_parity",
+                                    "no_early_take", "one_p_barrier", "no_turn_wait", "no_final_wait", "producer_parity",
                                     "no_q_empty_wait", "v_release_one_tile", "no_land_wait"])
 def test_planted_protocol_mistakes_are_caught(mutate):
     caught = 0

@@ -236,3 +236,31 @@ def test_prefill_over_several_launches(pa, cap):
     assert torch.equal(out, one)
     assert pa.get_status() == 0
     assert pa.lib().pa_prefill_test_items_per_launch(-1) == -1
+
+
+@pytest.mark.parametrize("name", ["g4_d128_b16", "g4_d64_b8"])
+def test_prefill_output_16_byte_aligned(pa, name):
+    """Output rows written into a view 16 bytes past a 32-byte boundary: full
+    tiles go out by TMA store from their staging buffer, a sequence's last
+    (partial) tile by 16-byte stores of each row; the elements on either side
+    of the view stay untouched."""
+    prev, new, H, Hkv, D, B = CASES[name]
+    b = _batch(sum(new) + 5 * len(prev), prev, new, H, Hkv, D, B)
+    T = int(b["qs"][-1])
+    n = T * H * D
+    sentinel = -7.0
+    base = torch.full((8 + n + 8,), sentinel, dtype=torch.bfloat16, device="cuda")
+    out = base[8:8 + n].view(T, H, D)
+    assert out.data_ptr() % 32 == 16
+    kc, vc = to_dev(b["kc"]), to_dev(b["vc"])
+    got = pa.prefill(to_dev(b["q"]), to_dev(b["k"]), to_dev(b["v"]), torch.from_numpy(b["slots"]).cuda(),
+                     torch.from_numpy(b["qs"]).cuda(), torch.from_numpy(b["ctx"]).cuda(),
+                     torch.from_numpy(b["tables"]).cuda(), int(np.diff(b["qs"]).max()), int(b["ctx"].max()),
+                     b["scale"], kc, vc, out=out)
+    torch.cuda.synchronize()
+    assert got.data_ptr() == out.data_ptr()
+    _, _, ref = oracle_prefill(b["q"], b["k"], b["v"], b["slots"], b["qs"], b["ctx"], b["tables"], b["kc"], b["vc"],
+                               b["scale"], "bf16")
+    assert_close(out, ref, "bf16", name + " (16-byte aligned output)")
+    assert bool((base[:8] == sentinel).all()) and bool((base[8 + n:] == sentinel).all())
+    assert pa.get_status() == 0

@@ -22,15 +22,16 @@
 // softmax finishes a step.  Roles:
 //  * warps 8 and 9 (producers): stream the keys (warp 8) and values (warp 9)
 //    of each item, 128 tokens (two steps) per stage, into rings of their
-//    own (2 stages each) that run on across items, with an L2 policy that keeps them
-//    for the other pairs of the same sequence and head, one TMA box per
-//    block (a 4D view of the cache: groups of 8 rows with both 64-dim
-//    halves, 128-byte swizzle, which is the layout of a K-major operand of
-//    the tensor cores for keys and of an MN-major one for values); chunks
-//    of cached tokens go out while the append kernel still runs, the first
-//    chunk that holds a new token after griddepcontrol.wait (the append
-//    writes only the new tokens' slots); lane b issues block b of a chunk from
-//    block-table entries fetched 32 at a time.  Warp 8 first loads the
+//    own (2 stages each) that run on across items, with an L2 policy that
+//    keeps them for the other pairs of the same sequence and head, one TMA
+//    box per block (a 4D view of the cache: groups of 8 rows with both
+//    64-dim halves, 128-byte swizzle, which is the layout of a K-major
+//    operand of the tensor cores for keys and of an MN-major one for
+//    values); chunks of cached tokens go out while the append kernel may
+//    still run, the first chunk that holds a new token after
+//    griddepcontrol.wait (the append writes only the new tokens' slots);
+//    lane b issues block b of a chunk from block-table entries fetched 32
+//    at a time.  Warp 8 first loads the
 //    item's query tiles, one 3D box per 64-dim half, once the previous
 //    item's last S has completed.  Value rows past a sequence's end (in its
 //    last block) are cleared by warp 9 once their copy has landed, and the

@@ -150,8 +150,8 @@ struct PfCfg {
   static constexpr int kOffV = kOffK + kStagesK * kKVStage;
   static constexpr int kOffOut = kOffV + kStagesV * kKVStage;  // one tile's output rows, staged for a TMA store
   static constexpr int kOffBars = kOffOut + kQTile;
-  // barriers: the rings, kTileBars per tile, q_empty and drained per tile, v_land, out_free
-  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 2 * kTiles + 2) * 8;
+  // barriers: the rings, kTileBars per tile, q_empty, drained and staged per tile, v_land, out_free
+  static constexpr int kOffMisc = kOffBars + (2 * (kStagesK + kStagesV) + kTiles * kTileBars + 3 * kTiles + 2) * 8;
   // misc: tensor-memory address, abort flag, the busiest CTA's load of each
   // candidate list (4), the CTA's item count; then its items
   static constexpr int kOffList = kOffMisc + 32;
@@ -391,7 +391,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   auto q_full = [&](int t) { return tile_bars + t * kTileBars + 4; };
   uint64_t* q_empty = tile_bars + kTiles * kTileBars;  // per tile: the item's last S is done, the query tile is free
   uint64_t* drained = q_empty + kTiles;                // per MMA warp: every MMA it issued is done
-  uint64_t* v_land = drained + kTiles;                 // the values of a chunk that holds rows past its sequence have landed
+  uint64_t* staged = drained + kTiles;                 // per tile: its warps have staged their output rows
+  uint64_t* v_land = staged + kTiles;                  // the values of a chunk that holds rows past its sequence have landed
   uint64_t* out_free = v_land + 1;                     // a tile's turn on the output staging buffer has ended
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
@@ -418,6 +419,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(q_empty + t, 1);
       mbar_init(drained + t, 1);
+      mbar_init(staged + t, kSoftWarps);  // one arrival per warp
     }
     mbar_init(v_land, 1);
     mbar_init(out_free, 1);
@@ -715,8 +717,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t s_base = lane_base + kColS + (uint32_t)t * 128;  // S buffer b at s_base + kSub·b
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     // Phases consumed per S buffer, chunks of keys (and values) before the
-    // item, items finished.
-    uint32_t sfc[2] = {0, 0}, ch = 0, done = 0;
+    // item, items finished, tiles staged for a TMA store.
+    uint32_t sfc[2] = {0, 0}, ch = 0, done = 0, nstaged = 0;
     bool ok = true;
     // Commit C(v) of an item of ns steps is the MMA thread's commit into
     // buffer v % 2 that follows S(v) (v = 0, 1) or P·V(v - 2) and, for
@@ -868,16 +870,20 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       // (tile 0 of an item, tile 1, tile 0 of the next item, ...), turn k
       // waiting for the end of turn k - 1.  Other tiles (a sequence's last)
       // store their rows directly.
+      // Every wait here is a bounded mbarrier wait, each warp its own: a
+      // warp that gave up earlier (a time-out) never leaves the others
+      // waiting without a limit.  The turn passes on only once all four
+      // warps have taken it (their arrivals on `staged`), so no warp's
+      // parity test can meet a later turn's phase.
       const uint32_t turn = 2 * done + (uint32_t)t;
-      bool turn_ok = true;
-      if (lt == 0 && turn > 0) turn_ok = mbar_wait(out_free, (turn - 1) & 1, abort);
-      if (!named_barrier_and(1 + t, kM, turn_ok)) {
+      ++done;
+      if (!__all_sync(0xffffffffu, turn == 0 || mbar_wait(out_free, (turn - 1) & 1, abort))) {
         ok = false;
         break;
       }
-      ++done;
-      if (row0 + kM <= it.rows) {
-        uint8_t* stage = base + C::kOffOut;
+      const bool full = row0 + kM <= it.rows;
+      uint8_t* stage = base + C::kOffOut;
+      if (full) {
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
@@ -885,16 +891,29 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             *reinterpret_cast<uint4*>(stage + h * kQHalf + lt * 128 + ((u ^ (lt & 7)) << 4)) =
                 make_uint4(w[32 * h + 4 * u], w[32 * h + 4 * u + 1], w[32 * h + 4 * u + 2], w[32 * h + 4 * u + 3]);
         fence_proxy_async_smem();  // the rows before the TMA unit reads them
-        named_barrier_sync(1 + t, kM);
-        if (lt == 0) {
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(staged + t);  // one arrival speaks for the warp
+      int staged_ok = 1;
+      if (lt == 0) {
+        staged_ok = mbar_wait(staged + t, nstaged & 1, abort);
+        if (staged_ok) {
+          if (full) {
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_store_3d(&omap, stage + h * kQHalf, 64 * h, it.kvh * p.g, it.q0 + row0 / p.g);
-          bulk_store_drain();  // the buffer has been read
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_store_3d(&omap, stage + h * kQHalf, 64 * h, it.kvh * p.g, it.q0 + row0 / p.g);
+            bulk_store_drain();  // the buffer has been read
+          }
           mbar_arrive(out_free);
         }
-      } else {
-        if (lt == 0) mbar_arrive(out_free);  // the turn passes at once
+      }
+      // the first warp of the tile leaves together (warp-wide shuffles follow)
+      if (warp % kSoftWarps == 0 && !__shfl_sync(0xffffffffu, staged_ok, 0)) {
+        ok = false;
+        break;
+      }
+      ++nstaged;
+      if (!full) {
         if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
           // The four lanes of a quad trade pieces (a 4 x 4 transpose of
           // 32-byte pieces per 128 bytes of row, two rounds of xor shuffles):

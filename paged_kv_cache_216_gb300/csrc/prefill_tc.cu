@@ -872,12 +872,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       // store their rows directly.
       // Every wait here is a bounded mbarrier wait, each warp its own: a
       // warp that gave up earlier (a time-out) never leaves the others
-      // waiting without a limit.  The turn passes on only once all four
-      // warps have taken it (their arrivals on `staged`), so no warp's
-      // parity test can meet a later turn's phase.
+      // waiting without a limit.  They spin rather than suspend in
+      // try_wait, which resumed several hundred cycles late here.  The
+      // turn passes on only once all four warps have taken it (their
+      // arrivals on `staged`), so no warp's parity test can meet a later
+      // turn's phase.
       const uint32_t turn = 2 * done + (uint32_t)t;
       ++done;
-      if (!__all_sync(0xffffffffu, turn == 0 || mbar_wait(out_free, (turn - 1) & 1, abort))) {
+      if (!__all_sync(0xffffffffu, turn == 0 || mbar_spin(out_free, (turn - 1) & 1, abort))) {
         ok = false;
         break;
       }
@@ -896,7 +898,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       if (lane == 0) mbar_arrive(staged + t);  // one arrival speaks for the warp
       int staged_ok = 1;
       if (lt == 0) {
-        staged_ok = mbar_wait(staged + t, nstaged & 1, abort);
+        staged_ok = mbar_spin(staged + t, nstaged & 1, abort);
         if (staged_ok) {
           if (full) {
 #pragma unroll

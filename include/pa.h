@@ -283,6 +283,18 @@ int pa_prefill(const void* q, const void* k, const void* v,
 int pa_prefill_test_items_per_launch(int items_per_launch);
 
 /*
+ * Test hook for the prefill's failure detection (every pipeline wait of the
+ * tcgen05 kernel gives up after 2 s, raises PA_STATUS_TIMEOUT, lets its
+ * copies and products in flight finish and exits): from now on the key
+ * producer of every CTA never issues its chunk number `chunk` (counted over
+ * the CTA's chunks of keys, from 0), so that the waits for it run out; -1
+ * restores normal operation.  Not for production.  Applies to the calls that
+ * follow, from every thread.  Returns PA_OK, or PA_ERR_INVALID for a chunk
+ * below -1.
+ */
+int pa_prefill_test_withhold(int chunk);
+
+/*
  * Paged decode over FP8 caches written by pa_cache_append_fp8: the result of
  * pa_decode with K = e4m3(code) * k_scale and V = e4m3(code) * v_scale.  q
  * and out are bf16; head_dim 128; products in FP16 on tensor cores, sums in

@@ -46,6 +46,7 @@ SIGNATURES = {
     "pa_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _vp]),
     "pa_prefill_test_items_per_launch": (_c_int, [_c_int]),
+    "pa_prefill_test_withhold": (_c_int, [_c_int]),
     "pa_decode_test_withhold": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_f, _vp, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_sz, _c_int, _c_int, _vp]),
     "pa_decode_plan_bytes": (_c_sz, [_c_int, _c_int, _c_int]),

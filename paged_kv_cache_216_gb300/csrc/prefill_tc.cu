@@ -370,7 +370,8 @@ template <int DH>
 __global__ void __launch_bounds__(kThreadsT, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-                      const __grid_constant__ PrefillArgs p, int pairs, int first_item, int num_items) {
+                      const __grid_constant__ PrefillArgs p, int pairs, int first_item, int num_items,
+                      int withhold) {
   using C = PfCfg<DH>;
   constexpr int kQTile = C::kQTile, kKVStage = C::kKVStage, kOffK = C::kOffK, kOffV = C::kOffV;
   constexpr uint32_t kColO = C::kColO, kColS = C::kColS;
@@ -542,16 +543,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           const bool clear = kv == 1 && z0 < z1;
           uint64_t* land = clear ? v_land : &fulls[st];
           int okc = 1;
+          // (test hook: the key warp never issues its CTA's chunk number
+          // `withhold`, so that the waits for it run out)
+          const bool issue = !(kv == 0 && k == (uint32_t)withhold);
           if (lane == 0) {
             okc = mbar_wait(&empties[st], ((k / stages) & 1) ^ 1, abort);
-            if (okc) mbar_arrive_expect_tx(land, (uint32_t)(nb * p.B * 128 * C::kHalves));
+            if (okc && issue) mbar_arrive_expect_tx(land, (uint32_t)(nb * p.B * 128 * C::kHalves));
           }
           if (!__shfl_sync(0xffffffffu, okc, 0)) {
             ok = false;
             break;
           }
           __syncwarp();  // the expected byte count is set before any copy can land
-          if (lane < nb) {  // block `lane` of the chunk: one box of B rows, both halves
+          if (issue && lane < nb) {  // block `lane` of the chunk: one box of B rows, both halves
             const int grp = (id * p.Hkv + it.kvh) * (p.B / 8);
             uint8_t* d = base + (kv == 0 ? kOffK : kOffV) + st * kKVStage + lane * p.B * 128 * C::kHalves;
             tma_load_4d(d, map, land, 0, 0, 0, grp, policy);
@@ -972,9 +976,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
 }
 
-// Test hook (pa_prefill_test_items_per_launch): a smaller bound on the
-// items of one launch; 0 for none.
+// Test hooks: a smaller bound on the items of one launch, 0 for none
+// (pa_prefill_test_items_per_launch); the key chunk every CTA withholds,
+// -1 for none (pa_prefill_test_withhold).
 std::atomic<int> g_items_per_launch{0};
+std::atomic<int> g_withhold{-1};
 
 template <int DH>
 cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -1005,6 +1011,7 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   long long per_launch = (long long)kListCap * sms[dev];
   const int cap = g_items_per_launch.load(std::memory_order_relaxed);
+  const int withhold = g_withhold.load(std::memory_order_relaxed);
   if (cap > 0) per_launch = std::min<long long>(per_launch, cap);
   for (long long first = 0; first < items; first += per_launch) {
     const long long n = std::min(per_launch, items - first);
@@ -1019,7 +1026,8 @@ cudaError_t launch_prefill_tc_dh(const PrefillArgs& a, const CUtensorMap& kmap, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, omap, a, pairs, (int)first, (int)n);
+    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DH>, kmap, vmap, qmap, omap, a, pairs, (int)first, (int)n,
+                           withhold);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1042,5 +1050,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const CUtensorMap& kmap, con
 extern "C" int pa_prefill_test_items_per_launch(int items_per_launch) {
   if (items_per_launch < 0) return pa_fail(PA_ERR_INVALID, "pa_prefill_test_items_per_launch: negative");
   pa::g_items_per_launch.store(items_per_launch, std::memory_order_relaxed);
+  return PA_OK;
+}
+
+extern "C" int pa_prefill_test_withhold(int chunk) {
+  if (chunk < -1) return pa_fail(PA_ERR_INVALID, "pa_prefill_test_withhold: chunk < -1");
+  pa::g_withhold.store(chunk, std::memory_order_relaxed);
   return PA_OK;
 }
